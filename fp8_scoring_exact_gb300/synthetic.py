@@ -1,0 +1,212 @@
+"""Seeded synthetic inputs for the DSA indexer (shared by the CUDA path's tests,
+the bench and the oracle's tests).
+
+This module only *draws* inputs: Gaussian activations, per-token FP8 e4m3
+quantisation (scale = amax / 448, round-to-nearest-even via torch's own
+float8_e4m3fn cast, saturated to +-448), causal valid ranges, paged caches and
+block tables.  It contains none of the indexer's arithmetic (no decoding, no
+scoring, no selection), so the oracle and the CUDA path stay independent.
+
+Workload shapes follow the problem statement of "Fusing Indexer Scoring and
+Exact Top-k for DeepSeek-V3.2" (section 2.3: FP8 Q [Q,64,128], keys [N,128]
+with scales, head weights [Q,64], per-row valid range) and the paged indexer
+of the contest write-up (DSA TopK Indexer: 64-token pages, per-token FP32
+key scales, block_table, seq_lens).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+H = 64     # indexer heads
+D = 128    # head dimension
+PAGE = 64  # tokens per KV-cache page
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3_per_token(x: np.ndarray):
+    """Per-token FP8 e4m3 quantisation of the last axis.
+
+    scale = amax / 448 (1.0 when a token is all zeros); the bytes are
+    torch's round-to-nearest-even float8_e4m3fn cast of x / scale, clamped to
+    +-448 first so that no NaN code is produced.  Returns (uint8 codes,
+    float32 scales) with scales shaped x.shape[:-1].
+    """
+    xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    amax = xt.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    y = (xt / scale.unsqueeze(-1)).clamp(-E4M3_MAX, E4M3_MAX)
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy().copy(), scale.numpy().astype(np.float32)
+
+
+def quantize_e4m3_per_row_shared(x: np.ndarray):
+    """Quantise q [..., H, D] with ONE scale per query token shared by all
+    heads (amax over the H*D values of the token)."""
+    shp = x.shape
+    flat = x.reshape(shp[:-2] + (shp[-2] * shp[-1],))
+    codes, scale = quantize_e4m3_per_token(flat)
+    return codes.reshape(shp), scale
+
+
+@dataclass
+class DenseInputs:
+    """One dense (prefill) indexer problem, all arrays C-contiguous numpy."""
+    q: np.ndarray          # uint8 [Q, H, D] e4m3 codes
+    q_scale: np.ndarray    # float32 [Q]
+    k: np.ndarray          # uint8 [N, D] e4m3 codes
+    k_scale: np.ndarray    # float32 [N]
+    w: np.ndarray          # float32 [Q, H]
+    row_begin: np.ndarray  # int32 [Q]
+    row_end: np.ndarray    # int32 [Q]
+    K: int = 2048
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def Q(self):
+        return self.q.shape[0]
+
+    @property
+    def N(self):
+        return self.k.shape[0]
+
+    def row_keys(self) -> int:
+        return int((self.row_end.astype(np.int64) - self.row_begin).sum())
+
+
+@dataclass
+class PagedInputs:
+    """One paged (decode) indexer problem."""
+    q: np.ndarray            # uint8 [B, next_n, H, D]
+    q_scale: np.ndarray      # float32 [B, next_n]
+    k_cache: np.ndarray      # uint8 [P, PAGE, D]
+    k_cache_scale: np.ndarray  # float32 [P, PAGE]
+    w: np.ndarray            # float32 [B, next_n, H]
+    block_table: np.ndarray  # int32 [B, max_pages]
+    seq_lens: np.ndarray     # int32 [B]
+    K: int = 2048
+    name: str = ""
+
+    @property
+    def B(self):
+        return self.q.shape[0]
+
+    @property
+    def next_n(self):
+        return self.q.shape[1]
+
+    @property
+    def max_pages(self):
+        return self.block_table.shape[1]
+
+    def row_lengths(self) -> np.ndarray:
+        """Valid length of every (b, i) row: seq_len - next_n + i + 1, >= 0."""
+        i = np.arange(self.next_n, dtype=np.int64)[None, :]
+        L = self.seq_lens.astype(np.int64)[:, None] - self.next_n + i + 1
+        return np.maximum(L, 0)
+
+    def row_keys(self) -> int:
+        return int(self.row_lengths().sum())
+
+
+def _gauss(rng, shape):
+    return rng.standard_normal(shape, dtype=np.float32)
+
+
+def causal_ranges(Q: int, N: int):
+    """Row t of a causal prefill chunk sees keys [0, N - Q + t + 1)."""
+    t = np.arange(Q, dtype=np.int64)
+    return np.zeros(Q, np.int32), (N - Q + t + 1).astype(np.int32)
+
+
+def make_dense(Q: int, N: int, *, K: int = 2048, seed: int = 0, causal: bool = True,
+               key_mode: str = "iid", n_distinct: int = 256, sparse_w_frac: float = 0.0,
+               name: str = "") -> DenseInputs:
+    """Draw one dense problem.
+
+    key_mode: "iid"     k ~ N(0,1)
+              "shared"  k = m + e, one shared N(0,1) direction m plus N(0,1) noise
+              "distinct" only `n_distinct` distinct (FP8 vector, scale) pairs,
+                         placed at uniformly random positions
+    sparse_w_frac: fraction of rows whose weights are zero except one random head.
+    """
+    rng = np.random.default_rng(seed)
+    q8, qs = quantize_e4m3_per_row_shared(_gauss(rng, (Q, H, D)))
+    if key_mode == "iid":
+        k8, ks = quantize_e4m3_per_token(_gauss(rng, (N, D)))
+    elif key_mode == "shared":
+        m = _gauss(rng, (1, D))
+        k8, ks = quantize_e4m3_per_token(m + _gauss(rng, (N, D)))
+    elif key_mode == "distinct":
+        t8, ts = quantize_e4m3_per_token(_gauss(rng, (n_distinct, D)))
+        pick = rng.integers(0, n_distinct, size=N)
+        k8, ks = t8[pick].copy(), ts[pick].copy()
+    else:
+        raise ValueError(key_mode)
+    w = (_gauss(rng, (Q, H)) / 8.0).astype(np.float32)
+    if sparse_w_frac > 0:
+        n_sparse = int(round(sparse_w_frac * Q))
+        rows = rng.choice(Q, size=n_sparse, replace=False)
+        heads = rng.integers(0, H, size=n_sparse)
+        keep = w[rows, heads].copy()
+        w[rows, :] = 0.0
+        w[rows, heads] = keep
+    if causal:
+        rb, re = causal_ranges(Q, N)
+    else:
+        rb, re = np.zeros(Q, np.int32), np.full(Q, N, np.int32)
+    return DenseInputs(q=q8, q_scale=qs.reshape(Q), k=k8, k_scale=ks, w=w,
+                       row_begin=rb, row_end=re, K=K, name=name)
+
+
+def make_paged(B: int, next_n: int, *, K: int = 2048, seed: int = 4, len_lo: int = 1024,
+               len_hi: int = 131072, n_short: int = 8, short_hi: int = 2048,
+               name: str = "") -> PagedInputs:
+    """Draw one paged decode batch: seq_lens ~ U[len_lo, len_hi] with `n_short`
+    sequences forced into [len_lo, short_hi]; the pages of all sequences are a
+    random permutation of the cache; unused block-table entries hold -1."""
+    rng = np.random.default_rng(seed)
+    seq = rng.integers(len_lo, len_hi + 1, size=B).astype(np.int64)
+    if n_short:
+        short = rng.choice(B, size=min(n_short, B), replace=False)
+        seq[short] = rng.integers(len_lo, min(short_hi, len_hi) + 1, size=len(short))
+    npages = (seq + PAGE - 1) // PAGE
+    P = int(npages.sum())
+    max_pages = int(npages.max())
+    perm = rng.permutation(P).astype(np.int32)
+    bt = np.full((B, max_pages), -1, np.int32)
+    off = 0
+    for b in range(B):
+        bt[b, :npages[b]] = perm[off:off + npages[b]]
+        off += npages[b]
+    kc8, kcs = quantize_e4m3_per_token(_gauss(rng, (P * PAGE, D)))
+    q8, qs = quantize_e4m3_per_row_shared(_gauss(rng, (B * next_n, H, D)))
+    w = (_gauss(rng, (B, next_n, H)) / 8.0).astype(np.float32)
+    return PagedInputs(q=q8.reshape(B, next_n, H, D), q_scale=qs.reshape(B, next_n),
+                       k_cache=kc8.reshape(P, PAGE, D), k_cache_scale=kcs.reshape(P, PAGE),
+                       w=w, block_table=bt, seq_lens=seq.astype(np.int32), K=K, name=name)
+
+
+# The five workloads of the indexer study, smallest first.  Sizes are the
+# published shapes; `scale` shrinks N (and Q) for CPU-sized parity cases.
+CONFIG_NAMES = ["tiny_q8_n8k", "causal_q2048_n16k", "causal_q4096_n128k",
+                "tiestress_q4096_n160k", "paged_b64_nn2"]
+
+
+def make_config(cid: int, seed: int | None = None):
+    seed = cid if seed is None else seed
+    if cid == 0:
+        return make_dense(8, 8192, seed=seed, causal=False, name=CONFIG_NAMES[0])
+    if cid == 1:
+        return make_dense(2048, 16384, seed=seed, key_mode="shared", name=CONFIG_NAMES[1])
+    if cid == 2:
+        return make_dense(4096, 131072, seed=seed, name=CONFIG_NAMES[2])
+    if cid == 3:
+        return make_dense(4096, 163840, seed=seed, key_mode="distinct", sparse_w_frac=0.05,
+                          name=CONFIG_NAMES[3])
+    if cid == 4:
+        return make_paged(64, 2, seed=seed, name=CONFIG_NAMES[4])
+    raise ValueError(cid)
