@@ -1,0 +1,601 @@
+// api.cu -- C ABI of the indexer library (include/dsa_indexer.h): argument
+// validation, per-(device, stream) scratch arena, tensor-map encoding and the
+// launch sequences of the fused, paged, unfused and standalone operators.
+//
+// Launch sequence of the fused operator (all on the caller's stream, no host
+// synchronisation):
+//   plan (ranges, pairs, work units) -> sample (thresholds, remapping path)
+//   -> persistent scorer in filter mode with TopK warps
+//   -> repair plan -> persistent scorer in store mode over the queued rows
+//   -> standalone exact select of those rows.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/dsa_indexer.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace dsa;
+
+namespace {
+
+// ---------------------------------------------------------------- options --
+std::mutex g_mu;
+int64_t g_chunk_tiles = 64;
+int64_t g_tau_bias = 0;
+int64_t g_profile = 0;
+int64_t g_grid = 0;
+int64_t g_target16 = 32;
+std::atomic<int64_t> g_launches{0};
+
+// ----------------------------------------------------------------- arena ----
+struct Layout {
+  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, group_done, cand_count, failed;
+  size_t cand_key, cand_idx, scores, total;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+Layout make_layout(int64_t R, int64_t G, bool cand, int64_t score_rows, int64_t ld) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.stats = take(sizeof(Stats));
+  L.rb = take(R * 4);
+  L.re = take(R * 4);
+  L.tau = take(R * 4);
+  L.groups = take(G * sizeof(Group));
+  L.unit_start = take((G + 1) * 4);
+  L.rgroups = take(R * sizeof(Group));
+  L.runit_start = take((R + 1) * 4);
+  L.group_done = take(G * 4);
+  L.cand_count = take(R * 4);
+  L.failed = take(R * 4);
+  L.cand_key = take(cand ? (size_t)R * CAND_CAP * 4 : 0);
+  L.cand_idx = take(cand ? (size_t)R * CAND_CAP * 4 : 0);
+  L.scores = take((size_t)score_rows * ld * 4);
+  L.total = off;
+  return L;
+}
+
+struct Arena {
+  uint8_t* base = nullptr;
+  size_t cap = 0;
+  Layout L{};
+  cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+  bool profiled = false;
+  bool used = false;
+};
+
+std::map<std::pair<int, cudaStream_t>, Arena> g_arenas;
+
+// Returns the arena of (current device, stream) with room for `need` bytes.
+Arena* get_arena(cudaStream_t stream, const Layout& L, int* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    *err = DSA_ERR_CUDA;
+    return nullptr;
+  }
+  Arena& a = g_arenas[{dev, stream}];
+  if (a.cap < L.total) {
+    if (a.base) {
+      cudaDeviceSynchronize();
+      cudaFree(a.base);
+      a.base = nullptr;
+      a.cap = 0;
+    }
+    const size_t want = align_up(L.total + L.total / 8, 1 << 20);
+    if (cudaMalloc(&a.base, want) != cudaSuccess) {
+      cudaGetLastError();
+      *err = DSA_ERR_CUDA;
+      return nullptr;
+    }
+    a.cap = want;
+  }
+  if (!a.ev0) {
+    cudaEventCreate(&a.ev0);
+    cudaEventCreate(&a.ev1);
+  }
+  a.L = L;
+  a.used = true;
+  return &a;
+}
+
+template <class T>
+T* at(Arena* a, size_t off) {
+  return reinterpret_cast<T*>(a->base + off);
+}
+
+// ------------------------------------------------------------ tensor maps --
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// rows of 128 FP8 bytes, 128-byte swizzle, box = 128 bytes x box_rows
+bool tmap_rows_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D};
+  cuuint32_t box[2] = {(cuuint32_t)D, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tmap_f32_1d(CUtensorMap* m, const float* base, uint64_t n, uint32_t box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[1] = {(cuuint64_t)n};
+  cuuint64_t strides[1] = {0};
+  cuuint32_t boxd[1] = {box};
+  cuuint32_t estr[1] = {1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(base), dims, strides, boxd, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+#define DSA_LAUNCH(expr)                        \
+  do {                                          \
+    cudaError_t e_ = (expr);                    \
+    g_launches.fetch_add(1);                    \
+    if (e_ != cudaSuccess) return DSA_ERR_CUDA; \
+  } while (0)
+
+struct Opts {
+  int chunk, grid, target16;
+  int64_t bias;
+  bool profile;
+};
+
+Opts read_opts() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Opts o;
+  o.chunk = (int)g_chunk_tiles;
+  o.bias = g_tau_bias;
+  o.profile = g_profile != 0;
+  o.target16 = (int)g_target16;
+  const int sms = sm_count();
+  o.grid = g_grid > 0 ? (int)g_grid : (sms > 0 ? sms : 1);
+  return o;
+}
+
+// ------------------------------------------------- shared launch sequence --
+// Fused pipeline over a row space whose keys are described by tm_k / tm_ks.
+int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+              const CUtensorMap& tm_ks, const uint8_t* k_raw, const float* ks_raw, const float* q_scale,
+              const float* w, const int32_t* row_begin, const int32_t* row_end, int32_t* out, cudaStream_t stream) {
+  const Opts o = read_opts();
+  const int G = n_pairs(rs);
+  const int64_t ld = align_up((size_t)rs.N, 4);
+  std::lock_guard<std::mutex> lk(g_mu);
+  int err = DSA_OK;
+  Arena* a = get_arena(stream, make_layout(rs.R, G, true, rs.R, ld), &err);
+  if (!a) return err;
+  const Layout& L = a->L;
+  Stats* st = at<Stats>(a, L.stats);
+
+  PlanParams pp{};
+  pp.rs = rs;
+  pp.repair = 0;
+  pp.K = K;
+  pp.trivial_len = K;
+  pp.chunk_tiles = o.chunk;
+  pp.row_begin_in = row_begin;
+  pp.row_end_in = row_end;
+  pp.rb = at<int32_t>(a, L.rb);
+  pp.re = at<int32_t>(a, L.re);
+  pp.groups = at<Group>(a, L.groups);
+  pp.unit_start = at<int32_t>(a, L.unit_start);
+  pp.group_done = at<int32_t>(a, L.group_done);
+  pp.cand_count = at<int32_t>(a, L.cand_count);
+  pp.failed_rows = at<int32_t>(a, L.failed);
+  pp.stats = st;
+  DSA_LAUNCH(launch_plan(pp, stream));
+
+  SampleParams sp{};
+  sp.rs = rs;
+  sp.K = K;
+  sp.target16 = o.target16;
+  sp.tau_bias = o.bias;
+  sp.k = k_raw;
+  sp.k_scale = ks_raw;
+  sp.q_scale = q_scale;
+  sp.w = w;
+  sp.rb = pp.rb;
+  sp.re = pp.re;
+  sp.tau = at<uint32_t>(a, L.tau);
+  sp.out = out;
+  sp.stats = st;
+  DSA_LAUNCH(launch_sample(tm_q, sp, G, stream));
+
+  ScoreParams cp{};
+  cp.rs = rs;
+  cp.mode = MODE_FILTER;
+  cp.K = K;
+  cp.chunk_tiles = o.chunk;
+  cp.repair = 0;
+  cp.q_scale = q_scale;
+  cp.w = w;
+  cp.rb = pp.rb;
+  cp.re = pp.re;
+  cp.groups = pp.groups;
+  cp.unit_start = pp.unit_start;
+  cp.tau = sp.tau;
+  cp.cand_key = at<uint32_t>(a, L.cand_key);
+  cp.cand_idx = at<int32_t>(a, L.cand_idx);
+  cp.cand_count = pp.cand_count;
+  cp.group_done = pp.group_done;
+  cp.failed_rows = at<int32_t>(a, L.failed);
+  cp.out = out;
+  cp.stats = st;
+  a->profiled = o.profile;
+  if (o.profile) cudaEventRecord(a->ev0, stream);
+  DSA_LAUNCH(launch_score(tm_q, tm_k, tm_ks, cp, o.grid, stream));
+  if (o.profile) cudaEventRecord(a->ev1, stream);
+
+  // exact repair of rows whose certificate failed
+  PlanParams rp = pp;
+  rp.repair = 1;
+  rp.groups = at<Group>(a, L.rgroups);
+  rp.unit_start = at<int32_t>(a, L.runit_start);
+  DSA_LAUNCH(launch_plan(rp, stream));
+
+  ScoreParams rcp = cp;
+  rcp.mode = MODE_STORE;
+  rcp.repair = 1;
+  rcp.groups = rp.groups;
+  rcp.unit_start = rp.unit_start;
+  rcp.scores = at<float>(a, L.scores);
+  rcp.ld = ld;
+  DSA_LAUNCH(launch_score(tm_q, tm_k, tm_ks, rcp, o.grid, stream));
+
+  SelectParams sel{};
+  sel.rs = rs;
+  sel.K = K;
+  sel.target16 = o.target16;
+  sel.list_mode = 1;
+  sel.list = rcp.failed_rows;
+  sel.scores = rcp.scores;
+  sel.ld = ld;
+  sel.rb = pp.rb;
+  sel.re = pp.re;
+  sel.out = out;
+  sel.stats = st;
+  DSA_LAUNCH(launch_select(sel, o.grid, stream));
+  return DSA_OK;
+}
+
+int check_dense(const uint8_t* q, const float* qs, const uint8_t* k, const float* ks, const float* w,
+                const int32_t* rb, const int32_t* re, int Q, int N) {
+  if (!q || !qs || !k || !ks || !w || !rb || !re) return DSA_ERR_ARG;
+  if (Q <= 0 || N <= 0) return DSA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(ks)) return DSA_ERR_ARG;
+  if ((int64_t)Q * H >= (1ll << 31) || (int64_t)N >= (1ll << 31) - TILE) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI ==
+extern "C" {
+
+int dsa_indexer_topk(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
+                     const float* w, const int32_t* row_begin, const int32_t* row_end, int Q, int N, int K,
+                     int32_t* out_idx, dsa_stream_t stream_) {
+  int rc = check_dense(q_fp8, q_scale, k_fp8, k_scale, w, row_begin, row_end, Q, N);
+  if (rc != DSA_OK) return rc;
+  if (!out_idx || K < 1 || K > DSA_MAX_K) return DSA_ERR_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  CUtensorMap tq, tk, tks;
+  if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)Q * H, H) || !tmap_rows_u8(&tk, k_fp8, N, TILE) ||
+      !tmap_f32_1d(&tks, k_scale, N, TILE))
+    return DSA_ERR_CUDA;
+  RowSpace rs{};
+  rs.R = Q;
+  rs.N = N;
+  return run_fused(rs, K, tq, tk, tks, k_fp8, k_scale, q_scale, w, row_begin, row_end, out_idx, stream);
+}
+
+int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_cache,
+                           const float* k_cache_scale, const float* w, const int32_t* block_table,
+                           const int32_t* seq_lens, int B, int next_n, int max_pages, int num_pages, int K,
+                           int32_t* out_idx, dsa_stream_t stream_) {
+  if (!q_fp8 || !q_scale || !k_cache || !k_cache_scale || !w || !block_table || !seq_lens || !out_idx)
+    return DSA_ERR_ARG;
+  if (B <= 0 || next_n <= 0 || max_pages <= 0 || num_pages <= 0 || K < 1 || K > DSA_MAX_K) return DSA_ERR_ARG;
+  if (!aligned16(q_fp8) || !aligned16(k_cache) || !aligned16(k_cache_scale)) return DSA_ERR_ARG;
+  const int64_t R = (int64_t)B * next_n;
+  if (R * H >= (1ll << 31) || (int64_t)max_pages * PAGE >= (1ll << 31) - TILE ||
+      (int64_t)num_pages * PAGE >= (1ll << 31))
+    return DSA_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  CUtensorMap tq, tk, tks;
+  if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)R * H, H) ||
+      !tmap_rows_u8(&tk, k_cache, (uint64_t)num_pages * PAGE, PAGE) ||
+      !tmap_f32_1d(&tks, k_cache_scale, (uint64_t)num_pages * PAGE, PAGE))
+    return DSA_ERR_CUDA;
+  RowSpace rs{};
+  rs.R = (int)R;
+  rs.N = max_pages * PAGE;
+  rs.paged = 1;
+  rs.block_table = block_table;
+  rs.seq_lens = seq_lens;
+  rs.max_pages = max_pages;
+  rs.next_n = next_n;
+  rs.num_pages = num_pages;
+  return run_fused(rs, K, tq, tk, tks, k_cache, k_cache_scale, q_scale, w, nullptr, nullptr, out_idx, stream);
+}
+
+static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
+                       const float* w, const int32_t* row_begin, const int32_t* row_end, int Q, int N, int K,
+                       float* scores, int64_t ld, int32_t* out_idx, cudaStream_t stream) {
+  // out_idx == nullptr: scores only (every non-empty row is scored)
+  const Opts o = read_opts();
+  CUtensorMap tq, tk, tks;
+  if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)Q * H, H) || !tmap_rows_u8(&tk, k_fp8, N, TILE) ||
+      !tmap_f32_1d(&tks, k_scale, N, TILE))
+    return DSA_ERR_CUDA;
+  RowSpace rs{};
+  rs.R = Q;
+  rs.N = N;
+  const int G = n_pairs(rs);
+  const int64_t own_ld = align_up((size_t)N, 4);
+  std::lock_guard<std::mutex> lk(g_mu);
+  int err = DSA_OK;
+  Arena* a = get_arena(stream, make_layout(Q, G, false, scores ? 0 : Q, own_ld), &err);
+  if (!a) return err;
+  const Layout& L = a->L;
+  Stats* st = at<Stats>(a, L.stats);
+  float* sbuf = scores ? scores : at<float>(a, L.scores);
+  const int64_t sld = scores ? ld : own_ld;
+
+  PlanParams pp{};
+  pp.rs = rs;
+  pp.K = K;
+  pp.trivial_len = out_idx ? K : 0;
+  pp.chunk_tiles = o.chunk;
+  pp.row_begin_in = row_begin;
+  pp.row_end_in = row_end;
+  pp.rb = at<int32_t>(a, L.rb);
+  pp.re = at<int32_t>(a, L.re);
+  pp.groups = at<Group>(a, L.groups);
+  pp.unit_start = at<int32_t>(a, L.unit_start);
+  pp.group_done = at<int32_t>(a, L.group_done);
+  pp.cand_count = at<int32_t>(a, L.cand_count);
+  pp.failed_rows = at<int32_t>(a, L.failed);
+  pp.stats = st;
+  DSA_LAUNCH(launch_plan(pp, stream));
+
+  ScoreParams cp{};
+  cp.rs = rs;
+  cp.mode = MODE_STORE;
+  cp.K = K;
+  cp.chunk_tiles = o.chunk;
+  cp.q_scale = q_scale;
+  cp.w = w;
+  cp.rb = pp.rb;
+  cp.re = pp.re;
+  cp.groups = pp.groups;
+  cp.unit_start = pp.unit_start;
+  cp.scores = sbuf;
+  cp.ld = sld;
+  cp.stats = st;
+  a->profiled = o.profile;
+  if (o.profile) cudaEventRecord(a->ev0, stream);
+  DSA_LAUNCH(launch_score(tq, tk, tks, cp, o.grid, stream));
+  if (o.profile) cudaEventRecord(a->ev1, stream);
+  if (!out_idx) return DSA_OK;
+
+  SelectParams sel{};
+  sel.rs = rs;
+  sel.K = K;
+  sel.target16 = o.target16;
+  sel.scores = sbuf;
+  sel.ld = sld;
+  sel.rb = pp.rb;
+  sel.re = pp.re;
+  sel.out = out_idx;
+  sel.stats = st;
+  DSA_LAUNCH(launch_select(sel, 2 * o.grid, stream));
+  return DSA_OK;
+}
+
+int dsa_indexer_topk_unfused(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
+                             const float* w, const int32_t* row_begin, const int32_t* row_end, int Q, int N, int K,
+                             int32_t* out_idx, dsa_stream_t stream) {
+  int rc = check_dense(q_fp8, q_scale, k_fp8, k_scale, w, row_begin, row_end, Q, N);
+  if (rc != DSA_OK) return rc;
+  if (!out_idx || K < 1 || K > DSA_MAX_K) return DSA_ERR_ARG;
+  return scores_impl(q_fp8, q_scale, k_fp8, k_scale, w, row_begin, row_end, Q, N, K, nullptr, 0, out_idx,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dsa_indexer_scores(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
+                       const float* w, const int32_t* row_begin, const int32_t* row_end, int Q, int N, float* scores,
+                       int64_t ld, dsa_stream_t stream) {
+  int rc = check_dense(q_fp8, q_scale, k_fp8, k_scale, w, row_begin, row_end, Q, N);
+  if (rc != DSA_OK) return rc;
+  if (!scores || ld < N || (ld & 3) || !aligned16(scores)) return DSA_ERR_ARG;
+  return scores_impl(q_fp8, q_scale, k_fp8, k_scale, w, row_begin, row_end, Q, N, 1, scores, ld, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t* row_begin, const int32_t* row_end,
+                                 int Q, int N, int K, int32_t* out_idx, dsa_stream_t stream_) {
+  if (!scores || !row_begin || !row_end || !out_idx) return DSA_ERR_ARG;
+  if (Q <= 0 || N <= 0 || ld < N || (ld & 3) || !aligned16(scores) || K < 1 || K > DSA_MAX_K) return DSA_ERR_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const Opts o = read_opts();
+  RowSpace rs{};
+  rs.R = Q;
+  rs.N = N;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int err = DSA_OK;
+  Arena* a = get_arena(stream, make_layout(Q, n_pairs(rs), false, 0, 0), &err);
+  if (!a) return err;
+  const Layout& L = a->L;
+  PlanParams pp{};
+  pp.rs = rs;
+  pp.K = K;
+  pp.trivial_len = 0x7fffffff;  // no scoring work: ranges and counters only
+  pp.chunk_tiles = o.chunk;
+  pp.row_begin_in = row_begin;
+  pp.row_end_in = row_end;
+  pp.rb = at<int32_t>(a, L.rb);
+  pp.re = at<int32_t>(a, L.re);
+  pp.groups = at<Group>(a, L.groups);
+  pp.unit_start = at<int32_t>(a, L.unit_start);
+  pp.group_done = at<int32_t>(a, L.group_done);
+  pp.cand_count = at<int32_t>(a, L.cand_count);
+  pp.failed_rows = at<int32_t>(a, L.failed);
+  pp.stats = at<Stats>(a, L.stats);
+  DSA_LAUNCH(launch_plan(pp, stream));
+  SelectParams sel{};
+  sel.rs = rs;
+  sel.K = K;
+  sel.target16 = o.target16;
+  sel.scores = scores;
+  sel.ld = ld;
+  sel.rb = pp.rb;
+  sel.re = pp.re;
+  sel.out = out_idx;
+  sel.stats = pp.stats;
+  a->profiled = false;
+  DSA_LAUNCH(launch_select(sel, 2 * o.grid, stream));
+  return DSA_OK;
+}
+
+int dsa_indexer_last_device_status(dsa_stream_t stream_, int32_t* failures_out) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_arenas.find({dev, stream});
+  if (it == g_arenas.end() || !it->second.used) {
+    if (failures_out) memset(failures_out, 0, 4 * sizeof(int32_t));
+    return DSA_OK;
+  }
+  Stats st;
+  if (cudaMemcpy(&st, it->second.base + it->second.L.stats, sizeof(Stats), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (failures_out) {
+    failures_out[0] = st.underflow;
+    failures_out[1] = st.overflow;
+    failures_out[2] = st.trivial;
+    failures_out[3] = st.cand_total;
+  }
+  if (st.status & ST_TIMEOUT) return DSA_ERR_TIMEOUT;
+  if (st.status & ST_RANGE) return DSA_ERR_RANGE;
+  return DSA_OK;
+}
+
+int dsa_indexer_set_option(int option, int64_t value) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  switch (option) {
+    case DSA_OPT_CHUNK_TILES:
+      if (value < 1 || value > (1 << 20)) return DSA_ERR_ARG;
+      g_chunk_tiles = value;
+      return DSA_OK;
+    case DSA_OPT_TAU_BIAS:
+      g_tau_bias = value;
+      return DSA_OK;
+    case DSA_OPT_PROFILE:
+      g_profile = value ? 1 : 0;
+      return DSA_OK;
+    case DSA_OPT_GRID_CTAS:
+      if (value < 0 || value > 65535) return DSA_ERR_ARG;
+      g_grid = value;
+      return DSA_OK;
+    case DSA_OPT_SAMPLE_TARGET:
+      if (value < 1 || value > 256) return DSA_ERR_ARG;
+      g_target16 = value;
+      return DSA_OK;
+    default:
+      return DSA_ERR_ARG;
+  }
+}
+
+int64_t dsa_indexer_get_option(int option) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  switch (option) {
+    case DSA_OPT_CHUNK_TILES:
+      return g_chunk_tiles;
+    case DSA_OPT_TAU_BIAS:
+      return g_tau_bias;
+    case DSA_OPT_PROFILE:
+      return g_profile;
+    case DSA_OPT_GRID_CTAS:
+      return g_grid;
+    case DSA_OPT_SAMPLE_TARGET:
+      return g_target16;
+    default:
+      return DSA_ERR_ARG;
+  }
+}
+
+float dsa_indexer_profiled_main_ms(dsa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1.f;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_arenas.find({dev, stream});
+  if (it == g_arenas.end() || !it->second.profiled) return -1.f;
+  if (cudaEventSynchronize(it->second.ev1) != cudaSuccess) return -1.f;
+  float ms = -1.f;
+  if (cudaEventElapsedTime(&ms, it->second.ev0, it->second.ev1) != cudaSuccess) return -1.f;
+  return ms;
+}
+
+int64_t dsa_indexer_launch_count(void) { return g_launches.load(); }
+
+const char* dsa_indexer_version(void) { return "dsa_indexer 0.1 (sm_103a, tcgen05 + TMA)"; }
+
+int dsa_indexer_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_arenas.empty()) cudaDeviceSynchronize();
+  for (auto& kv : g_arenas) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(kv.first.first);
+    if (kv.second.base) cudaFree(kv.second.base);
+    if (kv.second.ev0) cudaEventDestroy(kv.second.ev0);
+    if (kv.second.ev1) cudaEventDestroy(kv.second.ev1);
+    cudaSetDevice(cur);
+  }
+  g_arenas.clear();
+  return DSA_OK;
+}
+
+}  // extern "C"

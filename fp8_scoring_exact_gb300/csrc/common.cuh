@@ -1,0 +1,307 @@
+// common.cuh -- shared constants, plan structures and inline-PTX wrappers for
+// the sm_103a DSA indexer kernels (tcgen05 MMA with TMEM accumulators, TMA
+// tensor copies, mbarriers with bounded waits).
+//
+// Written from the public PTX ISA description of these instructions; no
+// library code is used.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsa {
+
+// ---------------------------------------------------------------- geometry --
+constexpr int H = 64;              // indexer heads
+constexpr int D = 128;             // head dimension (bytes per FP8 vector)
+constexpr int TILE = 128;          // keys per MMA tile (MMA M, one TMEM lane per key)
+constexpr int GROUP_ROWS = 2;      // query rows sharing one key stream (MMA N = 64 * rows)
+constexpr int PAGE = 64;           // tokens per paged-cache page
+
+// ------------------------------------------------------- persistent scorer --
+constexpr int STAGES = 6;          // key-tile ring depth (TMA -> MMA)
+constexpr int SC_STAGES = 12;      // key-scale ring depth (TMA -> epilogue)
+constexpr int ACC_BUFS = 4;        // TMEM accumulators (MMA -> epilogue)
+constexpr int ACC_COLS = 128;      // TMEM columns per accumulator (2 rows x 64 heads)
+constexpr int TOPK_QUEUE = 4;      // finished groups handed to the TopK warps
+constexpr int SCORE_THREADS = 384; // 12 warps: TMA, MMA, 2 TopK, 8 epilogue
+constexpr int TOPK_THREADS = 64;
+constexpr int EPI_THREADS = 256;
+
+// -------------------------------------------------------------- selection --
+constexpr int CAND_CAP = 8192;     // candidates kept per row (certificate capacity)
+constexpr int SAMPLE_STRIDE = 200; // one sample per 200 keys: ~0.5% of the row
+constexpr int SAMPLE_OFFSET = 100; // samples at keys 100 mod 200
+constexpr int MAX_SAMPLES = 1024;  // per row; longer rows widen the stride
+constexpr int SELECT_THREADS = 512;
+constexpr int SELECT_CAP = 12288;  // candidates the standalone selector keeps in SMEM
+
+enum Mode : int { MODE_STORE = 0, MODE_FILTER = 1 };
+
+// status word bits (per call)
+constexpr int ST_TIMEOUT = 1;
+constexpr int ST_RANGE = 2;
+
+// device counters of one call, laid out at the start of the arena
+struct Stats {
+  int status;
+  int underflow;     // rows whose candidate set had fewer than K entries
+  int overflow;      // rows whose candidate set exceeded CAND_CAP
+  int trivial;       // rows with L <= K (remapping path)
+  int cand_total;    // candidates appended (all rows)
+  int fail_count;    // rows queued for repair
+  int n_groups;      // main plan
+  int total_units;
+  int r_groups;      // repair plan
+  int r_units;
+  int pad[6];
+};
+
+// A work group: up to 2 query rows that stream the same keys.  Key range is
+// the union of the rows' valid ranges, in logical key coordinates.
+struct Group {
+  int nrows;
+  int row[GROUP_ROWS];   // logical row ids (dense: t; paged: b * next_n + i)
+  int slot[GROUP_ROWS];  // score-matrix row for MODE_STORE
+  int lo, hi;            // union key range [lo, hi)
+  int seq;               // paged: sequence b; dense: -1
+};
+
+// --------------------------------------------------------------- helpers ----
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Order-preserving float -> uint32 map (-0 canonicalised to +0).
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------- mbarriers ----
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Pipeline waits give up after this long (the kernel then records
+// ST_TIMEOUT, drains and returns instead of hanging the GPU).
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+// Bounded wait: true when the phase with `parity` completed; false when the
+// CTA-wide abort flag is set or the time limit passed (then it sets both the
+// abort flag and the status bit).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 7u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        atomicOr(status, ST_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform bounded wait: every lane polls (so every lane acquires the
+// phase) and every lane returns the same value, so code after it that needs
+// a converged warp (tcgen05.ld .sync.aligned, shuffles) never diverges.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int* status) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    const bool done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if ((it & 7u) == 7u) {
+      int give_up = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (*abort_flag) {
+          give_up = 1;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            atomicOr(status, ST_TIMEOUT);
+            give_up = 1;
+          }
+        }
+      }
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------- TMA ----
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* m, int x, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(bar)
+      : "memory");
+}
+// generic-proxy writes to shared memory -> visible to the async proxy (MMA)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// --------------------------------------------------------------- tcgen05 ----
+// Shared-memory matrix descriptor for a K-major operand stored in the 128-byte
+// swizzled layout TMA writes (rows of 128 bytes, 8-row / 1024-byte swizzle
+// atoms): start address >> 4, leading-byte offset 1 (unused for this layout),
+// stride-byte offset 1024 >> 4 between 8-row groups, descriptor version 1,
+// layout type 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
+  return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3
+// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
+// M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 32 e4m3 step.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// mbarrier arrives once when every tcgen05 op this thread issued so far completes.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------- radix select (shared) ----
+// Find the bucket of the K-th largest among `hist[256]` (counts of live keys
+// by the current byte), scanning from bucket 255 down.  Executed by one full
+// warp; writes the digit and the remaining rank (rank within that bucket) to
+// out[0], out[1].
+__device__ __forceinline__ void radix_pick_digit(const int* hist, int rem, int* out) {
+  const int lane = threadIdx.x & 31;
+  // lane l owns buckets 255-8l .. 248-8l (descending)
+  int c[8];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    c[i] = hist[255 - 8 * lane - i];
+    sum += c[i];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int excl = incl - sum;
+  const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
+  const int src = hit ? (__ffs(hit) - 1) : 31;
+  if (lane == src) {
+    int acc = excl;
+    int digit = 255 - 8 * lane - 7;
+    int r = rem - acc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (acc + c[i] >= rem) {
+        digit = 255 - 8 * lane - i;
+        r = rem - acc;
+        break;
+      }
+      acc += c[i];
+    }
+    out[0] = digit;
+    out[1] = r;
+  }
+}
+
+}  // namespace dsa

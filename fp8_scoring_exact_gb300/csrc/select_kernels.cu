@@ -1,0 +1,503 @@
+// select_kernels.cu -- device-side plan, sampled thresholds (with the
+// remapping path) and the standalone exact top-K over fp32 score rows.
+//
+// Method: "Fusing Indexer Scoring and Exact Top-k for DeepSeek-V3.2",
+// section 3.2 (sampled threshold aiming at ~2K candidates, compare-and-append,
+// four 8-bit radix passes over order-preserving keys, certificate, exact
+// repair) and section 3.4 (one shared-memory reservation per batch of items,
+// vector loads); remapping path for rows with at most K keys from the
+// contest write-up ("DSA TopK Indexer").
+#include "common.cuh"
+#include "kernels.h"
+#include "rows.cuh"
+
+namespace dsa {
+
+// ===================================================================== plan ==
+// One CTA of 1024 threads.  Main mode: validate every row's range, zero the
+// per-row counters, form the pairs and the unit prefix sum.  Repair mode: one
+// group per queued row.
+constexpr int PLAN_THREADS = 1024;
+
+__device__ __forceinline__ int block_inclusive_scan(int v, int* warp_sums) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int s = (lane < (int)(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;  // inclusive prefix over warps
+  }
+  __syncthreads();
+  const int res = x + (wid > 0 ? warp_sums[wid - 1] : 0);
+  __syncthreads();
+  return res;
+}
+
+__device__ __forceinline__ int group_units(int lo, int hi, int chunk) {
+  if (hi <= lo) return 0;
+  const int tiles = ceil_div(hi, TILE) - lo / TILE;
+  return ceil_div(tiles, chunk);
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_carry;
+  const RowSpace& rs = p.rs;
+  const int tid = threadIdx.x;
+  int G;
+  if (!p.repair) {
+    if (tid == 0) {
+      Stats z = {};
+      *p.stats = z;
+    }
+    __syncthreads();
+    int bad = 0;
+    for (int row = tid; row < rs.R; row += PLAN_THREADS) {
+      int b = 0, e = 0;
+      if (!rs.paged) {
+        b = p.row_begin_in[row];
+        e = p.row_end_in[row];
+        if (b < 0 || e > rs.N || b > e) {
+          bad = 1;
+          b = e = 0;
+        }
+      } else {
+        const int sq = row / rs.next_n, i = row % rs.next_n;
+        const int sl = rs.seq_lens[sq];
+        if (sl < 0 || sl > rs.max_pages * PAGE) {
+          bad = 1;
+        } else {
+          e = max(0, sl - rs.next_n + i + 1);
+        }
+      }
+      p.rb[row] = b;
+      p.re[row] = e;
+      p.cand_count[row] = 0;
+    }
+    if (bad) atomicOr(&p.stats->status, ST_RANGE);
+    __syncthreads();
+    G = n_pairs(rs);
+  } else {
+    G = p.stats->fail_count;
+  }
+
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < G; base += PLAN_THREADS) {
+    const int g = base + tid;
+    int units = 0;
+    if (g < G) {
+      Group grp;
+      grp.nrows = 0;
+      grp.lo = 0x7fffffff;
+      grp.hi = 0;
+      grp.row[0] = grp.row[1] = 0;
+      grp.slot[0] = grp.slot[1] = 0;
+      if (!p.repair) {
+        int rows[2];
+        const int nr = pair_rows(rs, g, rows);
+        grp.seq = rs.paged ? rows[0] / rs.next_n : -1;
+        for (int i = 0; i < nr; ++i) {
+          const int b = p.rb[rows[i]], e = p.re[rows[i]];
+          if (e - b > p.trivial_len) {
+            grp.row[grp.nrows] = rows[i];
+            grp.slot[grp.nrows] = rows[i];
+            ++grp.nrows;
+            grp.lo = min(grp.lo, b);
+            grp.hi = max(grp.hi, e);
+          }
+        }
+        p.group_done[g] = 0;
+      } else {
+        const int row = p.failed_rows[g];
+        grp.nrows = 1;
+        grp.row[0] = row;
+        grp.slot[0] = g;
+        grp.seq = rs.paged ? row / rs.next_n : -1;
+        grp.lo = p.rb[row];
+        grp.hi = p.re[row];
+      }
+      if (grp.nrows == 0) grp.lo = grp.hi = 0;
+      units = group_units(grp.lo, grp.hi, p.chunk_tiles);
+      p.groups[g] = grp;
+    }
+    const int incl = block_inclusive_scan(units, warp_sums);
+    const int carry = s_carry;
+    if (g < G) p.unit_start[g + 1] = carry + incl;
+    __syncthreads();
+    if (tid == PLAN_THREADS - 1) s_carry = carry + incl;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.unit_start[0] = 0;
+    if (!p.repair) {
+      p.stats->n_groups = G;
+      p.stats->total_units = s_carry;
+    } else {
+      p.stats->r_groups = G;
+      p.stats->r_units = s_carry;
+    }
+  }
+}
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
+  plan_kernel<<<1, PLAN_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ================================================================== sample ==
+// One CTA (4 warps) per query-row pair: rows with at most K keys take the
+// remapping path; the other rows score the keys on a 1-in-200 grid with
+// tcgen05 (keys gathered into a swizzled shared tile by the threads) and take
+// as threshold the sample of descending rank ceil(m * target / L).
+constexpr int SAMPLE_THREADS = 128;
+constexpr uint32_t SM_OFF_Q = 0;
+constexpr uint32_t SM_OFF_K = SM_OFF_Q + GROUP_ROWS * H * D;        // 16384
+constexpr uint32_t SM_OFF_SAMP = SM_OFF_K + TILE * D;               // 32768
+constexpr uint32_t SM_OFF_W = SM_OFF_SAMP + GROUP_ROWS * MAX_SAMPLES * 4;  // 40960
+constexpr uint32_t SM_OFF_SC = SM_OFF_W + GROUP_ROWS * H * 4;
+constexpr uint32_t SM_OFF_HIST = SM_OFF_SC + TILE * 4;
+constexpr uint32_t SM_OFF_MISC = SM_OFF_HIST + 256 * 4;
+// 64 KB per CTA keeps at most 3 CTAs (3 x 128 TMEM columns) on an SM
+constexpr uint32_t SAMPLE_SMEM = 64 * 1024;
+static_assert(SM_OFF_MISC + 64 + 1024 <= SAMPLE_SMEM, "sample smem");
+
+__global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                const SampleParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* samp = (uint32_t*)(smem + SM_OFF_SAMP);
+  float* wsm = (float*)(smem + SM_OFF_W);
+  float* scs = (float*)(smem + SM_OFF_SC);
+  int* hist = (int*)(smem + SM_OFF_HIST);
+  int* misc = (int*)(smem + SM_OFF_MISC);  // [0] tmem base, [1..2] digit, [3] abort, [4] wait verdict
+  const uint32_t bar = sbase + SM_OFF_MISC + 32;
+  const RowSpace& rs = p.rs;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int K = p.K;
+
+  int rows[2];
+  const int nr = pair_rows(rs, blockIdx.x, rows);
+  int act[2], nact = 0, lo = 0x7fffffff, hi = 0, ntriv = 0;
+  for (int i = 0; i < nr; ++i) {
+    const int b = p.rb[rows[i]], e = p.re[rows[i]];
+    if (e - b <= K) {
+      write_all_valid(rs, rows[i], b, e, K, p.out, tid, SAMPLE_THREADS);
+      ++ntriv;
+    } else {
+      act[nact++] = rows[i];
+      lo = min(lo, b);
+      hi = max(hi, e);
+    }
+  }
+  if (tid == 0 && ntriv) atomicAdd(&p.stats->trivial, ntriv);
+  if (nact == 0) return;
+  int first, m_u, S;
+  sample_grid(lo, hi, &first, &m_u, &S);
+  const int target = (int)(((int64_t)p.target16 * K) / 16);
+  if (m_u == 0) {
+    if (tid < nact) p.tau[act[tid]] = 0u;
+    return;
+  }
+
+  if (warp == 0) {
+    tmem_alloc(sbase + SM_OFF_MISC, TILE);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    misc[3] = 0;
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  for (int i = tid; i < nact * H; i += SAMPLE_THREADS) {
+    const int a = i / H, j = i % H;
+    wsm[i] = p.w[(int64_t)act[a] * H + j] * p.q_scale[act[a]];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = (uint32_t)misc[0];
+  volatile int* abort_flag = (volatile int*)&misc[3];
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, nact * H * D);
+    for (int a = 0; a < nact; ++a) tma_load_2d(sbase + SM_OFF_Q + a * H * D, &tm_q, 0, act[a] * H, bar);
+  }
+  // thread 0 waits (bounded) and the CTA follows its verdict
+  if (tid == 0) misc[4] = mbar_wait(bar, 0, abort_flag, &p.stats->status) ? 1 : 0;
+  __syncthreads();
+  bool ok = misc[4] != 0;
+  const uint32_t idesc = idesc_e4m3_f32(TILE, H * nact);
+  const int ntiles = ceil_div(m_u, TILE);
+  for (int tt = 0; tt < ntiles && ok; ++tt) {
+    const int j = tt * TILE + tid;
+    const bool vj = j < m_u;
+    const int s = first + j * S;
+    // gather one sample key per thread into the 128-byte-swizzled tile
+    uint4 chunk[8];
+    float ks = 0.f;
+    int64_t slot = s;
+    bool in_cache = vj;
+    if (vj && rs.paged) {
+      const int page = __ldg(&rs.block_table[(int64_t)(act[0] / rs.next_n) * rs.max_pages + (s >> 6)]);
+      in_cache = page >= 0 && page < rs.num_pages;  // a bad page id reads as a zero key
+      slot = (int64_t)page * PAGE + (s & (PAGE - 1));
+    }
+    if (in_cache) {
+      const uint4* src = (const uint4*)(p.k + slot * D);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) chunk[c] = __ldg(&src[c]);
+      ks = __ldg(&p.k_scale[slot]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) chunk[c] = make_uint4(0, 0, 0, 0);
+    }
+    uint8_t* krow = smem + SM_OFF_K + tid * D;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) *(uint4*)(krow + ((c ^ (tid & 7)) << 4)) = chunk[c];
+    scs[tid] = ks;
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k)
+        mma_e4m3(tmem, sw128_kmajor_desc(sbase + SM_OFF_K + 32 * k), sw128_kmajor_desc(sbase + SM_OFF_Q + 32 * k),
+                 idesc, k > 0);
+      mma_commit(bar);
+    }
+    if (tid == 0) misc[4] = mbar_wait(bar, (tt + 1) & 1, abort_flag, &p.stats->status) ? 1 : 0;
+    __syncthreads();
+    ok = misc[4] != 0;
+    if (!ok) break;
+    tc_fence_after();
+    for (int a = 0; a < nact; ++a) {
+      uint32_t v[H];
+      const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + a * H;
+      tmem_ld32(ta, v);
+      tmem_ld32(ta + 32, v + 32);
+      tmem_wait_ld();
+      float acc = 0.f;
+#pragma unroll
+      for (int h = 0; h < H; ++h) acc = fmaf(wsm[a * H + h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
+      if (vj) samp[a * MAX_SAMPLES + j] = ordered_key(acc * scs[tid]);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+
+  // threshold of each active row from the samples inside its own range
+  for (int a = 0; a < nact && ok; ++a) {
+    const int row = act[a];
+    const int b = p.rb[row], e = p.re[row];
+    const int j0 = max(0, ceil_div(b - first, S));
+    const int j1 = min(m_u, ceil_div(e - first, S));
+    const int m = max(0, j1 - j0);
+    const int rank = sample_rank(m, e - b, target);
+    uint32_t tau = 0u;
+    if (m > 0 && rank >= 1 && rank <= m) {
+      const uint32_t* sa = samp + a * MAX_SAMPLES + j0;
+      int rr;
+      group_radix_select([&](int i) { return sa[i]; }, m, rank, hist, misc + 1, tid, SAMPLE_THREADS, 0, tau, rr);
+      if (p.tau_bias != 0) {
+        const int64_t t = (int64_t)tau + p.tau_bias;
+        tau = (uint32_t)(t < 0 ? 0 : (t > 0xffffffffll ? 0xffffffffll : t));
+      }
+    }
+    if (tid == 0) p.tau[row] = tau;
+  }
+  if (!ok && tid < nact) p.tau[act[tid]] = 0u;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TILE);
+  }
+}
+
+cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_pairs_, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SAMPLE_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (n_pairs_ <= 0) return cudaSuccess;
+  sample_kernel<<<n_pairs_, SAMPLE_THREADS, SAMPLE_SMEM, s>>>(tm_q, p);
+  return cudaGetLastError();
+}
+
+// ================================================================== select ==
+// Standalone exact top-K of fp32 score rows: per row, sampled threshold ->
+// filter into shared memory (float4 loads, one shared atomic per warp batch)
+// -> radix select on the candidates; when the certificate fails (fewer than K
+// or more than SELECT_CAP candidates) the radix select runs over the whole row.
+constexpr uint32_t SEL_OFF_KEY = 0;
+constexpr uint32_t SEL_OFF_IDX = SEL_OFF_KEY + SELECT_CAP * 4;
+constexpr uint32_t SEL_OFF_SAMP = SEL_OFF_IDX + SELECT_CAP * 4;
+constexpr uint32_t SEL_OFF_HIST = SEL_OFF_SAMP + MAX_SAMPLES * 4;
+constexpr uint32_t SEL_OFF_MISC = SEL_OFF_HIST + 256 * 4;
+constexpr uint32_t SELECT_SMEM = SEL_OFF_MISC + 64;
+
+__device__ __forceinline__ void emit_one(uint32_t k, int32_t id, uint32_t theta, int rr, int K, int32_t* o,
+                                         int* s_above, int* s_eq) {
+  if (k > theta) {
+    o[atomicAdd(s_above, 1)] = id;
+  } else if (k == theta) {
+    const int e = atomicAdd(s_eq, 1);
+    if (e < rr) o[K - rr + e] = id;
+  }
+}
+
+__global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectParams p) {
+  extern __shared__ uint8_t smem[];
+  uint32_t* ckey = (uint32_t*)(smem + SEL_OFF_KEY);
+  int32_t* cidx = (int32_t*)(smem + SEL_OFF_IDX);
+  uint32_t* samp = (uint32_t*)(smem + SEL_OFF_SAMP);
+  int* hist = (int*)(smem + SEL_OFF_HIST);
+  int* misc = (int*)(smem + SEL_OFF_MISC);  // [0..1] digit, [2] count, [3] above, [4] eq, [5] tau
+  const RowSpace& rs = p.rs;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int K = p.K;
+  const int count = p.list_mode ? p.stats->fail_count : rs.R;
+  const int target = (int)(((int64_t)p.target16 * K) / 16);
+
+  for (int f = blockIdx.x; f < count; f += gridDim.x) {
+    const int row = p.list_mode ? p.list[f] : f;
+    const int b = p.rb[row], e = p.re[row];
+    const int L = e - b;
+    int32_t* o = p.out + (int64_t)row * K;
+    if (L <= K) {
+      write_all_valid(rs, row, b, e, K, p.out, tid, SELECT_THREADS);
+      continue;
+    }
+    const float* srow = p.scores + (int64_t)(p.list_mode ? f : row) * p.ld;
+
+    // sampled threshold
+    int first, m, S;
+    sample_grid(b, e, &first, &m, &S);
+    for (int j = tid; j < m; j += SELECT_THREADS) samp[j] = ordered_key(srow[first + j * S]);
+    if (tid == 0) {
+      misc[2] = 0;
+      misc[3] = 0;
+      misc[4] = 0;
+    }
+    __syncthreads();
+    const int rank = sample_rank(m, L, target);
+    uint32_t tau = 0u;
+    if (m > 0 && rank >= 1 && rank <= m) {
+      int rr;
+      group_radix_select([&](int i) { return samp[i]; }, m, rank, hist, misc, tid, SELECT_THREADS, 0, tau, rr);
+    }
+
+    // compare-and-append: 4 items per thread per step, one shared atomic per warp
+    const int a0 = min(e, (b + 3) & ~3);   // first 16-byte aligned index
+    const int a1 = max(a0, e & ~3);        // end of the aligned body
+    auto append = [&](int cnt, const uint32_t* ks, const int* ids) {
+      int incl = cnt;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o2);
+        if (lane >= o2) incl += y;
+      }
+      const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+      int base = 0;
+      if (lane == 31 && wtot) base = atomicAdd(&misc[2], wtot);
+      base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+      for (int i = 0; i < cnt; ++i)
+        if (base + i < SELECT_CAP) {
+          ckey[base + i] = ks[i];
+          cidx[base + i] = ids[i];
+        }
+    };
+    // scalar head and tail (at most 3 + 3 elements), then the aligned body
+    {
+      const int nh = (a0 - b) + (e - a1);
+      uint32_t ks[1];
+      int ids[1];
+      int cnt = 0;
+      if (tid < 32) {
+        if (lane < nh) {
+          const int i = lane < (a0 - b) ? b + lane : a1 + (lane - (a0 - b));
+          const uint32_t k = ordered_key(srow[i]);
+          if (k >= tau) {
+            ks[0] = k;
+            ids[0] = i;
+            cnt = 1;
+          }
+        }
+        append(cnt, ks, ids);
+      }
+    }
+    const int nvec = (a1 - a0) >> 2;
+    const float4* v4 = (const float4*)(srow + a0);
+    const int rounds = ceil_div(nvec, SELECT_THREADS);
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int vi = rd * SELECT_THREADS + tid;
+      uint32_t ks[4];
+      int ids[4];
+      int cnt = 0;
+      if (vi < nvec) {
+        const float4 x = __ldcs(&v4[vi]);
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t k = ordered_key(xs[c]);
+          if (k >= tau) {
+            ks[cnt] = k;
+            ids[cnt] = a0 + vi * 4 + c;
+            ++cnt;
+          }
+        }
+      }
+      append(cnt, ks, ids);
+    }
+    __syncthreads();
+    const int n = misc[2];
+    uint32_t theta;
+    int rr;
+    if (n >= K && n <= SELECT_CAP) {
+      group_radix_select([&](int i) { return ckey[i]; }, n, K, hist, misc, tid, SELECT_THREADS, 0, theta, rr);
+      for (int i = tid; i < n; i += SELECT_THREADS) {
+        const int id = rs.paged ? out_index(rs, row, cidx[i]) : cidx[i];
+        emit_one(ckey[i], id, theta, rr, K, o, &misc[3], &misc[4]);
+      }
+    } else {
+      // certificate failed: exact radix select over the whole row
+      group_radix_select([&](int i) { return ordered_key(srow[b + i]); }, L, K, hist, misc, tid, SELECT_THREADS, 0,
+                         theta, rr);
+      for (int i = tid; i < L; i += SELECT_THREADS) {
+        const uint32_t k = ordered_key(srow[b + i]);
+        if (k >= theta) {
+          const int id = rs.paged ? out_index(rs, row, b + i) : b + i;
+          emit_one(k, id, theta, rr, K, o, &misc[3], &misc[4]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SELECT_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  select_kernel<<<grid, SELECT_THREADS, SELECT_SMEM, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

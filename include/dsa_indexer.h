@@ -1,0 +1,192 @@
+/*
+ * dsa_indexer.h -- C ABI of the GB300 (sm_103a) DeepSeek-V3.2 DSA indexer with
+ * exact top-K selection.
+ *
+ * Operation ("Fusing Indexer Scoring and Exact Top-k for DeepSeek-V3.2",
+ * section 1.1 equation and section 2.3 problem definition): for every query
+ * row t and every valid key s in [row_begin[t], row_end[t])
+ *
+ *     I[t, s] = sum_{j=0..63} w[t, j] * ReLU( (q_scale[t] * q[t, j, :]) . (k_scale[s] * k[s, :]) )
+ *
+ * with q and k FP8 e4m3 codes (64 heads x 128 dims; keys shared by all heads),
+ * and return the K valid key indices with the largest I[t, s].
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers of the current CUDA device, owned by
+ *     the caller, C-contiguous, row-major, and must stay valid until the work
+ *     enqueued on `stream` has finished.  The library keeps no pointer to them
+ *     after the call returns.
+ *   - FP8 arrays and float scale arrays must be 16-byte aligned (the library
+ *     reads them with the Tensor Memory Accelerator); any cudaMalloc or torch
+ *     allocation is.
+ *   - Output rows are unordered (section 2.3).  A row with L = end - begin
+ *     valid keys and L >= K gets exactly K distinct indices of valid keys whose
+ *     scores are the K largest (ties resolve to any valid index).  A row with
+ *     L < K gets its L valid indices in slots [0, L) and -1 in slots [L, K).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream); no entry point except dsa_indexer_last_device_status()
+ *     synchronises the host.  Argument errors are returned synchronously
+ *     before anything is enqueued.  Errors the device detects (a row range
+ *     outside [0, N], a pipeline wait that timed out) are recorded in a
+ *     per-stream status word read by dsa_indexer_last_device_status().
+ *   - The library owns per-(device, stream) scratch memory (plan, thresholds,
+ *     candidate buffers, repair scores), allocated on first use and grown on
+ *     demand; growing synchronises the device once.  Calls on the same stream
+ *     are serialised by the stream; calls on different streams use different
+ *     scratch.  The scratch is released by dsa_indexer_release() or at exit.
+ *   - Fixed geometry: 64 heads, head dimension 128 (section 2.3); 1 <= K <=
+ *     DSA_MAX_K.
+ *
+ * Return values: DSA_OK (0) or a negative dsa_status.
+ */
+#ifndef DSA_INDEXER_H
+#define DSA_INDEXER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* dsa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_ARG = -1,          /* null pointer, non-positive size, misaligned pointer, K out of range */
+  DSA_ERR_UNSUPPORTED = -2,  /* a size beyond what the kernels address (e.g. N >= 2^31 / 128) */
+  DSA_ERR_CUDA = -3,         /* a CUDA runtime call failed (no device, launch failure, out of memory) */
+  DSA_ERR_TIMEOUT = -4,      /* device status: a bounded pipeline wait gave up (kernel returned early) */
+  DSA_ERR_RANGE = -5         /* device status: some row range was outside [0, N]; that row got all -1 */
+} dsa_status;
+
+#define DSA_HEADS 64
+#define DSA_HEAD_DIM 128
+#define DSA_MAX_K 2048
+
+/*
+ * Fused operator (sections 3.2 and 4 of the indexer study): sampled
+ * threshold per row, tcgen05 FP8 scoring with the ReLU / weight / head
+ * reduction applied on chip, compare-and-append of candidates, four-pass radix
+ * select in dedicated TopK warps, certificate check, and exact repair of rows
+ * whose candidate set underflowed or overflowed.  The [Q, N] score matrix is
+ * never written.
+ *
+ *   q_fp8     [Q, 64, 128] e4m3 codes           q_scale [Q]  fp32 (> 0)
+ *   k_fp8     [N, 128]     e4m3 codes           k_scale [N]  fp32 (> 0)
+ *   w         [Q, 64]      fp32 head weights
+ *   row_begin, row_end [Q] int32, 0 <= row_begin[t] <= row_end[t] <= N
+ *   out_idx   [Q, K]       int32 (written)
+ */
+DSA_API int dsa_indexer_topk(const uint8_t* q_fp8, const float* q_scale,
+                     const uint8_t* k_fp8, const float* k_scale,
+                     const float* w,
+                     const int32_t* row_begin, const int32_t* row_end,
+                     int Q, int N, int K,
+                     int32_t* out_idx, dsa_stream_t stream);
+
+/*
+ * Paged variant (contest write-up, "DSA TopK Indexer"): keys in a cache of
+ * 64-token pages with one fp32 scale per token; logical token s of sequence b
+ * lives in physical slot block_table[b][s / 64] * 64 + s % 64.  Query row i of
+ * sequence b (next_n query tokens per sequence) sees logical keys
+ * [0, seq_lens[b] - next_n + i + 1).  Returned indices are PHYSICAL slots.
+ * Rows with at most K valid keys take the index-remapping path (no scoring).
+ *
+ *   q_fp8         [B, next_n, 64, 128] e4m3     q_scale [B, next_n] fp32
+ *   k_cache       [P, 64, 128] e4m3             k_cache_scale [P, 64] fp32
+ *   w             [B, next_n, 64] fp32
+ *   block_table   [B, max_pages] int32 (entries past a sequence's pages unused)
+ *   seq_lens      [B] int32, 0 <= seq_lens[b] <= max_pages * 64
+ *   num_pages     P (bounds every block_table entry that is used)
+ *   out_idx       [B, next_n, K] int32 (written)
+ */
+DSA_API int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale,
+                           const uint8_t* k_cache, const float* k_cache_scale,
+                           const float* w,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           int B, int next_n, int max_pages, int num_pages, int K,
+                           int32_t* out_idx, dsa_stream_t stream);
+
+/*
+ * Unfused attribution baseline (section 1.1, "the usual implementation"):
+ * the same tcgen05 scorer writes the FP32 score matrix [Q, N] to device memory
+ * (entries of a touched tile outside the row's range hold -inf; other entries
+ * are not written), then the standalone exact top-K of section 3 reads it
+ * back.  Same arguments and result contract as dsa_indexer_topk.
+ */
+DSA_API int dsa_indexer_topk_unfused(const uint8_t* q_fp8, const float* q_scale,
+                             const uint8_t* k_fp8, const float* k_scale,
+                             const float* w,
+                             const int32_t* row_begin, const int32_t* row_end,
+                             int Q, int N, int K,
+                             int32_t* out_idx, dsa_stream_t stream);
+
+/*
+ * Scores only: scores[t, s] = I[t, s] in fp32 for s in [row_begin[t],
+ * row_end[t]) of every row; other entries of the 128-key tiles the row touches
+ * hold -inf; the rest of the row is left untouched.  scores is [Q, ld] fp32,
+ * ld >= N, ld % 4 == 0.
+ */
+DSA_API int dsa_indexer_scores(const uint8_t* q_fp8, const float* q_scale,
+                       const uint8_t* k_fp8, const float* k_scale,
+                       const float* w,
+                       const int32_t* row_begin, const int32_t* row_end,
+                       int Q, int N, float* scores, int64_t ld, dsa_stream_t stream);
+
+/*
+ * Standalone exact top-K over a given fp32 score matrix (section 3: sampled
+ * threshold, compare-and-append, four-pass radix select, certificate, and a
+ * full-row radix select when the certificate fails).  Row t considers
+ * scores[t, s] for s in [row_begin[t], row_end[t]) and returns the indices s.
+ * NaN scores are not supported.  scores is [Q, ld] fp32.
+ */
+DSA_API int dsa_indexer_topk_from_scores(const float* scores, int64_t ld,
+                                 const int32_t* row_begin, const int32_t* row_end,
+                                 int Q, int N, int K,
+                                 int32_t* out_idx, dsa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports the device status of the most recent
+ * call enqueued on it: DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_RANGE (or
+ * DSA_ERR_CUDA if synchronising failed).  failures_out (may be NULL) receives
+ * 4 counters of that call: rows repaired after candidate underflow, rows
+ * repaired after candidate overflow, rows taken by the remapping path
+ * (L <= K), and the total number of candidates appended.
+ */
+DSA_API int dsa_indexer_last_device_status(dsa_stream_t stream, int32_t* failures_out);
+
+/* Tuning and diagnostics (process-wide; take effect on the next call). */
+typedef enum {
+  DSA_OPT_CHUNK_TILES = 1,    /* 128-key tiles per work unit of the persistent scorer (default 64) */
+  DSA_OPT_TAU_BIAS = 2,       /* added to every sampled threshold key: >0 forces underflow, <0 overflow (test knob; default 0) */
+  DSA_OPT_PROFILE = 3,        /* 1: time the main kernel of each call with CUDA events (default 0) */
+  DSA_OPT_GRID_CTAS = 4,      /* CTAs of the persistent kernels (default: SM count) */
+  DSA_OPT_SAMPLE_TARGET = 5   /* candidates the threshold aims at, in units of K/16 (default 32 = 2K) */
+} dsa_option;
+DSA_API int dsa_indexer_set_option(int option, int64_t value);
+DSA_API int64_t dsa_indexer_get_option(int option);
+
+/* Milliseconds spent in the main kernel of the most recent profiled call on
+ * `stream` (synchronises the stream); -1 if none was profiled. */
+DSA_API float dsa_indexer_profiled_main_ms(dsa_stream_t stream);
+
+/* Number of kernels this process has launched through the library. */
+DSA_API int64_t dsa_indexer_launch_count(void);
+
+/* Library version string and the compute capability it was built for. */
+DSA_API const char* dsa_indexer_version(void);
+
+/* Frees all scratch memory the library holds (synchronises the device). */
+DSA_API int dsa_indexer_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_INDEXER_H */
