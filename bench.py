@@ -1,0 +1,405 @@
+"""Benchmark of the fused FP8 DSA indexer + exact top-2048 on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
+
+One step = one complete operator call (plan, sampled thresholds, fused
+tcgen05 scoring + candidate filter + TopK selection, repair) over the
+causal-prefill workload Q=4096 query rows x N=131072 keys, K=2048 (the
+"128K" chunk of the indexer study), inputs resident in HBM.  The metric is
+scored row-keys per second (sum over rows of the valid range length); the
+effective FP8 rate is 2*64*128 FLOP per row-key ("Fusing Indexer Scoring and
+Exact Top-k for DeepSeek-V3.2", section 5.1 equation).
+
+L2 is flushed (a 512 MiB write) before every timed step, outside the timed
+events.  With --gpus N under torchrun each rank runs an independent replica
+(no collective on the data path; weak scaling); rank 0 prints one JSON line.
+--impl reference times the CPU oracle (exact FP64 scores, full sort) on a
+bounded sample of rows of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADS, DIM = 64, 128
+FLOP_PER_ROW_KEY = 2 * HEADS * DIM          # 16384
+BYTES_PER_KEY = DIM + 4                     # FP8 vector + fp32 scale = 132
+FP8_OVER_BF16 = 2.0                         # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+CORE_OPS_PER_ROW_KEY = 2 * HEADS + 4        # ReLU + FMA per head, ~4 per key (scale, mask, compare)
+METRIC = "fused indexer+top-2048 row-keys/s and FP8 TFLOP/s (% of GB300 FP8 roofline), 1 GPU"
+
+
+# ------------------------------------------------------------- accounting --
+def algorithmic_bytes(Q: int, N: int, K: int) -> int:
+    """Bytes the operator must move at least once: q codes + q scale + weights,
+    every key once (codes + scale), the int32 output."""
+    return Q * HEADS * DIM + Q * 4 + Q * HEADS * 4 + N * BYTES_PER_KEY + Q * K * 4
+
+
+def score_matrix_bytes(Q: int, N: int) -> int:
+    """FP32 [Q, N] score matrix of the unfused pipeline (written once, read once)."""
+    return Q * N * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "sm_max_mhz": float(pk.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- workload --
+def make_workload(config: int):
+    from fp8_scoring_exact_gb300 import synthetic
+    return synthetic.make_config(config)
+
+
+def describe(inp, config):
+    Q, N = inp.Q, inp.N
+    return {"workload": f"{inp.name} (Q={Q} rows x N={N} keys, causal, K={inp.K})", "Q": Q, "N": N,
+            "K": inp.K, "row_keys": inp.row_keys(), "config_index": config,
+            "l2": "flushed by a 512 MiB write before each timed step (outside the timed events)",
+            "parallelism": "replicas (one independent problem per GPU)"}
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_rows(inp, n_rows, seed=123):
+    rng = np.random.default_rng(seed)
+    return sorted(rng.choice(inp.Q, size=min(n_rows, inp.Q), replace=False).tolist())
+
+
+def oracle_subset(inp, rows):
+    """The same workload restricted to `rows` (all keys kept)."""
+    from fp8_scoring_exact_gb300.synthetic import DenseInputs
+    r = np.asarray(rows)
+    return DenseInputs(q=inp.q[r], q_scale=inp.q_scale[r], k=inp.k, k_scale=inp.k_scale, w=inp.w[r],
+                       row_begin=inp.row_begin[r], row_end=inp.row_end[r], K=inp.K, name=inp.name)
+
+
+def cpu_procs():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(16, n))
+
+
+def time_oracle(inp, n_rows, procs, reps=1):
+    """(row-keys/s, seconds, rows) of the oracle over a seeded row sample."""
+    from oracle.indexer import OraclePool
+    rows = oracle_rows(inp, n_rows)
+    sub = oracle_subset(inp, rows)
+    rk = int((sub.row_end.astype(np.int64) - sub.row_begin).sum())
+    with OraclePool(sub, procs) as pool:
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            pool.topk(range(len(rows)))
+        dt = time.perf_counter() - t0
+    return rk * reps / dt, dt, rows
+
+
+# ------------------------------------------------------------ GPU arm -------
+def run_ours(args, rank, world, device):
+    import torch
+
+    from fp8_scoring_exact_gb300 import binding
+
+    inp = make_workload(args.config)
+    Q, N, K = inp.Q, inp.N, inp.K
+    R = inp.row_keys()
+    host = [np.ascontiguousarray(a) for a in (inp.q, inp.q_scale, inp.k, inp.k_scale, inp.w, inp.row_begin,
+                                               inp.row_end)]
+    dev = [torch.from_numpy(a).to(device) for a in host]
+    out = torch.empty((Q, K), dtype=torch.int32, device=device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        binding.indexer_topk(*dev, K=K, out=out)
+
+    binding.set_option("profile", 1)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    rc, counters = binding.last_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} after warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    main_ms = []
+    l0 = binding.launch_count()
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+            main_ms.append(binding.profiled_main_ms())  # waits for this step's main kernel
+        torch.cuda.synchronize(device)
+    barrier(world)
+    launches = binding.launch_count() - l0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+    ms_per_step = total_ms / args.steps
+    rc, counters = binding.last_device_status()
+    binding.set_option("profile", 0)
+
+    # unfused attribution baseline, same protocol
+    unf = []
+    for _ in range(max(1, args.warmup // 2)):
+        binding.indexer_topk_unfused(*dev, K=K, out=out)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        binding.indexer_topk_unfused(*dev, K=K, out=out)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    unf = [a.elapsed_time(b) for a, b in ev]
+    unf_ms = statistics.mean(unf)
+
+    # end to end through the public API from pinned host buffers
+    pinned = [torch.from_numpy(a).pin_memory() for a in host]
+    out_h = torch.empty((Q, K), dtype=torch.int32).pin_memory()
+    h2d = sum(a.nbytes for a in host)
+    d2h = out_h.numel() * 4
+    for i in range(args.steps + 1):
+        if i == 1:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        for d, h in zip(dev, pinned):
+            d.copy_(h, non_blocking=True)
+        binding.indexer_topk(*dev, K=K, out=out)
+        out_h.copy_(out, non_blocking=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / args.steps
+
+    peaks = load_peaks()
+    main_avg = statistics.mean(main_ms)
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    achieved = FLOP_PER_ROW_KEY * R / (main_avg * 1e-3) / 1e12
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    clocks = clk.summary()
+    f_sm = (clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]) * 1e6
+    t_tensor = FLOP_PER_ROW_KEY * R / (fp8_peak * 1e12) * 1e3
+    t_core = CORE_OPS_PER_ROW_KEY * R / (sms * 128 * f_sm) * 1e3
+    t_hbm = algorithmic_bytes(Q, N, K) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_roof = max(t_tensor, t_core, t_hbm)
+
+    res = {
+        "metric": METRIC,
+        "value": world * R / (ms_per_step * 1e-3),
+        "unit": "row-keys/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8e4m3 x fp8e4m3 -> f32",
+        "data": "synthetic (seeded Gaussian activations quantised to FP8 e4m3 per token)",
+        "config": describe(inp, args.config),
+        "tflops_effective": world * FLOP_PER_ROW_KEY * R / (ms_per_step * 1e-3) / 1e12,
+        "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "row-keys/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp8_peak, "traffic": None,
+                     "kernel": "score_kernel (filter mode: tcgen05 scoring + candidate filter + TopK warps)",
+                     "kernel_ms": main_avg,
+                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} "
+                                    "(nominal fp8/bf16 ratio), burst"},
+        "roofline_terms": {"t_tensor_ms": t_tensor, "t_core_ms": t_core, "t_hbm_ms": t_hbm, "t_roof_ms": t_roof,
+                           "frac_of_roofline": t_roof / ms_per_step, "sm_count": sms,
+                           "sm_clock_for_core_term_mhz": f_sm / 1e6},
+        "unfused": {"ms_per_step": unf_ms, "fused_speedup": unf_ms / ms_per_step},
+        "failures": counters,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        procs = cpu_procs()
+        rate, secs, rows = time_oracle(inp, 2 * procs, procs)
+        res["cpu_baseline"] = {"value": rate, "unit": "row-keys/s", "cores": procs, "kind": "oracle",
+                               "sample": f"{len(rows)} seeded rows of the same workload (all their keys), "
+                                         f"{secs:.1f} s on {procs} spawned single-thread processes"}
+    return res
+
+
+def run_reference(args, rank, world):
+    """CPU oracle as the reference arm: rank 0 only."""
+    if rank != 0:
+        return None
+    inp = make_workload(args.config)
+    procs = cpu_procs()
+    from oracle.indexer import OraclePool
+    rows = oracle_rows(inp, procs * (args.steps + args.warmup), seed=321)
+    sub = oracle_subset(inp, rows)
+    per = procs
+    with OraclePool(sub, procs) as pool:
+        for i in range(args.warmup):
+            pool.topk(range(i * per, (i + 1) * per))
+        t0 = time.perf_counter()
+        for i in range(args.warmup, args.warmup + args.steps):
+            pool.topk(range(i * per, (i + 1) * per))
+        dt = time.perf_counter() - t0
+    lens = (sub.row_end.astype(np.int64) - sub.row_begin)[args.warmup * per:]
+    rate = float(lens.sum()) / dt
+    res = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": rate,
+        "unit": "row-keys/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (exact integer dots, fp64 combination)",
+        "data": "synthetic (seeded Gaussian activations quantised to FP8 e4m3 per token)",
+        "config": describe(inp, args.config),
+        "cpu_baseline": {"value": rate, "unit": "row-keys/s", "cores": procs, "kind": "oracle",
+                         "sample": f"{per} seeded rows per step (all their keys), {args.steps} timed steps"},
+        "e2e": {"value": rate, "unit": "row-keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return res
+
+
+# ------------------------------------------------------------ distributed --
+def init_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="workload index (2 = causal Q4096 x N131072)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world = init_dist()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        import torch
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        device = torch.device("cuda", local)
+        torch.cuda.set_device(device)
+        if rank == 0:
+            import __graft_entry__
+            __graft_entry__.build()
+        barrier(world)
+        res = run_ours(args, rank, world, device)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -5,5 +5,5 @@ include/dsa_indexer.h); `binding` is its thin Python front end and
 `synthetic` draws seeded inputs shaped like the indexer workloads.
 """
 from .binding import (IndexerError, indexer_scores, indexer_topk, indexer_topk_paged,  # noqa: F401
-                      indexer_topk_unfused, last_device_status, launch_count, profiled_main_ms,
+                      indexer_topk_unfused, last_device_status, last_repaired_rows, launch_count, profiled_main_ms,
                       release, set_option, get_option, topk_from_scores, version)

@@ -36,6 +36,7 @@ SIGNATURES = {
     "dsa_indexer_scores": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I64, _P]),
     "dsa_indexer_topk_from_scores": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_last_device_status": (_I, [_P, _P]),
+    "dsa_indexer_last_repaired_rows": (_I, [_P, _P, _I]),
     "dsa_indexer_set_option": (_I, [_I, _I64]),
     "dsa_indexer_get_option": (_I64, [_I]),
     "dsa_indexer_profiled_main_ms": (ctypes.c_float, [_P]),
@@ -193,6 +194,15 @@ def last_device_status(stream=None):
     buf = (ctypes.c_int32 * 4)()
     rc = lib().dsa_indexer_last_device_status(_stream_ptr(stream), buf)
     return rc, {"underflow": buf[0], "overflow": buf[1], "trivial": buf[2], "candidates": buf[3]}
+
+
+def last_repaired_rows(stream=None, cap=1 << 20):
+    """Row ids the last fused call on the stream sent to exact repair."""
+    buf = (ctypes.c_int32 * cap)()
+    n = lib().dsa_indexer_last_repaired_rows(_stream_ptr(stream), buf, cap)
+    if n < 0:
+        raise IndexerError("dsa_indexer_last_repaired_rows", n)
+    return [buf[i] for i in range(min(n, cap))]
 
 
 def set_option(name: str, value: int):

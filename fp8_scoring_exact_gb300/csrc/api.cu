@@ -521,6 +521,25 @@ int dsa_indexer_last_device_status(dsa_stream_t stream_, int32_t* failures_out) 
   return DSA_OK;
 }
 
+int dsa_indexer_last_repaired_rows(dsa_stream_t stream_, int32_t* rows_out, int cap) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cap < 0 || (cap > 0 && !rows_out)) return DSA_ERR_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_arenas.find({dev, stream});
+  if (it == g_arenas.end() || !it->second.used) return 0;
+  Stats st;
+  const Arena& a = it->second;
+  if (cudaMemcpy(&st, a.base + a.L.stats, sizeof(Stats), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  const int n = st.fail_count < cap ? st.fail_count : cap;
+  if (n > 0 && cudaMemcpy(rows_out, a.base + a.L.failed, n * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  return st.fail_count;
+}
+
 int dsa_indexer_set_option(int option, int64_t value) {
   std::lock_guard<std::mutex> lk(g_mu);
   switch (option) {

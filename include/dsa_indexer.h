@@ -162,6 +162,14 @@ DSA_API int dsa_indexer_topk_from_scores(const float* scores, int64_t ld,
  */
 DSA_API int dsa_indexer_last_device_status(dsa_stream_t stream, int32_t* failures_out);
 
+/*
+ * Synchronises `stream` and copies the ids of the rows that the most recent
+ * fused call on it sent to exact repair (certificate failed) into rows_out
+ * (at most `cap` of them, in no particular order).  Returns their number
+ * (>= 0) or a negative dsa_status.
+ */
+DSA_API int dsa_indexer_last_repaired_rows(dsa_stream_t stream, int32_t* rows_out, int cap);
+
 /* Tuning and diagnostics (process-wide; take effect on the next call). */
 typedef enum {
   DSA_OPT_CHUNK_TILES = 1,    /* 128-key tiles per work unit of the persistent scorer (default 64) */

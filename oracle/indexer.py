@@ -174,6 +174,58 @@ def _paged_task(bi):
     return bi, out
 
 
+class OraclePool:
+    """A pool of `procs` spawned worker processes, each holding one oracle of
+    the same problem (decoded once) and running single-threaded BLAS, so the
+    pool uses exactly `procs` cores.  Use as a context manager."""
+
+    def __init__(self, inp, procs: int, kind: str = "dense"):
+        import multiprocessing as mp
+        import os
+        self.kind = kind
+        if kind == "dense":
+            arrays = (inp.q, inp.q_scale, inp.k, inp.k_scale, inp.w, inp.row_begin, inp.row_end, inp.K)
+        else:
+            arrays = (inp.q, inp.q_scale, inp.k_cache, inp.k_cache_scale, inp.w, inp.block_table,
+                      inp.seq_lens, inp.K)
+        saved = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                                 "MKL_NUM_THREADS")}
+        for v in saved:
+            os.environ[v] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(procs, initializer=_init_worker,
+                                                     initargs=(kind, arrays))
+            # make every worker finish its initialiser before timing starts
+            self.pool.map(_noop, range(procs), chunksize=1)
+        finally:
+            for v, old in saved.items():
+                if old is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = old
+        self.procs = procs
+
+    def topk(self, rows):
+        task = _dense_task if self.kind == "dense" else _paged_task
+        return dict(self.pool.map(task, list(rows), chunksize=1))
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+
+def _noop(i):
+    import time
+    time.sleep(0.2)
+    return i
+
+
 def parallel_topk(inp, rows, procs: int, kind: str = "dense"):
     """Oracle top-K of `rows` using `procs` spawned processes.
 

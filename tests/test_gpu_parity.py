@@ -1,0 +1,225 @@
+"""GPU parity: the CUDA library (through its C ABI binding) against the oracle.
+
+Criteria ("Fusing Indexer Scoring and Exact Top-k for DeepSeek-V3.2",
+section 2.3, with the float32 tolerance TOL * E of oracle.checks): indices
+valid, unique, min(L, K) of them then -1 padding (bit-exact); every selected
+score within TOL * E of the oracle's K-th score; on the small cases the sorted
+selected scores equal the oracle's element-wise.  Large cases are checked on
+seeded row samples plus every row the device sent to repair.
+"""
+import numpy as np
+import pytest
+
+from fp8_scoring_exact_gb300 import synthetic as S
+from oracle import checks, indexer
+
+from helpers import check_dense_rows, check_rows_parallel, dense_args, paged_args, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from fp8_scoring_exact_gb300 import binding
+    binding.lib()
+    binding.set_option("tau_bias", 0)
+    return binding
+
+
+def _status_ok(B):
+    rc, counters = B.last_device_status()
+    assert rc == 0, f"device status {B.STATUS_NAMES.get(rc, rc)}"
+    return counters
+
+
+# ------------------------------------------------------------ raw scores ----
+@pytest.mark.parametrize("N,causal", [(8192, False), (8192 + 77, True), (300, False)])
+def test_scores_match_oracle_elementwise(B, N, causal):
+    inp = S.make_dense(8 if N > 300 else 3, N, seed=N, causal=causal)
+    sc = B.indexer_scores(*dense_args(inp)).cpu().numpy()
+    _status_ok(B)
+    o = indexer.DenseOracle.from_inputs(inp)
+    for t in range(inp.Q):
+        ids, I, E = o.row_scores(t)
+        g = sc[t, ids].astype(np.float64)
+        assert np.all(np.abs(g - I) <= checks.TOL * E), f"row {t}: max rel {np.max(np.abs(g - I) / E)}"
+
+
+# ------------------------------------------------------ small full checks ----
+@pytest.mark.parametrize("fn", ["fused", "unfused"])
+def test_tiny_noncausal_all_rows(B, fn):
+    inp = S.make_config(0)
+    call = B.indexer_topk if fn == "fused" else B.indexer_topk_unfused
+    out = call(*dense_args(inp), K=inp.K).cpu().numpy()
+    _status_ok(B)
+    assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
+@pytest.mark.parametrize("fn", ["fused", "unfused"])
+@pytest.mark.parametrize("Q,N,K,seed", [(37, 5077, 256, 1), (9, 2049, 2048, 2), (64, 12345, 1024, 3),
+                                        (5, 640, 1, 4)])
+def test_ragged_causal_all_rows(B, fn, Q, N, K, seed):
+    inp = S.make_dense(Q, N, K=K, seed=seed, causal=True)
+    call = B.indexer_topk if fn == "fused" else B.indexer_topk_unfused
+    out = call(*dense_args(inp), K=K).cpu().numpy()
+    _status_ok(B)
+    assert check_dense_rows(inp, out, range(Q)) == {}
+
+
+def test_causal_q2048_n16k_all_rows(B):
+    """The 16K causal prefill chunk (shared-direction keys), every row."""
+    inp = S.make_config(1)
+    out = B.indexer_topk(*dense_args(inp), K=inp.K).cpu().numpy()
+    _status_ok(B)
+    bad = check_rows_parallel(inp, out, range(inp.Q))
+    assert bad == {}, list(bad.items())[:3]
+
+
+# ------------------------------------------------- full-size sampled rows ----
+def _sampled_rows(Q, n, seed):
+    rng = np.random.default_rng(seed)
+    return sorted(set(rng.choice(Q, size=n, replace=False).tolist()) | {0, Q // 2, Q - 1})
+
+
+@pytest.mark.parametrize("cid", [2, 3])
+def test_full_size_sampled_rows_and_repaired_rows(B, cid):
+    inp = S.make_config(cid)
+    args = dense_args(inp)
+    out = B.indexer_topk(*args, K=inp.K).cpu().numpy()
+    counters = _status_ok(B)
+    repaired = B.last_repaired_rows()
+    assert len(repaired) == counters["underflow"] + counters["overflow"]
+    if cid == 3:
+        assert len(repaired) > 0, "the tie-stress workload is built to exercise repair"
+    rows = sorted(set(_sampled_rows(inp.Q, 64, 100 + cid)) | set(repaired))
+    bad = check_rows_parallel(inp, out, rows)
+    assert bad == {}, list(bad.items())[:3]
+    # the unfused pipeline must select the same scores on the sampled rows
+    out_u = B.indexer_topk_unfused(*args, K=inp.K).cpu().numpy()
+    _status_ok(B)
+    bad = check_rows_parallel(inp, out_u, _sampled_rows(inp.Q, 16, 200 + cid))
+    assert bad == {}, list(bad.items())[:3]
+
+
+def test_paged_decode_batch_all_rows(B):
+    inp = S.make_config(4)
+    out = B.indexer_topk_paged(*paged_args(inp), K=inp.K).cpu().numpy()
+    counters = _status_ok(B)
+    L = inp.row_lengths()
+    assert counters["trivial"] == int((L <= inp.K).sum())
+    keys = [(b, i) for b in range(inp.B) for i in range(inp.next_n)]
+    bad = check_rows_parallel(inp, out, keys, kind="paged")
+    assert bad == {}, list(bad.items())[:3]
+
+
+# ------------------------------------------------------------------ paged ----
+@pytest.mark.parametrize("next_n", [1, 2, 3])
+def test_paged_small_all_rows(B, next_n):
+    inp = S.make_paged(7, next_n, K=300, seed=10 + next_n, len_lo=1, len_hi=5000, n_short=3, short_hi=310)
+    # a sequence shorter than next_n and one ending exactly on a page boundary
+    inp.seq_lens[0] = max(0, next_n - 1)
+    inp.seq_lens[1] = min(64 * int((inp.block_table[1] >= 0).sum()), 4096)
+    out = B.indexer_topk_paged(*paged_args(inp), K=inp.K).cpu().numpy()
+    _status_ok(B)
+    po = indexer.PagedOracle.from_inputs(inp)
+    for b in range(inp.B):
+        for i in range(inp.next_n):
+            slots, I, E = po.row_scores(b, i)
+            pr = checks.check_row(out[b, i], slots, I, E, inp.K, order_key=np.arange(len(slots)))
+            assert not pr, (b, i, pr)
+
+
+# ----------------------------------------------------------------- repair ----
+@pytest.mark.parametrize("bias,kind", [(1 << 31, "underflow"), (-(1 << 33), "overflow")])
+def test_forced_repair_is_exact(B, bias, kind):
+    """Threshold pushed to the top (every row underflows) or to zero (every
+    row's candidate set overflows): all rows go through exact repair."""
+    inp = S.make_dense(12, 20000, K=2048, seed=21, causal=True)
+    B.set_option("tau_bias", bias)
+    try:
+        out = B.indexer_topk(*dense_args(inp), K=inp.K).cpu().numpy()
+        counters = _status_ok(B)
+    finally:
+        B.set_option("tau_bias", 0)
+    assert counters[kind] == inp.Q
+    assert sorted(B.last_repaired_rows()) == list(range(inp.Q))
+    assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
+# ------------------------------------------------------------- edge cases ----
+def test_edge_ranges(B):
+    """Empty rows, L = K, L = K + 1, offset ranges, a single key."""
+    K = 64
+    inp = S.make_dense(8, 1000, K=K, seed=5, causal=False)
+    inp.row_begin[:] = [0, 10, 100, 0, 999, 500, 3, 0]
+    inp.row_end[:] = [0, 10 + K, 101 + K, 1000, 1000, 500, 900, 1]
+    for fn in (B.indexer_topk, B.indexer_topk_unfused):
+        out = fn(*dense_args(inp), K=K).cpu().numpy()
+        _status_ok(B)
+        assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
+def test_invalid_range_reports_status_and_pads(B):
+    inp = S.make_dense(4, 500, K=16, seed=6, causal=False)
+    inp.row_begin[1], inp.row_end[1] = 10, 501      # end past N
+    inp.row_begin[2], inp.row_end[2] = 30, 20       # begin after end
+    out = B.indexer_topk(*dense_args(inp), K=16).cpu().numpy()
+    rc, _ = B.last_device_status()
+    assert rc == B.DSA_ERR_RANGE
+    assert (out[1] == -1).all() and (out[2] == -1).all()
+    assert check_dense_rows(inp, out, [0, 3]) == {}
+
+
+def test_ties_everywhere(B):
+    """All keys identical: every valid index is a correct answer; the output
+    must still be K distinct valid indices."""
+    inp = S.make_dense(4, 5000, K=512, seed=7, causal=True)
+    inp.k[:] = inp.k[0]
+    inp.k_scale[:] = inp.k_scale[0]
+    for fn in (B.indexer_topk, B.indexer_topk_unfused):
+        out = fn(*dense_args(inp), K=inp.K).cpu().numpy()
+        _status_ok(B)
+        assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
+def test_argument_errors_are_synchronous(B):
+    import torch
+    inp = S.make_dense(2, 256, K=16, seed=8, causal=False)
+    args = dense_args(inp)
+    with pytest.raises(B.IndexerError) as e:
+        B.indexer_topk(*args, K=0)
+    assert e.value.code == B.DSA_ERR_ARG
+    with pytest.raises(B.IndexerError):
+        B.indexer_topk(*args, K=B.MAX_K + 1)
+    bad = torch.empty(256 * 128 + 1, dtype=torch.uint8, device="cuda")[1:].view(256, 128)
+    with pytest.raises(B.IndexerError):
+        B.indexer_topk(args[0], args[1], bad, *args[3:], K=16)
+
+
+# ----------------------------------------------------- standalone select ----
+def test_topk_from_scores_exact(B):
+    """Selection only: given fp32 scores the result is exactly determined up
+    to ties, so the sorted selected values must equal a full sort bit for bit."""
+    import torch
+    rng = np.random.default_rng(9)
+    Q, N, K = 16, 40000, 2048
+    sc = rng.standard_normal((Q, N)).astype(np.float32)
+    sc[3] = np.round(sc[3] * 4) / 4          # heavy ties
+    sc[4] = 0.0
+    sc[4, ::2] = -0.0                         # -0 and +0 tie
+    sc[5] = rng.choice(np.float32([1.0, 2.0]), N)
+    rb = rng.integers(0, 1000, Q).astype(np.int32)
+    re = (rb + rng.integers(0, N - 1000, Q)).astype(np.int32)
+    re[6] = rb[6] + K                         # exactly K
+    re[7] = rb[7] + 5                         # fewer than K
+    out = B.topk_from_scores(*to_dev(sc, rb, re), K=K).cpu().numpy()
+    _status_ok(B)
+    for t in range(Q):
+        L = re[t] - rb[t]
+        n = min(L, K)
+        sel = out[t, :n]
+        assert (out[t, n:] == -1).all()
+        assert len(np.unique(sel)) == n and np.all((sel >= rb[t]) & (sel < re[t]))
+        want = np.sort(sc[t, rb[t]:re[t]])[::-1][:n]
+        got = np.sort(sc[t, sel])[::-1]
+        assert np.array_equal(got, want), t
