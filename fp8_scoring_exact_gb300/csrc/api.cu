@@ -17,7 +17,7 @@
 #include <mutex>
 #include <utility>
 
-#include "../../include/dsa_indexer.h"
+#include "dsa_indexer.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -32,6 +32,8 @@ int64_t g_tau_bias = 0;
 int64_t g_profile = 0;
 int64_t g_grid = 0;
 int64_t g_target16 = 32;
+int64_t g_relu_alu8 = 0;
+int64_t g_fused_mode = 0;
 std::atomic<int64_t> g_launches{0};
 
 // ----------------------------------------------------------------- arena ----
@@ -173,7 +175,7 @@ int sm_count() {
   } while (0)
 
 struct Opts {
-  int chunk, grid, target16;
+  int chunk, grid, target16, relu_alu8, fused_mode;
   int64_t bias;
   bool profile;
 };
@@ -185,6 +187,8 @@ Opts read_opts() {
   o.bias = g_tau_bias;
   o.profile = g_profile != 0;
   o.target16 = (int)g_target16;
+  o.relu_alu8 = (int)g_relu_alu8;
+  o.fused_mode = (int)g_fused_mode;
   const int sms = sm_count();
   o.grid = g_grid > 0 ? (int)g_grid : (sms > 0 ? sms : 1);
   return o;
@@ -198,6 +202,10 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   const Opts o = read_opts();
   const int G = n_pairs(rs);
   const int64_t ld = align_up((size_t)rs.N, 4);
+  // whole pairs per CTA (candidates in shared memory, TopK warps in the same
+  // CTA) when there are enough pairs to balance the SMs; chunks split across
+  // CTAs with global candidates and a separate select otherwise
+  const bool slots = o.fused_mode == 1 || (o.fused_mode == 0 && !rs.paged && G >= 2 * o.grid);
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
   Arena* a = get_arena(stream, make_layout(rs.R, G, true, rs.R, ld), &err);
@@ -210,7 +218,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   pp.repair = 0;
   pp.K = K;
   pp.trivial_len = K;
-  pp.chunk_tiles = o.chunk;
+  pp.chunk_tiles = slots ? WHOLE_PAIR_TILES : o.chunk;
   pp.row_begin_in = row_begin;
   pp.row_end_in = row_end;
   pp.rb = at<int32_t>(a, L.rb);
@@ -241,9 +249,10 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
 
   ScoreParams cp{};
   cp.rs = rs;
-  cp.mode = MODE_FILTER;
+  cp.mode = slots ? MODE_FILTER_SLOTS : MODE_FILTER_GLOBAL;
   cp.K = K;
-  cp.chunk_tiles = o.chunk;
+  cp.chunk_tiles = pp.chunk_tiles;
+  cp.relu_alu8 = o.relu_alu8;
   cp.repair = 0;
   cp.q_scale = q_scale;
   cp.w = w;
@@ -264,15 +273,35 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   DSA_LAUNCH(launch_score(tm_q, tm_k, tm_ks, cp, o.grid, stream));
   if (o.profile) cudaEventRecord(a->ev1, stream);
 
+  if (!slots) {
+    // split chunks: select every row from its global candidate buffer
+    SelectParams cs{};
+    cs.rs = rs;
+    cs.K = K;
+    cs.target16 = o.target16;
+    cs.source = SELECT_FROM_CANDIDATES;
+    cs.cand_key = cp.cand_key;
+    cs.cand_idx = cp.cand_idx;
+    cs.cand_count = cp.cand_count;
+    cs.failed_rows = cp.failed_rows;
+    cs.rb = pp.rb;
+    cs.re = pp.re;
+    cs.out = out;
+    cs.stats = st;
+    DSA_LAUNCH(launch_select(cs, 2 * o.grid, stream));
+  }
+
   // exact repair of rows whose certificate failed
   PlanParams rp = pp;
   rp.repair = 1;
+  rp.chunk_tiles = o.chunk;
   rp.groups = at<Group>(a, L.rgroups);
   rp.unit_start = at<int32_t>(a, L.runit_start);
   DSA_LAUNCH(launch_plan(rp, stream));
 
   ScoreParams rcp = cp;
   rcp.mode = MODE_STORE;
+  rcp.chunk_tiles = o.chunk;
   rcp.repair = 1;
   rcp.groups = rp.groups;
   rcp.unit_start = rp.unit_start;
@@ -284,6 +313,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   sel.rs = rs;
   sel.K = K;
   sel.target16 = o.target16;
+  sel.source = SELECT_FROM_SCORES;
   sel.list_mode = 1;
   sel.list = rcp.failed_rows;
   sel.scores = rcp.scores;
@@ -402,6 +432,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   cp.mode = MODE_STORE;
   cp.K = K;
   cp.chunk_tiles = o.chunk;
+  cp.relu_alu8 = o.relu_alu8;
   cp.q_scale = q_scale;
   cp.w = w;
   cp.rb = pp.rb;
@@ -421,6 +452,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   sel.rs = rs;
   sel.K = K;
   sel.target16 = o.target16;
+  sel.source = SELECT_FROM_SCORES;
   sel.scores = sbuf;
   sel.ld = sld;
   sel.rb = pp.rb;
@@ -561,6 +593,14 @@ int dsa_indexer_set_option(int option, int64_t value) {
       if (value < 1 || value > 256) return DSA_ERR_ARG;
       g_target16 = value;
       return DSA_OK;
+    case DSA_OPT_RELU_ALU8:
+      if (value != 0 && value != 2 && value != 4 && value != 8) return DSA_ERR_ARG;
+      g_relu_alu8 = value;
+      return DSA_OK;
+    case DSA_OPT_FUSED_MODE:
+      if (value < 0 || value > 2) return DSA_ERR_ARG;
+      g_fused_mode = value;
+      return DSA_OK;
     default:
       return DSA_ERR_ARG;
   }
@@ -579,6 +619,10 @@ int64_t dsa_indexer_get_option(int option) {
       return g_grid;
     case DSA_OPT_SAMPLE_TARGET:
       return g_target16;
+    case DSA_OPT_RELU_ALU8:
+      return g_relu_alu8;
+    case DSA_OPT_FUSED_MODE:
+      return g_fused_mode;
     default:
       return DSA_ERR_ARG;
   }

@@ -20,14 +20,18 @@ constexpr int GROUP_ROWS = 2;      // query rows sharing one key stream (MMA N =
 constexpr int PAGE = 64;           // tokens per paged-cache page
 
 // ------------------------------------------------------- persistent scorer --
-constexpr int STAGES = 6;          // key-tile ring depth (TMA -> MMA)
-constexpr int SC_STAGES = 12;      // key-scale ring depth (TMA -> epilogue)
+constexpr int STAGES = 4;          // key-tile ring depth (TMA -> MMA)
+constexpr int SC_STAGES = 8;       // key-scale ring depth (TMA -> epilogue)
 constexpr int ACC_BUFS = 4;        // TMEM accumulators (MMA -> epilogue)
 constexpr int ACC_COLS = 128;      // TMEM columns per accumulator (2 rows x 64 heads)
 constexpr int TOPK_QUEUE = 4;      // finished groups handed to the TopK warps
-constexpr int SCORE_THREADS = 384; // 12 warps: TMA, MMA, 2 TopK, 8 epilogue
+constexpr int EPI_WGS = 4;         // epilogue warpgroups: (row of the pair) x (tile parity)
+constexpr int EPI_THREADS = EPI_WGS * 128;
 constexpr int TOPK_THREADS = 64;
-constexpr int EPI_THREADS = 256;
+constexpr int SCORE_THREADS = 128 + EPI_THREADS;  // warps 0-3: TMA, MMA, 2 TopK; then epilogue
+constexpr int STG_CAP = 1024;      // split mode: candidates a warpgroup stages per unit
+constexpr int SLOT_CAP = 7168;     // whole-group mode: candidate keys per row in a shared slot
+constexpr int TOPK_CMP_CAP = 1024; // keys of the K-th key's bucket the TopK warps compact
 
 // -------------------------------------------------------------- selection --
 constexpr int CAND_CAP = 8192;     // candidates kept per row (certificate capacity)
@@ -37,7 +41,11 @@ constexpr int MAX_SAMPLES = 1024;  // per row; longer rows widen the stride
 constexpr int SELECT_THREADS = 512;
 constexpr int SELECT_CAP = 12288;  // candidates the standalone selector keeps in SMEM
 
-enum Mode : int { MODE_STORE = 0, MODE_FILTER = 1 };
+// MODE_STORE: fp32 scores to a matrix.  MODE_FILTER_SLOTS: a CTA scores whole
+// row pairs, candidate keys stay in shared memory and the CTA's TopK warps
+// select them.  MODE_FILTER_GLOBAL: row pairs are split into chunks across
+// CTAs and candidates are flushed to global buffers for a separate select.
+enum Mode : int { MODE_STORE = 0, MODE_FILTER_SLOTS = 1, MODE_FILTER_GLOBAL = 2 };
 
 // status word bits (per call)
 constexpr int ST_TIMEOUT = 1;
@@ -94,8 +102,10 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
+// Named barrier over `nthreads` threads.  The non-aligned form: threads of a
+// warp may arrive at different times (e.g. after one lane waited alone).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------- mbarriers ----
@@ -262,11 +272,43 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------- epilogue arithmetic --
+// ReLU on the FMA pipe: x * 2^-25 saturated to [0, 1] equals ReLU(x) * 2^-25
+// exactly, because every accumulator of a 128-long e4m3 dot satisfies
+// |x| <= 128 * 448^2 < 2^25 and, when non-zero, |x| >= 2^-18 (so the scaled
+// value is a normal number and the power-of-two scaling is exact).  The
+// weight of such a head is stored pre-multiplied by 2^25.
+__device__ __forceinline__ float relu_scaled_fma_pipe(float x) {
+  float r;
+  asm("mul.rn.sat.f32 %0, %1, 0f33000000;" : "=f"(r) : "f"(x));
+  return r;
+}
+constexpr float RELU_SAT_WEIGHT_SCALE = 33554432.0f;  // 2^25
+
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+// acc += a * b on two fp32 lanes (sm_100+ packed FMA)
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+// 16 bytes of shared memory as two packed float pairs
+__device__ __forceinline__ void lds_2x64(uint32_t addr, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
+
 // ------------------------------------------------- radix select (shared) ----
 // Find the bucket of the K-th largest among `hist[256]` (counts of live keys
 // by the current byte), scanning from bucket 255 down.  Executed by one full
-// warp; writes the digit and the remaining rank (rank within that bucket) to
-// out[0], out[1].
+// warp; writes the digit, the remaining rank (rank within that bucket) and
+// the bucket's count to out[0], out[1], out[2].
 __device__ __forceinline__ void radix_pick_digit(const int* hist, int rem, int* out) {
   const int lane = threadIdx.x & 31;
   // lane l owns buckets 255-8l .. 248-8l (descending)
@@ -291,16 +333,20 @@ __device__ __forceinline__ void radix_pick_digit(const int* hist, int rem, int* 
     int digit = 255 - 8 * lane - 7;
     int r = rem - acc;
 #pragma unroll
+    int cnt = c[7];
+#pragma unroll
     for (int i = 0; i < 8; ++i) {
       if (acc + c[i] >= rem) {
         digit = 255 - 8 * lane - i;
         r = rem - acc;
+        cnt = c[i];
         break;
       }
       acc += c[i];
     }
     out[0] = digit;
     out[1] = r;
+    out[2] = cnt;
   }
 }
 

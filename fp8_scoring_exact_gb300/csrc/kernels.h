@@ -23,6 +23,9 @@ struct RowSpace {
   int num_pages;
 };
 
+// chunk size that makes every work unit a whole row pair (tiles per row < 2^24)
+constexpr int WHOLE_PAIR_TILES = 1 << 24;
+
 struct PlanParams {
   RowSpace rs;
   int repair;                  // 0: plan every row; 1: plan the rows queued for repair
@@ -63,6 +66,7 @@ struct ScoreParams {
   int K;
   int chunk_tiles;
   int repair;                  // which plan to read
+  int relu_alu8;               // heads (of every 8) whose ReLU uses the ALU pipe
   const float* q_scale;
   const float* w;
   const int32_t* rb;
@@ -83,12 +87,20 @@ struct ScoreParams {
   Stats* stats;
 };
 
+enum SelectSource : int { SELECT_FROM_SCORES = 0, SELECT_FROM_CANDIDATES = 1 };
+
 struct SelectParams {
   RowSpace rs;
   int K;
   int target16;
+  int source;                  // SelectSource
   int list_mode;               // 1: rows = failed_rows[0 .. stats->fail_count), score row f
   const int32_t* list;
+  // SELECT_FROM_CANDIDATES
+  const uint32_t* cand_key;    // [R, CAND_CAP]
+  const int32_t* cand_idx;
+  const int32_t* cand_count;
+  int32_t* failed_rows;
   const float* scores;
   int64_t ld;
   const int32_t* rb;

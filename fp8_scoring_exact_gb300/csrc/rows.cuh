@@ -49,35 +49,121 @@ __device__ __forceinline__ void group_sync(int bar_id, int nthr) {
     named_bar_sync(bar_id, nthr);
 }
 
+// Histogram of the current byte over keys matching (prefix, mask), one warp
+// iteration at a time: the bucket most lanes share (that of the first live
+// lane) is added once per warp, the others lane by lane.  Candidate keys
+// crowd into few buckets, so this removes most shared-atomic conflicts.
+__device__ __forceinline__ void hist_add(bool live, uint32_t bin, int lane, int* hist) {
+  const unsigned lv = __ballot_sync(0xffffffffu, live);
+  if (!lv) return;
+  const int first = __ffs(lv) - 1;
+  const uint32_t lead = __shfl_sync(0xffffffffu, bin, first);
+  const unsigned same = __ballot_sync(0xffffffffu, live && bin == lead);
+  if (lane == first) atomicAdd(&hist[lead], __popc(same));
+  if (live && bin != lead) atomicAdd(&hist[bin], 1);
+}
+
 // Four 8-bit radix passes, most significant byte first, over n keys given by
 // key_at(i): returns theta = the K-th largest key and r = how many keys equal
-// to theta belong to the top K.  Called by all nthr threads of a group whose
-// first warp is full (tid 0..31); hist[256] and sdig[2] are shared memory.
+// to theta belong to the top K.  Called by all nthr threads (a multiple of 32)
+// of a group whose first warp is full (tid 0..31); hist[256] and sdig[4] are
+// shared memory.  When the bucket that holds the K-th key has at most
+// `ccap` keys, they are compacted into cbuf (shared memory) and the remaining
+// passes scan only them.
 template <class KeyAt>
 __device__ __forceinline__ void group_radix_select(KeyAt key_at, int n, int K, int* hist, int* sdig, int tid,
-                                                   int nthr, int bar_id, uint32_t& theta, int& r) {
+                                                   int nthr, int bar_id, uint32_t& theta, int& r,
+                                                   uint32_t* cbuf = nullptr, int ccap = 0) {
   uint32_t prefix = 0, mask = 0;
   int rem = K;
+  const int lane = tid & 31;
+  int nc = -1;  // >= 0: live keys are compacted in cbuf[0, nc)
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     for (int b = tid; b < 256; b += nthr) hist[b] = 0;
     group_sync(bar_id, nthr);
-    for (int i = tid; i < n; i += nthr) {
-      const uint32_t k = key_at(i);
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 0xFFu], 1);
+    const int m = nc >= 0 ? nc : n;
+    for (int base = 0; base < m; base += nthr) {
+      const int i = base + tid;
+      uint32_t k = 0;
+      bool live = false;
+      if (i < m) {
+        k = nc >= 0 ? cbuf[i] : key_at(i);
+        live = (k & mask) == prefix;
+      }
+      hist_add(live, (k >> shift) & 0xFFu, lane, hist);
     }
     group_sync(bar_id, nthr);
     if (tid < 32) radix_pick_digit(hist, rem, sdig);
     group_sync(bar_id, nthr);
     const int digit = sdig[0];
     rem = sdig[1];
+    const int in_bucket = sdig[2];
     prefix |= (uint32_t)digit << shift;
     mask |= 0xFFu << shift;
-    group_sync(bar_id, nthr);  // sdig / hist reused by the next pass
+    group_sync(bar_id, nthr);  // sdig / hist reused below
+    if (pass < 3 && nc < 0 && cbuf && in_bucket <= ccap && in_bucket < n / 2) {
+      // compact the live bucket: later passes scan in_bucket keys, not n
+      if (tid == 0) sdig[3] = 0;
+      group_sync(bar_id, nthr);
+      for (int base = 0; base < n; base += nthr) {
+        const int i = base + tid;
+        uint32_t k = 0;
+        bool live = false;
+        if (i < n) {
+          k = key_at(i);
+          live = (k & mask) == prefix;
+        }
+        const unsigned lv = __ballot_sync(0xffffffffu, live);
+        int pos = 0;
+        if (lane == 0 && lv) pos = atomicAdd(&sdig[3], __popc(lv));
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        if (live) cbuf[pos + __popc(lv & ((1u << lane) - 1u))] = k;
+      }
+      group_sync(bar_id, nthr);
+      nc = in_bucket;
+    }
   }
   theta = prefix;
   r = rem;
+}
+
+// Emission after the select: every key above theta and the first rr keys
+// equal to theta go to o[] (the above ones to [0, K - rr), the equal ones to
+// [K - rr, K)); slots are reserved once per warp.  All nthr threads call it
+// with the same n; counters[0..1] are shared memory zeroed beforehand.
+template <class KeyAt, class IdAt>
+__device__ __forceinline__ void group_emit(KeyAt key_at, IdAt id_at, int n, uint32_t theta, int rr, int K,
+                                           int32_t* o, int* counters, int tid, int nthr) {
+  const int lane = tid & 31;
+  uint32_t lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  for (int base = 0; base < n; base += nthr) {
+    const int i = base + tid;
+    uint32_t k = 0;
+    int32_t id = 0;
+    if (i < n) {
+      k = key_at(i);
+      if (k >= theta) id = id_at(i);
+    }
+    const bool gt = (i < n) && k > theta;
+    const bool eq = (i < n) && k == theta;
+    const unsigned mg = __ballot_sync(0xffffffffu, gt);
+    const unsigned me = __ballot_sync(0xffffffffu, eq);
+    int bg = 0, be = 0;
+    if (lane == 0) {
+      if (mg) bg = atomicAdd(&counters[0], __popc(mg));
+      if (me) be = atomicAdd(&counters[1], __popc(me));
+    }
+    bg = __shfl_sync(0xffffffffu, bg, 0);
+    be = __shfl_sync(0xffffffffu, be, 0);
+    if (gt) o[bg + __popc(mg & lt)] = id;
+    if (eq) {
+      const int e = be + __popc(me & lt);
+      if (e < rr) o[K - rr + e] = id;
+    }
+  }
 }
 
 // Sample grid of a key range [lo, hi): keys congruent to SAMPLE_OFFSET modulo

@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
   float* wsm = (float*)(smem + SM_OFF_W);
   float* scs = (float*)(smem + SM_OFF_SC);
   int* hist = (int*)(smem + SM_OFF_HIST);
-  int* misc = (int*)(smem + SM_OFF_MISC);  // [0] tmem base, [1..2] digit, [3] abort, [4] wait verdict
+  int* misc = (int*)(smem + SM_OFF_MISC);  // [0] tmem base, [1..4] digit block, [5] abort, [6] wait verdict
   const uint32_t bar = sbase + SM_OFF_MISC + 32;
   const RowSpace& rs = p.rs;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
     tmem_relinquish();
   }
   if (tid == 0) {
-    misc[3] = 0;
+    misc[5] = 0;
     mbar_init(bar, 1);
     fence_mbar_init();
   }
@@ -229,15 +229,16 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = (uint32_t)misc[0];
-  volatile int* abort_flag = (volatile int*)&misc[3];
+  volatile int* abort_flag = (volatile int*)&misc[5];
   if (tid == 0) {
     mbar_arrive_expect_tx(bar, nact * H * D);
     for (int a = 0; a < nact; ++a) tma_load_2d(sbase + SM_OFF_Q + a * H * D, &tm_q, 0, act[a] * H, bar);
   }
   // thread 0 waits (bounded) and the CTA follows its verdict
-  if (tid == 0) misc[4] = mbar_wait(bar, 0, abort_flag, &p.stats->status) ? 1 : 0;
+  if (tid == 0) misc[6] = mbar_wait(bar, 0, abort_flag, &p.stats->status) ? 1 : 0;
+  __syncwarp();
   __syncthreads();
-  bool ok = misc[4] != 0;
+  bool ok = misc[6] != 0;
   const uint32_t idesc = idesc_e4m3_f32(TILE, H * nact);
   const int ntiles = ceil_div(m_u, TILE);
   for (int tt = 0; tt < ntiles && ok; ++tt) {
@@ -277,9 +278,10 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
                  idesc, k > 0);
       mma_commit(bar);
     }
-    if (tid == 0) misc[4] = mbar_wait(bar, (tt + 1) & 1, abort_flag, &p.stats->status) ? 1 : 0;
+    if (tid == 0) misc[6] = mbar_wait(bar, (tt + 1) & 1, abort_flag, &p.stats->status) ? 1 : 0;
+    __syncwarp();
     __syncthreads();
-    ok = misc[4] != 0;
+    ok = misc[6] != 0;
     if (!ok) break;
     tc_fence_after();
     for (int a = 0; a < nact; ++a) {
@@ -339,34 +341,32 @@ cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_
 }
 
 // ================================================================== select ==
-// Standalone exact top-K of fp32 score rows: per row, sampled threshold ->
-// filter into shared memory (float4 loads, one shared atomic per warp batch)
-// -> radix select on the candidates; when the certificate fails (fewer than K
-// or more than SELECT_CAP candidates) the radix select runs over the whole row.
+// Standalone exact top-K per row, one CTA per row at a time.  Two sources:
+//  - fp32 score rows: sampled threshold -> filter into shared memory (float4
+//    loads, one shared reservation per warp batch) -> radix select on the
+//    candidates; when the certificate fails (fewer than K or more than
+//    SELECT_CAP candidates) the radix select runs over the whole row;
+//  - candidate buffers of the split scorer (keys and indices of every score
+//    that reached the row's threshold): certificate check (K <= count <=
+//    CAND_CAP), then radix select; failing rows are queued for repair.
 constexpr uint32_t SEL_OFF_KEY = 0;
 constexpr uint32_t SEL_OFF_IDX = SEL_OFF_KEY + SELECT_CAP * 4;
 constexpr uint32_t SEL_OFF_SAMP = SEL_OFF_IDX + SELECT_CAP * 4;
-constexpr uint32_t SEL_OFF_HIST = SEL_OFF_SAMP + MAX_SAMPLES * 4;
+constexpr uint32_t SEL_OFF_CMP = SEL_OFF_SAMP + MAX_SAMPLES * 4;
+constexpr int SEL_CMP_CAP = 2048;
+constexpr uint32_t SEL_OFF_HIST = SEL_OFF_CMP + SEL_CMP_CAP * 4;
 constexpr uint32_t SEL_OFF_MISC = SEL_OFF_HIST + 256 * 4;
 constexpr uint32_t SELECT_SMEM = SEL_OFF_MISC + 64;
-
-__device__ __forceinline__ void emit_one(uint32_t k, int32_t id, uint32_t theta, int rr, int K, int32_t* o,
-                                         int* s_above, int* s_eq) {
-  if (k > theta) {
-    o[atomicAdd(s_above, 1)] = id;
-  } else if (k == theta) {
-    const int e = atomicAdd(s_eq, 1);
-    if (e < rr) o[K - rr + e] = id;
-  }
-}
+static_assert(SELECT_CAP >= CAND_CAP, "candidate rows must fit the selector");
 
 __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectParams p) {
   extern __shared__ uint8_t smem[];
   uint32_t* ckey = (uint32_t*)(smem + SEL_OFF_KEY);
   int32_t* cidx = (int32_t*)(smem + SEL_OFF_IDX);
   uint32_t* samp = (uint32_t*)(smem + SEL_OFF_SAMP);
+  uint32_t* cmp = (uint32_t*)(smem + SEL_OFF_CMP);
   int* hist = (int*)(smem + SEL_OFF_HIST);
-  int* misc = (int*)(smem + SEL_OFF_MISC);  // [0..1] digit, [2] count, [3] above, [4] eq, [5] tau
+  int* misc = (int*)(smem + SEL_OFF_MISC);  // [0..3] digit block, [4] count, [5..6] emit counters
   const RowSpace& rs = p.rs;
   const int tid = threadIdx.x, lane = tid & 31;
   const int K = p.K;
@@ -378,6 +378,37 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
     const int b = p.rb[row], e = p.re[row];
     const int L = e - b;
     int32_t* o = p.out + (int64_t)row * K;
+    if (tid == 0) {
+      misc[4] = 0;
+      misc[5] = 0;
+      misc[6] = 0;
+    }
+    if (p.source == SELECT_FROM_CANDIDATES) {
+      // rows of the split scorer: L <= K rows were written by the remapping path
+      if (L <= K) continue;
+      const int n = p.cand_count[row];
+      if (n < K || n > CAND_CAP) {
+        if (tid == 0) {
+          const int fi = atomicAdd(&p.stats->fail_count, 1);
+          p.failed_rows[fi] = row;
+          atomicAdd(n < K ? &p.stats->underflow : &p.stats->overflow, 1);
+        }
+        continue;
+      }
+      const uint32_t* ck = p.cand_key + (int64_t)row * CAND_CAP;
+      const int32_t* ci = p.cand_idx + (int64_t)row * CAND_CAP;
+      for (int i = tid; i < n; i += SELECT_THREADS) ckey[i] = ck[i];
+      if (tid == 0) atomicAdd(&p.stats->cand_total, n);
+      __syncthreads();
+      uint32_t theta;
+      int rr;
+      group_radix_select([&](int i) { return ckey[i]; }, n, K, hist, misc, tid, SELECT_THREADS, 0, theta, rr, cmp,
+                         SEL_CMP_CAP);
+      group_emit([&](int i) { return ckey[i]; }, [&](int i) { return ci[i]; }, n, theta, rr, K, o, misc + 5, tid,
+                 SELECT_THREADS);
+      __syncthreads();
+      continue;
+    }
     if (L <= K) {
       write_all_valid(rs, row, b, e, K, p.out, tid, SELECT_THREADS);
       continue;
@@ -388,11 +419,6 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
     int first, m, S;
     sample_grid(b, e, &first, &m, &S);
     for (int j = tid; j < m; j += SELECT_THREADS) samp[j] = ordered_key(srow[first + j * S]);
-    if (tid == 0) {
-      misc[2] = 0;
-      misc[3] = 0;
-      misc[4] = 0;
-    }
     __syncthreads();
     const int rank = sample_rank(m, L, target);
     uint32_t tau = 0u;
@@ -413,7 +439,7 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
       }
       const int wtot = __shfl_sync(0xffffffffu, incl, 31);
       int base = 0;
-      if (lane == 31 && wtot) base = atomicAdd(&misc[2], wtot);
+      if (lane == 31 && wtot) base = atomicAdd(&misc[4], wtot);
       base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
       for (int i = 0; i < cnt; ++i)
         if (base + i < SELECT_CAP) {
@@ -422,23 +448,21 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
         }
     };
     // scalar head and tail (at most 3 + 3 elements), then the aligned body
-    {
+    if (tid < 32) {
       const int nh = (a0 - b) + (e - a1);
       uint32_t ks[1];
       int ids[1];
       int cnt = 0;
-      if (tid < 32) {
-        if (lane < nh) {
-          const int i = lane < (a0 - b) ? b + lane : a1 + (lane - (a0 - b));
-          const uint32_t k = ordered_key(srow[i]);
-          if (k >= tau) {
-            ks[0] = k;
-            ids[0] = i;
-            cnt = 1;
-          }
+      if (lane < nh) {
+        const int i = lane < (a0 - b) ? b + lane : a1 + (lane - (a0 - b));
+        const uint32_t k = ordered_key(srow[i]);
+        if (k >= tau) {
+          ks[0] = k;
+          ids[0] = i;
+          cnt = 1;
         }
-        append(cnt, ks, ids);
       }
+      append(cnt, ks, ids);
     }
     const int nvec = (a1 - a0) >> 2;
     const float4* v4 = (const float4*)(srow + a0);
@@ -464,26 +488,22 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
       append(cnt, ks, ids);
     }
     __syncthreads();
-    const int n = misc[2];
+    const int n = misc[4];
     uint32_t theta;
     int rr;
     if (n >= K && n <= SELECT_CAP) {
-      group_radix_select([&](int i) { return ckey[i]; }, n, K, hist, misc, tid, SELECT_THREADS, 0, theta, rr);
-      for (int i = tid; i < n; i += SELECT_THREADS) {
-        const int id = rs.paged ? out_index(rs, row, cidx[i]) : cidx[i];
-        emit_one(ckey[i], id, theta, rr, K, o, &misc[3], &misc[4]);
-      }
+      group_radix_select([&](int i) { return ckey[i]; }, n, K, hist, misc, tid, SELECT_THREADS, 0, theta, rr, cmp,
+                         SEL_CMP_CAP);
+      group_emit([&](int i) { return ckey[i]; },
+                 [&](int i) { return rs.paged ? out_index(rs, row, cidx[i]) : cidx[i]; }, n, theta, rr, K, o,
+                 misc + 5, tid, SELECT_THREADS);
     } else {
       // certificate failed: exact radix select over the whole row
       group_radix_select([&](int i) { return ordered_key(srow[b + i]); }, L, K, hist, misc, tid, SELECT_THREADS, 0,
-                         theta, rr);
-      for (int i = tid; i < L; i += SELECT_THREADS) {
-        const uint32_t k = ordered_key(srow[b + i]);
-        if (k >= theta) {
-          const int id = rs.paged ? out_index(rs, row, b + i) : b + i;
-          emit_one(k, id, theta, rr, K, o, &misc[3], &misc[4]);
-        }
-      }
+                         theta, rr, cmp, SEL_CMP_CAP);
+      group_emit([&](int i) { return ordered_key(srow[b + i]); },
+                 [&](int i) { return rs.paged ? out_index(rs, row, b + i) : b + i; }, L, theta, rr, K, o, misc + 5,
+                 tid, SELECT_THREADS);
     }
     __syncthreads();
   }
