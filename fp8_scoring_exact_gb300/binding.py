@@ -35,6 +35,7 @@ SIGNATURES = {
     "dsa_indexer_topk_unfused": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_scores": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I64, _P]),
     "dsa_indexer_topk_from_scores": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
+    "dsa_indexer_topk_from_scores_noalloc": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_last_device_status": (_I, [_P, _P]),
     "dsa_indexer_last_repaired_rows": (_I, [_P, _P, _I]),
     "dsa_indexer_set_option": (_I, [_I, _I64]),
@@ -186,6 +187,23 @@ def topk_from_scores(scores, row_begin, row_end, K=2048, N=None, out=None, strea
                                             _ptr(_dev(row_end, "row_end", torch.int32)), Q, N, K,
                                             _ptr(_dev(out, "out", torch.int32)), _stream_ptr(stream))
     _check("dsa_indexer_topk_from_scores", rc)
+    return out
+
+
+def topk_from_scores_noalloc(scores, row_begin, row_end, K=2048, N=None, out=None, stream=None):
+    """Same as topk_from_scores, through the entry point that allocates nothing
+    (its scratch is a fixed array in device memory; at most 4096 rows).  The
+    output tensor is the caller's: pass `out` to avoid even that allocation."""
+    scores = _dev(scores, "scores", torch.float32)
+    Q, ld = scores.shape
+    N = ld if N is None else N
+    if out is None:
+        out = torch.empty((Q, K), dtype=torch.int32, device=scores.device)
+    rc = lib().dsa_indexer_topk_from_scores_noalloc(_ptr(scores), ld,
+                                                    _ptr(_dev(row_begin, "row_begin", torch.int32)),
+                                                    _ptr(_dev(row_end, "row_end", torch.int32)), Q, N, K,
+                                                    _ptr(_dev(out, "out", torch.int32)), _stream_ptr(stream))
+    _check("dsa_indexer_topk_from_scores_noalloc", rc)
     return out
 
 

@@ -335,6 +335,40 @@ int check_dense(const uint8_t* q, const float* qs, const uint8_t* k, const float
   return DSA_OK;
 }
 
+// ------------------------------------------------- no-allocation variant --
+// Scratch of dsa_indexer_topk_from_scores_noalloc: a fixed array in device
+// memory that exists on every GPU that loads this library, for callers that
+// must not allocate (see the declaration in the header).  The host-side name
+// g_noalloc_scratch is only a stand-in for the symbol: the kernels get the
+// device address that cudaGetSymbolAddress returns for the current device.
+constexpr int NOALLOC_MAX_ROWS = 4096;
+constexpr size_t NOALLOC_SCRATCH_BYTES = 512 * 1024;
+__device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+std::map<int, void*> g_noalloc_addr;  // device -> address of g_noalloc_scratch there
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the first call on a device does this lookup).
+void* noalloc_scratch(int* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    *err = DSA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  auto it = g_noalloc_addr.find(dev);
+  if (it != g_noalloc_addr.end()) return it->second;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    *err = DSA_ERR_CUDA;
+    return nullptr;
+  }
+  g_noalloc_addr[dev] = p;
+  return p;
+}
+
 }  // namespace
 
 // =================================================================== C ABI ==
@@ -524,6 +558,55 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   sel.out = out_idx;
   sel.stats = pp.stats;
   a->profiled = false;
+  DSA_LAUNCH(launch_select(sel, 2 * o.grid, stream));
+  return DSA_OK;
+}
+
+int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const int32_t* row_begin,
+                                         const int32_t* row_end, int Q, int N, int K, int32_t* out_idx,
+                                         dsa_stream_t stream_) {
+  if (!scores || !row_begin || !row_end || !out_idx) return DSA_ERR_ARG;
+  if (Q <= 0 || N <= 0 || ld < N || (ld & 3) || !aligned16(scores) || K < 1 || K > DSA_MAX_K) return DSA_ERR_ARG;
+  if (Q > NOALLOC_MAX_ROWS) return DSA_ERR_UNSUPPORTED;
+  RowSpace rs{};
+  rs.R = Q;
+  rs.N = N;
+  const Layout L = make_layout(Q, n_pairs(rs), false, 0, 0);
+  if (L.total > NOALLOC_SCRATCH_BYTES) return DSA_ERR_UNSUPPORTED;
+  int err = DSA_OK;
+  uint8_t* base = static_cast<uint8_t*>(noalloc_scratch(&err));
+  if (!base) return err;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const Opts o = read_opts();
+  // the plan kernel rewrites every part of the scratch this call reads:
+  // counters and status are zeroed, row ranges validated and stored
+  PlanParams pp{};
+  pp.rs = rs;
+  pp.K = K;
+  pp.trivial_len = 0x7fffffff;
+  pp.chunk_tiles = o.chunk;
+  pp.row_begin_in = row_begin;
+  pp.row_end_in = row_end;
+  pp.rb = reinterpret_cast<int32_t*>(base + L.rb);
+  pp.re = reinterpret_cast<int32_t*>(base + L.re);
+  pp.groups = reinterpret_cast<Group*>(base + L.groups);
+  pp.unit_start = reinterpret_cast<int32_t*>(base + L.unit_start);
+  pp.group_done = reinterpret_cast<int32_t*>(base + L.group_done);
+  pp.cand_count = reinterpret_cast<int32_t*>(base + L.cand_count);
+  pp.failed_rows = reinterpret_cast<int32_t*>(base + L.failed);
+  pp.stats = reinterpret_cast<Stats*>(base + L.stats);
+  DSA_LAUNCH(launch_plan(pp, stream));
+  SelectParams sel{};
+  sel.rs = rs;
+  sel.K = K;
+  sel.target16 = o.target16;
+  sel.source = SELECT_FROM_SCORES;
+  sel.scores = scores;
+  sel.ld = ld;
+  sel.rb = pp.rb;
+  sel.re = pp.re;
+  sel.out = out_idx;
+  sel.stats = pp.stats;
   DSA_LAUNCH(launch_select(sel, 2 * o.grid, stream));
   return DSA_OK;
 }

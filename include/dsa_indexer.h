@@ -153,6 +153,29 @@ DSA_API int dsa_indexer_topk_from_scores(const float* scores, int64_t ld,
                                  int32_t* out_idx, dsa_stream_t stream);
 
 /*
+ * Same operation and result as dsa_indexer_topk_from_scores, but this entry
+ * point allocates no memory at all, for callers that cannot call cudaMalloc
+ * (for example code running while a CUDA graph is being captured, or an
+ * embedding runtime that owns every device allocation and forbids others).
+ * The paper has no counterpart; it is a deployment convenience.
+ *
+ * Its scratch is one fixed device array of 512 KiB compiled into this
+ * library; every GPU that loads the library holds it until the process
+ * exits.  Limits: Q <= 4096 rows (larger Q returns DSA_ERR_UNSUPPORTED and
+ * enqueues nothing).  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture on that device.  Every call resets the parts of the
+ * array it reads, but all calls share the one array: calls that may overlap
+ * on the GPU (on different streams, or from different threads without
+ * ordering) race and must be serialised by the caller.  Calls to this entry
+ * point are not reported by dsa_indexer_last_device_status().
+ */
+DSA_API int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld,
+                                                 const int32_t* row_begin, const int32_t* row_end,
+                                                 int Q, int N, int K,
+                                                 int32_t* out_idx, dsa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports the device status of the most recent
  * call enqueued on it: DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_RANGE (or
  * DSA_ERR_CUDA if synchronising failed).  failures_out (may be NULL) receives
