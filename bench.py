@@ -53,6 +53,22 @@ def score_matrix_bytes(Q: int, N: int) -> int:
     return Q * N * 4
 
 
+def measured_traffic(config: int, rows: int, keys: int):
+    """DRAM bytes per launch of the main kernel from the committed ncu record,
+    or None when the workload differs or the kernel sources changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "score_kernel_traffic_c2.json")
+    if config != 2 or rows or keys or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -121,8 +137,12 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- workload --
-def make_workload(config: int):
+def make_workload(config: int, rows: int = 0, keys: int = 0):
+    """The indexed workload, or a causal prefill chunk of `rows` x `keys`
+    drawn like it (for profiling smaller cases of the same kernels)."""
     from fp8_scoring_exact_gb300 import synthetic
+    if rows and keys:
+        return synthetic.make_dense(rows, keys, seed=config, name=f"causal_q{rows}_n{keys}")
     return synthetic.make_config(config)
 
 
@@ -171,14 +191,39 @@ def time_oracle(inp, n_rows, procs, reps=1):
 
 
 # ------------------------------------------------------------ GPU arm -------
+def _e2e(args, dev, host, out, stream, world, device, binding, R, K):
+    """Same metric through the public API with host buffers: every step copies
+    the inputs from pinned host memory and reads the indices back."""
+    import torch
+    pinned = [torch.from_numpy(a).pin_memory() for a in host]
+    out_h = torch.empty(tuple(out.shape), dtype=torch.int32).pin_memory()
+    h2d = sum(a.nbytes for a in host)
+    d2h = out_h.numel() * 4
+    for i in range(args.steps + 1):
+        if i == 1:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        for d, h in zip(dev, pinned):
+            d.copy_(h, non_blocking=True)
+        binding.indexer_topk(*dev, K=K, out=out)
+        out_h.copy_(out, non_blocking=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / args.steps
+    return {"value": world * R / (e2e_ms * 1e-3), "unit": "row-keys/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+
 def run_ours(args, rank, world, device):
     import torch
 
     from fp8_scoring_exact_gb300 import binding
 
-    inp = make_workload(args.config)
+    inp = make_workload(args.config, args.rows, args.keys)
     Q, N, K = inp.Q, inp.N, inp.K
     R = inp.row_keys()
+    legs = set(args.legs.split(","))
     host = [np.ascontiguousarray(a) for a in (inp.q, inp.q_scale, inp.k, inp.k_scale, inp.w, inp.row_begin,
                                                inp.row_end)]
     dev = [torch.from_numpy(a).to(device) for a in host]
@@ -219,36 +264,22 @@ def run_ours(args, rank, world, device):
     binding.set_option("profile", 0)
 
     # unfused attribution baseline, same protocol
-    unf = []
-    for _ in range(max(1, args.warmup // 2)):
+    unf_ms = None
+    for _ in range(max(1, args.warmup // 2) if "unfused" in legs else 0):
         binding.indexer_topk_unfused(*dev, K=K, out=out)
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        binding.indexer_topk_unfused(*dev, K=K, out=out)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize(device)
-    unf = [a.elapsed_time(b) for a, b in ev]
-    unf_ms = statistics.mean(unf)
+    if "unfused" in legs:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            binding.indexer_topk_unfused(*dev, K=K, out=out)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(device)
+        unf_ms = statistics.mean([a.elapsed_time(b) for a, b in ev])
 
     # end to end through the public API from pinned host buffers
-    pinned = [torch.from_numpy(a).pin_memory() for a in host]
-    out_h = torch.empty((Q, K), dtype=torch.int32).pin_memory()
-    h2d = sum(a.nbytes for a in host)
-    d2h = out_h.numel() * 4
-    for i in range(args.steps + 1):
-        if i == 1:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        for d, h in zip(dev, pinned):
-            d.copy_(h, non_blocking=True)
-        binding.indexer_topk(*dev, K=K, out=out)
-        out_h.copy_(out, non_blocking=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / args.steps
-
+    e2e = None
+    if "e2e" in legs:
+        e2e = _e2e(args, dev, host, out, stream, world, device, binding, R, K)
     peaks = load_peaks()
     main_avg = statistics.mean(main_ms)
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
@@ -276,12 +307,11 @@ def run_ours(args, rank, world, device):
         "data": "synthetic (seeded Gaussian activations quantised to FP8 e4m3 per token)",
         "config": describe(inp, args.config),
         "tflops_effective": world * FLOP_PER_ROW_KEY * R / (ms_per_step * 1e-3) / 1e12,
-        "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "row-keys/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": None,
+                     "frac": achieved / fp8_peak, "traffic": measured_traffic(args.config, args.rows, args.keys),
                      "kernel": "score_kernel (filter mode: tcgen05 scoring + candidate filter + TopK warps)",
                      "kernel_ms": main_avg,
                      "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} "
@@ -289,7 +319,7 @@ def run_ours(args, rank, world, device):
         "roofline_terms": {"t_tensor_ms": t_tensor, "t_core_ms": t_core, "t_hbm_ms": t_hbm, "t_roof_ms": t_roof,
                            "frac_of_roofline": t_roof / ms_per_step, "sm_count": sms,
                            "sm_clock_for_core_term_mhz": f_sm / 1e6},
-        "unfused": {"ms_per_step": unf_ms, "fused_speedup": unf_ms / ms_per_step},
+        "unfused": ({"ms_per_step": unf_ms, "fused_speedup": unf_ms / ms_per_step} if unf_ms else None),
         "failures": counters,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -305,7 +335,7 @@ def run_reference(args, rank, world):
     """CPU oracle as the reference arm: rank 0 only."""
     if rank != 0:
         return None
-    inp = make_workload(args.config)
+    inp = make_workload(args.config, args.rows, args.keys)
     procs = cpu_procs()
     from oracle.indexer import OraclePool
     rows = oracle_rows(inp, procs * (args.steps + args.warmup), seed=321)
@@ -378,6 +408,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, help="workload index (2 = causal Q4096 x N131072)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=0, help="override: causal workload with this many query rows")
+    ap.add_argument("--keys", type=int, default=0, help="override: causal workload with this many keys")
+    ap.add_argument("--legs", default="fused,unfused,e2e",
+                    help="comma list of legs to run besides the timed fused leg (unfused, e2e)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
