@@ -32,19 +32,19 @@ int64_t g_tau_bias = 0;
 int64_t g_profile = 0;
 int64_t g_grid = 0;
 int64_t g_target16 = 32;
-int64_t g_relu_alu8 = 0;
-int64_t g_fused_mode = 0;
 std::atomic<int64_t> g_launches{0};
 
 // ----------------------------------------------------------------- arena ----
 struct Layout {
-  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, group_done, cand_count, failed;
+  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, group_done, unit_count, failed;
   size_t cand_key, cand_idx, scores, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-Layout make_layout(int64_t R, int64_t G, bool cand, int64_t score_rows, int64_t ld) {
+// cand_stride: candidate slots per row (0: no candidate buffers); max_units:
+// work units per group at most (per-row unit counts)
+Layout make_layout(int64_t R, int64_t G, int64_t cand_stride, int64_t max_units, int64_t score_rows, int64_t ld) {
   Layout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -61,10 +61,10 @@ Layout make_layout(int64_t R, int64_t G, bool cand, int64_t score_rows, int64_t 
   L.rgroups = take(R * sizeof(Group));
   L.runit_start = take((R + 1) * 4);
   L.group_done = take(G * 4);
-  L.cand_count = take(R * 4);
+  L.unit_count = take((size_t)R * max_units * 4);
   L.failed = take(R * 4);
-  L.cand_key = take(cand ? (size_t)R * CAND_CAP * 4 : 0);
-  L.cand_idx = take(cand ? (size_t)R * CAND_CAP * 4 : 0);
+  L.cand_key = take((size_t)R * cand_stride * 4);
+  L.cand_idx = take((size_t)R * cand_stride * 4);
   L.scores = take((size_t)score_rows * ld * 4);
   L.total = off;
   return L;
@@ -175,7 +175,7 @@ int sm_count() {
   } while (0)
 
 struct Opts {
-  int chunk, grid, target16, relu_alu8, fused_mode;
+  int chunk, grid, target16;
   int64_t bias;
   bool profile;
 };
@@ -187,8 +187,6 @@ Opts read_opts() {
   o.bias = g_tau_bias;
   o.profile = g_profile != 0;
   o.target16 = (int)g_target16;
-  o.relu_alu8 = (int)g_relu_alu8;
-  o.fused_mode = (int)g_fused_mode;
   const int sms = sm_count();
   o.grid = g_grid > 0 ? (int)g_grid : (sms > 0 ? sms : 1);
   return o;
@@ -200,15 +198,13 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
               const CUtensorMap& tm_ks, const uint8_t* k_raw, const float* ks_raw, const float* q_scale,
               const float* w, const int32_t* row_begin, const int32_t* row_end, int32_t* out, cudaStream_t stream) {
   const Opts o = read_opts();
-  const int G = n_pairs(rs);
+  const int G = n_groups(rs);
   const int64_t ld = align_up((size_t)rs.N, 4);
-  // whole pairs per CTA (candidates in shared memory, TopK warps in the same
-  // CTA) when there are enough pairs to balance the SMs; chunks split across
-  // CTAs with global candidates and a separate select otherwise
-  const bool slots = o.fused_mode == 1 || (o.fused_mode == 0 && !rs.paged && G >= 2 * o.grid);
+  const int max_units = ceil_div(ceil_div(rs.N, TILE), o.chunk);
+  const int64_t cand_stride = (int64_t)max_units * UCAP;
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
-  Arena* a = get_arena(stream, make_layout(rs.R, G, true, rs.R, ld), &err);
+  Arena* a = get_arena(stream, make_layout(rs.R, G, cand_stride, max_units, rs.R, ld), &err);
   if (!a) return err;
   const Layout& L = a->L;
   Stats* st = at<Stats>(a, L.stats);
@@ -218,7 +214,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   pp.repair = 0;
   pp.K = K;
   pp.trivial_len = K;
-  pp.chunk_tiles = slots ? WHOLE_PAIR_TILES : o.chunk;
+  pp.chunk_tiles = o.chunk;
   pp.row_begin_in = row_begin;
   pp.row_end_in = row_end;
   pp.rb = at<int32_t>(a, L.rb);
@@ -226,7 +222,6 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   pp.groups = at<Group>(a, L.groups);
   pp.unit_start = at<int32_t>(a, L.unit_start);
   pp.group_done = at<int32_t>(a, L.group_done);
-  pp.cand_count = at<int32_t>(a, L.cand_count);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = st;
   DSA_LAUNCH(launch_plan(pp, stream));
@@ -245,14 +240,13 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   sp.tau = at<uint32_t>(a, L.tau);
   sp.out = out;
   sp.stats = st;
-  DSA_LAUNCH(launch_sample(tm_q, sp, G, stream));
+  DSA_LAUNCH(launch_sample(tm_q, sp, n_pairs(rs), stream));
 
   ScoreParams cp{};
   cp.rs = rs;
-  cp.mode = slots ? MODE_FILTER_SLOTS : MODE_FILTER_GLOBAL;
+  cp.mode = MODE_FILTER;
   cp.K = K;
-  cp.chunk_tiles = pp.chunk_tiles;
-  cp.relu_alu8 = o.relu_alu8;
+  cp.chunk_tiles = o.chunk;
   cp.repair = 0;
   cp.q_scale = q_scale;
   cp.w = w;
@@ -263,7 +257,9 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cp.tau = sp.tau;
   cp.cand_key = at<uint32_t>(a, L.cand_key);
   cp.cand_idx = at<int32_t>(a, L.cand_idx);
-  cp.cand_count = pp.cand_count;
+  cp.unit_count = at<int32_t>(a, L.unit_count);
+  cp.cand_stride = cand_stride;
+  cp.max_units = max_units;
   cp.group_done = pp.group_done;
   cp.failed_rows = at<int32_t>(a, L.failed);
   cp.out = out;
@@ -273,35 +269,15 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   DSA_LAUNCH(launch_score(tm_q, tm_k, tm_ks, cp, o.grid, stream));
   if (o.profile) cudaEventRecord(a->ev1, stream);
 
-  if (!slots) {
-    // split chunks: select every row from its global candidate buffer
-    SelectParams cs{};
-    cs.rs = rs;
-    cs.K = K;
-    cs.target16 = o.target16;
-    cs.source = SELECT_FROM_CANDIDATES;
-    cs.cand_key = cp.cand_key;
-    cs.cand_idx = cp.cand_idx;
-    cs.cand_count = cp.cand_count;
-    cs.failed_rows = cp.failed_rows;
-    cs.rb = pp.rb;
-    cs.re = pp.re;
-    cs.out = out;
-    cs.stats = st;
-    DSA_LAUNCH(launch_select(cs, 2 * o.grid, stream));
-  }
-
   // exact repair of rows whose certificate failed
   PlanParams rp = pp;
   rp.repair = 1;
-  rp.chunk_tiles = o.chunk;
   rp.groups = at<Group>(a, L.rgroups);
   rp.unit_start = at<int32_t>(a, L.runit_start);
   DSA_LAUNCH(launch_plan(rp, stream));
 
   ScoreParams rcp = cp;
   rcp.mode = MODE_STORE;
-  rcp.chunk_tiles = o.chunk;
   rcp.repair = 1;
   rcp.groups = rp.groups;
   rcp.unit_start = rp.unit_start;
@@ -313,9 +289,8 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   sel.rs = rs;
   sel.K = K;
   sel.target16 = o.target16;
-  sel.source = SELECT_FROM_SCORES;
   sel.list_mode = 1;
-  sel.list = rcp.failed_rows;
+  sel.list = pp.failed_rows;
   sel.scores = rcp.scores;
   sel.ld = ld;
   sel.rb = pp.rb;
@@ -433,11 +408,11 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   RowSpace rs{};
   rs.R = Q;
   rs.N = N;
-  const int G = n_pairs(rs);
+  const int G = n_groups(rs);
   const int64_t own_ld = align_up((size_t)N, 4);
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
-  Arena* a = get_arena(stream, make_layout(Q, G, false, scores ? 0 : Q, own_ld), &err);
+  Arena* a = get_arena(stream, make_layout(Q, G, 0, 0, scores ? 0 : Q, own_ld), &err);
   if (!a) return err;
   const Layout& L = a->L;
   Stats* st = at<Stats>(a, L.stats);
@@ -456,7 +431,6 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   pp.groups = at<Group>(a, L.groups);
   pp.unit_start = at<int32_t>(a, L.unit_start);
   pp.group_done = at<int32_t>(a, L.group_done);
-  pp.cand_count = at<int32_t>(a, L.cand_count);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = st;
   DSA_LAUNCH(launch_plan(pp, stream));
@@ -466,7 +440,6 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   cp.mode = MODE_STORE;
   cp.K = K;
   cp.chunk_tiles = o.chunk;
-  cp.relu_alu8 = o.relu_alu8;
   cp.q_scale = q_scale;
   cp.w = w;
   cp.rb = pp.rb;
@@ -486,7 +459,6 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   sel.rs = rs;
   sel.K = K;
   sel.target16 = o.target16;
-  sel.source = SELECT_FROM_SCORES;
   sel.scores = sbuf;
   sel.ld = sld;
   sel.rb = pp.rb;
@@ -528,7 +500,7 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   rs.N = N;
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
-  Arena* a = get_arena(stream, make_layout(Q, n_pairs(rs), false, 0, 0), &err);
+  Arena* a = get_arena(stream, make_layout(Q, n_groups(rs), 0, 0, 0, 0), &err);
   if (!a) return err;
   const Layout& L = a->L;
   PlanParams pp{};
@@ -543,7 +515,6 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   pp.groups = at<Group>(a, L.groups);
   pp.unit_start = at<int32_t>(a, L.unit_start);
   pp.group_done = at<int32_t>(a, L.group_done);
-  pp.cand_count = at<int32_t>(a, L.cand_count);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = at<Stats>(a, L.stats);
   DSA_LAUNCH(launch_plan(pp, stream));
@@ -571,7 +542,7 @@ int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const 
   RowSpace rs{};
   rs.R = Q;
   rs.N = N;
-  const Layout L = make_layout(Q, n_pairs(rs), false, 0, 0);
+  const Layout L = make_layout(Q, n_groups(rs), 0, 0, 0, 0);
   if (L.total > NOALLOC_SCRATCH_BYTES) return DSA_ERR_UNSUPPORTED;
   int err = DSA_OK;
   uint8_t* base = static_cast<uint8_t*>(noalloc_scratch(&err));
@@ -592,7 +563,6 @@ int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const 
   pp.groups = reinterpret_cast<Group*>(base + L.groups);
   pp.unit_start = reinterpret_cast<int32_t*>(base + L.unit_start);
   pp.group_done = reinterpret_cast<int32_t*>(base + L.group_done);
-  pp.cand_count = reinterpret_cast<int32_t*>(base + L.cand_count);
   pp.failed_rows = reinterpret_cast<int32_t*>(base + L.failed);
   pp.stats = reinterpret_cast<Stats*>(base + L.stats);
   DSA_LAUNCH(launch_plan(pp, stream));
@@ -600,7 +570,6 @@ int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const 
   sel.rs = rs;
   sel.K = K;
   sel.target16 = o.target16;
-  sel.source = SELECT_FROM_SCORES;
   sel.scores = scores;
   sel.ld = ld;
   sel.rb = pp.rb;
@@ -676,14 +645,7 @@ int dsa_indexer_set_option(int option, int64_t value) {
       if (value < 1 || value > 256) return DSA_ERR_ARG;
       g_target16 = value;
       return DSA_OK;
-    case DSA_OPT_RELU_ALU8:
-      if (value != 0 && value != 2 && value != 4 && value != 8) return DSA_ERR_ARG;
-      g_relu_alu8 = value;
-      return DSA_OK;
-    case DSA_OPT_FUSED_MODE:
-      if (value < 0 || value > 2) return DSA_ERR_ARG;
-      g_fused_mode = value;
-      return DSA_OK;
+
     default:
       return DSA_ERR_ARG;
   }
@@ -702,10 +664,7 @@ int64_t dsa_indexer_get_option(int option) {
       return g_grid;
     case DSA_OPT_SAMPLE_TARGET:
       return g_target16;
-    case DSA_OPT_RELU_ALU8:
-      return g_relu_alu8;
-    case DSA_OPT_FUSED_MODE:
-      return g_fused_mode;
+
     default:
       return DSA_ERR_ARG;
   }

@@ -16,36 +16,34 @@ namespace dsa {
 constexpr int H = 64;              // indexer heads
 constexpr int D = 128;             // head dimension (bytes per FP8 vector)
 constexpr int TILE = 128;          // keys per MMA tile (MMA M, one TMEM lane per key)
-constexpr int GROUP_ROWS = 2;      // query rows sharing one key stream (MMA N = 64 * rows)
+constexpr int GROUP_ROWS = 4;      // query rows sharing one key stream (MMA N = 64 * rows <= 256)
+constexpr int SAMPLE_ROWS = 2;     // query rows per CTA of the threshold-sampling kernel
 constexpr int PAGE = 64;           // tokens per paged-cache page
 
 // ------------------------------------------------------- persistent scorer --
-constexpr int STAGES = 4;          // key-tile ring depth (TMA -> MMA)
+constexpr int STAGES = 5;          // key-tile ring depth (TMA -> MMA)
 constexpr int SC_STAGES = 8;       // key-scale ring depth (TMA -> epilogue)
-constexpr int ACC_BUFS = 4;        // TMEM accumulators (MMA -> epilogue)
-constexpr int ACC_COLS = 128;      // TMEM columns per accumulator (2 rows x 64 heads)
+constexpr int ACC_BUFS = 2;        // TMEM accumulators (MMA -> epilogue)
+constexpr int ACC_COLS = 256;      // TMEM columns per accumulator (4 rows x 64 heads)
 constexpr int TOPK_QUEUE = 4;      // finished groups handed to the TopK warps
-constexpr int EPI_WGS = 4;         // epilogue warpgroups: (row of the pair) x (tile parity)
+constexpr int EPI_WGS = GROUP_ROWS; // epilogue warpgroups: one per row of the group
 constexpr int EPI_THREADS = EPI_WGS * 128;
 constexpr int TOPK_THREADS = 64;
 constexpr int SCORE_THREADS = 128 + EPI_THREADS;  // warps 0-3: TMA, MMA, 2 TopK; then epilogue
-constexpr int STG_CAP = 1024;      // split mode: candidates a warpgroup stages per unit
-constexpr int SLOT_CAP = 7168;     // whole-group mode: candidate keys per row in a shared slot
+constexpr int UCAP = 1024;         // candidates one work unit may leave for one row
 constexpr int TOPK_CMP_CAP = 1024; // keys of the K-th key's bucket the TopK warps compact
 
 // -------------------------------------------------------------- selection --
-constexpr int CAND_CAP = 8192;     // candidates kept per row (certificate capacity)
+constexpr int CAND_CAP = 8192;     // candidates selected per row (certificate capacity)
 constexpr int SAMPLE_STRIDE = 200; // one sample per 200 keys: ~0.5% of the row
 constexpr int SAMPLE_OFFSET = 100; // samples at keys 100 mod 200
 constexpr int MAX_SAMPLES = 1024;  // per row; longer rows widen the stride
 constexpr int SELECT_THREADS = 512;
 constexpr int SELECT_CAP = 12288;  // candidates the standalone selector keeps in SMEM
 
-// MODE_STORE: fp32 scores to a matrix.  MODE_FILTER_SLOTS: a CTA scores whole
-// row pairs, candidate keys stay in shared memory and the CTA's TopK warps
-// select them.  MODE_FILTER_GLOBAL: row pairs are split into chunks across
-// CTAs and candidates are flushed to global buffers for a separate select.
-enum Mode : int { MODE_STORE = 0, MODE_FILTER_SLOTS = 1, MODE_FILTER_GLOBAL = 2 };
+// MODE_STORE: fp32 scores to a matrix.  MODE_FILTER: scores at or above the
+// row's threshold become candidates that the TopK warps select.
+enum Mode : int { MODE_STORE = 0, MODE_FILTER = 1 };
 
 // status word bits (per call)
 constexpr int ST_TIMEOUT = 1;
@@ -122,14 +120,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// Test (or wait for) completion of the phase with `parity`.  The suspend-time
+// hint lets the hardware park the thread until the phase completes (or the
+// hint elapses) instead of returning at once, so waiting warps take no issue
+// slots from the warps doing the work.
+constexpr uint32_t WAIT_SUSPEND_HINT_NS = 100000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(WAIT_SUSPEND_HINT_NS)
       : "memory");
   return ok != 0;
 }
@@ -205,6 +208,17 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(bar)
       : "memory");
 }
+// contiguous global -> shared copy by the TMA engine (16-byte aligned
+// addresses, size a multiple of 16), completing on an mbarrier
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// order generic-proxy global accesses before later async-proxy (TMA) ones
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 // generic-proxy writes to shared memory -> visible to the async proxy (MMA)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -271,6 +285,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 16 lanes x 64 columns: thread t receives, for each block m of 8 columns,
+// columns 8m + 2(t % 4) + {0, 1} of lanes base + t / 4 (r[4m], r[4m+1]) and
+// base + 8 + t / 4 (r[4m+2], r[4m+3]).
+__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// release / acquire at GPU scope on a global counter
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // ---------------------------------------------------- epilogue arithmetic --
 // ReLU on the FMA pipe: x * 2^-25 saturated to [0, 1] equals ReLU(x) * 2^-25

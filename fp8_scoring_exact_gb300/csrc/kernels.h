@@ -39,7 +39,6 @@ struct PlanParams {
   Group* groups;               // [G]
   int32_t* unit_start;         // [G + 1]
   int32_t* group_done;         // [G]
-  int32_t* cand_count;         // [R]
   const int32_t* failed_rows;  // repair mode input
   Stats* stats;
 };
@@ -66,19 +65,21 @@ struct ScoreParams {
   int K;
   int chunk_tiles;
   int repair;                  // which plan to read
-  int relu_alu8;               // heads (of every 8) whose ReLU uses the ALU pipe
   const float* q_scale;
   const float* w;
   const int32_t* rb;
   const int32_t* re;
   const Group* groups;
   const int32_t* unit_start;
-  // MODE_FILTER
+  // MODE_FILTER: unit c of a group leaves at most UCAP candidates of a row in
+  // region [c * UCAP, (c + 1) * UCAP) of that row's buffers
   const uint32_t* tau;
-  uint32_t* cand_key;          // [R, CAND_CAP]
-  int32_t* cand_idx;           // [R, CAND_CAP]
-  int32_t* cand_count;         // [R]
-  int32_t* group_done;         // [G]
+  uint32_t* cand_key;          // [R, cand_stride]
+  int32_t* cand_idx;           // [R, cand_stride]
+  int32_t* unit_count;         // [R, max_units]: candidates unit c left for the row
+  int64_t cand_stride;         // max_units * UCAP
+  int max_units;               // units per group, at most
+  int32_t* group_done;         // [G]: warpgroup-units finished (release / acquire)
   int32_t* failed_rows;        // [R]
   int32_t* out;                // [R, K]
   // MODE_STORE
@@ -87,20 +88,12 @@ struct ScoreParams {
   Stats* stats;
 };
 
-enum SelectSource : int { SELECT_FROM_SCORES = 0, SELECT_FROM_CANDIDATES = 1 };
-
 struct SelectParams {
   RowSpace rs;
   int K;
   int target16;
-  int source;                  // SelectSource
   int list_mode;               // 1: rows = failed_rows[0 .. stats->fail_count), score row f
   const int32_t* list;
-  // SELECT_FROM_CANDIDATES
-  const uint32_t* cand_key;    // [R, CAND_CAP]
-  const int32_t* cand_idx;
-  const int32_t* cand_count;
-  int32_t* failed_rows;
   const float* scores;
   int64_t ld;
   const int32_t* rb;
@@ -116,11 +109,14 @@ cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
                          const ScoreParams& p, int grid, cudaStream_t s);
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
 
-// number of query-row pairs (work groups) for a row space
-__host__ __device__ inline int n_pairs(const RowSpace& rs) {
-  if (!rs.paged) return (rs.R + 1) / 2;
-  const int per = (rs.next_n + 1) / 2;
+// number of work groups of G query rows for a row space
+template <int G>
+__host__ __device__ inline int n_row_groups(const RowSpace& rs) {
+  if (!rs.paged) return (rs.R + G - 1) / G;
+  const int per = (rs.next_n + G - 1) / G;
   return (rs.R / rs.next_n) * per;
 }
+__host__ __device__ inline int n_groups(const RowSpace& rs) { return n_row_groups<GROUP_ROWS>(rs); }
+__host__ __device__ inline int n_pairs(const RowSpace& rs) { return n_row_groups<SAMPLE_ROWS>(rs); }
 
 }  // namespace dsa

@@ -83,11 +83,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
       }
       p.rb[row] = b;
       p.re[row] = e;
-      p.cand_count[row] = 0;
     }
     if (bad) atomicOr(&p.stats->status, ST_RANGE);
     __syncthreads();
-    G = n_pairs(rs);
+    G = n_groups(rs);
   } else {
     G = p.stats->fail_count;
   }
@@ -102,11 +101,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
       grp.nrows = 0;
       grp.lo = 0x7fffffff;
       grp.hi = 0;
-      grp.row[0] = grp.row[1] = 0;
-      grp.slot[0] = grp.slot[1] = 0;
+      for (int i = 0; i < GROUP_ROWS; ++i) grp.row[i] = grp.slot[i] = 0;
       if (!p.repair) {
-        int rows[2];
-        const int nr = pair_rows(rs, g, rows);
+        int rows[GROUP_ROWS];
+        const int nr = rows_of_group<GROUP_ROWS>(rs, g, rows);
         grp.seq = rs.paged ? rows[0] / rs.next_n : -1;
         for (int i = 0; i < nr; ++i) {
           const int b = p.rb[rows[i]], e = p.re[rows[i]];
@@ -163,10 +161,10 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
 // as threshold the sample of descending rank ceil(m * target / L).
 constexpr int SAMPLE_THREADS = 128;
 constexpr uint32_t SM_OFF_Q = 0;
-constexpr uint32_t SM_OFF_K = SM_OFF_Q + GROUP_ROWS * H * D;        // 16384
+constexpr uint32_t SM_OFF_K = SM_OFF_Q + SAMPLE_ROWS * H * D;       // 16384
 constexpr uint32_t SM_OFF_SAMP = SM_OFF_K + TILE * D;               // 32768
-constexpr uint32_t SM_OFF_W = SM_OFF_SAMP + GROUP_ROWS * MAX_SAMPLES * 4;  // 40960
-constexpr uint32_t SM_OFF_SC = SM_OFF_W + GROUP_ROWS * H * 4;
+constexpr uint32_t SM_OFF_W = SM_OFF_SAMP + SAMPLE_ROWS * MAX_SAMPLES * 4;  // 40960
+constexpr uint32_t SM_OFF_SC = SM_OFF_W + SAMPLE_ROWS * H * 4;
 constexpr uint32_t SM_OFF_HIST = SM_OFF_SC + TILE * 4;
 constexpr uint32_t SM_OFF_MISC = SM_OFF_HIST + 256 * 4;
 // 64 KB per CTA keeps at most 3 CTAs (3 x 128 TMEM columns) on an SM
@@ -188,8 +186,8 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
   const int tid = threadIdx.x, warp = tid >> 5;
   const int K = p.K;
 
-  int rows[2];
-  const int nr = pair_rows(rs, blockIdx.x, rows);
+  int rows[SAMPLE_ROWS];
+  const int nr = rows_of_group<SAMPLE_ROWS>(rs, blockIdx.x, rows);
   int act[2], nact = 0, lo = 0x7fffffff, hi = 0, ntriv = 0;
   for (int i = 0; i < nr; ++i) {
     const int b = p.rb[rows[i]], e = p.re[rows[i]];
@@ -341,14 +339,12 @@ cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_
 }
 
 // ================================================================== select ==
-// Standalone exact top-K per row, one CTA per row at a time.  Two sources:
-//  - fp32 score rows: sampled threshold -> filter into shared memory (float4
-//    loads, one shared reservation per warp batch) -> radix select on the
-//    candidates; when the certificate fails (fewer than K or more than
-//    SELECT_CAP candidates) the radix select runs over the whole row;
-//  - candidate buffers of the split scorer (keys and indices of every score
-//    that reached the row's threshold): certificate check (K <= count <=
-//    CAND_CAP), then radix select; failing rows are queued for repair.
+// Standalone exact top-K of fp32 score rows, one CTA per row at a time:
+// sampled threshold -> filter into shared memory (float4 loads, one shared
+// reservation per warp) -> radix select on the candidates.  The certificate
+// holds for any threshold, so a failed filter (fewer than K or more than
+// SELECT_CAP candidates) retries with a relaxed threshold; when no threshold
+// separates the top K (massive ties) the radix select runs over the row.
 constexpr uint32_t SEL_OFF_KEY = 0;
 constexpr uint32_t SEL_OFF_IDX = SEL_OFF_KEY + SELECT_CAP * 4;
 constexpr uint32_t SEL_OFF_SAMP = SEL_OFF_IDX + SELECT_CAP * 4;
@@ -357,7 +353,6 @@ constexpr int SEL_CMP_CAP = 2048;
 constexpr uint32_t SEL_OFF_HIST = SEL_OFF_CMP + SEL_CMP_CAP * 4;
 constexpr uint32_t SEL_OFF_MISC = SEL_OFF_HIST + 256 * 4;
 constexpr uint32_t SELECT_SMEM = SEL_OFF_MISC + 64;
-static_assert(SELECT_CAP >= CAND_CAP, "candidate rows must fit the selector");
 
 __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectParams p) {
   extern __shared__ uint8_t smem[];
@@ -383,112 +378,86 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
       misc[5] = 0;
       misc[6] = 0;
     }
-    if (p.source == SELECT_FROM_CANDIDATES) {
-      // rows of the split scorer: L <= K rows were written by the remapping path
-      if (L <= K) continue;
-      const int n = p.cand_count[row];
-      if (n < K || n > CAND_CAP) {
-        if (tid == 0) {
-          const int fi = atomicAdd(&p.stats->fail_count, 1);
-          p.failed_rows[fi] = row;
-          atomicAdd(n < K ? &p.stats->underflow : &p.stats->overflow, 1);
-        }
-        continue;
-      }
-      const uint32_t* ck = p.cand_key + (int64_t)row * CAND_CAP;
-      const int32_t* ci = p.cand_idx + (int64_t)row * CAND_CAP;
-      for (int i = tid; i < n; i += SELECT_THREADS) ckey[i] = ck[i];
-      if (tid == 0) atomicAdd(&p.stats->cand_total, n);
-      __syncthreads();
-      uint32_t theta;
-      int rr;
-      group_radix_select([&](int i) { return ckey[i]; }, n, K, hist, misc, tid, SELECT_THREADS, 0, theta, rr, cmp,
-                         SEL_CMP_CAP);
-      group_emit([&](int i) { return ckey[i]; }, [&](int i) { return ci[i]; }, n, theta, rr, K, o, misc + 5, tid,
-                 SELECT_THREADS);
-      __syncthreads();
-      continue;
-    }
     if (L <= K) {
       write_all_valid(rs, row, b, e, K, p.out, tid, SELECT_THREADS);
       continue;
     }
     const float* srow = p.scores + (int64_t)(p.list_mode ? f : row) * p.ld;
 
-    // sampled threshold
+    // sampled threshold: the sample of descending rank `rk` (0 = every key)
     int first, m, S;
     sample_grid(b, e, &first, &m, &S);
     for (int j = tid; j < m; j += SELECT_THREADS) samp[j] = ordered_key(srow[first + j * S]);
     __syncthreads();
-    const int rank = sample_rank(m, L, target);
-    uint32_t tau = 0u;
-    if (m > 0 && rank >= 1 && rank <= m) {
+    auto tau_at_rank = [&](int rk) -> uint32_t {
+      if (m <= 0 || rk < 1 || rk > m) return 0u;
+      uint32_t t;
       int rr;
-      group_radix_select([&](int i) { return samp[i]; }, m, rank, hist, misc, tid, SELECT_THREADS, 0, tau, rr);
-    }
+      group_radix_select([&](int i) { return samp[i]; }, m, rk, hist, misc, tid, SELECT_THREADS, 0, t, rr);
+      return t;
+    };
 
     // compare-and-append: 4 items per thread per step, one shared atomic per warp
     const int a0 = min(e, (b + 3) & ~3);   // first 16-byte aligned index
     const int a1 = max(a0, e & ~3);        // end of the aligned body
-    auto append = [&](int cnt, const uint32_t* ks, const int* ids) {
-      int incl = cnt;
-#pragma unroll
-      for (int o2 = 1; o2 < 32; o2 <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o2);
-        if (lane >= o2) incl += y;
-      }
-      const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-      int base = 0;
-      if (lane == 31 && wtot) base = atomicAdd(&misc[4], wtot);
-      base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
-      for (int i = 0; i < cnt; ++i)
-        if (base + i < SELECT_CAP) {
-          ckey[base + i] = ks[i];
-          cidx[base + i] = ids[i];
-        }
-    };
-    // scalar head and tail (at most 3 + 3 elements), then the aligned body
-    if (tid < 32) {
-      const int nh = (a0 - b) + (e - a1);
-      uint32_t ks[1];
-      int ids[1];
-      int cnt = 0;
-      if (lane < nh) {
-        const int i = lane < (a0 - b) ? b + lane : a1 + (lane - (a0 - b));
-        const uint32_t k = ordered_key(srow[i]);
-        if (k >= tau) {
-          ks[0] = k;
-          ids[0] = i;
-          cnt = 1;
-        }
-      }
-      append(cnt, ks, ids);
-    }
+    const int nh = (a0 - b) + (e - a1);    // scalar head + tail (<= 6)
     const int nvec = (a1 - a0) >> 2;
     const float4* v4 = (const float4*)(srow + a0);
     const int rounds = ceil_div(nvec, SELECT_THREADS);
-    for (int rd = 0; rd < rounds; ++rd) {
-      const int vi = rd * SELECT_THREADS + tid;
-      uint32_t ks[4];
-      int ids[4];
-      int cnt = 0;
-      if (vi < nvec) {
-        const float4 x = __ldcs(&v4[vi]);
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t k = ordered_key(xs[c]);
-          if (k >= tau) {
-            ks[cnt] = k;
-            ids[cnt] = a0 + vi * 4 + c;
-            ++cnt;
-          }
-        }
+    // every key of [b, e) once: f(key, index, valid) on all lanes of a warp
+    auto visit_row = [&](auto&& f) {
+      if (tid < 32) {
+        const bool v = lane < nh;
+        const int i = !v ? b : (lane < (a0 - b) ? b + lane : a1 + (lane - (a0 - b)));
+        f(v ? ordered_key(srow[i]) : 0u, i, v);
       }
-      append(cnt, ks, ids);
+      for (int rd = 0; rd < rounds; ++rd) {
+        const int vi = rd * SELECT_THREADS + tid;
+        const bool v = vi < nvec;
+        const float4 x = v ? __ldcs(&v4[vi]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        f(ordered_key(x.x), a0 + vi * 4 + 0, v);
+        f(ordered_key(x.y), a0 + vi * 4 + 1, v);
+        f(ordered_key(x.z), a0 + vi * 4 + 2, v);
+        f(ordered_key(x.w), a0 + vi * 4 + 3, v);
+      }
+    };
+    uint32_t lt;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+    auto filter = [&](uint32_t tau) -> int {
+      if (tid == 0) misc[4] = 0;
+      __syncthreads();
+      visit_row([&](uint32_t k, int i, bool v) {
+        const bool pass = v && k >= tau;
+        const unsigned mp = __ballot_sync(0xffffffffu, pass);
+        if (!mp) return;
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&misc[4], __popc(mp));
+        base = __shfl_sync(0xffffffffu, base, 0) + __popc(mp & lt);
+        if (pass && base < SELECT_CAP) {
+          ckey[base] = k;
+          cidx[base] = i;
+        }
+      });
+      __syncthreads();
+      return misc[4];
+    };
+
+    // the certificate holds for any threshold: retry with a relaxed one when
+    // the first leaves fewer than K candidates or more than fit
+    int rk = sample_rank(m, L, target);
+    uint32_t tau = tau_at_rank(rk);
+    int n = filter(tau);
+    for (int att = 0; att < 3 && !(n >= K && n <= SELECT_CAP); ++att) {
+      if (n < K) {
+        if (tau == 0u) break;
+        rk *= 4;
+      } else {
+        if (rk <= 1) break;
+        rk = max(1, rk / 4);
+      }
+      tau = tau_at_rank(rk);
+      n = filter(tau);
     }
-    __syncthreads();
-    const int n = misc[4];
     uint32_t theta;
     int rr;
     if (n >= K && n <= SELECT_CAP) {
@@ -498,12 +467,44 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
                  [&](int i) { return rs.paged ? out_index(rs, row, cidx[i]) : cidx[i]; }, n, theta, rr, K, o,
                  misc + 5, tid, SELECT_THREADS);
     } else {
-      // certificate failed: exact radix select over the whole row
-      group_radix_select([&](int i) { return ordered_key(srow[b + i]); }, L, K, hist, misc, tid, SELECT_THREADS, 0,
-                         theta, rr, cmp, SEL_CMP_CAP);
-      group_emit([&](int i) { return ordered_key(srow[b + i]); },
-                 [&](int i) { return rs.paged ? out_index(rs, row, b + i) : b + i; }, L, theta, rr, K, o, misc + 5,
-                 tid, SELECT_THREADS);
+      // no threshold separates the top K (massive ties): four radix passes
+      // over the whole row, then emission
+      uint32_t prefix = 0, mask = 0;
+      int rem = K;
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int bb = tid; bb < 256; bb += SELECT_THREADS) hist[bb] = 0;
+        __syncthreads();
+        visit_row([&](uint32_t k, int, bool v) {
+          hist_add(v && (k & mask) == prefix, (k >> shift) & 0xFFu, lane, hist);
+        });
+        __syncthreads();
+        if (tid < 32) radix_pick_digit(hist, rem, misc);
+        __syncthreads();
+        prefix |= (uint32_t)misc[0] << shift;
+        mask |= 0xFFu << shift;
+        rem = misc[1];
+        __syncthreads();
+      }
+      theta = prefix;
+      rr = rem;
+      visit_row([&](uint32_t k, int i, bool v) {
+        const bool gt = v && k > theta, eq = v && k == theta;
+        const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
+        int bg = 0, be = 0;
+        if (lane == 0) {
+          if (mg) bg = atomicAdd(&misc[5], __popc(mg));
+          if (me) be = atomicAdd(&misc[6], __popc(me));
+        }
+        bg = __shfl_sync(0xffffffffu, bg, 0);
+        be = __shfl_sync(0xffffffffu, be, 0);
+        if (gt) o[bg + __popc(mg & lt)] = rs.paged ? out_index(rs, row, i) : i;
+        if (eq) {
+          const int q2 = be + __popc(me & lt);
+          if (q2 < rr) o[K - rr + q2] = rs.paged ? out_index(rs, row, i) : i;
+        }
+      });
     }
     __syncthreads();
   }

@@ -195,13 +195,12 @@ DSA_API int dsa_indexer_last_repaired_rows(dsa_stream_t stream, int32_t* rows_ou
 
 /* Tuning and diagnostics (process-wide; take effect on the next call). */
 typedef enum {
-  DSA_OPT_CHUNK_TILES = 1,    /* 128-key tiles per work unit of the persistent scorer (default 64) */
+  DSA_OPT_CHUNK_TILES = 1,    /* 128-key tiles per work unit of the persistent scorer (default 64); each unit may
+                                 leave at most 1024 candidates per row (more fails the certificate -> repair) */
   DSA_OPT_TAU_BIAS = 2,       /* added to every sampled threshold key: >0 forces underflow, <0 overflow (test knob; default 0) */
   DSA_OPT_PROFILE = 3,        /* 1: time the main kernel of each call with CUDA events (default 0) */
   DSA_OPT_GRID_CTAS = 4,      /* CTAs of the persistent kernels (default: SM count) */
-  DSA_OPT_SAMPLE_TARGET = 5,  /* candidates the threshold aims at, in units of K/16 (default 32 = 2K) */
-  DSA_OPT_RELU_ALU8 = 6,      /* epilogue ReLU: heads of every 8 on the ALU pipe, rest on the FMA pipe (0, 2, 4, 8; default 0) */
-  DSA_OPT_FUSED_MODE = 7      /* 0 auto, 1 whole row pairs per CTA with in-kernel TopK, 2 chunks split across CTAs + separate select */
+  DSA_OPT_SAMPLE_TARGET = 5   /* candidates the threshold aims at, in units of K/16 (default 32 = 2K) */
 } dsa_option;
 DSA_API int dsa_indexer_set_option(int option, int64_t value);
 DSA_API int64_t dsa_indexer_get_option(int option);
