@@ -36,7 +36,7 @@ std::atomic<int64_t> g_launches{0};
 
 // ----------------------------------------------------------------- arena ----
 struct Layout {
-  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, group_done, unit_count, failed;
+  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, unit_count, failed;
   size_t cand_key, cand_idx, scores, total;
 };
 
@@ -60,8 +60,7 @@ Layout make_layout(int64_t R, int64_t G, int64_t cand_stride, int64_t max_units,
   L.unit_start = take((G + 1) * 4);
   L.rgroups = take(R * sizeof(Group));
   L.runit_start = take((R + 1) * 4);
-  L.group_done = take(G * 4);
-  L.unit_count = take((size_t)R * max_units * 4);
+  L.unit_count = take((size_t)R * max_units * 4 * 4);
   L.failed = take(R * 4);
   L.cand_key = take((size_t)R * cand_stride * 4);
   L.cand_idx = take((size_t)R * cand_stride * 4);
@@ -146,18 +145,6 @@ bool tmap_rows_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tmap_f32_1d(CUtensorMap* m, const float* base, uint64_t n, uint32_t box) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[1] = {(cuuint64_t)n};
-  cuuint64_t strides[1] = {0};
-  cuuint32_t boxd[1] = {box};
-  cuuint32_t estr[1] = {1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(base), dims, strides, boxd, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int sm_count() {
@@ -193,9 +180,9 @@ Opts read_opts() {
 }
 
 // ------------------------------------------------- shared launch sequence --
-// Fused pipeline over a row space whose keys are described by tm_k / tm_ks.
-int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-              const CUtensorMap& tm_ks, const uint8_t* k_raw, const float* ks_raw, const float* q_scale,
+// Fused pipeline over a row space whose keys are described by tm_k.
+int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensorMap& tm_k, const uint8_t* k_raw,
+              const float* ks_raw, const float* q_scale,
               const float* w, const int32_t* row_begin, const int32_t* row_end, int32_t* out, cudaStream_t stream) {
   const Opts o = read_opts();
   const int G = n_groups(rs);
@@ -221,7 +208,6 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   pp.re = at<int32_t>(a, L.re);
   pp.groups = at<Group>(a, L.groups);
   pp.unit_start = at<int32_t>(a, L.unit_start);
-  pp.group_done = at<int32_t>(a, L.group_done);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = st;
   DSA_LAUNCH(launch_plan(pp, stream));
@@ -245,9 +231,9 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   ScoreParams cp{};
   cp.rs = rs;
   cp.mode = MODE_FILTER;
-  cp.K = K;
   cp.chunk_tiles = o.chunk;
   cp.repair = 0;
+  cp.k_scale = ks_raw;
   cp.q_scale = q_scale;
   cp.w = w;
   cp.rb = pp.rb;
@@ -260,14 +246,26 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cp.unit_count = at<int32_t>(a, L.unit_count);
   cp.cand_stride = cand_stride;
   cp.max_units = max_units;
-  cp.group_done = pp.group_done;
-  cp.failed_rows = at<int32_t>(a, L.failed);
-  cp.out = out;
   cp.stats = st;
   a->profiled = o.profile;
   if (o.profile) cudaEventRecord(a->ev0, stream);
-  DSA_LAUNCH(launch_score(tm_q, tm_k, tm_ks, cp, o.grid, stream));
+  DSA_LAUNCH(launch_score(tm_q, tm_k, cp, o.grid, stream));
   if (o.profile) cudaEventRecord(a->ev1, stream);
+
+  CandParams cs{};
+  cs.rs = rs;
+  cs.K = K;
+  cs.groups = pp.groups;
+  cs.unit_start = pp.unit_start;
+  cs.unit_count = cp.unit_count;
+  cs.cand_key = cp.cand_key;
+  cs.cand_idx = cp.cand_idx;
+  cs.cand_stride = cand_stride;
+  cs.max_units = max_units;
+  cs.failed_rows = at<int32_t>(a, L.failed);
+  cs.out = out;
+  cs.stats = st;
+  DSA_LAUNCH(launch_cand_select(cs, 3 * o.grid, stream));
 
   // exact repair of rows whose certificate failed
   PlanParams rp = pp;
@@ -283,7 +281,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   rcp.unit_start = rp.unit_start;
   rcp.scores = at<float>(a, L.scores);
   rcp.ld = ld;
-  DSA_LAUNCH(launch_score(tm_q, tm_k, tm_ks, rcp, o.grid, stream));
+  DSA_LAUNCH(launch_score(tm_q, tm_k, rcp, o.grid, stream));
 
   SelectParams sel{};
   sel.rs = rs;
@@ -356,14 +354,12 @@ int dsa_indexer_topk(const uint8_t* q_fp8, const float* q_scale, const uint8_t* 
   if (rc != DSA_OK) return rc;
   if (!out_idx || K < 1 || K > DSA_MAX_K) return DSA_ERR_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  CUtensorMap tq, tk, tks;
-  if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)Q * H, H) || !tmap_rows_u8(&tk, k_fp8, N, TILE) ||
-      !tmap_f32_1d(&tks, k_scale, N, TILE))
-    return DSA_ERR_CUDA;
+  CUtensorMap tq, tk;
+  if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)Q * H, H) || !tmap_rows_u8(&tk, k_fp8, N, TILE)) return DSA_ERR_CUDA;
   RowSpace rs{};
   rs.R = Q;
   rs.N = N;
-  return run_fused(rs, K, tq, tk, tks, k_fp8, k_scale, q_scale, w, row_begin, row_end, out_idx, stream);
+  return run_fused(rs, K, tq, tk, k_fp8, k_scale, q_scale, w, row_begin, row_end, out_idx, stream);
 }
 
 int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_cache,
@@ -379,10 +375,9 @@ int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uin
       (int64_t)num_pages * PAGE >= (1ll << 31))
     return DSA_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  CUtensorMap tq, tk, tks;
+  CUtensorMap tq, tk;
   if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)R * H, H) ||
-      !tmap_rows_u8(&tk, k_cache, (uint64_t)num_pages * PAGE, PAGE) ||
-      !tmap_f32_1d(&tks, k_cache_scale, (uint64_t)num_pages * PAGE, PAGE))
+      !tmap_rows_u8(&tk, k_cache, (uint64_t)num_pages * PAGE, PAGE))
     return DSA_ERR_CUDA;
   RowSpace rs{};
   rs.R = (int)R;
@@ -393,7 +388,7 @@ int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uin
   rs.max_pages = max_pages;
   rs.next_n = next_n;
   rs.num_pages = num_pages;
-  return run_fused(rs, K, tq, tk, tks, k_cache, k_cache_scale, q_scale, w, nullptr, nullptr, out_idx, stream);
+  return run_fused(rs, K, tq, tk, k_cache, k_cache_scale, q_scale, w, nullptr, nullptr, out_idx, stream);
 }
 
 static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
@@ -401,10 +396,8 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
                        float* scores, int64_t ld, int32_t* out_idx, cudaStream_t stream) {
   // out_idx == nullptr: scores only (every non-empty row is scored)
   const Opts o = read_opts();
-  CUtensorMap tq, tk, tks;
-  if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)Q * H, H) || !tmap_rows_u8(&tk, k_fp8, N, TILE) ||
-      !tmap_f32_1d(&tks, k_scale, N, TILE))
-    return DSA_ERR_CUDA;
+  CUtensorMap tq, tk;
+  if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)Q * H, H) || !tmap_rows_u8(&tk, k_fp8, N, TILE)) return DSA_ERR_CUDA;
   RowSpace rs{};
   rs.R = Q;
   rs.N = N;
@@ -430,7 +423,6 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   pp.re = at<int32_t>(a, L.re);
   pp.groups = at<Group>(a, L.groups);
   pp.unit_start = at<int32_t>(a, L.unit_start);
-  pp.group_done = at<int32_t>(a, L.group_done);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = st;
   DSA_LAUNCH(launch_plan(pp, stream));
@@ -438,8 +430,8 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   ScoreParams cp{};
   cp.rs = rs;
   cp.mode = MODE_STORE;
-  cp.K = K;
   cp.chunk_tiles = o.chunk;
+  cp.k_scale = k_scale;
   cp.q_scale = q_scale;
   cp.w = w;
   cp.rb = pp.rb;
@@ -451,7 +443,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   cp.stats = st;
   a->profiled = o.profile;
   if (o.profile) cudaEventRecord(a->ev0, stream);
-  DSA_LAUNCH(launch_score(tq, tk, tks, cp, o.grid, stream));
+  DSA_LAUNCH(launch_score(tq, tk, cp, o.grid, stream));
   if (o.profile) cudaEventRecord(a->ev1, stream);
   if (!out_idx) return DSA_OK;
 
@@ -514,7 +506,6 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   pp.re = at<int32_t>(a, L.re);
   pp.groups = at<Group>(a, L.groups);
   pp.unit_start = at<int32_t>(a, L.unit_start);
-  pp.group_done = at<int32_t>(a, L.group_done);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = at<Stats>(a, L.stats);
   DSA_LAUNCH(launch_plan(pp, stream));
@@ -562,7 +553,6 @@ int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const 
   pp.re = reinterpret_cast<int32_t*>(base + L.re);
   pp.groups = reinterpret_cast<Group*>(base + L.groups);
   pp.unit_start = reinterpret_cast<int32_t*>(base + L.unit_start);
-  pp.group_done = reinterpret_cast<int32_t*>(base + L.group_done);
   pp.failed_rows = reinterpret_cast<int32_t*>(base + L.failed);
   pp.stats = reinterpret_cast<Stats*>(base + L.stats);
   DSA_LAUNCH(launch_plan(pp, stream));

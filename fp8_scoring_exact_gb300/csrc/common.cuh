@@ -21,20 +21,19 @@ constexpr int SAMPLE_ROWS = 2;     // query rows per CTA of the threshold-sampli
 constexpr int PAGE = 64;           // tokens per paged-cache page
 
 // ------------------------------------------------------- persistent scorer --
-constexpr int STAGES = 5;          // key-tile ring depth (TMA -> MMA)
-constexpr int SC_STAGES = 8;       // key-scale ring depth (TMA -> epilogue)
+constexpr int STAGES = 6;          // key-tile ring depth (TMA -> MMA)
 constexpr int ACC_BUFS = 2;        // TMEM accumulators (MMA -> epilogue)
 constexpr int ACC_COLS = 256;      // TMEM columns per accumulator (4 rows x 64 heads)
-constexpr int TOPK_QUEUE = 4;      // finished groups handed to the TopK warps
 constexpr int EPI_WGS = GROUP_ROWS; // epilogue warpgroups: one per row of the group
 constexpr int EPI_THREADS = EPI_WGS * 128;
-constexpr int TOPK_THREADS = 64;
-constexpr int SCORE_THREADS = 128 + EPI_THREADS;  // warps 0-3: TMA, MMA, 2 TopK; then epilogue
-constexpr int UCAP = 1024;         // candidates one work unit may leave for one row
-constexpr int TOPK_CMP_CAP = 1024; // keys of the K-th key's bucket the TopK warps compact
+constexpr int SCORE_THREADS = 64 + EPI_THREADS;  // warp 0: TMA, warp 1: MMA; then the epilogue
+constexpr int UCAP = 1024;         // candidates one work unit may leave for one row ...
+constexpr int WCAP = UCAP / 4;     // ... in four regions, one per epilogue warp (TMEM lane quarter)
 
 // -------------------------------------------------------------- selection --
 constexpr int CAND_CAP = 8192;     // candidates selected per row (certificate capacity)
+constexpr int CAND_THREADS = 256;  // candidate selector: threads per CTA
+constexpr int CAND_MAX_REGIONS = 1024;  // regions (units x 4) one row may have
 constexpr int SAMPLE_STRIDE = 200; // one sample per 200 keys: ~0.5% of the row
 constexpr int SAMPLE_OFFSET = 100; // samples at keys 100 mod 200
 constexpr int MAX_SAMPLES = 1024;  // per row; longer rows widen the stride
@@ -42,7 +41,7 @@ constexpr int SELECT_THREADS = 512;
 constexpr int SELECT_CAP = 12288;  // candidates the standalone selector keeps in SMEM
 
 // MODE_STORE: fp32 scores to a matrix.  MODE_FILTER: scores at or above the
-// row's threshold become candidates that the TopK warps select.
+// row's threshold become candidates for the candidate selector.
 enum Mode : int { MODE_STORE = 0, MODE_FILTER = 1 };
 
 // status word bits (per call)
@@ -120,19 +119,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-// Test (or wait for) completion of the phase with `parity`.  The suspend-time
-// hint lets the hardware park the thread until the phase completes (or the
-// hint elapses) instead of returning at once, so waiting warps take no issue
-// slots from the warps doing the work.
-constexpr uint32_t WAIT_SUSPEND_HINT_NS = 100000;
+// Test (or briefly wait for) completion of the phase with `parity`.  An
+// explicit suspend-time hint was measured and made the scorer slower, so the
+// system default window is used.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(WAIT_SUSPEND_HINT_NS)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -143,10 +140,10 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
 // Bounded wait: true when the phase with `parity` completed; false when the
 // CTA-wide abort flag is set or the time limit passed (then it sets both the
-// abort flag and the status bit).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// abort flag and the status bit).  The polling loop is out of line: the hot
+// loops only pay for one test when the phase has already completed.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            int* status) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -160,12 +157,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
   }
 }
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, status);
+}
 
 // Warp-uniform bounded wait: every lane polls (so every lane acquires the
 // phase) and every lane returns the same value, so code after it that needs
 // a converged warp (tcgen05.ld .sync.aligned, shuffles) never diverges.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               int* status) {
+static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                 int* status) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     const bool done = mbar_try_wait(bar, parity);
@@ -189,6 +191,21 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
       if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int* status) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return mbar_wait_warp_slow(bar, parity, abort_flag, status);
+}
+
+// One arrival per warp, from the lane elect.sync picks (the warp must be
+// converged); no branch around it.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
+      : "memory");
 }
 
 // ------------------------------------------------------------------- TMA ----
@@ -333,6 +350,12 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
   return r;
 }
+// a * b on two fp32 lanes
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 // acc += a * b on two fp32 lanes (sm_100+ packed FMA)
 __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
@@ -370,7 +393,6 @@ __device__ __forceinline__ void radix_pick_digit(const int* hist, int rem, int* 
     int acc = excl;
     int digit = 255 - 8 * lane - 7;
     int r = rem - acc;
-#pragma unroll
     int cnt = c[7];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

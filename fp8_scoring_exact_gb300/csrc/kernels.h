@@ -38,7 +38,6 @@ struct PlanParams {
   int32_t* re;
   Group* groups;               // [G]
   int32_t* unit_start;         // [G + 1]
-  int32_t* group_done;         // [G]
   const int32_t* failed_rows;  // repair mode input
   Stats* stats;
 };
@@ -62,29 +61,44 @@ struct SampleParams {
 struct ScoreParams {
   RowSpace rs;
   int mode;                    // MODE_STORE or MODE_FILTER
-  int K;
   int chunk_tiles;
   int repair;                  // which plan to read
+  const float* k_scale;        // dense [N] or paged [P * 64]; read by the epilogue
   const float* q_scale;
   const float* w;
   const int32_t* rb;
   const int32_t* re;
   const Group* groups;
   const int32_t* unit_start;
-  // MODE_FILTER: unit c of a group leaves at most UCAP candidates of a row in
-  // region [c * UCAP, (c + 1) * UCAP) of that row's buffers
+  // MODE_FILTER: epilogue warp q of unit c leaves at most WCAP candidates of
+  // a row in region (4 c + q) of that row's buffers
   const uint32_t* tau;
   uint32_t* cand_key;          // [R, cand_stride]
   int32_t* cand_idx;           // [R, cand_stride]
-  int32_t* unit_count;         // [R, max_units]: candidates unit c left for the row
+  int32_t* unit_count;         // [R, max_units, 4]: candidates region (c, q) holds (WCAP + 1: lost some)
   int64_t cand_stride;         // max_units * UCAP
   int max_units;               // units per group, at most
-  int32_t* group_done;         // [G]: warpgroup-units finished (release / acquire)
-  int32_t* failed_rows;        // [R]
-  int32_t* out;                // [R, K]
   // MODE_STORE
   float* scores;               // [slots, ld]
   int64_t ld;
+  Stats* stats;
+};
+
+// Candidate selector: exact top-K of each planned row from the candidate
+// regions the filter left, with the certificate (K <= n, nothing lost,
+// n <= CAND_CAP); rows that fail it are queued for repair.
+struct CandParams {
+  RowSpace rs;
+  int K;
+  const Group* groups;
+  const int32_t* unit_start;
+  const int32_t* unit_count;
+  const uint32_t* cand_key;
+  const int32_t* cand_idx;
+  int64_t cand_stride;
+  int max_units;
+  int32_t* failed_rows;        // [R] (appended, count in stats->fail_count)
+  int32_t* out;                // [R, K]
   Stats* stats;
 };
 
@@ -105,9 +119,10 @@ struct SelectParams {
 // host launchers (return cudaGetLastError() of the launch)
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_pairs, cudaStream_t s);
-cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_ks,
-                         const ScoreParams& p, int grid, cudaStream_t s);
+cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
+                         cudaStream_t s);
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
+cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s);
 
 // number of work groups of G query rows for a row space
 template <int G>

@@ -116,7 +116,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
             grp.hi = max(grp.hi, e);
           }
         }
-        p.group_done[g] = 0;
       } else {
         const int row = p.failed_rows[g];
         grp.nrows = 1;
@@ -508,6 +507,126 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
     }
     __syncthreads();
   }
+}
+
+// ======================================================== candidate select ==
+// Exact top-K of each planned row from the candidates the filter left
+// ("Fusing Indexer Scoring and Exact Top-k for DeepSeek-V3.2", section 3.2:
+// every key at or above the threshold is a candidate, and when there are at
+// least K of them the top K of the candidates are the top K of the row).
+// One CTA per (group, row) item at a time: certificate over the region
+// counts, gather of the regions into shared memory, radix select, emission.
+constexpr uint32_t CS_OFF_KEY = 0;
+constexpr uint32_t CS_OFF_IDX = CS_OFF_KEY + CAND_CAP * 4;
+constexpr uint32_t CS_OFF_OFF = CS_OFF_IDX + CAND_CAP * 4;
+constexpr uint32_t CS_OFF_HIST = CS_OFF_OFF + (CAND_MAX_REGIONS + 1) * 4;
+constexpr uint32_t CS_OFF_MISC = CS_OFF_HIST + 256 * 4;
+constexpr uint32_t CAND_SMEM = CS_OFF_MISC + 32 * 4;
+constexpr int CS_PER_THREAD = CAND_MAX_REGIONS / CAND_THREADS;  // regions scanned per thread
+static_assert(CAND_MAX_REGIONS % CAND_THREADS == 0, "region scan");
+
+__global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* ckey = (uint32_t*)(smem + CS_OFF_KEY);
+  int32_t* cidx = (int32_t*)(smem + CS_OFF_IDX);
+  int* off = (int*)(smem + CS_OFF_OFF);     // region start offsets, [nreg] = total
+  int* hist = (int*)(smem + CS_OFF_HIST);
+  int* misc = (int*)(smem + CS_OFF_MISC);   // [0..3] digits, [4..5] emit counters, [8..15] warp sums, [16] lost
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NWARPS = CAND_THREADS / 32;
+  const int K = p.K;
+  const int items = p.stats->n_groups * GROUP_ROWS;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int g = it / GROUP_ROWS, r = it % GROUP_ROWS;
+    const Group* gp = p.groups + g;
+    if (r >= gp->nrows) continue;  // uniform over the CTA
+    const int row = gp->row[r];
+    const int nreg = (p.unit_start[g + 1] - p.unit_start[g]) * 4;
+    const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * 4;
+    // certificate: region counts (WCAP + 1 = lost candidates), exclusive scan
+    int c[CS_PER_THREAD];
+    int tsum = 0;
+    bool lost = nreg > CAND_MAX_REGIONS;
+#pragma unroll
+    for (int i = 0; i < CS_PER_THREAD; ++i) {
+      const int j = tid * CS_PER_THREAD + i;
+      const int x = j < nreg && j < CAND_MAX_REGIONS ? __ldcg(&cnt[j]) : 0;
+      lost |= x > WCAP;
+      c[i] = min(x, WCAP);
+      tsum += c[i];
+    }
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const bool any_lost = __syncthreads_or(lost);
+    if (lane == 31) misc[8 + warp] = incl;
+    if (tid == 0) {
+      misc[4] = 0;
+      misc[5] = 0;
+    }
+    __syncthreads();
+    int wbase = 0, n = 0;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) {
+      const int ws = misc[8 + w];
+      wbase += w < warp ? ws : 0;
+      n += ws;
+    }
+    int run = wbase + incl - tsum;
+#pragma unroll
+    for (int i = 0; i < CS_PER_THREAD; ++i) {
+      const int j = tid * CS_PER_THREAD + i;
+      if (j < CAND_MAX_REGIONS) off[j] = run;
+      run += c[i];
+    }
+    if (n < K || any_lost || n > CAND_CAP) {
+      if (tid == 0) {
+        const int f = atomicAdd(&p.stats->fail_count, 1);
+        p.failed_rows[f] = row;
+        atomicAdd(n < K ? &p.stats->underflow : &p.stats->overflow, 1);
+      }
+      __syncthreads();
+      continue;
+    }
+    __syncthreads();
+    // gather: warp w copies regions w, w + NWARPS, ... (coalesced 128-byte rows)
+    const uint32_t* ck = p.cand_key + (int64_t)row * p.cand_stride;
+    const int32_t* ci = p.cand_idx + (int64_t)row * p.cand_stride;
+    for (int j = warp; j < nreg; j += NWARPS) {
+      const int o = off[j], x = min(__ldcg(&cnt[j]), WCAP);
+      for (int i = lane; i < x; i += 32) {
+        ckey[o + i] = __ldcg(&ck[(int64_t)j * WCAP + i]);
+        cidx[o + i] = __ldcg(&ci[(int64_t)j * WCAP + i]);
+      }
+    }
+    // key 0 pads the list to a multiple of 4 (every real key is non-zero)
+    const int n4 = (n + 3) >> 2;
+    if (tid < 4 * n4 - n) {
+      ckey[n + tid] = 0u;
+      cidx[n + tid] = -1;
+    }
+    if (tid == 0) atomicAdd(&p.stats->cand_total, n);
+    __syncthreads();
+    uint32_t theta;
+    int rr;
+    group_radix_select4(ckey, n4, K, hist, misc, tid, CAND_THREADS, 0, theta, rr);
+    group_emit4(ckey, cidx, n4, theta, rr, K, p.out + (int64_t)row * K, misc + 4, tid, CAND_THREADS);
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(cand_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CAND_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cand_select_kernel<<<grid, CAND_THREADS, CAND_SMEM, s>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s) {
