@@ -516,12 +516,17 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
 // least K of them the top K of the candidates are the top K of the row).
 // One CTA per (group, row) item at a time: certificate over the region
 // counts, gather of the regions into shared memory, radix select, emission.
+constexpr uint32_t cs_align16(uint32_t x) { return (x + 15u) & ~15u; }
 constexpr uint32_t CS_OFF_KEY = 0;
 constexpr uint32_t CS_OFF_IDX = CS_OFF_KEY + CAND_CAP * 4;
 constexpr uint32_t CS_OFF_OFF = CS_OFF_IDX + CAND_CAP * 4;
-constexpr uint32_t CS_OFF_HIST = CS_OFF_OFF + (CAND_MAX_REGIONS + 1) * 4;
-constexpr uint32_t CS_OFF_MISC = CS_OFF_HIST + 256 * 4;
-constexpr uint32_t CAND_SMEM = CS_OFF_MISC + 32 * 4;
+constexpr uint32_t CS_OFF_HIST = cs_align16(CS_OFF_OFF + CAND_MAX_REGIONS * 4);
+constexpr uint32_t CS_OFF_MISC = cs_align16(CS_OFF_HIST + 256 * 4);
+constexpr uint32_t CS_OFF_BAR = cs_align16(CS_OFF_MISC + 32 * 4);
+constexpr uint32_t CAND_SMEM = CS_OFF_BAR + 16;
+// bulk-copy destinations and uint4 reads need 16 bytes, the mbarrier 8
+static_assert(CS_OFF_IDX % 16 == 0 && CS_OFF_HIST % 16 == 0 && CS_OFF_MISC % 16 == 0 && CS_OFF_BAR % 16 == 0,
+              "candidate selector layout");
 constexpr int CS_PER_THREAD = CAND_MAX_REGIONS / CAND_THREADS;  // regions scanned per thread
 static_assert(CAND_MAX_REGIONS % CAND_THREADS == 0, "region scan");
 
@@ -529,13 +534,22 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* ckey = (uint32_t*)(smem + CS_OFF_KEY);
   int32_t* cidx = (int32_t*)(smem + CS_OFF_IDX);
-  int* off = (int*)(smem + CS_OFF_OFF);     // region start offsets, [nreg] = total
+  int* off = (int*)(smem + CS_OFF_OFF);     // region start offsets (regions padded to 4 entries)
   int* hist = (int*)(smem + CS_OFF_HIST);
-  int* misc = (int*)(smem + CS_OFF_MISC);   // [0..3] digits, [4..5] emit counters, [8..15] warp sums, [16] lost
+  // [0..3] digits, [4..5] emit counters, [6] gather verdict, [7] abort flag, [8..15] warp sums
+  int* misc = (int*)(smem + CS_OFF_MISC);
+  const uint32_t bar = smem_u32(smem + CS_OFF_BAR);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWARPS = CAND_THREADS / 32;
   const int K = p.K;
   const int items = p.stats->n_groups * GROUP_ROWS;
+  if (tid == 0) {
+    misc[7] = 0;
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int g = it / GROUP_ROWS, r = it % GROUP_ROWS;
     const Group* gp = p.groups + g;
@@ -543,9 +557,10 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
     const int row = gp->row[r];
     const int nreg = (p.unit_start[g + 1] - p.unit_start[g]) * 4;
     const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * 4;
-    // certificate: region counts (WCAP + 1 = lost candidates), exclusive scan
+    // certificate over the region counts (WCAP + 1 = candidates were lost),
+    // and an exclusive scan of the 4-padded counts
     int c[CS_PER_THREAD];
-    int tsum = 0;
+    int tpad = 0, treal = 0;
     bool lost = nreg > CAND_MAX_REGIONS;
 #pragma unroll
     for (int i = 0; i < CS_PER_THREAD; ++i) {
@@ -553,68 +568,91 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
       const int x = j < nreg && j < CAND_MAX_REGIONS ? __ldcg(&cnt[j]) : 0;
       lost |= x > WCAP;
       c[i] = min(x, WCAP);
-      tsum += c[i];
+      treal += c[i];
+      tpad += (c[i] + 3) & ~3;
     }
-    int incl = tsum;
+    int incl = tpad;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
+    const int wreal = __reduce_add_sync(0xffffffffu, treal);
     const bool any_lost = __syncthreads_or(lost);
     if (lane == 31) misc[8 + warp] = incl;
+    if (lane == 0) misc[16 + warp] = wreal;
     if (tid == 0) {
       misc[4] = 0;
       misc[5] = 0;
     }
     __syncthreads();
-    int wbase = 0, n = 0;
+    int wbase = 0, npad = 0, n = 0;
 #pragma unroll
     for (int w = 0; w < NWARPS; ++w) {
       const int ws = misc[8 + w];
       wbase += w < warp ? ws : 0;
-      n += ws;
+      npad += ws;
+      n += misc[16 + w];
     }
-    int run = wbase + incl - tsum;
+    int run = wbase + incl - tpad;
 #pragma unroll
     for (int i = 0; i < CS_PER_THREAD; ++i) {
       const int j = tid * CS_PER_THREAD + i;
       if (j < CAND_MAX_REGIONS) off[j] = run;
-      run += c[i];
+      run += (c[i] + 3) & ~3;
     }
-    if (n < K || any_lost || n > CAND_CAP) {
+    if (n < K || any_lost || npad > CAND_CAP) {
       if (tid == 0) {
         const int f = atomicAdd(&p.stats->fail_count, 1);
         p.failed_rows[f] = row;
+        misc[6] = f;
         atomicAdd(n < K ? &p.stats->underflow : &p.stats->overflow, 1);
       }
+      __syncthreads();
+      // the repair's radix histogram of this list entry starts from zero
+      const int f = misc[6];
+      for (int i = tid; i < 256; i += CAND_THREADS) p.wide_hist[(int64_t)f * 256 + i] = 0;
       __syncthreads();
       continue;
     }
     __syncthreads();
-    // gather: warp w copies regions w, w + NWARPS, ... (coalesced 128-byte rows)
+    // gather: one bulk copy per non-empty region and array, issued by warp 0
     const uint32_t* ck = p.cand_key + (int64_t)row * p.cand_stride;
     const int32_t* ci = p.cand_idx + (int64_t)row * p.cand_stride;
-    for (int j = warp; j < nreg; j += NWARPS) {
-      const int o = off[j], x = min(__ldcg(&cnt[j]), WCAP);
-      for (int i = lane; i < x; i += 32) {
-        ckey[o + i] = __ldcg(&ck[(int64_t)j * WCAP + i]);
-        cidx[o + i] = __ldcg(&ci[(int64_t)j * WCAP + i]);
+    if (warp == 0) {
+      fence_proxy_async_smem();  // the previous item's reads of these buffers come first
+      if (lane == 0) mbar_arrive_expect_tx(bar, 2u * npad * 4u);
+      __syncwarp();
+      for (int j = lane; j < nreg; j += 32) {
+        const uint32_t bytes = (uint32_t)((min(__ldcg(&cnt[j]), WCAP) + 3) & ~3) * 4u;
+        if (bytes) {
+          bulk_g2s(smem_u32(ckey + off[j]), ck + (int64_t)j * WCAP, bytes, bar);
+          bulk_g2s(smem_u32(cidx + off[j]), ci + (int64_t)j * WCAP, bytes, bar);
+        }
       }
+      if (lane == 0) misc[6] = mbar_wait(bar, phase & 1, (volatile int*)&misc[7], &p.stats->status) ? 1 : 0;
+      __syncwarp();
     }
-    // key 0 pads the list to a multiple of 4 (every real key is non-zero)
-    const int n4 = (n + 3) >> 2;
-    if (tid < 4 * n4 - n) {
-      ckey[n + tid] = 0u;
-      cidx[n + tid] = -1;
+    ++phase;
+    __syncthreads();
+    if (!misc[6]) break;  // the copies did not land in time (status records it)
+    // key 0 in the pad slots (they hold whatever the regions held there)
+    for (int j = tid; j < nreg; j += CAND_THREADS) {
+      const int x = min(__ldcg(&cnt[j]), WCAP);
+      for (int i = x; i < ((x + 3) & ~3); ++i) ckey[off[j] + i] = 0u;
     }
     if (tid == 0) atomicAdd(&p.stats->cand_total, n);
     __syncthreads();
     uint32_t theta;
     int rr;
-    group_radix_select4(ckey, n4, K, hist, misc, tid, CAND_THREADS, 0, theta, rr);
-    group_emit4(ckey, cidx, n4, theta, rr, K, p.out + (int64_t)row * K, misc + 4, tid, CAND_THREADS);
+    group_radix_select4(ckey, npad >> 2, K, hist, misc, tid, CAND_THREADS, 0, theta, rr);
+    group_emit4(ckey, cidx, npad >> 2, theta, rr, K, p.out + (int64_t)row * K, misc + 4, tid, CAND_THREADS);
     __syncthreads();
+  }
+  // a copy still in flight after a timeout must land before the CTA exits
+  if (misc[7] && tid == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
   }
 }
 
@@ -626,6 +664,135 @@ cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s) {
     attr_set = true;
   }
   cand_select_kernel<<<grid, CAND_THREADS, CAND_SMEM, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ============================================================ wide select ==
+// The rows whose certificate failed are few and long: their exact top-K runs
+// over the whole GPU.  Keys are the order-preserving images of the repaired
+// fp32 scores; each pass fixes one byte of the K-th largest key (the radix
+// select of the method, spread over row slices).
+constexpr int WIDE_THREADS = 256;
+constexpr int WIDE_SLICES = 32;  // CTAs per row and pass
+
+// Visits the keys of slice `sl` of list entry f: f(key, index, valid) on all
+// lanes, four keys per float4 load (the slice bounds are 4-aligned; keys
+// outside [b, e) come with valid = false).
+template <class F>
+__device__ __forceinline__ void wide_visit(const WideParams& p, int f, int sl, int b, int e, F&& fn) {
+  const float* srow = p.scores + (int64_t)f * p.ld;
+  const int a = b & ~3;
+  const int n4 = ((e + 3) >> 2) - (a >> 2);              // float4s covering [a, e)
+  const int per = ceil_div(n4, WIDE_SLICES);
+  const int v0 = sl * per, v1 = min(n4, v0 + per);
+  const float4* v4 = reinterpret_cast<const float4*>(srow + a);
+  for (int base = v0; base < v1; base += WIDE_THREADS) {
+    const int vi = base + (int)threadIdx.x;
+    const bool in = vi < v1;
+    const float4 x = in ? __ldcg(&v4[vi]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int i0 = a + 4 * vi;
+    fn(ordered_key(x.x), i0 + 0, in && i0 + 0 >= b && i0 + 0 < e);
+    fn(ordered_key(x.y), i0 + 1, in && i0 + 1 >= b && i0 + 1 < e);
+    fn(ordered_key(x.z), i0 + 2, in && i0 + 2 >= b && i0 + 2 < e);
+    fn(ordered_key(x.w), i0 + 3, in && i0 + 3 >= b && i0 + 3 < e);
+  }
+}
+
+__global__ void __launch_bounds__(WIDE_THREADS) wide_hist_kernel(const WideParams p) {
+  __shared__ int h[256];
+  const int lane = threadIdx.x & 31;
+  const int shift = 24 - 8 * p.pass;
+  const int items = p.stats->fail_count * WIDE_SLICES;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int f = it / WIDE_SLICES, sl = it % WIDE_SLICES;
+    const int row = p.list[f];
+    const int32_t* st = p.state + (int64_t)f * WIDE_STATE;
+    const uint32_t prefix = p.pass ? (uint32_t)st[0] : 0u, mask = p.pass ? (uint32_t)st[1] : 0u;
+    for (int i = threadIdx.x; i < 256; i += WIDE_THREADS) h[i] = 0;
+    __syncthreads();
+    wide_visit(p, f, sl, p.rb[row], p.re[row], [&](uint32_t k, int, bool v) {
+      hist_add(v && (k & mask) == prefix, (k >> shift) & 0xFFu, lane, h);
+    });
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += WIDE_THREADS)
+      if (h[i]) atomicAdd(&p.hist[(int64_t)f * 256 + i], h[i]);
+    __syncthreads();
+  }
+}
+
+// One warp per list entry: the digit of this pass, then the histogram is
+// cleared for the next pass (and the emission counters after the last).
+__global__ void __launch_bounds__(WIDE_THREADS) wide_pick_kernel(const WideParams p) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (WIDE_THREADS / 32);
+  const int shift = 24 - 8 * p.pass;
+  const int nf = p.stats->fail_count;
+  for (int f = blockIdx.x * (WIDE_THREADS / 32) + (threadIdx.x >> 5); f < nf; f += nwarps) {
+    int32_t* st = p.state + (int64_t)f * WIDE_STATE;
+    int32_t* hist = p.hist + (int64_t)f * 256;
+    const int rem = p.pass ? st[2] : p.K;
+    radix_pick_digit(hist, rem, st + 8);
+    __syncwarp();
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    if (lane == 0) {
+      const uint32_t prefix = (p.pass ? (uint32_t)st[0] : 0u) | ((uint32_t)st[8] << shift);
+      const uint32_t mask = (p.pass ? (uint32_t)st[1] : 0u) | (0xFFu << shift);
+      st[0] = (int32_t)prefix;
+      st[1] = (int32_t)mask;
+      st[2] = st[9];
+      st[3] = 0;
+      st[4] = 0;
+    }
+  }
+}
+
+// Every key above the K-th key and the first `rem` keys equal to it (the
+// pass-3 prefix is that key), slots reserved once per warp.
+__global__ void __launch_bounds__(WIDE_THREADS) wide_emit_kernel(const WideParams p) {
+  const int lane = threadIdx.x & 31;
+  uint32_t lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  const int K = p.K;
+  const int items = p.stats->fail_count * WIDE_SLICES;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int f = it / WIDE_SLICES, sl = it % WIDE_SLICES;
+    const int row = p.list[f];
+    int32_t* st = p.state + (int64_t)f * WIDE_STATE;
+    const uint32_t theta = (uint32_t)st[0];
+    const int rr = st[2];
+    int32_t* o = p.out + (int64_t)row * K;
+    wide_visit(p, f, sl, p.rb[row], p.re[row], [&](uint32_t k, int i, bool v) {
+      const bool gt = v && k > theta, eq = v && k == theta;
+      const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
+      if (!(mg | me)) return;
+      int bg = 0, be = 0;
+      if (lane == 0) {
+        if (mg) bg = atomicAdd(&st[3], __popc(mg));
+        if (me) be = atomicAdd(&st[4], __popc(me));
+      }
+      bg = __shfl_sync(0xffffffffu, bg, 0);
+      be = __shfl_sync(0xffffffffu, be, 0);
+      const int qg = bg + __popc(mg & lt);
+      if (gt && qg < K - rr) o[qg] = p.rs.paged ? out_index(p.rs, row, i) : i;
+      if (eq) {
+        const int q = be + __popc(me & lt);
+        if (q < rr) o[K - rr + q] = p.rs.paged ? out_index(p.rs, row, i) : i;
+      }
+    });
+  }
+}
+
+cudaError_t launch_wide_hist(const WideParams& p, int grid, cudaStream_t s) {
+  wide_hist_kernel<<<grid, WIDE_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_wide_pick(const WideParams& p, cudaStream_t s) {
+  const int grid = max(1, ceil_div(p.rs.R, WIDE_THREADS / 32));
+  wide_pick_kernel<<<min(grid, 256), WIDE_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_wide_emit(const WideParams& p, int grid, cudaStream_t s) {
+  wide_emit_kernel<<<grid, WIDE_THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 
