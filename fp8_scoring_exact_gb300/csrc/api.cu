@@ -60,7 +60,7 @@ Layout make_layout(int64_t R, int64_t G, int64_t cand_stride, int64_t max_units,
   L.unit_start = take((G + 1) * 4);
   L.rgroups = take(R * sizeof(Group));
   L.runit_start = take((R + 1) * 4);
-  L.unit_count = take((size_t)R * max_units * 4 * 4);
+  L.unit_count = take((size_t)R * max_units * UNIT_REGIONS * 4);
   L.failed = take(R * 4);
   L.wide_hist = cand_stride ? take((size_t)R * 256 * 4) : 0;
   L.wide_state = cand_stride ? take((size_t)R * WIDE_STATE * 4) : 0;

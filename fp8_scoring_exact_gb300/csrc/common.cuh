@@ -28,7 +28,8 @@ constexpr int EPI_WGS = GROUP_ROWS; // epilogue warpgroups: one per row of the g
 constexpr int EPI_THREADS = EPI_WGS * 128;
 constexpr int SCORE_THREADS = 64 + EPI_THREADS;  // warp 0: TMA, warp 1: MMA; then the epilogue
 constexpr int UCAP = 1024;         // candidates one work unit may leave for one row ...
-constexpr int WCAP = UCAP / 4;     // ... in four regions, one per epilogue warp (TMEM lane quarter)
+constexpr int UNIT_REGIONS = 4;    // ... in 4 regions (one per epilogue warp: TMEM lane quarter) ...
+constexpr int WCAP = UCAP / UNIT_REGIONS;  // ... of this many each
 
 // -------------------------------------------------------------- selection --
 constexpr int CAND_CAP = 8192;     // candidates selected per row (certificate capacity)
@@ -81,6 +82,14 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   uint32_t u = __float_as_uint(f);
   if (u == 0x80000000u) u = 0u;
   return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+
+// The float T with (x >= T) == (ordered_key(x) >= key) for every non-NaN x:
+// the filter compares scores against it instead of mapping each score.
+__device__ __forceinline__ float key_threshold_float(uint32_t key) {
+  if (key <= 0x007FFFFFu) return -__int_as_float(0x7f800000);  // at or below -inf's key: all pass
+  if (key > 0xFF800000u) return __int_as_float(0x7fffffff);     // above +inf's key: none (NaN)
+  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t lt_mask = lanemask_lt();
   volatile int* abort_flag = &misc->abort_flag;
   int* status = &p.stats->status;
   constexpr bool filter = (MODE == MODE_FILTER);
@@ -259,11 +260,11 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       const bool active = r < G.nrows;
       const int row = active ? __ldg(&gp->row[r]) : 0;
       int rb = 0, re = 0;
-      uint32_t tau = 0;
+      float tauf = 0.f;
       float* srow = nullptr;
       int64_t store_lim = 0;
       // this warp's candidate region of the unit
-      const int64_t region = (int64_t)row * p.cand_stride + (int64_t)(un.c * 4 + quarter) * WCAP;
+      const int64_t region = (int64_t)row * p.cand_stride + (int64_t)(un.c * UNIT_REGIONS + quarter) * WCAP;
       uint32_t* ck = p.cand_key + region;
       int32_t* ci = p.cand_idx + region;
       int wcnt = 0;
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         rb = __ldg(&p.rb[row]);
         re = __ldg(&p.re[row]);
         if (filter) {
-          tau = __ldg(&p.tau[row]);
+          tauf = key_threshold_float(__ldg(&p.tau[row]));
         } else {
           srow = p.scores + (int64_t)__ldg(&gp->slot[r]) * p.ld;
           store_lim = min((int64_t)p.rs.N, p.ld);
@@ -362,19 +363,19 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           if (s < store_lim) srow[s] = valid ? score : -__int_as_float(0x7f800000);
           continue;
         }
-        const uint32_t key = ordered_key(score);
-        const bool pred = valid && (key >= tau);
+        // score >= the threshold's float  <=>  its key >= the threshold key
+        const bool pred = valid && score >= tauf;
         const uint32_t m = __ballot_sync(0xffffffffu, pred);
-        const int pos = wcnt + __popc(m & lanemask_lt());
+        const int pos = wcnt + __popc(m & lt_mask);
         wcnt += __popc(m);
         if (pred && pos < WCAP) {
-          ck[pos] = key;
+          ck[pos] = ordered_key(score);
           ci[pos] = paged ? page * PAGE + (s & (PAGE - 1)) : s;
         }
       }
       // unit done: the warp's count (WCAP + 1 = some were lost)
       if (filter && active && ok && lane == 0)
-        p.unit_count[(int64_t)row * p.max_units * 4 + un.c * 4 + quarter] = min(wcnt, WCAP + 1);
+        p.unit_count[(int64_t)row * p.max_units * UNIT_REGIONS + un.c * UNIT_REGIONS + quarter] = min(wcnt, WCAP + 1);
     }
   }
 

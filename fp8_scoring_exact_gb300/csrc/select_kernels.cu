@@ -555,8 +555,8 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
     const Group* gp = p.groups + g;
     if (r >= gp->nrows) continue;  // uniform over the CTA
     const int row = gp->row[r];
-    const int nreg = (p.unit_start[g + 1] - p.unit_start[g]) * 4;
-    const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * 4;
+    const int nreg = (p.unit_start[g + 1] - p.unit_start[g]) * UNIT_REGIONS;
+    const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * UNIT_REGIONS;
     // certificate over the region counts (WCAP + 1 = candidates were lost),
     // and an exclusive scan of the 4-padded counts
     int c[CS_PER_THREAD];
