@@ -3,9 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
 
 One step = one complete operator call (plan, sampled thresholds, fused
-tcgen05 scoring + candidate filter + TopK selection, repair) over the
-causal-prefill workload Q=4096 query rows x N=131072 keys, K=2048 (the
-"128K" chunk of the indexer study), inputs resident in HBM.  The metric is
+tcgen05 scoring + candidate filter, exact selection of the candidates,
+repair) over the causal-prefill workload Q=4096 query rows x N=131072 keys,
+K=2048 (the "128K" chunk of the indexer study), inputs resident in HBM.
+--config 4 runs the paged decode batch through the paged entry point.  The metric is
 scored row-keys per second (sum over rows of the valid range length); the
 effective FP8 rate is 2*64*128 FLOP per row-key ("Fusing Indexer Scoring and
 Exact Top-k for DeepSeek-V3.2", section 5.1 equation).
@@ -46,6 +47,16 @@ def algorithmic_bytes(Q: int, N: int, K: int) -> int:
     """Bytes the operator must move at least once: q codes + q scale + weights,
     every key once (codes + scale), the int32 output."""
     return Q * HEADS * DIM + Q * 4 + Q * HEADS * 4 + N * BYTES_PER_KEY + Q * K * 4
+
+
+def algorithmic_bytes_of(inp) -> int:
+    """algorithmic_bytes for a dense or a paged problem (paged: every
+    sequence's keys once, its rows share them)."""
+    if hasattr(inp, "block_table"):
+        R = inp.B * inp.next_n
+        keys = int(inp.seq_lens.astype(np.int64).sum())
+        return R * HEADS * DIM + R * 4 + R * HEADS * 4 + keys * BYTES_PER_KEY + R * inp.K * 4
+    return algorithmic_bytes(inp.Q, inp.N, inp.K)
 
 
 def score_matrix_bytes(Q: int, N: int) -> int:
@@ -147,6 +158,14 @@ def make_workload(config: int, rows: int = 0, keys: int = 0):
 
 
 def describe(inp, config):
+    if hasattr(inp, "block_table"):
+        return {"workload": f"{inp.name} (paged decode: B={inp.B} sequences x next_n={inp.next_n} rows, "
+                            f"64-token pages, seq_len {int(inp.seq_lens.min())}..{int(inp.seq_lens.max())}, "
+                            f"K={inp.K})",
+                "B": inp.B, "next_n": inp.next_n, "K": inp.K, "row_keys": inp.row_keys(),
+                "config_index": config,
+                "l2": "flushed by a 512 MiB write before each timed step (outside the timed events)",
+                "parallelism": "replicas (one independent problem per GPU)"}
     Q, N = inp.Q, inp.N
     return {"workload": f"{inp.name} (Q={Q} rows x N={N} keys, causal, K={inp.K})", "Q": Q, "N": N,
             "K": inp.K, "row_keys": inp.row_keys(), "config_index": config,
@@ -168,6 +187,32 @@ def oracle_subset(inp, rows):
                        row_begin=inp.row_begin[r], row_end=inp.row_end[r], K=inp.K, name=inp.name)
 
 
+def paged_subset(inp, n_seq, seed=123):
+    """`n_seq` seeded sequences of a paged problem with their pages gathered
+    into a compact cache (block tables renumbered), and the (b, i) rows of
+    the subset."""
+    from fp8_scoring_exact_gb300.synthetic import PagedInputs
+    rng = np.random.default_rng(seed)
+    bs = sorted(rng.choice(inp.B, size=min(n_seq, inp.B), replace=False).tolist())
+    pages, tables = [], []
+    for b in bs:
+        n = (int(inp.seq_lens[b]) + 63) // 64
+        pages.append(inp.block_table[b, :n])
+    maxp = max(len(x) for x in pages)
+    base = 0
+    for x in pages:
+        t = np.full(maxp, -1, np.int32)
+        t[:len(x)] = np.arange(base, base + len(x), dtype=np.int32)
+        tables.append(t)
+        base += len(x)
+    allp = np.concatenate(pages)
+    sub = PagedInputs(q=inp.q[bs], q_scale=inp.q_scale[bs], k_cache=inp.k_cache[allp],
+                      k_cache_scale=inp.k_cache_scale[allp], w=inp.w[bs], block_table=np.stack(tables),
+                      seq_lens=inp.seq_lens[bs], K=inp.K, name=inp.name)
+    rows = [(b, i) for b in range(len(bs)) for i in range(inp.next_n)]
+    return sub, rows
+
+
 def cpu_procs():
     try:
         n = len(os.sched_getaffinity(0))
@@ -179,19 +224,26 @@ def cpu_procs():
 def time_oracle(inp, n_rows, procs, reps=1):
     """(row-keys/s, seconds, rows) of the oracle over a seeded row sample."""
     from oracle.indexer import OraclePool
-    rows = oracle_rows(inp, n_rows)
-    sub = oracle_subset(inp, rows)
-    rk = int((sub.row_end.astype(np.int64) - sub.row_begin).sum())
-    with OraclePool(sub, procs) as pool:
+    if hasattr(inp, "block_table"):
+        sub, rows = paged_subset(inp, max(1, n_rows // inp.next_n))
+        rk = int(sub.row_lengths().sum())
+        kind = "paged"
+    else:
+        rows = oracle_rows(inp, n_rows)
+        sub = oracle_subset(inp, rows)
+        rk = int((sub.row_end.astype(np.int64) - sub.row_begin).sum())
+        rows = range(len(rows))
+        kind = "dense"
+    with OraclePool(sub, procs, kind) as pool:
         t0 = time.perf_counter()
         for _ in range(reps):
-            pool.topk(range(len(rows)))
+            pool.topk(rows)
         dt = time.perf_counter() - t0
-    return rk * reps / dt, dt, rows
+    return rk * reps / dt, dt, list(rows)
 
 
 # ------------------------------------------------------------ GPU arm -------
-def _e2e(args, dev, host, out, stream, world, device, binding, R, K):
+def _e2e(args, dev, host, out, stream, world, device, call, R):
     """Same metric through the public API with host buffers: every step copies
     the inputs from pinned host memory and reads the indices back."""
     import torch
@@ -205,7 +257,7 @@ def _e2e(args, dev, host, out, stream, world, device, binding, R, K):
             e0.record(stream)
         for d, h in zip(dev, pinned):
             d.copy_(h, non_blocking=True)
-        binding.indexer_topk(*dev, K=K, out=out)
+        call(dev, out)
         out_h.copy_(out, non_blocking=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e1.record(stream)
@@ -215,24 +267,37 @@ def _e2e(args, dev, host, out, stream, world, device, binding, R, K):
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
+def problem(inp, binding):
+    """(host arrays, output shape, fused call, unfused call or None) of a
+    dense or a paged workload."""
+    K = inp.K
+    if hasattr(inp, "block_table"):
+        host = [np.ascontiguousarray(a) for a in (inp.q, inp.q_scale, inp.k_cache, inp.k_cache_scale, inp.w,
+                                                   inp.block_table, inp.seq_lens)]
+        return (host, (inp.B, inp.next_n, K),
+                lambda dev, out: binding.indexer_topk_paged(*dev, K=K, out=out), None)
+    host = [np.ascontiguousarray(a) for a in (inp.q, inp.q_scale, inp.k, inp.k_scale, inp.w, inp.row_begin,
+                                               inp.row_end)]
+    return (host, (inp.Q, K), lambda dev, out: binding.indexer_topk(*dev, K=K, out=out),
+            lambda dev, out: binding.indexer_topk_unfused(*dev, K=K, out=out))
+
+
 def run_ours(args, rank, world, device):
     import torch
 
     from fp8_scoring_exact_gb300 import binding
 
     inp = make_workload(args.config, args.rows, args.keys)
-    Q, N, K = inp.Q, inp.N, inp.K
     R = inp.row_keys()
     legs = set(args.legs.split(","))
-    host = [np.ascontiguousarray(a) for a in (inp.q, inp.q_scale, inp.k, inp.k_scale, inp.w, inp.row_begin,
-                                               inp.row_end)]
+    host, out_shape, call, call_unfused = problem(inp, binding)
     dev = [torch.from_numpy(a).to(device) for a in host]
-    out = torch.empty((Q, K), dtype=torch.int32, device=device)
+    out = torch.empty(out_shape, dtype=torch.int32, device=device)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
     def step():
-        binding.indexer_topk(*dev, K=K, out=out)
+        call(dev, out)
 
     binding.set_option("profile", 1)
     for _ in range(args.warmup):
@@ -265,13 +330,15 @@ def run_ours(args, rank, world, device):
 
     # unfused attribution baseline, same protocol
     unf_ms = None
+    if call_unfused is None:
+        legs.discard("unfused")
     for _ in range(max(1, args.warmup // 2) if "unfused" in legs else 0):
-        binding.indexer_topk_unfused(*dev, K=K, out=out)
+        call_unfused(dev, out)
     if "unfused" in legs:
         for i in range(args.steps):
             flush.zero_()
             ev[i][0].record(stream)
-            binding.indexer_topk_unfused(*dev, K=K, out=out)
+            call_unfused(dev, out)
             ev[i][1].record(stream)
         torch.cuda.synchronize(device)
         unf_ms = statistics.mean([a.elapsed_time(b) for a, b in ev])
@@ -279,7 +346,7 @@ def run_ours(args, rank, world, device):
     # end to end through the public API from pinned host buffers
     e2e = None
     if "e2e" in legs:
-        e2e = _e2e(args, dev, host, out, stream, world, device, binding, R, K)
+        e2e = _e2e(args, dev, host, out, stream, world, device, call, R)
     peaks = load_peaks()
     main_avg = statistics.mean(main_ms)
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
@@ -289,8 +356,20 @@ def run_ours(args, rank, world, device):
     f_sm = (clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]) * 1e6
     t_tensor = FLOP_PER_ROW_KEY * R / (fp8_peak * 1e12) * 1e3
     t_core = CORE_OPS_PER_ROW_KEY * R / (sms * 128 * f_sm) * 1e3
-    t_hbm = algorithmic_bytes(Q, N, K) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_hbm = algorithmic_bytes_of(inp) / (peaks["hbm_gbs"] * 1e9) * 1e3
     t_roof = max(t_tensor, t_core, t_hbm)
+    kernel_name = "score_kernel (filter mode: tcgen05 scoring + candidate filter)"
+    peak_note = f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} (nominal fp8/bf16 ratio), burst"
+    if t_hbm > t_tensor:
+        # paged decode: every row reads its own keys, the HBM term dominates
+        gbs = algorithmic_bytes_of(inp) / (main_avg * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": kernel_name, "kernel_ms": main_avg,
+                    "peak_source": f"{peaks['source']} HBM copy bandwidth"}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp8_peak, "traffic": measured_traffic(args.config, args.rows, args.keys),
+                    "kernel": kernel_name, "kernel_ms": main_avg, "peak_source": peak_note}
 
     res = {
         "metric": METRIC,
@@ -310,12 +389,7 @@ def run_ours(args, rank, world, device):
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": measured_traffic(args.config, args.rows, args.keys),
-                     "kernel": "score_kernel (filter mode: tcgen05 scoring + candidate filter + TopK warps)",
-                     "kernel_ms": main_avg,
-                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} "
-                                    "(nominal fp8/bf16 ratio), burst"},
+        "roofline": roofline,
         "roofline_terms": {"t_tensor_ms": t_tensor, "t_core_ms": t_core, "t_hbm_ms": t_hbm, "t_roof_ms": t_roof,
                            "frac_of_roofline": t_roof / ms_per_step, "sm_count": sms,
                            "sm_clock_for_core_term_mhz": f_sm / 1e6},
@@ -338,17 +412,33 @@ def run_reference(args, rank, world):
     inp = make_workload(args.config, args.rows, args.keys)
     procs = cpu_procs()
     from oracle.indexer import OraclePool
-    rows = oracle_rows(inp, procs * (args.steps + args.warmup), seed=321)
-    sub = oracle_subset(inp, rows)
     per = procs
-    with OraclePool(sub, procs) as pool:
+    if hasattr(inp, "block_table"):
+        n_seq = max(1, per // inp.next_n)
+        sub, allrows = paged_subset(inp, n_seq * (args.steps + args.warmup), seed=321)
+        kind = "paged"
+        per = n_seq * inp.next_n
+        lens_all = sub.row_lengths().reshape(-1)
+    else:
+        rows = oracle_rows(inp, procs * (args.steps + args.warmup), seed=321)
+        sub = oracle_subset(inp, rows)
+        allrows = list(range(len(rows)))
+        kind = "dense"
+        lens_all = sub.row_end.astype(np.int64) - sub.row_begin
+    n_all = len(allrows)
+    per = min(per, n_all)
+
+    def window(i):  # step i's rows, cycling when the sample is short
+        return [(i * per + j) % n_all for j in range(per)]
+
+    with OraclePool(sub, procs, kind) as pool:
         for i in range(args.warmup):
-            pool.topk(range(i * per, (i + 1) * per))
+            pool.topk([allrows[j] for j in window(i)])
         t0 = time.perf_counter()
         for i in range(args.warmup, args.warmup + args.steps):
-            pool.topk(range(i * per, (i + 1) * per))
+            pool.topk([allrows[j] for j in window(i)])
         dt = time.perf_counter() - t0
-    lens = (sub.row_end.astype(np.int64) - sub.row_begin)[args.warmup * per:]
+    lens = np.concatenate([lens_all[window(i)] for i in range(args.warmup, args.warmup + args.steps)])
     rate = float(lens.sum()) / dt
     res = {
         "impl": "reference",

@@ -190,7 +190,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   const int G = n_groups(rs);
   const int64_t ld = align_up((size_t)rs.N, 4);
   const int max_units = ceil_div(ceil_div(rs.N, TILE), o.chunk);
-  const int64_t cand_stride = (int64_t)max_units * UCAP;
+  const int64_t cand_stride = ROW_SLOTS;
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
   Arena* a = get_arena(stream, make_layout(rs.R, G, cand_stride, max_units, rs.R, ld), &err);
@@ -246,7 +246,6 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cp.cand_key = at<uint32_t>(a, L.cand_key);
   cp.cand_idx = at<int32_t>(a, L.cand_idx);
   cp.unit_count = at<int32_t>(a, L.unit_count);
-  cp.cand_stride = cand_stride;
   cp.max_units = max_units;
   cp.stats = st;
   a->profiled = o.profile;
@@ -262,7 +261,6 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cs.unit_count = cp.unit_count;
   cs.cand_key = cp.cand_key;
   cs.cand_idx = cp.cand_idx;
-  cs.cand_stride = cand_stride;
   cs.max_units = max_units;
   cs.failed_rows = at<int32_t>(a, L.failed);
   cs.wide_hist = at<int32_t>(a, L.wide_hist);

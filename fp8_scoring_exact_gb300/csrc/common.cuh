@@ -27,9 +27,16 @@ constexpr int ACC_COLS = 256;      // TMEM columns per accumulator (4 rows x 64 
 constexpr int EPI_WGS = GROUP_ROWS; // epilogue warpgroups: one per row of the group
 constexpr int EPI_THREADS = EPI_WGS * 128;
 constexpr int SCORE_THREADS = 64 + EPI_THREADS;  // warp 0: TMA, warp 1: MMA; then the epilogue
-constexpr int UCAP = 1024;         // candidates one work unit may leave for one row ...
-constexpr int UNIT_REGIONS = 4;    // ... in 4 regions (one per epilogue warp: TMEM lane quarter) ...
-constexpr int WCAP = UCAP / UNIT_REGIONS;  // ... of this many each
+// Candidate slots of a row, shared evenly by its regions: every work unit of
+// the row's group leaves candidates in UNIT_REGIONS regions (one per epilogue
+// warp, i.e. TMEM lane quarter).  Splitting a fixed budget keeps each region
+// about 4x its expected fill whatever the row length: ~2K candidates spread
+// over the row's regions.
+constexpr int ROW_SLOTS = 16384;
+constexpr int UNIT_REGIONS = 4;
+__host__ __device__ constexpr int region_cap(int nunits) {
+  return (ROW_SLOTS / (nunits * UNIT_REGIONS)) & ~3;
+}
 
 // -------------------------------------------------------------- selection --
 constexpr int CAND_CAP = 8192;     // candidates selected per row (certificate capacity)

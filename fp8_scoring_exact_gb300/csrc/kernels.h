@@ -70,13 +70,12 @@ struct ScoreParams {
   const int32_t* re;
   const Group* groups;
   const int32_t* unit_start;
-  // MODE_FILTER: epilogue warp q of unit c leaves at most WCAP candidates of
-  // a row in region (4 c + q) of that row's buffers
+  // MODE_FILTER: epilogue warp q of unit c leaves at most region_cap(units)
+  // candidates of a row in region (4 c + q) of that row's ROW_SLOTS
   const uint32_t* tau;
-  uint32_t* cand_key;          // [R, cand_stride]
-  int32_t* cand_idx;           // [R, cand_stride]
-  int32_t* unit_count;         // [R, max_units, 4]: candidates region (c, q) holds (WCAP + 1: lost some)
-  int64_t cand_stride;         // max_units * UCAP
+  uint32_t* cand_key;          // [R, ROW_SLOTS]
+  int32_t* cand_idx;           // [R, ROW_SLOTS]
+  int32_t* unit_count;         // [R, max_units, 4]: candidates region (c, q) holds (cap + 1: lost some)
   int max_units;               // units per group, at most
   // MODE_STORE
   float* scores;               // [slots, ld]
@@ -93,9 +92,8 @@ struct CandParams {
   const Group* groups;
   const int32_t* unit_start;
   const int32_t* unit_count;
-  const uint32_t* cand_key;
+  const uint32_t* cand_key;     // [R, ROW_SLOTS]
   const int32_t* cand_idx;
-  int64_t cand_stride;
   int max_units;
   int32_t* failed_rows;        // [R] (appended, count in stats->fail_count)
   int32_t* wide_hist;          // [R, 256]: cleared for each row queued for repair

@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       float* srow = nullptr;
       int64_t store_lim = 0;
       // this warp's candidate region of the unit
-      const int64_t region = (int64_t)row * p.cand_stride + (int64_t)(un.c * UNIT_REGIONS + quarter) * WCAP;
+      const int wcap = region_cap(un.nunits);
+      const int64_t region = (int64_t)row * ROW_SLOTS + (int64_t)(un.c * UNIT_REGIONS + quarter) * wcap;
       uint32_t* ck = p.cand_key + region;
       int32_t* ci = p.cand_idx + region;
       int wcnt = 0;
@@ -368,14 +369,14 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         const uint32_t m = __ballot_sync(0xffffffffu, pred);
         const int pos = wcnt + __popc(m & lt_mask);
         wcnt += __popc(m);
-        if (pred && pos < WCAP) {
+        if (pred && pos < wcap) {
           ck[pos] = ordered_key(score);
           ci[pos] = paged ? page * PAGE + (s & (PAGE - 1)) : s;
         }
       }
-      // unit done: the warp's count (WCAP + 1 = some were lost)
+      // unit done: the warp's count (wcap + 1 = some were lost)
       if (filter && active && ok && lane == 0)
-        p.unit_count[(int64_t)row * p.max_units * UNIT_REGIONS + un.c * UNIT_REGIONS + quarter] = min(wcnt, WCAP + 1);
+        p.unit_count[(int64_t)row * p.max_units * UNIT_REGIONS + un.c * UNIT_REGIONS + quarter] = min(wcnt, wcap + 1);
     }
   }
 

@@ -555,9 +555,11 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
     const Group* gp = p.groups + g;
     if (r >= gp->nrows) continue;  // uniform over the CTA
     const int row = gp->row[r];
-    const int nreg = (p.unit_start[g + 1] - p.unit_start[g]) * UNIT_REGIONS;
+    const int nu = p.unit_start[g + 1] - p.unit_start[g];
+    const int nreg = nu * UNIT_REGIONS;
+    const int wcap = region_cap(max(nu, 1));
     const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * UNIT_REGIONS;
-    // certificate over the region counts (WCAP + 1 = candidates were lost),
+    // certificate over the region counts (wcap + 1 = candidates were lost),
     // and an exclusive scan of the 4-padded counts
     int c[CS_PER_THREAD];
     int tpad = 0, treal = 0;
@@ -566,8 +568,8 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
     for (int i = 0; i < CS_PER_THREAD; ++i) {
       const int j = tid * CS_PER_THREAD + i;
       const int x = j < nreg && j < CAND_MAX_REGIONS ? __ldcg(&cnt[j]) : 0;
-      lost |= x > WCAP;
-      c[i] = min(x, WCAP);
+      lost |= x > wcap;
+      c[i] = min(x, wcap);
       treal += c[i];
       tpad += (c[i] + 3) & ~3;
     }
@@ -617,17 +619,17 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
     }
     __syncthreads();
     // gather: one bulk copy per non-empty region and array, issued by warp 0
-    const uint32_t* ck = p.cand_key + (int64_t)row * p.cand_stride;
-    const int32_t* ci = p.cand_idx + (int64_t)row * p.cand_stride;
+    const uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
+    const int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
     if (warp == 0) {
       fence_proxy_async_smem();  // the previous item's reads of these buffers come first
       if (lane == 0) mbar_arrive_expect_tx(bar, 2u * npad * 4u);
       __syncwarp();
       for (int j = lane; j < nreg; j += 32) {
-        const uint32_t bytes = (uint32_t)((min(__ldcg(&cnt[j]), WCAP) + 3) & ~3) * 4u;
+        const uint32_t bytes = (uint32_t)((min(__ldcg(&cnt[j]), wcap) + 3) & ~3) * 4u;
         if (bytes) {
-          bulk_g2s(smem_u32(ckey + off[j]), ck + (int64_t)j * WCAP, bytes, bar);
-          bulk_g2s(smem_u32(cidx + off[j]), ci + (int64_t)j * WCAP, bytes, bar);
+          bulk_g2s(smem_u32(ckey + off[j]), ck + (int64_t)j * wcap, bytes, bar);
+          bulk_g2s(smem_u32(cidx + off[j]), ci + (int64_t)j * wcap, bytes, bar);
         }
       }
       if (lane == 0) misc[6] = mbar_wait(bar, phase & 1, (volatile int*)&misc[7], &p.stats->status) ? 1 : 0;
@@ -638,7 +640,7 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
     if (!misc[6]) break;  // the copies did not land in time (status records it)
     // key 0 in the pad slots (they hold whatever the regions held there)
     for (int j = tid; j < nreg; j += CAND_THREADS) {
-      const int x = min(__ldcg(&cnt[j]), WCAP);
+      const int x = min(__ldcg(&cnt[j]), wcap);
       for (int i = x; i < ((x + 3) & ~3); ++i) ckey[off[j] + i] = 0u;
     }
     if (tid == 0) atomicAdd(&p.stats->cand_total, n);
