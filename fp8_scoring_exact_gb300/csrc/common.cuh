@@ -333,6 +333,17 @@ __device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, uint32_t* r) {
       : "r"(taddr)
       : "memory");
 }
+// 16 lanes x 32 columns: the first four 8-column blocks of the .x8 layout
+// above (r[4m .. 4m+3] for m = 0..3).
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
 // release / acquire at GPU scope on a global counter
 __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -351,7 +362,7 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 // weight of such a head is stored pre-multiplied by 2^25.
 __device__ __forceinline__ float relu_scaled_fma_pipe(float x) {
   float r;
-  asm("mul.rn.sat.f32 %0, %1, 0f33000000;" : "=f"(r) : "f"(x));
+  asm volatile("mul.rn.sat.f32 %0, %1, 0f33000000;" : "=f"(r) : "f"(x));
   return r;
 }
 constexpr float RELU_SAT_WEIGHT_SCALE = 33554432.0f;  // 2^25
@@ -369,12 +380,12 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
 // a * b on two fp32 lanes
 __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  asm volatile("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 // acc += a * b on two fp32 lanes (sm_100+ packed FMA)
 __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+  asm volatile("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 // 16 bytes of shared memory as two packed float pairs
 __device__ __forceinline__ void lds_2x64(uint32_t addr, uint64_t& a, uint64_t& b) {

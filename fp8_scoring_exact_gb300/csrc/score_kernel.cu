@@ -91,18 +91,21 @@ __device__ __forceinline__ Unit decode_unit(const ScoreParams& p, int n_groups, 
   return un;
 }
 
-// Partial sums of two keys over this thread's 16 heads from one 16x256b.x8
-// TMEM load: ReLU on the FMA pipe (saturating multiply by 2^-25, exact since
-// |x| < 2^25), weights pre-scaled by 2^25, one packed f32x2 chain per key.
-__device__ __forceinline__ void two_key_partials(const uint32_t* v, const uint64_t* w, float& pa, float& pb) {
-  uint64_t a = 0, b = 0;
+// One 16x256b.x4 TMEM chunk (two keys x 8 of this thread's heads: column
+// blocks m0 .. m0 + 3 of the row) into the packed accumulators of the two
+// keys: ReLU on the FMA pipe (saturating multiply by 2^-25, exact since
+// |x| < 2^25), weights pre-scaled by 2^25, one f32x2 FMA chain per key.  The
+// arithmetic is volatile asm, so it stays between the TMEM loads and waits it
+// is written between (measured: letting the compiler move it is slower).
+template <bool FIRST>
+__device__ __forceinline__ void chunk_partials(const uint32_t* v, const uint64_t* w, uint64_t& a, uint64_t& b) {
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
+  for (int m = 0; m < 4; ++m) {
     const uint64_t xa = pack2(relu_scaled_fma_pipe(__uint_as_float(v[4 * m])),
                               relu_scaled_fma_pipe(__uint_as_float(v[4 * m + 1])));
     const uint64_t xb = pack2(relu_scaled_fma_pipe(__uint_as_float(v[4 * m + 2])),
                               relu_scaled_fma_pipe(__uint_as_float(v[4 * m + 3])));
-    if (m == 0) {
+    if (FIRST && m == 0) {
       a = fmul2(xa, w[0]);
       b = fmul2(xb, w[0]);
     } else {
@@ -110,11 +113,11 @@ __device__ __forceinline__ void two_key_partials(const uint32_t* v, const uint64
       ffma2(b, xb, w[m]);
     }
   }
-  const float2 x = unpack2(a), y = unpack2(b);
-  pa = x.x + x.y;
-  pb = y.x + y.y;
 }
-
+__device__ __forceinline__ float hsum2(uint64_t v) {
+  const float2 x = unpack2(v);
+  return x.x + x.y;
+}
 }  // namespace
 
 // Compiled once per (mode, key layout): the hot loops carry no mode tests.
@@ -331,19 +334,30 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         tc_fence_after();
         float part[4] = {0.f, 0.f, 0.f, 0.f};
         if (active) {
-          // the two 16-lane halves of this warp's 32 keys; the buffer goes
-          // back to the MMA as soon as the second half is in registers
-          // (measured faster than loading both halves before any arithmetic)
+          // four 16x256b.x4 chunks (lanes +0 / +16 x heads 0-31 / 32-63)
+          // through two register buffers: each load is in flight while the
+          // previous chunk is reduced; the buffer goes back to the MMA once
+          // the last chunk is in registers
           const uint32_t col = tmem_base + ab * ACC_COLS + r * H + ((uint32_t)(quarter * 32) << 16);
-          uint32_t v[32];
-          tmem_ld16x256b_x8(col, v);
+          uint32_t va[16], vb[16];
+          uint64_t aL, bL, aH, bH;
+          tmem_ld16x256b_x4(col, va);
+          tmem_ld16x256b_x4(col + 32, vb);
           tmem_wait_ld();
-          two_key_partials(v, w2, part[0], part[1]);
-          tmem_ld16x256b_x8(col + (16u << 16), v);
+          chunk_partials<true>(va, w2, aL, bL);
+          tmem_ld16x256b_x4(col + (16u << 16), va);
+          chunk_partials<false>(vb, w2 + 4, aL, bL);
+          tmem_wait_ld();
+          tmem_ld16x256b_x4(col + (16u << 16) + 32, vb);
+          chunk_partials<true>(va, w2, aH, bH);
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive_warp(acc_empty(ab));
-          two_key_partials(v, w2, part[2], part[3]);
+          chunk_partials<false>(vb, w2 + 4, aH, bH);
+          part[0] = hsum2(aL);
+          part[1] = hsum2(bL);
+          part[2] = hsum2(aH);
+          part[3] = hsum2(bH);
         } else {
           tc_fence_before();
           mbar_arrive_warp(acc_empty(ab));
