@@ -344,6 +344,19 @@ __device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t* r) {
       : "r"(taddr)
       : "memory");
 }
+// Read-only global loads issued where they are written (volatile): a load at
+// the top of a loop iteration whose value is used at its end keeps its
+// latency behind the iteration's work.
+__device__ __forceinline__ float ldg_pinned_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int ldg_pinned_s32(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
 // release / acquire at GPU scope on a global counter
 __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

@@ -291,43 +291,26 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           store_lim = min((int64_t)p.rs.N, p.ld);
         }
       }
-      // Key scale of this thread's key in tile t.  Paged: the page holding
-      // it (the same clamping as the producer's: a page id outside the cache
-      // and a page past the sequence read as zero keys, scale 0).
+      // Key scale of this thread's key in tile t, loaded at the top of the
+      // tile's iteration and used at its end.  Paged: the page holding it
+      // (the same clamping as the producer's: a page id outside the cache and
+      // a page past the sequence read as zero keys, scale 0).
       const int32_t* bt = paged ? p.rs.block_table + (int64_t)G.seq * p.rs.max_pages : nullptr;
       const int ghi = G.hi;
-      auto page_of = [&](int t) {
-        const int j = 2 * t + (kt >> 6);
-        int pg = num_pages;
-        if (j * PAGE < ghi) {
-          pg = __ldg(&bt[j]);
-          if (pg < 0 || pg >= num_pages) pg = num_pages;
-        }
-        return pg;
-      };
-      auto scale_of = [&](int t, int pg) {
+      for (int t = un.t0; t < un.t1 && ok; ++t, ++ait) {
+        int page = 0;
+        float ks;
         if constexpr (paged) {
-          return pg < num_pages ? __ldg(&p.k_scale[(int64_t)pg * PAGE + (kt & (PAGE - 1))]) : 0.f;
+          const int j = 2 * t + (kt >> 6);
+          page = num_pages;
+          if (j * PAGE < ghi) {
+            page = ldg_pinned_s32(&bt[j]);
+            if (page < 0 || page >= num_pages) page = num_pages;
+          }
+          ks = page < num_pages ? ldg_pinned_f32(&p.k_scale[(int64_t)page * PAGE + (kt & (PAGE - 1))]) : 0.f;
         } else {
           const int s = t * TILE + kt;
-          return s < p.rs.N ? __ldg(&p.k_scale[s]) : 0.f;
-        }
-      };
-      // key scale (and page) of the current tile; the next tile's are loaded
-      // at the top of each tile, one tile ahead of their use
-      int pg0 = 0, pg1 = 0;
-      if (paged) {
-        pg0 = page_of(un.t0);
-        if (un.t0 + 1 < un.t1) pg1 = page_of(un.t0 + 1);
-      }
-      float q0 = scale_of(un.t0, pg0);
-      for (int t = un.t0; t < un.t1 && ok; ++t, ++ait) {
-        const float ks = q0;
-        const int page = pg0;
-        q0 = (t + 1 < un.t1) ? scale_of(t + 1, pg1) : 0.f;
-        if (paged) {
-          pg0 = pg1;
-          pg1 = (t + 2 < un.t1) ? page_of(t + 2) : 0;
+          ks = s < p.rs.N ? ldg_pinned_f32(&p.k_scale[s]) : 0.f;
         }
         const int ab = ait & (ACC_BUFS - 1);
         if (!(ok = mbar_wait_warp(acc_full(ab), (ait / ACC_BUFS) & 1, abort_flag, status))) break;
