@@ -74,9 +74,9 @@ typedef enum {
  * Fused operator (sections 3.2 and 4 of the indexer study): sampled
  * threshold per row, tcgen05 FP8 scoring with the ReLU / weight / head
  * reduction applied on chip, compare-and-append of candidates, four-pass radix
- * select in dedicated TopK warps, certificate check, and exact repair of rows
+ * select of each row's candidates, certificate check, and exact repair of rows
  * whose candidate set underflowed or overflowed.  The [Q, N] score matrix is
- * never written.
+ * never written (only the repaired rows' scores are, in library scratch).
  *
  *   q_fp8     [Q, 64, 128] e4m3 codes           q_scale [Q]  fp32 (> 0)
  *   k_fp8     [N, 128]     e4m3 codes           k_scale [N]  fp32 (> 0)
@@ -195,8 +195,9 @@ DSA_API int dsa_indexer_last_repaired_rows(dsa_stream_t stream, int32_t* rows_ou
 
 /* Tuning and diagnostics (process-wide; take effect on the next call). */
 typedef enum {
-  DSA_OPT_CHUNK_TILES = 1,    /* 128-key tiles per work unit of the persistent scorer (default 64); each unit may
-                                 leave at most 1024 candidates per row (more fails the certificate -> repair) */
+  DSA_OPT_CHUNK_TILES = 1,    /* 128-key tiles per work unit of the persistent scorer (default 64); a row's
+                                 16384 candidate slots are split evenly over its units' regions, and a region
+                                 that fills up fails the row's certificate (-> repair) */
   DSA_OPT_TAU_BIAS = 2,       /* added to every sampled threshold key: >0 forces underflow, <0 overflow (test knob; default 0) */
   DSA_OPT_PROFILE = 3,        /* 1: time the main kernel of each call with CUDA events (default 0) */
   DSA_OPT_GRID_CTAS = 4,      /* CTAs of the persistent kernels (default: SM count) */
