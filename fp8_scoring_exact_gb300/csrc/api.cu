@@ -266,7 +266,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cs.wide_hist = at<int32_t>(a, L.wide_hist);
   cs.out = out;
   cs.stats = st;
-  DSA_LAUNCH(launch_cand_select(cs, 3 * o.grid, stream));
+  DSA_LAUNCH(launch_cand_select(cs, 3 * o.grid, stream));  // 3 CTAs per SM (shared memory)
 
   // exact repair of rows whose certificate failed
   PlanParams rp = pp;

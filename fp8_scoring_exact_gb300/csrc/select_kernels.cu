@@ -519,37 +519,30 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
 constexpr uint32_t cs_align16(uint32_t x) { return (x + 15u) & ~15u; }
 constexpr uint32_t CS_OFF_KEY = 0;
 constexpr uint32_t CS_OFF_IDX = CS_OFF_KEY + CAND_CAP * 4;
-constexpr uint32_t CS_OFF_OFF = CS_OFF_IDX + CAND_CAP * 4;
+constexpr uint32_t CS_OFF_OFF = CS_OFF_IDX + CAND_CAP * 4;  // region offsets, then the compaction buffer
 constexpr uint32_t CS_OFF_HIST = cs_align16(CS_OFF_OFF + CAND_MAX_REGIONS * 4);
-constexpr uint32_t CS_OFF_MISC = cs_align16(CS_OFF_HIST + 256 * 4);
-constexpr uint32_t CS_OFF_BAR = cs_align16(CS_OFF_MISC + 32 * 4);
-constexpr uint32_t CAND_SMEM = CS_OFF_BAR + 16;
-// bulk-copy destinations and uint4 reads need 16 bytes, the mbarrier 8
-static_assert(CS_OFF_IDX % 16 == 0 && CS_OFF_HIST % 16 == 0 && CS_OFF_MISC % 16 == 0 && CS_OFF_BAR % 16 == 0,
+constexpr uint32_t CS_OFF_MISC = cs_align16(CS_OFF_HIST + 4 * 256 * 4);
+constexpr uint32_t CAND_SMEM = CS_OFF_MISC + 32 * 4;
+static_assert(CS_OFF_IDX % 16 == 0 && CS_OFF_OFF % 16 == 0 && CS_OFF_HIST % 16 == 0 && CS_OFF_MISC % 16 == 0,
               "candidate selector layout");
+static_assert(CAND_THREADS == 256, "block_select_kth / block_emit are written for 256 threads");
+static_assert(3 * (CAND_SMEM + 1024) <= 228 * 1024, "three candidate-selector CTAs per SM");
 constexpr int CS_PER_THREAD = CAND_MAX_REGIONS / CAND_THREADS;  // regions scanned per thread
 static_assert(CAND_MAX_REGIONS % CAND_THREADS == 0, "region scan");
 
-__global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandParams p) {
+__global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const CandParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* ckey = (uint32_t*)(smem + CS_OFF_KEY);
   int32_t* cidx = (int32_t*)(smem + CS_OFF_IDX);
-  int* off = (int*)(smem + CS_OFF_OFF);     // region start offsets (regions padded to 4 entries)
-  int* hist = (int*)(smem + CS_OFF_HIST);
-  // [0..3] digits, [4..5] emit counters, [6] gather verdict, [7] abort flag, [8..15] warp sums
+  int* off = (int*)(smem + CS_OFF_OFF);
+  int* shist = (int*)(smem + CS_OFF_HIST);
+  // [0..5] selection scratch, [6] failed-row slot, [8..15] warp sums, [16..23] warp real counts,
+  // [24..25] emission counters
   int* misc = (int*)(smem + CS_OFF_MISC);
-  const uint32_t bar = smem_u32(smem + CS_OFF_BAR);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWARPS = CAND_THREADS / 32;
   const int K = p.K;
   const int items = p.stats->n_groups * GROUP_ROWS;
-  if (tid == 0) {
-    misc[7] = 0;
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  uint32_t phase = 0;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int g = it / GROUP_ROWS, r = it % GROUP_ROWS;
     const Group* gp = p.groups + g;
@@ -560,9 +553,9 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
     const int wcap = region_cap(max(nu, 1));
     const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * UNIT_REGIONS;
     // certificate over the region counts (wcap + 1 = candidates were lost),
-    // and an exclusive scan of the 4-padded counts
+    // and an exclusive scan of the counts
     int c[CS_PER_THREAD];
-    int tpad = 0, treal = 0;
+    int tsum = 0;
     bool lost = nreg > CAND_MAX_REGIONS;
 #pragma unroll
     for (int i = 0; i < CS_PER_THREAD; ++i) {
@@ -570,40 +563,36 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
       const int x = j < nreg && j < CAND_MAX_REGIONS ? __ldcg(&cnt[j]) : 0;
       lost |= x > wcap;
       c[i] = min(x, wcap);
-      treal += c[i];
-      tpad += (c[i] + 3) & ~3;
+      tsum += c[i];
     }
-    int incl = tpad;
+    int incl = tsum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    const int wreal = __reduce_add_sync(0xffffffffu, treal);
     const bool any_lost = __syncthreads_or(lost);
     if (lane == 31) misc[8 + warp] = incl;
-    if (lane == 0) misc[16 + warp] = wreal;
     if (tid == 0) {
-      misc[4] = 0;
-      misc[5] = 0;
+      misc[24] = 0;
+      misc[25] = 0;
     }
     __syncthreads();
-    int wbase = 0, npad = 0, n = 0;
+    int wbase = 0, n = 0;
 #pragma unroll
     for (int w = 0; w < NWARPS; ++w) {
       const int ws = misc[8 + w];
       wbase += w < warp ? ws : 0;
-      npad += ws;
-      n += misc[16 + w];
+      n += ws;
     }
-    int run = wbase + incl - tpad;
+    int run = wbase + incl - tsum;
 #pragma unroll
     for (int i = 0; i < CS_PER_THREAD; ++i) {
       const int j = tid * CS_PER_THREAD + i;
       if (j < CAND_MAX_REGIONS) off[j] = run;
-      run += (c[i] + 3) & ~3;
+      run += c[i];
     }
-    if (n < K || any_lost || npad > CAND_CAP) {
+    if (n < K || any_lost || n > CAND_CAP) {
       if (tid == 0) {
         const int f = atomicAdd(&p.stats->fail_count, 1);
         p.failed_rows[f] = row;
@@ -618,43 +607,50 @@ __global__ void __launch_bounds__(CAND_THREADS) cand_select_kernel(const CandPar
       continue;
     }
     __syncthreads();
-    // gather: one bulk copy per non-empty region and array, issued by warp 0
+    // gather: tpr threads per region (more when regions are few), up to 16
+    // entries of each array in flight per thread; region sizes from the
+    // offsets (no count reload)
     const uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
     const int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
-    if (warp == 0) {
-      fence_proxy_async_smem();  // the previous item's reads of these buffers come first
-      if (lane == 0) mbar_arrive_expect_tx(bar, 2u * npad * 4u);
-      __syncwarp();
-      for (int j = lane; j < nreg; j += 32) {
-        const uint32_t bytes = (uint32_t)((min(__ldcg(&cnt[j]), wcap) + 3) & ~3) * 4u;
-        if (bytes) {
-          bulk_g2s(smem_u32(ckey + off[j]), ck + (int64_t)j * wcap, bytes, bar);
-          bulk_g2s(smem_u32(cidx + off[j]), ci + (int64_t)j * wcap, bytes, bar);
+    int tpr = 4;
+    while (tpr < 32 && tpr * 2 * nreg <= CAND_THREADS) tpr *= 2;
+    for (int j = tid / tpr; j < nreg; j += CAND_THREADS / tpr) {
+      const int o = off[j];
+      const int x = (j + 1 < nreg ? off[j + 1] : n) - o;
+      const uint32_t* sk = ck + (int64_t)j * wcap;
+      const int32_t* si = ci + (int64_t)j * wcap;
+      for (int i = tid % tpr; i < x; i += 16 * tpr) {
+        uint32_t kv[16];
+        int32_t iv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int e = i + tpr * q;
+          kv[q] = e < x ? __ldcg(&sk[e]) : 0u;
+          iv[q] = e < x ? __ldcg(&si[e]) : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int e = i + tpr * q;
+          if (e < x) {
+            ckey[o + e] = kv[q];
+            cidx[o + e] = iv[q];
+          }
         }
       }
-      if (lane == 0) misc[6] = mbar_wait(bar, phase & 1, (volatile int*)&misc[7], &p.stats->status) ? 1 : 0;
-      __syncwarp();
     }
-    ++phase;
-    __syncthreads();
-    if (!misc[6]) break;  // the copies did not land in time (status records it)
-    // key 0 in the pad slots (they hold whatever the regions held there)
-    for (int j = tid; j < nreg; j += CAND_THREADS) {
-      const int x = min(__ldcg(&cnt[j]), wcap);
-      for (int i = x; i < ((x + 3) & ~3); ++i) ckey[off[j] + i] = 0u;
+    // key 0 pads the list to a multiple of 4 (every real key is non-zero)
+    const int n4 = (n + 3) & ~3;
+    if (tid < n4 - n) {
+      ckey[n + tid] = 0u;
+      cidx[n + tid] = -1;
     }
     if (tid == 0) atomicAdd(&p.stats->cand_total, n);
     __syncthreads();
     uint32_t theta;
     int rr;
-    group_radix_select4(ckey, npad >> 2, K, hist, misc, tid, CAND_THREADS, 0, theta, rr);
-    group_emit4(ckey, cidx, npad >> 2, theta, rr, K, p.out + (int64_t)row * K, misc + 4, tid, CAND_THREADS);
+    block_select_kth(ckey, n4, K, shist, (uint32_t*)off, CAND_MAX_REGIONS, misc, theta, rr);
+    block_emit(ckey, cidx, n4, theta, rr, K, p.out + (int64_t)row * K, misc + 24);
     __syncthreads();
-  }
-  // a copy still in flight after a timeout must land before the CTA exits
-  if (misc[7] && tid == 0) {
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
   }
 }
 
