@@ -36,7 +36,7 @@ std::atomic<int64_t> g_launches{0};
 
 // ----------------------------------------------------------------- arena ----
 struct Layout {
-  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, unit_count, failed, wide_hist, wide_state;
+  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, unit_count, failed, wide_state;
   size_t cand_key, cand_idx, scores, total;
 };
 
@@ -62,7 +62,6 @@ Layout make_layout(int64_t R, int64_t G, int64_t cand_stride, int64_t max_units,
   L.runit_start = take((R + 1) * 4);
   L.unit_count = take((size_t)R * max_units * UNIT_REGIONS * 4);
   L.failed = take(R * 4);
-  L.wide_hist = cand_stride ? take((size_t)R * 256 * 4) : 0;
   L.wide_state = cand_stride ? take((size_t)R * WIDE_STATE * 4) : 0;
   L.cand_key = take((size_t)R * cand_stride * 4);
   L.cand_idx = take((size_t)R * cand_stride * 4);
@@ -263,7 +262,6 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cs.cand_idx = cp.cand_idx;
   cs.max_units = max_units;
   cs.failed_rows = at<int32_t>(a, L.failed);
-  cs.wide_hist = at<int32_t>(a, L.wide_hist);
   cs.out = out;
   cs.stats = st;
   DSA_LAUNCH(launch_cand_select(cs, 3 * o.grid, stream));  // 3 CTAs per SM (shared memory)
@@ -284,7 +282,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   rcp.ld = ld;
   DSA_LAUNCH(launch_score(tm_q, tm_k, rcp, o.grid, stream));
 
-  // their exact top-K over the whole GPU: four radix passes, then emission
+  // their exact top-K: one thread-block cluster per row
   WideParams wp{};
   wp.rs = rs;
   wp.K = K;
@@ -293,16 +291,10 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   wp.ld = ld;
   wp.rb = pp.rb;
   wp.re = pp.re;
-  wp.hist = cs.wide_hist;
   wp.state = at<int32_t>(a, L.wide_state);
   wp.out = out;
   wp.stats = st;
-  for (int pass = 0; pass < 4; ++pass) {
-    wp.pass = pass;
-    DSA_LAUNCH(launch_wide_hist(wp, 2 * o.grid, stream));
-    DSA_LAUNCH(launch_wide_pick(wp, stream));
-  }
-  DSA_LAUNCH(launch_wide_emit(wp, 2 * o.grid, stream));
+  DSA_LAUNCH(launch_wide_select(wp, o.grid / 4 > 0 ? o.grid / 4 : 1, stream));
   return DSA_OK;
 }
 

@@ -96,7 +96,6 @@ struct CandParams {
   const int32_t* cand_idx;
   int max_units;
   int32_t* failed_rows;        // [R] (appended, count in stats->fail_count)
-  int32_t* wide_hist;          // [R, 256]: cleared for each row queued for repair
   int32_t* out;                // [R, K]
   Stats* stats;
 };
@@ -115,20 +114,18 @@ struct SelectParams {
   Stats* stats;
 };
 
-// Grid-wide exact top-K of the score rows of the repair list (few long rows):
-// four 8-bit radix passes, each a histogram over row slices by many CTAs and
-// a digit pick by one warp per row, then emission by slices.
+// Exact top-K of the score rows of the repair list (few long rows): one
+// thread-block cluster per row, four 8-bit radix passes over row slices,
+// then emission by slices.
 struct WideParams {
   RowSpace rs;
   int K;
-  int pass;                    // 0..3 for wide_hist / wide_pick
   const int32_t* list;         // repair rows; count in stats->fail_count
   const float* scores;         // score row of list entry f at f * ld
   int64_t ld;
   const int32_t* rb;
   const int32_t* re;
-  int32_t* hist;               // [R, 256], zero before pass 0
-  int32_t* state;              // [R, WIDE_STATE]: prefix, mask, rem, emitted above, emitted equal, pick scratch
+  int32_t* state;              // [R, WIDE_STATE]: [3], [4] emission counters
   int32_t* out;                // [R, K]
   const Stats* stats;
 };
@@ -141,9 +138,7 @@ cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
                          cudaStream_t s);
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
 cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s);
-cudaError_t launch_wide_hist(const WideParams& p, int grid, cudaStream_t s);
-cudaError_t launch_wide_pick(const WideParams& p, cudaStream_t s);
-cudaError_t launch_wide_emit(const WideParams& p, int grid, cudaStream_t s);
+cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s);
 
 // number of work groups of G query rows for a row space
 template <int G>

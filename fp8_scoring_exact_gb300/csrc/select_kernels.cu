@@ -166,8 +166,8 @@ constexpr uint32_t SM_OFF_W = SM_OFF_SAMP + SAMPLE_ROWS * MAX_SAMPLES * 4;  // 4
 constexpr uint32_t SM_OFF_SC = SM_OFF_W + SAMPLE_ROWS * H * 4;
 constexpr uint32_t SM_OFF_HIST = SM_OFF_SC + TILE * 4;
 constexpr uint32_t SM_OFF_MISC = SM_OFF_HIST + 256 * 4;
-// 64 KB per CTA keeps at most 3 CTAs (3 x 128 TMEM columns) on an SM
-constexpr uint32_t SAMPLE_SMEM = 64 * 1024;
+// 52 KB per CTA: 4 CTAs (4 x 128 TMEM columns, all 512) fit on an SM
+constexpr uint32_t SAMPLE_SMEM = 52 * 1024;
 static_assert(SM_OFF_MISC + 64 + 1024 <= SAMPLE_SMEM, "sample smem");
 
 __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -238,20 +238,21 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
   bool ok = misc[6] != 0;
   const uint32_t idesc = idesc_e4m3_f32(TILE, H * nact);
   const int ntiles = ceil_div(m_u, TILE);
-  for (int tt = 0; tt < ntiles && ok; ++tt) {
+  // one sample key per thread: its 128 bytes and scale; the next tile's are
+  // loaded while the current tile is multiplied and reduced
+  uint4 chunk[8];
+  float ks = 0.f;
+  auto fetch = [&](int tt) {
     const int j = tt * TILE + tid;
-    const bool vj = j < m_u;
     const int s = first + j * S;
-    // gather one sample key per thread into the 128-byte-swizzled tile
-    uint4 chunk[8];
-    float ks = 0.f;
     int64_t slot = s;
-    bool in_cache = vj;
-    if (vj && rs.paged) {
+    bool in_cache = j < m_u;
+    if (in_cache && rs.paged) {
       const int page = __ldg(&rs.block_table[(int64_t)(act[0] / rs.next_n) * rs.max_pages + (s >> 6)]);
       in_cache = page >= 0 && page < rs.num_pages;  // a bad page id reads as a zero key
       slot = (int64_t)page * PAGE + (s & (PAGE - 1));
     }
+    ks = 0.f;
     if (in_cache) {
       const uint4* src = (const uint4*)(p.k + slot * D);
 #pragma unroll
@@ -261,6 +262,12 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
 #pragma unroll
       for (int c = 0; c < 8; ++c) chunk[c] = make_uint4(0, 0, 0, 0);
     }
+  };
+  fetch(0);
+  for (int tt = 0; tt < ntiles && ok; ++tt) {
+    const int j = tt * TILE + tid;
+    const bool vj = j < m_u;
+    // the fetched key into the 128-byte-swizzled tile
     uint8_t* krow = smem + SM_OFF_K + tid * D;
 #pragma unroll
     for (int c = 0; c < 8; ++c) *(uint4*)(krow + ((c ^ (tid & 7)) << 4)) = chunk[c];
@@ -275,6 +282,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
                  idesc, k > 0);
       mma_commit(bar);
     }
+    if (tt + 1 < ntiles) fetch(tt + 1);
     if (tid == 0) misc[6] = mbar_wait(bar, (tt + 1) & 1, abort_flag, &p.stats->status) ? 1 : 0;
     __syncwarp();
     __syncthreads();
@@ -596,13 +604,8 @@ __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const Cand
       if (tid == 0) {
         const int f = atomicAdd(&p.stats->fail_count, 1);
         p.failed_rows[f] = row;
-        misc[6] = f;
         atomicAdd(n < K ? &p.stats->underflow : &p.stats->overflow, 1);
       }
-      __syncthreads();
-      // the repair's radix histogram of this list entry starts from zero
-      const int f = misc[6];
-      for (int i = tid; i < 256; i += CAND_THREADS) p.wide_hist[(int64_t)f * 256 + i] = 0;
       __syncthreads();
       continue;
     }
@@ -666,107 +669,124 @@ cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s) {
 }
 
 // ============================================================ wide select ==
-// The rows whose certificate failed are few and long: their exact top-K runs
-// over the whole GPU.  Keys are the order-preserving images of the repaired
-// fp32 scores; each pass fixes one byte of the K-th largest key (the radix
-// select of the method, spread over row slices).
-constexpr int WIDE_THREADS = 256;
-constexpr int WIDE_SLICES = 32;  // CTAs per row and pass
+// The rows whose certificate failed are few and long: each is selected by a
+// cluster of WIDE_CLUSTER CTAs (thread-block cluster), one slice of the row
+// per CTA.  Keys are the order-preserving images of the repaired fp32
+// scores; each radix pass fixes one byte of the K-th largest key: every CTA
+// histograms its slice, rank 0 sums the cluster's histograms through
+// distributed shared memory and picks the digit, and every CTA reads it
+// back; hardware cluster barriers separate the phases.  One launch for all
+// rows, which exits at once when no row failed.
+constexpr int WIDE_CLUSTER = 8;
+constexpr int WIDE_THREADS = 512;
 
-// Visits the keys of slice `sl` of list entry f: f(key, index, valid) on all
-// lanes, four keys per float4 load (the slice bounds are 4-aligned; keys
-// outside [b, e) come with valid = false).
-template <class F>
-__device__ __forceinline__ void wide_visit(const WideParams& p, int f, int sl, int b, int e, F&& fn) {
-  const float* srow = p.scores + (int64_t)f * p.ld;
-  const int a = b & ~3;
-  const int n4 = ((e + 3) >> 2) - (a >> 2);              // float4s covering [a, e)
-  const int per = ceil_div(n4, WIDE_SLICES);
-  const int v0 = sl * per, v1 = min(n4, v0 + per);
-  const float4* v4 = reinterpret_cast<const float4*>(srow + a);
-  for (int base = v0; base < v1; base += WIDE_THREADS) {
-    const int vi = base + (int)threadIdx.x;
-    const bool in = vi < v1;
-    const float4 x = in ? __ldcg(&v4[vi]) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const int i0 = a + 4 * vi;
-    fn(ordered_key(x.x), i0 + 0, in && i0 + 0 >= b && i0 + 0 < e);
-    fn(ordered_key(x.y), i0 + 1, in && i0 + 1 >= b && i0 + 1 < e);
-    fn(ordered_key(x.z), i0 + 2, in && i0 + 2 >= b && i0 + 2 < e);
-    fn(ordered_key(x.w), i0 + 3, in && i0 + 3 >= b && i0 + 3 < e);
-  }
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// all threads of all CTAs of the cluster; orders shared and global memory
+// at cluster scope
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// 32-bit load from the shared memory of CTA `rank` of the cluster, at the
+// offset `p` has in this CTA
+__device__ __forceinline__ int ld_dsmem(const int* p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
 }
 
-__global__ void __launch_bounds__(WIDE_THREADS) wide_hist_kernel(const WideParams p) {
-  __shared__ int h[256];
-  const int lane = threadIdx.x & 31;
-  const int shift = 24 - 8 * p.pass;
-  const int items = p.stats->fail_count * WIDE_SLICES;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int f = it / WIDE_SLICES, sl = it % WIDE_SLICES;
-    const int row = p.list[f];
-    const int32_t* st = p.state + (int64_t)f * WIDE_STATE;
-    const uint32_t prefix = p.pass ? (uint32_t)st[0] : 0u, mask = p.pass ? (uint32_t)st[1] : 0u;
-    for (int i = threadIdx.x; i < 256; i += WIDE_THREADS) h[i] = 0;
-    __syncthreads();
-    wide_visit(p, f, sl, p.rb[row], p.re[row], [&](uint32_t k, int, bool v) {
-      hist_add(v && (k & mask) == prefix, (k >> shift) & 0xFFu, lane, h);
-    });
-    __syncthreads();
-    for (int i = threadIdx.x; i < 256; i += WIDE_THREADS)
-      if (h[i]) atomicAdd(&p.hist[(int64_t)f * 256 + i], h[i]);
-    __syncthreads();
-  }
-}
-
-// One warp per list entry: the digit of this pass, then the histogram is
-// cleared for the next pass (and the emission counters after the last).
-__global__ void __launch_bounds__(WIDE_THREADS) wide_pick_kernel(const WideParams p) {
-  const int lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * (WIDE_THREADS / 32);
-  const int shift = 24 - 8 * p.pass;
+__global__ void __cluster_dims__(WIDE_CLUSTER, 1, 1) __launch_bounds__(WIDE_THREADS)
+    wide_cluster_kernel(const WideParams p) {
+  __shared__ int hist[256];
+  __shared__ int tot[256];
+  __shared__ int ctl[4];  // rank 0: digit, remaining rank
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
   const int nf = p.stats->fail_count;
-  for (int f = blockIdx.x * (WIDE_THREADS / 32) + (threadIdx.x >> 5); f < nf; f += nwarps) {
-    int32_t* st = p.state + (int64_t)f * WIDE_STATE;
-    int32_t* hist = p.hist + (int64_t)f * 256;
-    const int rem = p.pass ? st[2] : p.K;
-    radix_pick_digit(hist, rem, st + 8);
-    __syncwarp();
-    for (int i = lane; i < 256; i += 32) hist[i] = 0;
-    if (lane == 0) {
-      const uint32_t prefix = (p.pass ? (uint32_t)st[0] : 0u) | ((uint32_t)st[8] << shift);
-      const uint32_t mask = (p.pass ? (uint32_t)st[1] : 0u) | (0xFFu << shift);
-      st[0] = (int32_t)prefix;
-      st[1] = (int32_t)mask;
-      st[2] = st[9];
-      st[3] = 0;
-      st[4] = 0;
-    }
-  }
-}
-
-// Every key above the K-th key and the first `rem` keys equal to it (the
-// pass-3 prefix is that key), slots reserved once per warp.
-__global__ void __launch_bounds__(WIDE_THREADS) wide_emit_kernel(const WideParams p) {
-  const int lane = threadIdx.x & 31;
+  const int K = p.K;
   uint32_t lt;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
-  const int K = p.K;
-  const int items = p.stats->fail_count * WIDE_SLICES;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int f = it / WIDE_SLICES, sl = it % WIDE_SLICES;
+  for (int f = (int)cluster_id_x(); f < nf; f += (int)cluster_count_x()) {
     const int row = p.list[f];
-    int32_t* st = p.state + (int64_t)f * WIDE_STATE;
-    const uint32_t theta = (uint32_t)st[0];
-    const int rr = st[2];
+    const int b = p.rb[row], e = p.re[row];
+    const float* srow = p.scores + (int64_t)f * p.ld;
+    // this CTA's slice: float4s covering [a, e) split in WIDE_CLUSTER parts
+    const int a = b & ~3;
+    const int n4 = ((e + 3) >> 2) - (a >> 2);
+    const int per = ceil_div(n4, WIDE_CLUSTER);
+    const int v0 = (int)rank * per, v1 = min(n4, v0 + per);
+    const float4* v4 = reinterpret_cast<const float4*>(srow + a);
+    auto visit = [&](auto&& fn) {  // fn(key, index, valid) on all lanes, 4 keys per float4
+      for (int base = v0; base < v1; base += WIDE_THREADS) {
+        const int vi = base + tid;
+        const bool in = vi < v1;
+        const float4 x = in ? __ldcg(&v4[vi]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int i0 = a + 4 * vi;
+        fn(ordered_key(x.x), i0 + 0, in && i0 + 0 >= b && i0 + 0 < e);
+        fn(ordered_key(x.y), i0 + 1, in && i0 + 1 >= b && i0 + 1 < e);
+        fn(ordered_key(x.z), i0 + 2, in && i0 + 2 >= b && i0 + 2 < e);
+        fn(ordered_key(x.w), i0 + 3, in && i0 + 3 >= b && i0 + 3 < e);
+      }
+    };
+    uint32_t prefix = 0, mask = 0;
+    int rem = K;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = tid; i < 256; i += WIDE_THREADS) hist[i] = 0;
+      __syncthreads();
+      visit([&](uint32_t k, int, bool v) { hist_add(v && (k & mask) == prefix, (k >> shift) & 0xFFu, lane, hist); });
+      cluster_sync_all();  // every CTA's histogram is complete
+      if (rank == 0) {
+        for (int i = tid; i < 256; i += WIDE_THREADS) {
+          int sum = 0;
+#pragma unroll
+          for (int r = 0; r < WIDE_CLUSTER; ++r) sum += ld_dsmem(&hist[i], (uint32_t)r);
+          tot[i] = sum;
+        }
+        __syncthreads();
+        if (tid < 32) radix_pick_digit(tot, rem, ctl);
+      }
+      cluster_sync_all();  // the digit is in rank 0's ctl
+      const uint32_t digit = (uint32_t)ld_dsmem(&ctl[0], 0);
+      rem = ld_dsmem(&ctl[1], 0);
+      prefix |= digit << shift;
+      mask |= 0xFFu << shift;
+      if (pass == 3 && rank == 0 && tid == 0) {
+        p.state[(int64_t)f * WIDE_STATE + 3] = 0;  // emission counters
+        p.state[(int64_t)f * WIDE_STATE + 4] = 0;
+      }
+      cluster_sync_all();  // everyone read the digit before the next pass rewrites it
+    }
+    // every key above the K-th key and the first `rem` keys equal to it,
+    // slots reserved once per warp
+    const uint32_t theta = prefix;
+    const int rr = rem;
+    int32_t* cnt = p.state + (int64_t)f * WIDE_STATE;
     int32_t* o = p.out + (int64_t)row * K;
-    wide_visit(p, f, sl, p.rb[row], p.re[row], [&](uint32_t k, int i, bool v) {
+    visit([&](uint32_t k, int i, bool v) {
       const bool gt = v && k > theta, eq = v && k == theta;
       const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
       if (!(mg | me)) return;
       int bg = 0, be = 0;
       if (lane == 0) {
-        if (mg) bg = atomicAdd(&st[3], __popc(mg));
-        if (me) be = atomicAdd(&st[4], __popc(me));
+        if (mg) bg = atomicAdd(&cnt[3], __popc(mg));
+        if (me) be = atomicAdd(&cnt[4], __popc(me));
       }
       bg = __shfl_sync(0xffffffffu, bg, 0);
       be = __shfl_sync(0xffffffffu, be, 0);
@@ -777,20 +797,12 @@ __global__ void __launch_bounds__(WIDE_THREADS) wide_emit_kernel(const WideParam
         if (q < rr) o[K - rr + q] = p.rs.paged ? out_index(p.rs, row, i) : i;
       }
     });
+    cluster_sync_all();  // the row is done before the cluster moves on
   }
 }
 
-cudaError_t launch_wide_hist(const WideParams& p, int grid, cudaStream_t s) {
-  wide_hist_kernel<<<grid, WIDE_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
-}
-cudaError_t launch_wide_pick(const WideParams& p, cudaStream_t s) {
-  const int grid = max(1, ceil_div(p.rs.R, WIDE_THREADS / 32));
-  wide_pick_kernel<<<min(grid, 256), WIDE_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
-}
-cudaError_t launch_wide_emit(const WideParams& p, int grid, cudaStream_t s) {
-  wide_emit_kernel<<<grid, WIDE_THREADS, 0, s>>>(p);
+cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s) {
+  wide_cluster_kernel<<<clusters * WIDE_CLUSTER, WIDE_THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 
