@@ -37,10 +37,14 @@ std::atomic<int64_t> g_launches{0};
 // ----------------------------------------------------------------- arena ----
 struct Layout {
   size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, unit_count, failed, wide_state;
-  size_t cand_key, cand_idx, scores, total;
+  size_t cand_key, cand_idx, scores;
+  size_t srb, sre, sgroups, sunit_start, skeys, sks, sscores;  // dense sampled thresholds
+  size_t total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int64_t SAMPLE_LD = (MAX_SAMPLES + 2 + 3) / 4 * 4;  // sample-score row stride
 
 // cand_stride: candidate slots per row (0: no candidate buffers); max_units:
 // work units per group at most (per-row unit counts)
@@ -66,6 +70,15 @@ Layout make_layout(int64_t R, int64_t G, int64_t cand_stride, int64_t max_units,
   L.cand_key = take((size_t)R * cand_stride * 4);
   L.cand_idx = take((size_t)R * cand_stride * 4);
   L.scores = take((size_t)score_rows * ld * 4);
+  if (cand_stride) {  // fused calls: the sample grid's key set and its scores
+    L.srb = take(R * 4);
+    L.sre = take(R * 4);
+    L.sgroups = take(G * sizeof(Group));
+    L.sunit_start = take((G + 1) * 4);
+    L.skeys = take((size_t)(MAX_SAMPLES + 2) * D);
+    L.sks = take((size_t)(MAX_SAMPLES + 2) * 4);
+    L.sscores = take((size_t)R * SAMPLE_LD * 4);
+  }
   L.total = off;
   return L;
 }
@@ -199,7 +212,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
 
   PlanParams pp{};
   pp.rs = rs;
-  pp.repair = 0;
+  pp.plan = PLAN_MAIN;
   pp.K = K;
   pp.trivial_len = K;
   pp.chunk_tiles = o.chunk;
@@ -213,27 +226,97 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   pp.stats = st;
   DSA_LAUNCH(launch_plan(pp, stream));
 
-  SampleParams sp{};
-  sp.rs = rs;
-  sp.K = K;
-  sp.target16 = o.target16;
-  sp.tau_bias = o.bias;
-  sp.k = k_raw;
-  sp.k_scale = ks_raw;
-  sp.q_scale = q_scale;
-  sp.w = w;
-  sp.rb = pp.rb;
-  sp.re = pp.re;
-  sp.tau = at<uint32_t>(a, L.tau);
-  sp.out = out;
-  sp.stats = st;
-  DSA_LAUNCH(launch_sample(tm_q, sp, n_pairs(rs), stream));
+  uint32_t* tau = at<uint32_t>(a, L.tau);
+  const int S = sample_stride_for(rs.N);
+  const int ns = rs.N > SAMPLE_OFFSET ? ceil_div(rs.N - SAMPLE_OFFSET, S) : 0;
+  if (!rs.paged && ns > TILE) {
+    // sampled thresholds: the grid keys gathered once, scored by the scorer
+    // for every row, then one threshold per row (a grid of one tile or less
+    // is cheaper in the per-pair sampling kernel below)
+    SamplePrepParams sx{};
+    sx.rs = rs;
+    sx.K = K;
+    sx.stride = S;
+    sx.n_samples = ns;
+    sx.k = k_raw;
+    sx.k_scale = ks_raw;
+    sx.sk = at<uint8_t>(a, L.skeys);
+    sx.sks = at<float>(a, L.sks);
+    sx.rb = pp.rb;
+    sx.re = pp.re;
+    sx.out = out;
+    sx.stats = st;
+    DSA_LAUNCH(launch_sample_prep(sx, stream));
+    PlanParams spl = pp;
+    spl.plan = PLAN_SAMPLE;
+    spl.sample_stride = S;
+    spl.chunk_tiles = WHOLE_PAIR_TILES;
+    spl.row_begin_in = pp.rb;
+    spl.row_end_in = pp.re;
+    spl.rb = at<int32_t>(a, L.srb);
+    spl.re = at<int32_t>(a, L.sre);
+    spl.groups = at<Group>(a, L.sgroups);
+    spl.unit_start = at<int32_t>(a, L.sunit_start);
+    DSA_LAUNCH(launch_plan(spl, stream));
+    {
+      CUtensorMap tks;
+      if (!tmap_rows_u8(&tks, sx.sk, (uint64_t)ns, TILE)) return DSA_ERR_CUDA;
+      RowSpace srs = rs;
+      srs.N = ns;
+      ScoreParams scp{};
+      scp.rs = srs;
+      scp.mode = MODE_STORE;
+      scp.chunk_tiles = WHOLE_PAIR_TILES;
+      scp.plan = PLAN_SAMPLE;
+      scp.k_scale = sx.sks;
+      scp.q_scale = q_scale;
+      scp.w = w;
+      scp.rb = spl.rb;
+      scp.re = spl.re;
+      scp.groups = spl.groups;
+      scp.unit_start = spl.unit_start;
+      scp.scores = at<float>(a, L.sscores);
+      scp.ld = SAMPLE_LD;
+      scp.stats = st;
+      DSA_LAUNCH(launch_score(tm_q, tks, scp, o.grid, stream));
+    }
+    SampleTauParams tp{};
+    tp.rs = rs;
+    tp.K = K;
+    tp.target16 = o.target16;
+    tp.tau_bias = o.bias;
+    tp.rb = pp.rb;
+    tp.re = pp.re;
+    tp.srb = spl.rb;
+    tp.sre = spl.re;
+    tp.sscores = at<float>(a, L.sscores);
+    tp.sld = SAMPLE_LD;
+    tp.tau = tau;
+    tp.stats = st;
+    DSA_LAUNCH(launch_sample_tau(tp, stream));
+  } else {
+    SampleParams sp{};
+    sp.rs = rs;
+    sp.K = K;
+    sp.target16 = o.target16;
+    sp.tau_bias = o.bias;
+    sp.k = k_raw;
+    sp.k_scale = ks_raw;
+    sp.q_scale = q_scale;
+    sp.w = w;
+    sp.rb = pp.rb;
+    sp.re = pp.re;
+    sp.tau = tau;
+    sp.out = out;
+    sp.stats = st;
+    DSA_LAUNCH(launch_sample(tm_q, sp, n_pairs(rs), stream));
+  }
 
   ScoreParams cp{};
   cp.rs = rs;
   cp.mode = MODE_FILTER;
   cp.chunk_tiles = o.chunk;
-  cp.repair = 0;
+  cp.plan = PLAN_MAIN;
   cp.k_scale = ks_raw;
   cp.q_scale = q_scale;
   cp.w = w;
@@ -241,7 +324,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cp.re = pp.re;
   cp.groups = pp.groups;
   cp.unit_start = pp.unit_start;
-  cp.tau = sp.tau;
+  cp.tau = tau;
   cp.cand_key = at<uint32_t>(a, L.cand_key);
   cp.cand_idx = at<int32_t>(a, L.cand_idx);
   cp.unit_count = at<int32_t>(a, L.unit_count);
@@ -268,14 +351,14 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
 
   // exact repair of rows whose certificate failed
   PlanParams rp = pp;
-  rp.repair = 1;
+  rp.plan = PLAN_REPAIR;
   rp.groups = at<Group>(a, L.rgroups);
   rp.unit_start = at<int32_t>(a, L.runit_start);
   DSA_LAUNCH(launch_plan(rp, stream));
 
   ScoreParams rcp = cp;
   rcp.mode = MODE_STORE;
-  rcp.repair = 1;
+  rcp.plan = PLAN_REPAIR;
   rcp.groups = rp.groups;
   rcp.unit_start = rp.unit_start;
   rcp.scores = at<float>(a, L.scores);

@@ -48,6 +48,10 @@ constexpr int MAX_SAMPLES = 1024;  // per row; longer rows widen the stride
 constexpr int SELECT_THREADS = 512;
 constexpr int SELECT_CAP = 12288;  // candidates the standalone selector keeps in SMEM
 
+// Which plan a kernel reads: every row, the rows queued for repair, or the
+// rows' sample grids.
+enum Plan : int { PLAN_MAIN = 0, PLAN_REPAIR = 1, PLAN_SAMPLE = 2 };
+
 // MODE_STORE: fp32 scores to a matrix.  MODE_FILTER: scores at or above the
 // row's threshold become candidates for the candidate selector.
 enum Mode : int { MODE_STORE = 0, MODE_FILTER = 1 };
@@ -68,7 +72,9 @@ struct Stats {
   int total_units;
   int r_groups;      // repair plan
   int r_units;
-  int pad[6];
+  int s_groups;      // sample plan
+  int s_units;
+  int pad[4];
 };
 
 // A work group: up to 2 query rows that stream the same keys.  Key range is

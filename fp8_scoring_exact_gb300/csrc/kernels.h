@@ -28,13 +28,14 @@ constexpr int WHOLE_PAIR_TILES = 1 << 24;
 
 struct PlanParams {
   RowSpace rs;
-  int repair;                  // 0: plan every row; 1: plan the rows queued for repair
+  int plan;                    // PLAN_MAIN: every row; PLAN_REPAIR: the queued rows; PLAN_SAMPLE: sample grids
+  int sample_stride;           // PLAN_SAMPLE: grid keys are SAMPLE_OFFSET + j * sample_stride
   int K;
   int trivial_len;             // rows with L <= trivial_len are not scored
   int chunk_tiles;
   const int32_t* row_begin_in; // dense input ranges
   const int32_t* row_end_in;
-  int32_t* rb;                 // [R] validated ranges (written in main mode)
+  int32_t* rb;                 // [R] validated ranges (written in main mode; sample-grid ranges in sample mode)
   int32_t* re;
   Group* groups;               // [G]
   int32_t* unit_start;         // [G + 1]
@@ -62,7 +63,7 @@ struct ScoreParams {
   RowSpace rs;
   int mode;                    // MODE_STORE or MODE_FILTER
   int chunk_tiles;
-  int repair;                  // which plan to read
+  int plan;                    // which plan to read (PLAN_*)
   const float* k_scale;        // dense [N] or paged [P * 64]; read by the epilogue
   const float* q_scale;
   const float* w;
@@ -114,6 +115,13 @@ struct SelectParams {
   Stats* stats;
 };
 
+// grid stride of the sampled thresholds for rows up to N keys: 200, widened
+// so that no row has more than MAX_SAMPLES grid keys
+__host__ __device__ inline int sample_stride_for(int N) {
+  const int widen = (N + SAMPLE_STRIDE * MAX_SAMPLES - 1) / (SAMPLE_STRIDE * MAX_SAMPLES);
+  return SAMPLE_STRIDE * (widen > 1 ? widen : 1);
+}
+
 // Exact top-K of the score rows of the repair list (few long rows): one
 // thread-block cluster per row, four 8-bit radix passes over row slices,
 // then emission by slices.
@@ -131,9 +139,44 @@ struct WideParams {
 };
 constexpr int WIDE_STATE = 16;
 
+// Sampled thresholds of dense rows from the scorer: sample_prep gathers the
+// grid keys (SAMPLE_OFFSET + j * stride) into a contiguous key set and writes
+// the trivial rows; the scorer (store mode, sample plan) scores every row's
+// grid keys; sample_tau selects each row's threshold from its sample scores.
+struct SamplePrepParams {
+  RowSpace rs;                 // dense
+  int K;
+  int stride;
+  int n_samples;               // grid keys below N
+  const uint8_t* k;            // [N, 128]
+  const float* k_scale;
+  uint8_t* sk;                 // [n_samples, 128] (written)
+  float* sks;                  // [n_samples] (written)
+  const int32_t* rb;           // validated ranges
+  const int32_t* re;
+  int32_t* out;                // [R, K]: trivial rows written
+  Stats* stats;
+};
+struct SampleTauParams {
+  RowSpace rs;
+  int K;
+  int target16;
+  int64_t tau_bias;
+  const int32_t* rb;           // key-space ranges
+  const int32_t* re;
+  const int32_t* srb;          // sample-grid ranges
+  const int32_t* sre;
+  const float* sscores;        // [R, sld] sample scores (row r at r * sld)
+  int64_t sld;
+  uint32_t* tau;               // [R] (written for rows with L > K)
+  Stats* stats;
+};
+
 // host launchers (return cudaGetLastError() of the launch)
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_pairs, cudaStream_t s);
+cudaError_t launch_sample_prep(const SamplePrepParams& p, cudaStream_t s);
+cudaError_t launch_sample_tau(const SampleTauParams& p, cudaStream_t s);
 cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
                          cudaStream_t s);
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);

@@ -125,8 +125,12 @@ template <int MODE, bool PAGED>
 __global__ void __launch_bounds__(SCORE_THREADS, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const ScoreParams p) {
-  const int n_groups = p.repair ? p.stats->r_groups : p.stats->n_groups;
-  const int total = p.repair ? p.stats->r_units : p.stats->total_units;
+  const int n_groups = p.plan == PLAN_REPAIR   ? p.stats->r_groups
+                       : p.plan == PLAN_SAMPLE ? p.stats->s_groups
+                                               : p.stats->n_groups;
+  const int total = p.plan == PLAN_REPAIR   ? p.stats->r_units
+                    : p.plan == PLAN_SAMPLE ? p.stats->s_units
+                                            : p.stats->total_units;
   if ((int)blockIdx.x >= total) return;  // uniform over the CTA: no work
 
   extern __shared__ uint8_t smem_raw[];

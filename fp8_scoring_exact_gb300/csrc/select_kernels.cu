@@ -14,9 +14,11 @@
 namespace dsa {
 
 // ===================================================================== plan ==
-// One CTA of 1024 threads.  Main mode: validate every row's range, zero the
-// per-row counters, form the pairs and the unit prefix sum.  Repair mode: one
-// group per queued row.
+// One CTA of 1024 threads.  Main plan: validate every row's range, zero the
+// per-call counters, form the row groups and the unit prefix sum.  Repair
+// plan: one group per queued row.  Sample plan (dense): the same groups over
+// each row's sample-grid range (rows with L <= K left out), written to
+// rb / re in grid-index space.
 constexpr int PLAN_THREADS = 1024;
 
 __device__ __forceinline__ int block_inclusive_scan(int v, int* warp_sums) {
@@ -56,7 +58,19 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
   const RowSpace& rs = p.rs;
   const int tid = threadIdx.x;
   int G;
-  if (!p.repair) {
+  if (p.plan == PLAN_SAMPLE) {
+    // grid key j sits at SAMPLE_OFFSET + j * S: row [b, e) holds j in [j0, j1)
+    const int S = p.sample_stride;
+    for (int row = tid; row < rs.R; row += PLAN_THREADS) {
+      const int b = p.row_begin_in[row], e = p.row_end_in[row];
+      const int j0 = b > SAMPLE_OFFSET ? ceil_div(b - SAMPLE_OFFSET, S) : 0;
+      const int j1 = e > SAMPLE_OFFSET ? ceil_div(e - SAMPLE_OFFSET, S) : 0;
+      p.rb[row] = j0;
+      p.re[row] = max(j0, j1);
+    }
+    __syncthreads();
+    G = n_groups(rs);
+  } else if (p.plan == PLAN_MAIN) {
     if (tid == 0) {
       Stats z = {};
       *p.stats = z;
@@ -102,13 +116,15 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
       grp.lo = 0x7fffffff;
       grp.hi = 0;
       for (int i = 0; i < GROUP_ROWS; ++i) grp.row[i] = grp.slot[i] = 0;
-      if (!p.repair) {
+      if (p.plan != PLAN_REPAIR) {
         int rows[GROUP_ROWS];
         const int nr = rows_of_group<GROUP_ROWS>(rs, g, rows);
         grp.seq = rs.paged ? rows[0] / rs.next_n : -1;
         for (int i = 0; i < nr; ++i) {
           const int b = p.rb[rows[i]], e = p.re[rows[i]];
-          if (e - b > p.trivial_len) {
+          // the sample plan leaves out the rows the main plan calls trivial
+          const int len = p.plan == PLAN_SAMPLE ? p.row_end_in[rows[i]] - p.row_begin_in[rows[i]] : e - b;
+          if (len > p.trivial_len && e > b) {
             grp.row[grp.nrows] = rows[i];
             grp.slot[grp.nrows] = rows[i];
             ++grp.nrows;
@@ -138,12 +154,15 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
   }
   if (tid == 0) {
     p.unit_start[0] = 0;
-    if (!p.repair) {
+    if (p.plan == PLAN_MAIN) {
       p.stats->n_groups = G;
       p.stats->total_units = s_carry;
-    } else {
+    } else if (p.plan == PLAN_REPAIR) {
       p.stats->r_groups = G;
       p.stats->r_units = s_carry;
+    } else {
+      p.stats->s_groups = G;
+      p.stats->s_units = s_carry;
     }
   }
 }
@@ -342,6 +361,108 @@ cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_
   }
   if (n_pairs_ <= 0) return cudaSuccess;
   sample_kernel<<<n_pairs_, SAMPLE_THREADS, SAMPLE_SMEM, s>>>(tm_q, p);
+  return cudaGetLastError();
+}
+
+// ============================================================ sample (dense) ==
+// Dense rows sample one global grid of keys (SAMPLE_OFFSET + j * stride, the
+// same keys for every row; a row uses the grid keys inside its range), so
+// the grid is gathered once into a contiguous key set and scored by the
+// persistent scorer like any key set.  This kernel gathers it and writes the
+// rows with L <= K (their output is every valid index).
+constexpr int PREP_THREADS = 256;
+
+__global__ void __launch_bounds__(PREP_THREADS) sample_prep_kernel(const SamplePrepParams p) {
+  const int gt = blockIdx.x * PREP_THREADS + threadIdx.x;
+  const int nthreads = gridDim.x * PREP_THREADS;
+  // 8 threads per grid key: 16 bytes each
+  for (int i = gt; i < p.n_samples * 8; i += nthreads) {
+    const int j = i >> 3, c = i & 7;
+    const int64_t src = (int64_t)SAMPLE_OFFSET + (int64_t)j * p.stride;
+    reinterpret_cast<uint4*>(p.sk + (int64_t)j * D)[c] = __ldg(reinterpret_cast<const uint4*>(p.k + src * D) + c);
+    if (c == 0) p.sks[j] = __ldg(&p.k_scale[src]);
+  }
+  // trivial rows: one warp per row
+  const int warp = gt >> 5, nwarps = nthreads >> 5, lane = threadIdx.x & 31;
+  int ntriv = 0;
+  for (int row = warp; row < p.rs.R; row += nwarps) {
+    const int b = p.rb[row], e = p.re[row];
+    if (e - b > p.K) continue;
+    int32_t* o = p.out + (int64_t)row * p.K;
+    for (int i = lane; i < p.K; i += 32) o[i] = i < e - b ? b + i : -1;
+    ++ntriv;
+  }
+  if (lane == 0 && ntriv) atomicAdd(&p.stats->trivial, ntriv);
+}
+
+// One warp per row with L > K: the threshold is the sample of descending rank
+// ceil(m * target / L) among the row's m grid-key scores (radix select in a
+// per-warp histogram), plus the test bias; 0 (every key passes) when the
+// rank falls outside the sample.
+constexpr int TAU_THREADS = 256;
+constexpr int TAU_KEYS_PER_LANE = MAX_SAMPLES / 32;
+
+__global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTauParams p) {
+  __shared__ int hist_all[TAU_THREADS / 32][256];
+  __shared__ int pick_all[TAU_THREADS / 32][4];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int* hist = hist_all[wid];
+  int* pick = pick_all[wid];
+  const int warp = blockIdx.x * (TAU_THREADS / 32) + wid, nwarps = gridDim.x * (TAU_THREADS / 32);
+  const int target = (int)(((int64_t)p.target16 * p.K) / 16);
+  for (int row = warp; row < p.rs.R; row += nwarps) {
+    const int L = p.re[row] - p.rb[row];
+    if (L <= p.K) continue;
+    const int j0 = p.srb[row];
+    const int m = min(p.sre[row] - j0, MAX_SAMPLES);
+    const int rank = sample_rank(m, L, target);
+    uint32_t tau = 0u;
+    if (m > 0 && rank >= 1 && rank <= m) {
+      uint32_t key[TAU_KEYS_PER_LANE];
+      const float* sr = p.sscores + (int64_t)row * p.sld + j0;
+#pragma unroll
+      for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
+        const int i = q * 32 + lane;
+        key[q] = i < m ? ordered_key(__ldcg(&sr[i])) : 0u;
+      }
+      uint32_t prefix = 0, mask = 0;
+      int rem = rank;
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+#pragma unroll
+        for (int i = lane; i < 256; i += 32) hist[i] = 0;
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
+          const int i = q * 32 + lane;
+          if (i < m && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & 0xFFu], 1);
+        }
+        __syncwarp();
+        radix_pick_digit(hist, rem, pick);
+        __syncwarp();
+        prefix |= (uint32_t)pick[0] << shift;
+        mask |= 0xFFu << shift;
+        rem = pick[1];
+        __syncwarp();
+      }
+      tau = prefix;
+      if (p.tau_bias != 0) {
+        const int64_t t = (int64_t)tau + p.tau_bias;
+        tau = (uint32_t)(t < 0 ? 0 : (t > 0xffffffffll ? 0xffffffffll : t));
+      }
+    }
+    if (lane == 0) p.tau[row] = tau;
+  }
+}
+
+cudaError_t launch_sample_prep(const SamplePrepParams& p, cudaStream_t s) {
+  sample_prep_kernel<<<64, PREP_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_sample_tau(const SampleTauParams& p, cudaStream_t s) {
+  const int blocks = max(1, min(1024, ceil_div(p.rs.R, TAU_THREADS / 32)));
+  sample_tau_kernel<<<blocks, TAU_THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 

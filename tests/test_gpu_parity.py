@@ -159,6 +159,20 @@ def test_edge_ranges(B):
         assert check_dense_rows(inp, out, range(inp.Q)) == {}
 
 
+def test_grid_sampling_with_offset_ranges(B):
+    """Rows long enough that the thresholds come from the shared sample grid
+    scored by the main scorer (more than one 128-key tile of grid keys):
+    ranges starting on, just before and just after grid keys, L = K, L = K + 1,
+    empty, short and long rows, all exact."""
+    K, N = 2048, 40000
+    inp = S.make_dense(16, N, K=K, seed=9, causal=False)
+    inp.row_begin[:] = [0, 1, 99, 100, 101, 12345, 39000, 5000, 5000, 20000, 300, 7, 25000, 0, 150, 33333]
+    inp.row_end[:] = [N, N, N, 30000, 30000, 39999, N, 5000 + K + 1, 5000 + K, 20000, 2900, 28001, N, 12001, N - 1, N]
+    out = B.indexer_topk(*dense_args(inp), K=K).cpu().numpy()
+    _status_ok(B)
+    assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
 def test_invalid_range_reports_status_and_pads(B):
     inp = S.make_dense(4, 500, K=16, seed=6, causal=False)
     inp.row_begin[1], inp.row_end[1] = 10, 501      # end past N
