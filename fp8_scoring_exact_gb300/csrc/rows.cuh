@@ -132,114 +132,6 @@ __device__ __forceinline__ void group_radix_select(KeyAt key_at, int n, int K, i
   r = rem;
 }
 
-// Radix select over keys[0, n4 * 4) in shared memory (16-byte aligned; pad
-// entries hold key 0, which never reaches a top K of real candidates: every
-// real order-preserving key of a finite score exceeds 0x007FFFFF), four keys
-// per thread per step.  Bytes shared by every key are skipped: their value
-// is fixed before the first histogram.  Same contract as group_radix_select.
-__device__ __forceinline__ void group_radix_select4(const uint32_t* keys, int n4, int K, int* hist, int* sdig,
-                                                    int tid, int nthr, int bar_id, uint32_t& theta, int& r) {
-  const int lane = tid & 31;
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-  if (tid == 0) {
-    sdig[2] = -1;
-    sdig[3] = 0;
-  }
-  group_sync(bar_id, nthr);
-  // common prefix of the real keys: bits where AND == OR over all non-zero keys
-  uint32_t a = 0xffffffffu, o = 0u;
-  for (int i = tid; i < n4; i += nthr) {
-    const uint4 v = k4[i];
-    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (x[c]) {
-        a &= x[c];
-        o |= x[c];
-      }
-  }
-  a = __reduce_and_sync(0xffffffffu, a);
-  o = __reduce_or_sync(0xffffffffu, o);
-  if (lane == 0) {
-    atomicAnd((unsigned*)&sdig[2], a);
-    atomicOr((unsigned*)&sdig[3], o);
-  }
-  group_sync(bar_id, nthr);
-  const uint32_t diff = (uint32_t)sdig[2] ^ (uint32_t)sdig[3];
-  group_sync(bar_id, nthr);
-  int pass = 0;
-  uint32_t prefix = 0, mask = 0;
-  while (pass < 3 && ((diff >> (24 - 8 * pass)) & 0xFFu) == 0) {  // byte shared by every key
-    mask |= 0xFFu << (24 - 8 * pass);
-    ++pass;
-  }
-  prefix = (uint32_t)sdig[3] & mask;
-  int rem = K;
-#pragma unroll 1
-  for (; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int b = tid; b < 256; b += nthr) hist[b] = 0;
-    group_sync(bar_id, nthr);
-    for (int base = 0; base < n4; base += nthr) {
-      const int i = base + tid;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (i < n4) v = k4[i];
-      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) hist_add(i < n4 && (x[c] & mask) == prefix, (x[c] >> shift) & 0xFFu, lane, hist);
-    }
-    group_sync(bar_id, nthr);
-    if (tid < 32) radix_pick_digit(hist, rem, sdig);
-    group_sync(bar_id, nthr);
-    prefix |= (uint32_t)sdig[0] << shift;
-    mask |= 0xFFu << shift;
-    rem = sdig[1];
-    group_sync(bar_id, nthr);
-  }
-  theta = prefix;
-  r = rem;
-}
-
-// Emission for group_radix_select4's layout: keys and ids in shared memory,
-// four per thread per step; counters[0..1] zeroed beforehand.
-__device__ __forceinline__ void group_emit4(const uint32_t* keys, const int32_t* ids, int n4, uint32_t theta, int rr,
-                                            int K, int32_t* o, int* counters, int tid, int nthr) {
-  const int lane = tid & 31;
-  uint32_t lt;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-  const int4* i4 = reinterpret_cast<const int4*>(ids);
-  for (int base = 0; base < n4; base += nthr) {
-    const int i = base + tid;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    int4 d = make_int4(0, 0, 0, 0);
-    if (i < n4) {
-      v = k4[i];
-      d = i4[i];
-    }
-    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-    const int32_t id[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const bool gt = x[c] > theta, eq = x[c] == theta;
-      const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
-      if (!(mg | me)) continue;
-      int bg = 0, be = 0;
-      if (lane == 0) {
-        if (mg) bg = atomicAdd(&counters[0], __popc(mg));
-        if (me) be = atomicAdd(&counters[1], __popc(me));
-      }
-      bg = __shfl_sync(0xffffffffu, bg, 0);
-      be = __shfl_sync(0xffffffffu, be, 0);
-      if (gt) o[bg + __popc(mg & lt)] = id[c];
-      if (eq) {
-        const int q = be + __popc(me & lt);
-        if (q < rr) o[K - rr + q] = id[c];
-      }
-    }
-  }
-}
-
 // Emission after the select: every key above theta and the first rr keys
 // equal to theta go to o[] (the above ones to [0, K - rr), the equal ones to
 // [K - rr, K)); slots are reserved once per warp.  All nthr threads call it
