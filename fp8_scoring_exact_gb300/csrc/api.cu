@@ -27,7 +27,7 @@ namespace {
 
 // ---------------------------------------------------------------- options --
 std::mutex g_mu;
-int64_t g_chunk_tiles = 64;
+int64_t g_chunk_tiles = -1;  // -1: chosen per call (chunk_for)
 int64_t g_tau_bias = 0;
 int64_t g_profile = 0;
 int64_t g_grid = 0;
@@ -181,6 +181,18 @@ struct Opts {
   bool profile;
 };
 
+// Tiles per work unit: the option when set, else 64 for dense rows and 32
+// for paged ones (decode batches mix very short and very long sequences:
+// smaller units balance the long tail), halved (down to 16) while the row
+// groups would give fewer than 4 units per CTA.  Measured on GB300.
+int chunk_for(const Opts& o, const RowSpace& rs) {
+  if (o.chunk > 0) return o.chunk;
+  const int64_t tiles = (int64_t)n_groups(rs) * ceil_div(rs.N, TILE);
+  int c = rs.paged ? 32 : 64;
+  while (c > 16 && tiles / c < 4LL * o.grid) c >>= 1;
+  return c;
+}
+
 Opts read_opts() {
   std::lock_guard<std::mutex> lk(g_mu);
   Opts o;
@@ -199,9 +211,10 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
               const float* ks_raw, const float* q_scale,
               const float* w, const int32_t* row_begin, const int32_t* row_end, int32_t* out, cudaStream_t stream) {
   const Opts o = read_opts();
+  const int chunk = chunk_for(o, rs);
   const int G = n_groups(rs);
   const int64_t ld = align_up((size_t)rs.N, 4);
-  const int max_units = ceil_div(ceil_div(rs.N, TILE), o.chunk);
+  const int max_units = ceil_div(ceil_div(rs.N, TILE), chunk);
   const int64_t cand_stride = ROW_SLOTS;
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
@@ -215,7 +228,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   pp.plan = PLAN_MAIN;
   pp.K = K;
   pp.trivial_len = K;
-  pp.chunk_tiles = o.chunk;
+  pp.chunk_tiles = chunk;
   pp.row_begin_in = row_begin;
   pp.row_end_in = row_end;
   pp.rb = at<int32_t>(a, L.rb);
@@ -315,7 +328,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   ScoreParams cp{};
   cp.rs = rs;
   cp.mode = MODE_FILTER;
-  cp.chunk_tiles = o.chunk;
+  cp.chunk_tiles = chunk;
   cp.plan = PLAN_MAIN;
   cp.k_scale = ks_raw;
   cp.q_scale = q_scale;
@@ -498,7 +511,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   pp.rs = rs;
   pp.K = K;
   pp.trivial_len = out_idx ? K : 0;
-  pp.chunk_tiles = o.chunk;
+  pp.chunk_tiles = chunk_for(o, rs);
   pp.row_begin_in = row_begin;
   pp.row_end_in = row_end;
   pp.rb = at<int32_t>(a, L.rb);
@@ -512,7 +525,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   ScoreParams cp{};
   cp.rs = rs;
   cp.mode = MODE_STORE;
-  cp.chunk_tiles = o.chunk;
+  cp.chunk_tiles = pp.chunk_tiles;
   cp.k_scale = k_scale;
   cp.q_scale = q_scale;
   cp.w = w;
@@ -581,7 +594,7 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   pp.rs = rs;
   pp.K = K;
   pp.trivial_len = 0x7fffffff;  // no scoring work: ranges and counters only
-  pp.chunk_tiles = o.chunk;
+  pp.chunk_tiles = 64;
   pp.row_begin_in = row_begin;
   pp.row_end_in = row_end;
   pp.rb = at<int32_t>(a, L.rb);
@@ -628,7 +641,7 @@ int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const 
   pp.rs = rs;
   pp.K = K;
   pp.trivial_len = 0x7fffffff;
-  pp.chunk_tiles = o.chunk;
+  pp.chunk_tiles = 64;
   pp.row_begin_in = row_begin;
   pp.row_end_in = row_end;
   pp.rb = reinterpret_cast<int32_t*>(base + L.rb);
@@ -700,7 +713,7 @@ int dsa_indexer_set_option(int option, int64_t value) {
   std::lock_guard<std::mutex> lk(g_mu);
   switch (option) {
     case DSA_OPT_CHUNK_TILES:
-      if (value < 1 || value > (1 << 20)) return DSA_ERR_ARG;
+      if (value != -1 && (value < 1 || value > (1 << 20))) return DSA_ERR_ARG;
       g_chunk_tiles = value;
       return DSA_OK;
     case DSA_OPT_TAU_BIAS:

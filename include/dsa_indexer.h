@@ -195,7 +195,9 @@ DSA_API int dsa_indexer_last_repaired_rows(dsa_stream_t stream, int32_t* rows_ou
 
 /* Tuning and diagnostics (process-wide; take effect on the next call). */
 typedef enum {
-  DSA_OPT_CHUNK_TILES = 1,    /* 128-key tiles per work unit of the persistent scorer (default 64); a row's
+  DSA_OPT_CHUNK_TILES = 1,    /* 128-key tiles per work unit of the persistent scorer (default -1: chosen per
+                                 call, 64 dense / 32 paged, halved down to 16 while there would be fewer than
+                                 4 units per SM); a row's
                                  16384 candidate slots are split evenly over its units' regions, and a region
                                  that fills up fails the row's certificate (-> repair) */
   DSA_OPT_TAU_BIAS = 2,       /* added to every sampled threshold key: >0 forces underflow, <0 overflow (test knob; default 0) */
