@@ -173,6 +173,27 @@ def test_grid_sampling_with_offset_ranges(B):
     assert check_dense_rows(inp, out, range(inp.Q)) == {}
 
 
+@pytest.mark.parametrize("K", [256, 1024])
+def test_grid_sampling_other_k(B, K):
+    """The grid-sampling path with K below 2048 (thresholds aim at 2K)."""
+    inp = S.make_dense(24, 50000, K=K, seed=10 + K)
+    out = B.indexer_topk(*dense_args(inp), K=K).cpu().numpy()
+    _status_ok(B)
+    assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
+def test_grid_sampling_widened_stride(B):
+    """Rows longer than 1024 grid keys at stride 200 (N > 204800): the grid
+    stride widens so every row keeps at most 1024 samples."""
+    K, N = 2048, 262144 + 999
+    inp = S.make_dense(8, N, K=K, seed=11, causal=False)
+    inp.row_begin[:] = [0, 0, 1, 150000, 262000, 3, 100000, 200]
+    inp.row_end[:] = [N, 204800, N, N, N, 100000, 100000 + K, N - 5]
+    out = B.indexer_topk(*dense_args(inp), K=K).cpu().numpy()
+    _status_ok(B)
+    assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
 def test_invalid_range_reports_status_and_pads(B):
     inp = S.make_dense(4, 500, K=16, seed=6, causal=False)
     inp.row_begin[1], inp.row_end[1] = 10, 501      # end past N
