@@ -390,7 +390,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   wp.state = at<int32_t>(a, L.wide_state);
   wp.out = out;
   wp.stats = st;
-  DSA_LAUNCH(launch_wide_select(wp, o.grid / 4 > 0 ? o.grid / 4 : 1, stream));
+  DSA_LAUNCH(launch_wide_select(wp, o.grid / 2 > 0 ? o.grid / 2 : 1, stream));  // 4 CTAs per SM
   return DSA_OK;
 }
 

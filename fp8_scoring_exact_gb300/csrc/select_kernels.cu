@@ -102,7 +102,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
     __syncthreads();
     G = n_groups(rs);
   } else {
-    G = p.stats->fail_count;
+    // dense rows all read one key array: four failed rows share a group
+    // (scored over the union of their ranges); paged rows, one per group
+    G = rs.paged ? p.stats->fail_count : ceil_div(p.stats->fail_count, GROUP_ROWS);
   }
 
   if (tid == 0) s_carry = 0;
@@ -132,14 +134,26 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
             grp.hi = max(grp.hi, e);
           }
         }
-      } else {
+      } else if (rs.paged) {
         const int row = p.failed_rows[g];
         grp.nrows = 1;
         grp.row[0] = row;
         grp.slot[0] = g;
-        grp.seq = rs.paged ? row / rs.next_n : -1;
+        grp.seq = row / rs.next_n;
         grp.lo = p.rb[row];
         grp.hi = p.re[row];
+      } else {
+        // failed-list entries 4g .. 4g + 3; slot = the entry (its score row)
+        const int nf = p.stats->fail_count;
+        grp.seq = -1;
+        for (int i = 0; i < GROUP_ROWS && GROUP_ROWS * g + i < nf; ++i) {
+          const int f = GROUP_ROWS * g + i, row = p.failed_rows[f];
+          grp.row[grp.nrows] = row;
+          grp.slot[grp.nrows] = f;
+          ++grp.nrows;
+          grp.lo = min(grp.lo, p.rb[row]);
+          grp.hi = max(grp.hi, p.re[row]);
+        }
       }
       if (grp.nrows == 0) grp.lo = grp.hi = 0;
       units = group_units(grp.lo, grp.hi, p.chunk_tiles);
