@@ -6,7 +6,10 @@
 // Roles:
 //   warp 0       TMA producer: q rows of the group (64 heads x 128 B each),
 //                key tiles (128 keys x 128 B, 128-byte swizzle) into a
-//                STAGES-deep ring;
+//                STAGES-deep ring; paged keys: also each tile's 128 key
+//                scales and two page ids into a SCALE_SLOTS-deep ring that
+//                the epilogue releases (the block-table entry and the scale
+//                behind it are two dependent reads that mostly miss L2);
 //   warp 1       MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 per
 //                tile, M = 128 keys, N = 64 heads x rows (256 for 4 rows),
 //                K = 32, fp32 accumulators in one of two 256-column TMEM
@@ -18,7 +21,9 @@
 //                weights with packed f32x2 FMAs, and a three-shuffle
 //                reduce-scatter over 4 lanes leaves one key's 64-head sum per
 //                thread; then score = sum * k_scale, the key scale loaded from
-//                global memory one tile ahead.
+//                global memory at the top of the tile's iteration (dense: the
+//                scales are contiguous and stay in L2) or read from the scale
+//                ring (paged).
 //                MODE_STORE writes the fp32 score.  MODE_FILTER keeps the
 //                scores that reach the row's sampled threshold: key
 //                (order-preserving uint32) and index go to the warp's region
@@ -44,16 +49,28 @@ constexpr int KEY_STAGE_BYTES = TILE * D;            // 16384
 constexpr int Q_ROW_BYTES = H * D;                   // 8192
 constexpr int Q_SLOT_BYTES = GROUP_ROWS * Q_ROW_BYTES;  // 32768
 
+// key-scale ring of paged keys: deeper than the key ring plus the
+// accumulators, so waiting for a free slot never holds the producer back
+// further than the key ring.  (For dense keys the ring's barrier work per
+// tile cost more epilogue issue slots than the direct load: measured 6%.)
+constexpr int SCALE_SLOTS = 8;
+constexpr int SCALE_SLOT_BYTES = TILE * 4;  // 128 fp32 scales (paged: two pages of 64)
+static_assert(SCALE_SLOTS >= STAGES + ACC_BUFS, "scale ring depth");
+
 constexpr uint32_t OFF_KEYS = 0;
 constexpr uint32_t OFF_Q = OFF_KEYS + STAGES * KEY_STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_Q + 2 * Q_SLOT_BYTES;
-constexpr int N_BARS = 2 * STAGES + 4 + 2 * ACC_BUFS;
+constexpr uint32_t OFF_SCALE = OFF_Q + 2 * Q_SLOT_BYTES;
+constexpr uint32_t OFF_PAGE = OFF_SCALE + SCALE_SLOTS * SCALE_SLOT_BYTES;  // paged: [SCALE_SLOTS][2] page ids
+constexpr uint32_t OFF_BAR = OFF_PAGE + 128;
+constexpr int N_BARS = 2 * STAGES + 4 + 2 * ACC_BUFS + 2 * SCALE_SLOTS;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr uint32_t MISC_BYTES = 64;
 constexpr uint32_t SMEM_USED = OFF_MISC + MISC_BYTES;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_Q % 1024 == 0 && OFF_KEYS % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(OFF_SCALE % 128 == 0 && SCALE_SLOT_BYTES % 128 == 0, "TMA destinations 128-byte aligned");
+static_assert(SCALE_SLOTS * 2 * 4 <= 128, "page-id block");
 static_assert(ACC_BUFS * ACC_COLS <= 512, "TMEM columns");
 
 struct Misc {
@@ -124,7 +141,7 @@ __device__ __forceinline__ float hsum2(uint64_t v) {
 template <int MODE, bool PAGED>
 __global__ void __launch_bounds__(SCORE_THREADS, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const ScoreParams p) {
+                 const __grid_constant__ CUtensorMap tm_ks, const ScoreParams p) {
   const int n_groups = p.plan == PLAN_REPAIR   ? p.stats->r_groups
                        : p.plan == PLAN_SAMPLE ? p.stats->s_groups
                                                : p.stats->n_groups;
@@ -144,6 +161,10 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
   auto q_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
   auto acc_full = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + i); };
   auto acc_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + ACC_BUFS + i); };
+  auto scale_full = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + 2 * ACC_BUFS + i); };
+  auto scale_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + 2 * ACC_BUFS + SCALE_SLOTS + i); };
+  const float* scale_ring = (const float*)(smem + OFF_SCALE);
+  int* page_ring = (int*)(smem + OFF_PAGE);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -167,6 +188,10 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       mbar_init(acc_full(i), 1);
       mbar_init(acc_empty(i), EPI_THREADS / 32);
     }
+    for (int i = 0; i < SCALE_SLOTS; ++i) {
+      mbar_init(scale_full(i), 1);
+      mbar_init(scale_empty(i), EPI_THREADS / 32);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -183,6 +208,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
+      if (paged) tma_prefetch_desc(&tm_ks);
       uint32_t kit = 0, ui = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ui) {
@@ -217,6 +243,19 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
             mbar_arrive_expect_tx(key_full(st), (pg1 >= 0 ? 2 : 1) * PAGE * D);
             tma_load_2d(kdst, &tm_k, 0, pg0 * PAGE, key_full(st));
             if (pg1 >= 0) tma_load_2d(kdst + PAGE * D, &tm_k, 0, pg1 * PAGE, key_full(st));
+          }
+          if (paged) {
+            // the tile's page ids and key scales (a page past the sequence
+            // reads as the page past the cache: scale 0)
+            const int ss = kit % SCALE_SLOTS;
+            if (!(ok = mbar_wait(scale_empty(ss), ((kit / SCALE_SLOTS) & 1) ^ 1, abort_flag, status))) break;
+            const uint32_t sdst = sbase + OFF_SCALE + ss * SCALE_SLOT_BYTES;
+            const int pg1s = pg1 >= 0 ? pg1 : p.rs.num_pages;
+            page_ring[2 * ss] = pg0;
+            page_ring[2 * ss + 1] = pg1s;
+            mbar_arrive_expect_tx(scale_full(ss), SCALE_SLOT_BYTES);
+            tma_load_1d(sdst, &tm_ks, pg0 * PAGE, scale_full(ss));
+            tma_load_1d(sdst + PAGE * 4, &tm_ks, pg1s * PAGE, scale_full(ss));
           }
         }
       }
@@ -257,7 +296,6 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
     // after the reduce-scatter this thread owns key (lane / 4) + 8 (lane % 4)
     // of its warp's 32 TMEM lanes
     const int kt = quarter * 32 + (lane >> 2) + 8 * (lane & 3);
-    const int num_pages = p.rs.num_pages;
     uint32_t ait = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -295,23 +333,17 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           store_lim = min((int64_t)p.rs.N, p.ld);
         }
       }
-      // Key scale of this thread's key in tile t, loaded at the top of the
-      // tile's iteration and used at its end.  Paged: the page holding it
-      // (the same clamping as the producer's: a page id outside the cache and
-      // a page past the sequence read as zero keys, scale 0).
-      const int32_t* bt = paged ? p.rs.block_table + (int64_t)G.seq * p.rs.max_pages : nullptr;
-      const int ghi = G.hi;
       for (int t = un.t0; t < un.t1 && ok; ++t, ++ait) {
-        int page = 0;
+        // this thread's key scale, used at the end of the iteration (paged:
+        // and the page holding the key, from the scale ring; the slot is
+        // released with the accumulator)
+        const int ss = ait % SCALE_SLOTS;
         float ks;
+        int page = 0;
         if constexpr (paged) {
-          const int j = 2 * t + (kt >> 6);
-          page = num_pages;
-          if (j * PAGE < ghi) {
-            page = ldg_pinned_s32(&bt[j]);
-            if (page < 0 || page >= num_pages) page = num_pages;
-          }
-          ks = page < num_pages ? ldg_pinned_f32(&p.k_scale[(int64_t)page * PAGE + (kt & (PAGE - 1))]) : 0.f;
+          if (!(ok = mbar_wait_warp(scale_full(ss), (ait / SCALE_SLOTS) & 1, abort_flag, status))) break;
+          ks = scale_ring[ss * TILE + kt];
+          page = page_ring[2 * ss + (kt >> 6)];
         } else {
           const int s = t * TILE + kt;
           ks = s < p.rs.N ? ldg_pinned_f32(&p.k_scale[s]) : 0.f;
@@ -340,6 +372,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive_warp(acc_empty(ab));
+          if (paged) mbar_arrive_warp(scale_empty(ss));
           chunk_partials<false>(vb, w2 + 4, aH, bH);
           part[0] = hsum2(aL);
           part[1] = hsum2(bL);
@@ -348,6 +381,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         } else {
           tc_fence_before();
           mbar_arrive_warp(acc_empty(ab));
+          if (paged) mbar_arrive_warp(scale_empty(ss));
         }
         if (!active) continue;
         // reduce-scatter over the 4 lanes sharing keys: part[j] covers key
@@ -398,8 +432,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
 }
 
 template <int MODE, bool PAGED>
-static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
-                                  cudaStream_t s) {
+static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_ks,
+                                  const ScoreParams& p, int grid, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(score_kernel<MODE, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -407,18 +441,18 @@ static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  score_kernel<MODE, PAGED><<<grid, SCORE_THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, p);
+  score_kernel<MODE, PAGED><<<grid, SCORE_THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, tm_ks, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
-                         cudaStream_t s) {
+cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_ks,
+                         const ScoreParams& p, int grid, cudaStream_t s) {
   const bool paged = p.rs.paged != 0;
   if (p.mode == MODE_FILTER)
-    return paged ? launch_variant<MODE_FILTER, true>(tm_q, tm_k, p, grid, s)
-                 : launch_variant<MODE_FILTER, false>(tm_q, tm_k, p, grid, s);
-  return paged ? launch_variant<MODE_STORE, true>(tm_q, tm_k, p, grid, s)
-               : launch_variant<MODE_STORE, false>(tm_q, tm_k, p, grid, s);
+    return paged ? launch_variant<MODE_FILTER, true>(tm_q, tm_k, tm_ks, p, grid, s)
+                 : launch_variant<MODE_FILTER, false>(tm_q, tm_k, tm_ks, p, grid, s);
+  return paged ? launch_variant<MODE_STORE, true>(tm_q, tm_k, tm_ks, p, grid, s)
+               : launch_variant<MODE_STORE, false>(tm_q, tm_k, tm_ks, p, grid, s);
 }
 
 }  // namespace dsa
