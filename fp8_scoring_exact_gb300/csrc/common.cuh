@@ -220,6 +220,35 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
   return mbar_wait_warp_slow(bar, parity, abort_flag, status);
 }
 
+// Warp-uniform bounded wait for a warp whose wake-up latency has slack (the
+// TMA producer, which runs ahead of the MMA): between polls it sleeps, so it
+// takes no issue slots from the epilogue warps that share its SM
+// sub-partition (measured: 1% on the dense scorer).
+static __device__ __noinline__ bool mbar_wait_warp_backoff_slow(uint32_t bar, uint32_t parity,
+                                                         volatile int* abort_flag, int* status) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(128);
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    int give_up = 0;
+    if ((threadIdx.x & 31) == 0) {
+      if (*abort_flag) {
+        give_up = 1;
+      } else if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        atomicOr(status, ST_TIMEOUT);
+        give_up = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+  }
+}
+__device__ __forceinline__ bool mbar_wait_warp_backoff(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                       int* status) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return mbar_wait_warp_backoff_slow(bar, parity, abort_flag, status);
+}
+
 // One arrival per warp, from the lane elect.sync picks (the warp must be
 // converged); no branch around it.
 __device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {

@@ -7,9 +7,10 @@
 //   warp 0       TMA producer: q rows of the group (64 heads x 128 B each),
 //                key tiles (128 keys x 128 B, 128-byte swizzle) into a
 //                STAGES-deep ring; paged keys: also each tile's 128 key
-//                scales and two page ids into a SCALE_SLOTS-deep ring that
-//                the epilogue releases (the block-table entry and the scale
-//                behind it are two dependent reads that mostly miss L2);
+//                scales and two page ids into the same stage (the
+//                block-table entry and the scale behind it are two dependent
+//                reads that mostly miss L2), and the stage is then released
+//                by the MMA and by every epilogue warp;
 //   warp 1       MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 per
 //                tile, M = 128 keys, N = 64 heads x rows (256 for 4 rows),
 //                K = 32, fp32 accumulators in one of two 256-column TMEM
@@ -22,8 +23,8 @@
 //                reduce-scatter over 4 lanes leaves one key's 64-head sum per
 //                thread; then score = sum * k_scale, the key scale loaded from
 //                global memory at the top of the tile's iteration (dense: the
-//                scales are contiguous and stay in L2) or read from the scale
-//                ring (paged).
+//                scales are contiguous and stay in L2) or read from the key
+//                stage (paged).
 //                MODE_STORE writes the fp32 score.  MODE_FILTER keeps the
 //                scores that reach the row's sampled threshold: key
 //                (order-preserving uint32) and index go to the warp's region
@@ -49,28 +50,25 @@ constexpr int KEY_STAGE_BYTES = TILE * D;            // 16384
 constexpr int Q_ROW_BYTES = H * D;                   // 8192
 constexpr int Q_SLOT_BYTES = GROUP_ROWS * Q_ROW_BYTES;  // 32768
 
-// key-scale ring of paged keys: deeper than the key ring plus the
-// accumulators, so waiting for a free slot never holds the producer back
-// further than the key ring.  (For dense keys the ring's barrier work per
-// tile cost more epilogue issue slots than the direct load: measured 6%.)
-constexpr int SCALE_SLOTS = 8;
-constexpr int SCALE_SLOT_BYTES = TILE * 4;  // 128 fp32 scales (paged: two pages of 64)
-static_assert(SCALE_SLOTS >= STAGES + ACC_BUFS, "scale ring depth");
+// paged keys: each key stage also holds the tile's 128 key scales (two pages
+// of 64) and its two page ids.  (Dense keys load their scales directly: the
+// extra barrier work per tile cost more epilogue issue slots, measured 6%.)
+constexpr int SCALE_STAGE_BYTES = TILE * 4;
 
 constexpr uint32_t OFF_KEYS = 0;
 constexpr uint32_t OFF_Q = OFF_KEYS + STAGES * KEY_STAGE_BYTES;
 constexpr uint32_t OFF_SCALE = OFF_Q + 2 * Q_SLOT_BYTES;
-constexpr uint32_t OFF_PAGE = OFF_SCALE + SCALE_SLOTS * SCALE_SLOT_BYTES;  // paged: [SCALE_SLOTS][2] page ids
+constexpr uint32_t OFF_PAGE = OFF_SCALE + STAGES * SCALE_STAGE_BYTES;  // paged: [STAGES][2] page ids
 constexpr uint32_t OFF_BAR = OFF_PAGE + 128;
-constexpr int N_BARS = 2 * STAGES + 4 + 2 * ACC_BUFS + 2 * SCALE_SLOTS;
+constexpr int N_BARS = 2 * STAGES + 4 + 2 * ACC_BUFS;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr uint32_t MISC_BYTES = 64;
 constexpr uint32_t SMEM_USED = OFF_MISC + MISC_BYTES;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_Q % 1024 == 0 && OFF_KEYS % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-static_assert(OFF_SCALE % 128 == 0 && SCALE_SLOT_BYTES % 128 == 0, "TMA destinations 128-byte aligned");
-static_assert(SCALE_SLOTS * 2 * 4 <= 128, "page-id block");
+static_assert(OFF_SCALE % 128 == 0 && SCALE_STAGE_BYTES % 128 == 0, "TMA destinations 128-byte aligned");
+static_assert(STAGES * 2 * 4 <= 128, "page-id block");
 static_assert(ACC_BUFS * ACC_COLS <= 512, "TMEM columns");
 
 struct Misc {
@@ -161,10 +159,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
   auto q_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
   auto acc_full = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + i); };
   auto acc_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + ACC_BUFS + i); };
-  auto scale_full = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + 2 * ACC_BUFS + i); };
-  auto scale_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + 2 * ACC_BUFS + SCALE_SLOTS + i); };
-  const float* scale_ring = (const float*)(smem + OFF_SCALE);
-  int* page_ring = (int*)(smem + OFF_PAGE);
+  const float* stage_scales = (const float*)(smem + OFF_SCALE);
+  int* stage_pages = (int*)(smem + OFF_PAGE);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -178,7 +174,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
     misc->abort_flag = 0;
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(key_full(i), 1);
-      mbar_init(key_empty(i), 1);
+      // paged: the epilogue warps read the stage's scales and page ids too
+      mbar_init(key_empty(i), paged ? 1 + EPI_THREADS / 32 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(q_full(i), 1);
@@ -187,10 +184,6 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
     for (int i = 0; i < ACC_BUFS; ++i) {
       mbar_init(acc_full(i), 1);
       mbar_init(acc_empty(i), EPI_THREADS / 32);
-    }
-    for (int i = 0; i < SCALE_SLOTS; ++i) {
-      mbar_init(scale_full(i), 1);
-      mbar_init(scale_empty(i), EPI_THREADS / 32);
     }
     fence_mbar_init();
   }
@@ -205,58 +198,72 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer --
+    // The whole warp runs the loop (uniform control flow); lane 0 arms the
+    // barriers.  Paged keys: lanes 0-3 issue a tile's four copies (two key
+    // pages, two scale blocks) in one go, and the block-table entries come
+    // in batches of 16 tiles, one entry per lane, so the per-tile chain of
+    // this warp holds no global load (measured: a one-thread producer with
+    // a load and four copies per tile was the paged pipeline's bound).
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       if (paged) tma_prefetch_desc(&tm_ks);
-      uint32_t kit = 0, ui = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ui) {
-        Group G;
-        const Unit un = decode_unit(p, n_groups, u, G);
-        const int qs = ui & 1;
-        if (!(ok = mbar_wait(q_empty(qs), ((ui >> 1) & 1) ^ 1, abort_flag, status))) break;
-        mbar_arrive_expect_tx(q_full(qs), G.nrows * Q_ROW_BYTES);
-        for (int r = 0; r < G.nrows; ++r)
+    }
+    const int num_pages = p.rs.num_pages;
+    uint32_t kit = 0, ui = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ui) {
+      Group G;
+      const Unit un = decode_unit(p, n_groups, u, G);
+      const int qs = ui & 1;
+      if (!(ok = mbar_wait_warp_backoff(q_empty(qs), ((ui >> 1) & 1) ^ 1, abort_flag, status))) break;
+      if (lane == 0) mbar_arrive_expect_tx(q_full(qs), G.nrows * Q_ROW_BYTES);
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < GROUP_ROWS; ++r)
+        if (lane == r && r < G.nrows)
           tma_load_2d(sbase + OFF_Q + qs * Q_SLOT_BYTES + r * Q_ROW_BYTES, &tm_q, 0, G.row[r] * H, q_full(qs));
-        for (int t = un.t0; t < un.t1; ++t, ++kit) {
-          const int st = kit % STAGES;
-          const uint32_t ph = (kit / STAGES) & 1;
-          if (!(ok = mbar_wait(key_empty(st), ph ^ 1, abort_flag, status))) break;
-          int pg0 = 0, pg1 = -1;
-          if (paged) {
-            const int32_t* bt = p.rs.block_table + (int64_t)G.seq * p.rs.max_pages;
-            // a page id outside the cache is clamped to the first row past it:
-            // TMA then reads zeros there instead of touching foreign memory
-            pg0 = __ldg(&bt[2 * t]);
-            if (pg0 < 0 || pg0 >= p.rs.num_pages) pg0 = p.rs.num_pages;
-            if (t * TILE + PAGE < G.hi) {
-              pg1 = __ldg(&bt[2 * t + 1]);
-              if (pg1 < 0 || pg1 >= p.rs.num_pages) pg1 = p.rs.num_pages;
-            }
+      const int32_t* bt = paged ? p.rs.block_table + (int64_t)G.seq * p.rs.max_pages : nullptr;
+      int btv = -1;  // paged: lane j holds entry 2 tb + j of the batch starting at tile tb
+      for (int t = un.t0; t < un.t1; ++t, ++kit) {
+        const int st = kit % STAGES;
+        if (paged && ((t - un.t0) & 15) == 0) {
+          // a page id outside the cache is clamped to the first row past
+          // it (TMA then reads zeros there instead of foreign memory); -1:
+          // the entry is past the sequence
+          const int j = 2 * t + lane;
+          btv = -1;
+          if ((int64_t)j * PAGE < G.hi) {
+            btv = __ldg(&bt[j]);
+            if (btv < 0 || btv >= num_pages) btv = num_pages;
           }
-          const uint32_t kdst = sbase + OFF_KEYS + st * KEY_STAGE_BYTES;
-          if (!paged) {
+        }
+        if (!(ok = mbar_wait_warp_backoff(key_empty(st), ((kit / STAGES) & 1) ^ 1, abort_flag, status))) break;
+        const uint32_t kdst = sbase + OFF_KEYS + st * KEY_STAGE_BYTES;
+        if (!paged) {
+          if (lane == 0) {
             mbar_arrive_expect_tx(key_full(st), KEY_STAGE_BYTES);
             tma_load_2d(kdst, &tm_k, 0, t * TILE, key_full(st));
-          } else {
-            mbar_arrive_expect_tx(key_full(st), (pg1 >= 0 ? 2 : 1) * PAGE * D);
-            tma_load_2d(kdst, &tm_k, 0, pg0 * PAGE, key_full(st));
-            if (pg1 >= 0) tma_load_2d(kdst + PAGE * D, &tm_k, 0, pg1 * PAGE, key_full(st));
           }
-          if (paged) {
-            // the tile's page ids and key scales (a page past the sequence
-            // reads as the page past the cache: scale 0)
-            const int ss = kit % SCALE_SLOTS;
-            if (!(ok = mbar_wait(scale_empty(ss), ((kit / SCALE_SLOTS) & 1) ^ 1, abort_flag, status))) break;
-            const uint32_t sdst = sbase + OFF_SCALE + ss * SCALE_SLOT_BYTES;
-            const int pg1s = pg1 >= 0 ? pg1 : p.rs.num_pages;
-            page_ring[2 * ss] = pg0;
-            page_ring[2 * ss + 1] = pg1s;
-            mbar_arrive_expect_tx(scale_full(ss), SCALE_SLOT_BYTES);
-            tma_load_1d(sdst, &tm_ks, pg0 * PAGE, scale_full(ss));
-            tma_load_1d(sdst + PAGE * 4, &tm_ks, pg1s * PAGE, scale_full(ss));
+        } else {
+          // keys, page ids and key scales of the tile in one stage (a page
+          // past the sequence reads as the page past the cache: scale 0);
+          // the page ids are plain stores, published by the arrive
+          const int i0 = 2 * ((t - un.t0) & 15);
+          const int pg0 = __shfl_sync(0xffffffffu, btv, i0);
+          const int pg1 = __shfl_sync(0xffffffffu, btv, i0 + 1);
+          const int pg1s = pg1 >= 0 ? pg1 : num_pages;
+          if (lane == 0) {
+            stage_pages[2 * st] = pg0;
+            stage_pages[2 * st + 1] = pg1s;
+            mbar_arrive_expect_tx(key_full(st), (pg1 >= 0 ? 2 : 1) * PAGE * D + SCALE_STAGE_BYTES);
           }
+          __syncwarp();
+          const uint32_t sdst = sbase + OFF_SCALE + st * SCALE_STAGE_BYTES;
+          if (lane == 0 || (lane == 1 && pg1 >= 0))
+            tma_load_2d(kdst + lane * PAGE * D, &tm_k, 0, (lane ? pg1 : pg0) * PAGE, key_full(st));
+          else if (lane == 2 || lane == 3)
+            tma_load_1d(sdst + (lane - 2) * PAGE * 4, &tm_ks, (lane == 2 ? pg0 : pg1s) * PAGE, key_full(st));
         }
       }
     }
@@ -335,15 +342,16 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       }
       for (int t = un.t0; t < un.t1 && ok; ++t, ++ait) {
         // this thread's key scale, used at the end of the iteration (paged:
-        // and the page holding the key, from the scale ring; the slot is
-        // released with the accumulator)
-        const int ss = ait % SCALE_SLOTS;
+        // and the page holding the key, from the tile's key stage, which
+        // this warp then releases with the accumulator; the stage cannot be
+        // refilled before that, so its full phase is still this tile's)
+        const int kst = ait % STAGES;
         float ks;
         int page = 0;
         if constexpr (paged) {
-          if (!(ok = mbar_wait_warp(scale_full(ss), (ait / SCALE_SLOTS) & 1, abort_flag, status))) break;
-          ks = scale_ring[ss * TILE + kt];
-          page = page_ring[2 * ss + (kt >> 6)];
+          if (!(ok = mbar_wait_warp(key_full(kst), (ait / STAGES) & 1, abort_flag, status))) break;
+          ks = stage_scales[kst * TILE + kt];
+          page = stage_pages[2 * kst + (kt >> 6)];
         } else {
           const int s = t * TILE + kt;
           ks = s < p.rs.N ? ldg_pinned_f32(&p.k_scale[s]) : 0.f;
@@ -372,7 +380,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive_warp(acc_empty(ab));
-          if (paged) mbar_arrive_warp(scale_empty(ss));
+          if (paged) mbar_arrive_warp(key_empty(kst));
           chunk_partials<false>(vb, w2 + 4, aH, bH);
           part[0] = hsum2(aL);
           part[1] = hsum2(bL);
@@ -381,7 +389,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         } else {
           tc_fence_before();
           mbar_arrive_warp(acc_empty(ab));
-          if (paged) mbar_arrive_warp(scale_empty(ss));
+          if (paged) mbar_arrive_warp(key_empty(kst));
         }
         if (!active) continue;
         // reduce-scatter over the 4 lanes sharing keys: part[j] covers key

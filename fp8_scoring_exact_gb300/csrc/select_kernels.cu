@@ -745,9 +745,10 @@ __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const Cand
       continue;
     }
     __syncthreads();
-    // gather: tpr threads per region (more when regions are few), up to 16
-    // entries of each array in flight per thread; region sizes from the
-    // offsets (no count reload)
+    // gather: tpr threads per region (more when regions are few), 16-byte
+    // loads (a region starts on a 4-entry boundary and holds a multiple of
+    // 4 slots, so the last load stays inside it), up to 4 of each array in
+    // flight per thread; region sizes from the offsets (no count reload)
     const uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
     const int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
     int tpr = 4;
@@ -757,22 +758,25 @@ __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const Cand
       const int x = (j + 1 < nreg ? off[j + 1] : n) - o;
       const uint32_t* sk = ck + (int64_t)j * wcap;
       const int32_t* si = ci + (int64_t)j * wcap;
-      for (int i = tid % tpr; i < x; i += 16 * tpr) {
-        uint32_t kv[16];
-        int32_t iv[16];
+      const uint4* sk4 = reinterpret_cast<const uint4*>(sk);
+      const int4* si4 = reinterpret_cast<const int4*>(si);
+      const int x4 = (x + 3) >> 2;
+      for (int i = tid % tpr; i < x4; i += 4 * tpr) {
+        uint4 kv[4];
+        int4 iv[4];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < 4; ++q) {
           const int e = i + tpr * q;
-          kv[q] = e < x ? __ldcg(&sk[e]) : 0u;
-          iv[q] = e < x ? __ldcg(&si[e]) : 0;
+          kv[q] = e < x4 ? __ldcg(&sk4[e]) : make_uint4(0, 0, 0, 0);
+          iv[q] = e < x4 ? __ldcg(&si4[e]) : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int e = i + tpr * q;
-          if (e < x) {
-            ckey[o + e] = kv[q];
-            cidx[o + e] = iv[q];
-          }
+        for (int q = 0; q < 4; ++q) {
+          const int e = 4 * (i + tpr * q);
+          if (e < x) { ckey[o + e] = kv[q].x; cidx[o + e] = iv[q].x; }
+          if (e + 1 < x) { ckey[o + e + 1] = kv[q].y; cidx[o + e + 1] = iv[q].y; }
+          if (e + 2 < x) { ckey[o + e + 2] = kv[q].z; cidx[o + e + 2] = iv[q].z; }
+          if (e + 3 < x) { ckey[o + e + 3] = kv[q].w; cidx[o + e + 3] = iv[q].w; }
         }
       }
     }
