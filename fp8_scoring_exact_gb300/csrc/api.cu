@@ -159,20 +159,6 @@ bool tmap_rows_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// a fp32 vector of n values, box = box values (elements past n read as 0):
-// the paged cache's key scales, one 64-value box per page
-bool tmap_f32_vec(CUtensorMap* m, const float* base, uint64_t n, uint32_t box) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[1] = {(cuuint64_t)n};
-  cuuint64_t strides[1] = {0};  // rank 1: no strides
-  cuuint32_t boxd[1] = {box};
-  cuuint32_t estr[1] = {1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(base), dims, strides, boxd, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int sm_count() {
@@ -221,14 +207,16 @@ Opts read_opts() {
 
 // ------------------------------------------------- shared launch sequence --
 // Fused pipeline over a row space whose keys are described by tm_k.
-int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_ks,
-              const uint8_t* k_raw, const float* ks_raw, const float* q_scale,
+int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensorMap& tm_k, const uint8_t* k_raw,
+              const float* ks_raw, const float* q_scale,
               const float* w, const int32_t* row_begin, const int32_t* row_end, int32_t* out, cudaStream_t stream) {
   const Opts o = read_opts();
   const int chunk = chunk_for(o, rs);
   const int G = n_groups(rs);
   const int64_t ld = align_up((size_t)rs.N, 4);
-  const int max_units = ceil_div(ceil_div(rs.N, TILE), chunk);
+  // candidate-region units per row: paged, twice the work units (a group of
+  // at most two rows runs two epilogue teams per unit)
+  const int max_units = (rs.paged ? 2 : 1) * ceil_div(ceil_div(rs.N, TILE), chunk);
   const int64_t cand_stride = ROW_SLOTS;
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
@@ -305,7 +293,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
       scp.scores = at<float>(a, L.sscores);
       scp.ld = SAMPLE_LD;
       scp.stats = st;
-      DSA_LAUNCH(launch_score(tm_q, tks, tks, scp, o.grid, stream));  // dense: no scale map
+      DSA_LAUNCH(launch_score(tm_q, tks, scp, o.grid, stream));
     }
     SampleTauParams tp{};
     tp.rs = rs;
@@ -359,7 +347,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cp.stats = st;
   a->profiled = o.profile;
   if (o.profile) cudaEventRecord(a->ev0, stream);
-  DSA_LAUNCH(launch_score(tm_q, tm_k, tm_ks, cp, o.grid, stream));
+  DSA_LAUNCH(launch_score(tm_q, tm_k, cp, o.grid, stream));
   if (o.profile) cudaEventRecord(a->ev1, stream);
 
   CandParams cs{};
@@ -390,7 +378,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   rcp.unit_start = rp.unit_start;
   rcp.scores = at<float>(a, L.scores);
   rcp.ld = ld;
-  DSA_LAUNCH(launch_score(tm_q, tm_k, tm_ks, rcp, o.grid, stream));
+  DSA_LAUNCH(launch_score(tm_q, tm_k, rcp, o.grid, stream));
 
   // their exact top-K: one thread-block cluster per row
   WideParams wp{};
@@ -468,8 +456,7 @@ int dsa_indexer_topk(const uint8_t* q_fp8, const float* q_scale, const uint8_t* 
   RowSpace rs{};
   rs.R = Q;
   rs.N = N;
-  // dense keys: the scorer loads key scales directly (tk stands in for the scale map)
-  return run_fused(rs, K, tq, tk, tk, k_fp8, k_scale, q_scale, w, row_begin, row_end, out_idx, stream);
+  return run_fused(rs, K, tq, tk, k_fp8, k_scale, q_scale, w, row_begin, row_end, out_idx, stream);
 }
 
 int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_cache,
@@ -485,10 +472,9 @@ int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uin
       (int64_t)num_pages * PAGE >= (1ll << 31))
     return DSA_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  CUtensorMap tq, tk, tks;
+  CUtensorMap tq, tk;
   if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)R * H, H) ||
-      !tmap_rows_u8(&tk, k_cache, (uint64_t)num_pages * PAGE, PAGE) ||
-      !tmap_f32_vec(&tks, k_cache_scale, (uint64_t)num_pages * PAGE, PAGE))
+      !tmap_rows_u8(&tk, k_cache, (uint64_t)num_pages * PAGE, PAGE))
     return DSA_ERR_CUDA;
   RowSpace rs{};
   rs.R = (int)R;
@@ -499,7 +485,7 @@ int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uin
   rs.max_pages = max_pages;
   rs.next_n = next_n;
   rs.num_pages = num_pages;
-  return run_fused(rs, K, tq, tk, tks, k_cache, k_cache_scale, q_scale, w, nullptr, nullptr, out_idx, stream);
+  return run_fused(rs, K, tq, tk, k_cache, k_cache_scale, q_scale, w, nullptr, nullptr, out_idx, stream);
 }
 
 static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
@@ -554,7 +540,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   cp.stats = st;
   a->profiled = o.profile;
   if (o.profile) cudaEventRecord(a->ev0, stream);
-  DSA_LAUNCH(launch_score(tq, tk, tk, cp, o.grid, stream));  // dense: no scale map
+  DSA_LAUNCH(launch_score(tq, tk, cp, o.grid, stream));
   if (o.profile) cudaEventRecord(a->ev1, stream);
   if (!out_idx) return DSA_OK;
 

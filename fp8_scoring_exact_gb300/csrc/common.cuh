@@ -249,6 +249,17 @@ __device__ __forceinline__ bool mbar_wait_warp_backoff(uint32_t bar, uint32_t pa
   return mbar_wait_warp_backoff_slow(bar, parity, abort_flag, status);
 }
 
+// n arrivals (a warp arriving for itself and n - 1 others), from the lane
+// elect.sync picks (the warp must be converged).
+__device__ __forceinline__ void mbar_arrive_warp_n(uint32_t bar, uint32_t n) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(n)
+      : "memory");
+}
+
 // One arrival per warp, from the lane elect.sync picks (the warp must be
 // converged); no branch around it.
 __device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
@@ -288,6 +299,16 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 // generic-proxy writes to shared memory -> visible to the async proxy (MMA)
+// 16 bytes global -> shared without registers (cp.async); n_src = 0 writes
+// zeros and reads nothing.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int n_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n_src) : "memory");
+}
+// The mbarrier tracks this thread's earlier cp.async copies: its pending
+// count rises by one now and falls by one when they have landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

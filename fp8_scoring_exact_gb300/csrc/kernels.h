@@ -64,7 +64,7 @@ struct ScoreParams {
   int mode;                    // MODE_STORE or MODE_FILTER
   int chunk_tiles;
   int plan;                    // which plan to read (PLAN_*)
-  const float* k_scale;        // dense [N] (paged key scales come through the scale tensor map)
+  const float* k_scale;        // dense [N] or paged [P * 64]
   const float* q_scale;
   const float* w;
   const int32_t* rb;
@@ -77,7 +77,7 @@ struct ScoreParams {
   uint32_t* cand_key;          // [R, ROW_SLOTS]
   int32_t* cand_idx;           // [R, ROW_SLOTS]
   int32_t* unit_count;         // [R, max_units, 4]: candidates region (c, q) holds (cap + 1: lost some)
-  int max_units;               // units per group, at most
+  int max_units;               // candidate-region units per row, at most (2 x work units)
   // MODE_STORE
   float* scores;               // [slots, ld]
   int64_t ld;
@@ -177,9 +177,8 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_pairs, cudaStream_t s);
 cudaError_t launch_sample_prep(const SamplePrepParams& p, cudaStream_t s);
 cudaError_t launch_sample_tau(const SampleTauParams& p, cudaStream_t s);
-// tm_ks: paged key scales as a 1-D fp32 tensor, box 64 (unused for dense keys)
-cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_ks,
-                         const ScoreParams& p, int grid, cudaStream_t s);
+cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
+                         cudaStream_t s);
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
 cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s);

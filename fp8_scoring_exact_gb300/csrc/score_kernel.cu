@@ -16,7 +16,12 @@
 //                K = 32, fp32 accumulators in one of two 256-column TMEM
 //                buffers; owns the TMEM allocation;
 //   warps 2-17   epilogue: warps 2 + 4r .. 5 + 4r handle row r of the group,
-//                warp w the TMEM lane quarter w % 4.  Each thread reads two
+//                warp w the TMEM lane quarter w % 4.  A paged group of at
+//                most two rows splits them into two teams (rows 0-1 and rows
+//                2-3 of the warps) that take alternate tiles, one
+//                accumulator buffer each, so no warp idles (decode batches
+//                have one or two rows per sequence; dense groups keep the
+//                plain loop, whose issue slots the extra test would cost).  Each thread reads two
 //                keys x 16 heads per TMEM load (16x256b shape), keeps the 16
 //                weights w * q_scale in registers, applies ReLU and the
 //                weights with packed f32x2 FMAs, and a three-shuffle
@@ -139,7 +144,7 @@ __device__ __forceinline__ float hsum2(uint64_t v) {
 template <int MODE, bool PAGED>
 __global__ void __launch_bounds__(SCORE_THREADS, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_ks, const ScoreParams p) {
+                 const ScoreParams p) {
   const int n_groups = p.plan == PLAN_REPAIR   ? p.stats->r_groups
                        : p.plan == PLAN_SAMPLE ? p.stats->s_groups
                                                : p.stats->n_groups;
@@ -199,15 +204,15 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer --
     // The whole warp runs the loop (uniform control flow); lane 0 arms the
-    // barriers.  Paged keys: lanes 0-3 issue a tile's four copies (two key
-    // pages, two scale blocks) in one go, and the block-table entries come
-    // in batches of 16 tiles, one entry per lane, so the per-tile chain of
-    // this warp holds no global load (measured: a one-thread producer with
-    // a load and four copies per tile was the paged pipeline's bound).
+    // barriers and issues the TMA copies.  Paged keys: the block-table
+    // entries come in batches of 16 tiles, one entry per lane, and the
+    // tile's 128 key scales are one cp.async of 16 bytes per lane, so the
+    // tile costs two TMA issues (one per page) and no global load in this
+    // warp's chain (measured: each TMA issue takes this warp 100-200 cycles,
+    // and four of them per tile bounded the paged pipeline).
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      if (paged) tma_prefetch_desc(&tm_ks);
     }
     const int num_pages = p.rs.num_pages;
     uint32_t kit = 0, ui = 0;
@@ -253,17 +258,21 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           const int pg0 = __shfl_sync(0xffffffffu, btv, i0);
           const int pg1 = __shfl_sync(0xffffffffu, btv, i0 + 1);
           const int pg1s = pg1 >= 0 ? pg1 : num_pages;
+          // lane l copies scales 4 (l % 16) .. +3 of page l < 16 ? pg0 : pg1
+          // (zeros for the page past the cache); the barrier counts the
+          // copies before the arrive below can complete its phase
+          const int pl = lane < 16 ? pg0 : pg1s;
+          cp_async_16(sbase + OFF_SCALE + st * SCALE_STAGE_BYTES + lane * 16,
+                      p.k_scale + (int64_t)min(pl, num_pages - 1) * PAGE + 4 * (lane & 15), pl < num_pages ? 16 : 0);
+          cp_async_mbar_arrive(key_full(st));
+          __syncwarp();
           if (lane == 0) {
             stage_pages[2 * st] = pg0;
             stage_pages[2 * st + 1] = pg1s;
-            mbar_arrive_expect_tx(key_full(st), (pg1 >= 0 ? 2 : 1) * PAGE * D + SCALE_STAGE_BYTES);
+            mbar_arrive_expect_tx(key_full(st), (pg1 >= 0 ? 2 : 1) * PAGE * D);
+            tma_load_2d(kdst, &tm_k, 0, pg0 * PAGE, key_full(st));
+            if (pg1 >= 0) tma_load_2d(kdst + PAGE * D, &tm_k, 0, pg1 * PAGE, key_full(st));
           }
-          __syncwarp();
-          const uint32_t sdst = sbase + OFF_SCALE + st * SCALE_STAGE_BYTES;
-          if (lane == 0 || (lane == 1 && pg1 >= 0))
-            tma_load_2d(kdst + lane * PAGE * D, &tm_k, 0, (lane ? pg1 : pg0) * PAGE, key_full(st));
-          else if (lane == 2 || lane == 3)
-            tma_load_1d(sdst + (lane - 2) * PAGE * 4, &tm_ks, (lane == 2 ? pg0 : pg1s) * PAGE, key_full(st));
         }
       }
     }
@@ -298,8 +307,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue --
-    const int r = (warp - 2) >> 2;  // row of the group these four warps handle
-    const int quarter = warp & 3;   // TMEM lane quarter of this warp
+    const int r4 = (warp - 2) >> 2;  // row slot of these four warps (0-3)
+    const int quarter = warp & 3;    // TMEM lane quarter of this warp
     // after the reduce-scatter this thread owns key (lane / 4) + 8 (lane % 4)
     // of its warp's 32 TMEM lanes
     const int kt = quarter * 32 + (lane >> 2) + 8 * (lane & 3);
@@ -309,6 +318,16 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       Group G;
       const Unit un = decode_unit(p, n_groups, u, G);
       const Group* gp = p.groups + un.g;
+      // two teams for a paged group of at most two rows: team t handles the
+      // tiles of accumulator buffer t, and its candidate regions are those
+      // of the virtual unit 2 c + t; a warp's arrivals then count for its
+      // idle twin of the other team as well
+      const bool split = paged && G.nrows <= 2;
+      const int team = split ? (r4 >> 1) : 0;
+      const int r = split ? (r4 & 1) : r4;
+      const int vunits = split ? 2 * un.nunits : un.nunits;
+      const int vc = split ? 2 * un.c + team : un.c;
+      const uint32_t arrivals = split ? 2u : 1u;
       const bool active = r < G.nrows;
       const int row = active ? __ldg(&gp->row[r]) : 0;
       int rb = 0, re = 0;
@@ -316,8 +335,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       float* srow = nullptr;
       int64_t store_lim = 0;
       // this warp's candidate region of the unit
-      const int wcap = region_cap(un.nunits);
-      const int64_t region = (int64_t)row * ROW_SLOTS + (int64_t)(un.c * UNIT_REGIONS + quarter) * wcap;
+      const int wcap = region_cap(vunits);
+      const int64_t region = (int64_t)row * ROW_SLOTS + (int64_t)(vc * UNIT_REGIONS + quarter) * wcap;
       uint32_t* ck = p.cand_key + region;
       int32_t* ci = p.cand_idx + region;
       int wcnt = 0;
@@ -341,6 +360,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         }
       }
       for (int t = un.t0; t < un.t1 && ok; ++t, ++ait) {
+        if (split && (int)(ait & 1) != team) continue;  // the other team's tile
         // this thread's key scale, used at the end of the iteration (paged:
         // and the page holding the key, from the tile's key stage, which
         // this warp then releases with the accumulator; the stage cannot be
@@ -379,8 +399,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           chunk_partials<true>(va, w2, aH, bH);
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive_warp(acc_empty(ab));
-          if (paged) mbar_arrive_warp(key_empty(kst));
+          mbar_arrive_warp_n(acc_empty(ab), arrivals);
+          if (paged) mbar_arrive_warp_n(key_empty(kst), arrivals);
           chunk_partials<false>(vb, w2 + 4, aH, bH);
           part[0] = hsum2(aL);
           part[1] = hsum2(bL);
@@ -388,8 +408,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           part[3] = hsum2(bH);
         } else {
           tc_fence_before();
-          mbar_arrive_warp(acc_empty(ab));
-          if (paged) mbar_arrive_warp(key_empty(kst));
+          mbar_arrive_warp_n(acc_empty(ab), arrivals);
+          if (paged) mbar_arrive_warp_n(key_empty(kst), arrivals);
         }
         if (!active) continue;
         // reduce-scatter over the 4 lanes sharing keys: part[j] covers key
@@ -419,7 +439,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       }
       // unit done: the warp's count (wcap + 1 = some were lost)
       if (filter && active && ok && lane == 0)
-        p.unit_count[(int64_t)row * p.max_units * UNIT_REGIONS + un.c * UNIT_REGIONS + quarter] = min(wcnt, wcap + 1);
+        p.unit_count[(int64_t)row * p.max_units * UNIT_REGIONS + vc * UNIT_REGIONS + quarter] = min(wcnt, wcap + 1);
     }
   }
 
@@ -440,8 +460,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
 }
 
 template <int MODE, bool PAGED>
-static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_ks,
-                                  const ScoreParams& p, int grid, cudaStream_t s) {
+static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
+                                  cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(score_kernel<MODE, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -449,18 +469,18 @@ static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  score_kernel<MODE, PAGED><<<grid, SCORE_THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, tm_ks, p);
+  score_kernel<MODE, PAGED><<<grid, SCORE_THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_ks,
-                         const ScoreParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
+                         cudaStream_t s) {
   const bool paged = p.rs.paged != 0;
   if (p.mode == MODE_FILTER)
-    return paged ? launch_variant<MODE_FILTER, true>(tm_q, tm_k, tm_ks, p, grid, s)
-                 : launch_variant<MODE_FILTER, false>(tm_q, tm_k, tm_ks, p, grid, s);
-  return paged ? launch_variant<MODE_STORE, true>(tm_q, tm_k, tm_ks, p, grid, s)
-               : launch_variant<MODE_STORE, false>(tm_q, tm_k, tm_ks, p, grid, s);
+    return paged ? launch_variant<MODE_FILTER, true>(tm_q, tm_k, p, grid, s)
+                 : launch_variant<MODE_FILTER, false>(tm_q, tm_k, p, grid, s);
+  return paged ? launch_variant<MODE_STORE, true>(tm_q, tm_k, p, grid, s)
+               : launch_variant<MODE_STORE, false>(tm_q, tm_k, p, grid, s);
 }
 
 }  // namespace dsa

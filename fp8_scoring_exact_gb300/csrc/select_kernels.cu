@@ -691,7 +691,9 @@ __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const Cand
     const Group* gp = p.groups + g;
     if (r >= gp->nrows) continue;  // uniform over the CTA
     const int row = gp->row[r];
-    const int nu = p.unit_start[g + 1] - p.unit_start[g];
+    // a paged group of at most two rows has two candidate teams per unit
+    // (the scorer's virtual units 2 c and 2 c + 1)
+    const int nu = (p.rs.paged && gp->nrows <= 2 ? 2 : 1) * (p.unit_start[g + 1] - p.unit_start[g]);
     const int nreg = nu * UNIT_REGIONS;
     const int wcap = region_cap(max(nu, 1));
     const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * UNIT_REGIONS;
