@@ -113,7 +113,7 @@ def test_paged_decode_batch_all_rows(B):
 
 
 # ------------------------------------------------------------------ paged ----
-@pytest.mark.parametrize("next_n", [1, 2, 3])
+@pytest.mark.parametrize("next_n", [1, 2, 3, 5])
 def test_paged_small_all_rows(B, next_n):
     inp = S.make_paged(7, next_n, K=300, seed=10 + next_n, len_lo=1, len_hi=5000, n_short=3, short_hi=310)
     # a sequence shorter than next_n and one ending exactly on a page boundary
@@ -144,6 +144,28 @@ def test_forced_repair_is_exact(B, bias, kind):
     assert counters[kind] == inp.Q
     assert sorted(B.last_repaired_rows()) == list(range(inp.Q))
     assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
+@pytest.mark.parametrize("bias,kind", [(1 << 31, "underflow"), (-(1 << 33), "overflow")])
+def test_forced_repair_paged_is_exact(B, bias, kind):
+    """The same for paged decode rows: groups of one and two rows (whose
+    epilogue runs as two teams on alternate tiles) and of four rows, all
+    through exact repair over the physical slots.  Every row is longer than
+    the 8192 candidates a row may keep, so a zero threshold overflows it."""
+    inp = S.make_paged(6, 5, K=256, seed=33, len_lo=9000, len_hi=20000, n_short=0)
+    B.set_option("tau_bias", bias)
+    try:
+        out = B.indexer_topk_paged(*paged_args(inp), K=inp.K).cpu().numpy()
+        counters = _status_ok(B)
+    finally:
+        B.set_option("tau_bias", 0)
+    assert counters[kind] == inp.B * inp.next_n
+    po = indexer.PagedOracle.from_inputs(inp)
+    for b in range(inp.B):
+        for i in range(inp.next_n):
+            slots, I, E = po.row_scores(b, i)
+            pr = checks.check_row(out[b, i], slots, I, E, inp.K, order_key=np.arange(len(slots)))
+            assert not pr, (b, i, pr)
 
 
 # ------------------------------------------------------------- edge cases ----
