@@ -304,6 +304,10 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int n_src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n_src) : "memory");
 }
+// 4 bytes global -> shared (cp.async; both addresses 4-byte aligned)
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
 // The mbarrier tracks this thread's earlier cp.async copies: its pending
 // count rises by one now and falls by one when they have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {

@@ -4,7 +4,11 @@
 // the work units of a plan built on the device: a unit is a group of up to 4
 // query rows (which stream the same keys) with a chunk of 128-key tiles.
 // Roles:
-//   warp 0       TMA producer: q rows of the group (64 heads x 128 B each),
+//   warp 0       TMA producer: q rows of the group (64 heads x 128 B each)
+//                and, beside them, the unit's descriptor and its rows'
+//                weights, q scales, ranges and thresholds (cp.async), so the
+//                MMA and epilogue warps start a unit from shared memory
+//                instead of a binary search and a chain of global loads;
 //                key tiles (128 keys x 128 B, 128-byte swizzle) into a
 //                STAGES-deep ring; paged keys: also each tile's 128 key
 //                scales and two page ids into the same stage (the
@@ -64,7 +68,19 @@ constexpr uint32_t OFF_KEYS = 0;
 constexpr uint32_t OFF_Q = OFF_KEYS + STAGES * KEY_STAGE_BYTES;
 constexpr uint32_t OFF_SCALE = OFF_Q + 2 * Q_SLOT_BYTES;
 constexpr uint32_t OFF_PAGE = OFF_SCALE + STAGES * SCALE_STAGE_BYTES;  // paged: [STAGES][2] page ids
-constexpr uint32_t OFF_BAR = OFF_PAGE + 128;
+// per q slot: the unit those q rows belong to, as the MMA and epilogue
+// warps need it (producer-written)
+struct UnitSlot {
+  int t0, t1, c, nunits, nrows, pad[3];
+  int row[GROUP_ROWS], slot[GROUP_ROWS];
+  float w[GROUP_ROWS][H];  // the rows' head weights (cp.async)
+  float qsc[GROUP_ROWS];   // q scales (cp.async)
+  int rb[GROUP_ROWS], re[GROUP_ROWS];
+  uint32_t tau[GROUP_ROWS];  // threshold keys (filter mode)
+};
+static_assert(sizeof(UnitSlot) % 16 == 0 && offsetof(UnitSlot, w) % 16 == 0, "unit slot layout");
+constexpr uint32_t OFF_UNIT = OFF_PAGE + 128;
+constexpr uint32_t OFF_BAR = OFF_UNIT + 2 * sizeof(UnitSlot);
 constexpr int N_BARS = 2 * STAGES + 4 + 2 * ACC_BUFS;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr uint32_t MISC_BYTES = 64;
@@ -165,6 +181,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
   auto acc_full = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + i); };
   auto acc_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + ACC_BUFS + i); };
   const float* stage_scales = (const float*)(smem + OFF_SCALE);
+  UnitSlot* unit_slots = (UnitSlot*)(smem + OFF_UNIT);
   int* stage_pages = (int*)(smem + OFF_PAGE);
 
   const int warp = threadIdx.x >> 5;
@@ -184,7 +201,9 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(q_full(i), 1);
-      mbar_init(q_empty(i), 1);
+      // released by the MMA (last tile of the unit) and by every epilogue
+      // warp (once it holds the unit's slot data in registers)
+      mbar_init(q_empty(i), 1 + EPI_THREADS / 32);
     }
     for (int i = 0; i < ACC_BUFS; ++i) {
       mbar_init(acc_full(i), 1);
@@ -222,6 +241,55 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       const Unit un = decode_unit(p, n_groups, u, G);
       const int qs = ui & 1;
       if (!(ok = mbar_wait_warp_backoff(q_empty(qs), ((ui >> 1) & 1) ^ 1, abort_flag, status))) break;
+      {
+        // the unit's slot: row data by cp.async (4-byte weight copies when
+        // the weight array is not 16-byte aligned), which q_full tracks,
+        // and the descriptor by plain stores, published by the arrive below
+        UnitSlot* us = unit_slots + qs;
+        int rowr[GROUP_ROWS];
+#pragma unroll
+        for (int r = 0; r < GROUP_ROWS; ++r) rowr[r] = r < G.nrows ? G.row[r] : 0;
+        // row id of a lane-dependent row index, without indexing registers
+        auto row_of = [&](int r) { return r == 0 ? rowr[0] : r == 1 ? rowr[1] : r == 2 ? rowr[2] : rowr[3]; };
+        const bool w16 = (reinterpret_cast<uintptr_t>(p.w) & 15u) == 0;
+        if (w16) {
+#pragma unroll
+          for (int k = lane; k < GROUP_ROWS * H / 4; k += 32) {
+            const int r = k / (H / 4), ch = k % (H / 4);
+            if (r < G.nrows) cp_async_16(smem_u32(&us->w[r][4 * ch]), p.w + (int64_t)row_of(r) * H + 4 * ch, 16);
+          }
+        } else {
+#pragma unroll
+          for (int k = lane; k < GROUP_ROWS * H; k += 32) {
+            const int r = k / H, h = k % H;
+            if (r < G.nrows) cp_async_4(smem_u32(&us->w[r][h]), p.w + (int64_t)row_of(r) * H + h);
+          }
+        }
+        if (lane < 4 * GROUP_ROWS) {
+          const int r = lane >> 2, f = lane & 3;
+          if (r < G.nrows) {
+            const int row = row_of(r);
+            if (f == 0) cp_async_4(smem_u32(&us->qsc[r]), p.q_scale + row);
+            if (f == 1) cp_async_4(smem_u32(&us->rb[r]), p.rb + row);
+            if (f == 2) cp_async_4(smem_u32(&us->re[r]), p.re + row);
+            if (f == 3 && p.tau) cp_async_4(smem_u32(&us->tau[r]), p.tau + row);
+          }
+        }
+        cp_async_mbar_arrive(q_full(qs));
+        if (lane == 0) {
+          us->t0 = un.t0;
+          us->t1 = un.t1;
+          us->c = un.c;
+          us->nunits = un.nunits;
+          us->nrows = G.nrows;
+#pragma unroll
+          for (int r = 0; r < GROUP_ROWS; ++r) {
+            us->row[r] = rowr[r];
+            us->slot[r] = r < G.nrows ? G.slot[r] : 0;
+          }
+        }
+      }
+      __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(q_full(qs), G.nrows * Q_ROW_BYTES);
       __syncwarp();
 #pragma unroll
@@ -282,13 +350,13 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       uint32_t kit = 0, ait = 0, ui = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ui) {
-        Group G;
-        const Unit un = decode_unit(p, n_groups, u, G);
         const int qs = ui & 1;
         if (!(ok = mbar_wait(q_full(qs), (ui >> 1) & 1, abort_flag, status))) break;
-        const uint32_t idesc = idesc_e4m3_f32(TILE, H * G.nrows);
+        const UnitSlot* us = unit_slots + qs;
+        const int t0 = us->t0, t1 = us->t1;
+        const uint32_t idesc = idesc_e4m3_f32(TILE, H * us->nrows);
         const uint64_t qdesc = sw128_kmajor_desc(sbase + OFF_Q + qs * Q_SLOT_BYTES);
-        for (int t = un.t0; t < un.t1; ++t, ++kit, ++ait) {
+        for (int t = t0; t < t1; ++t, ++kit, ++ait) {
           const int st = kit % STAGES;
           if (!(ok = mbar_wait(key_full(st), (kit / STAGES) & 1, abort_flag, status))) break;
           const int ab = ait % ACC_BUFS;
@@ -312,24 +380,27 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
     // after the reduce-scatter this thread owns key (lane / 4) + 8 (lane % 4)
     // of its warp's 32 TMEM lanes
     const int kt = quarter * 32 + (lane >> 2) + 8 * (lane & 3);
-    uint32_t ait = 0;
+    uint32_t ait = 0, ui = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      Group G;
-      const Unit un = decode_unit(p, n_groups, u, G);
-      const Group* gp = p.groups + un.g;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ui) {
+      // the unit as the producer staged it beside its q rows; the slot is
+      // released as soon as this warp holds what it needs in registers
+      const int qs = ui & 1;
+      if (!(ok = mbar_wait_warp(q_full(qs), (ui >> 1) & 1, abort_flag, status))) break;
+      const UnitSlot* us = unit_slots + qs;
+      const int t0 = us->t0, t1 = us->t1, nrows = us->nrows;
       // two teams for a paged group of at most two rows: team t handles the
       // tiles of accumulator buffer t, and its candidate regions are those
       // of the virtual unit 2 c + t; a warp's arrivals then count for its
       // idle twin of the other team as well
-      const bool split = paged && G.nrows <= 2;
+      const bool split = paged && nrows <= 2;
       const int team = split ? (r4 >> 1) : 0;
       const int r = split ? (r4 & 1) : r4;
-      const int vunits = split ? 2 * un.nunits : un.nunits;
-      const int vc = split ? 2 * un.c + team : un.c;
+      const int vunits = split ? 2 * us->nunits : us->nunits;
+      const int vc = split ? 2 * us->c + team : us->c;
       const uint32_t arrivals = split ? 2u : 1u;
-      const bool active = r < G.nrows;
-      const int row = active ? __ldg(&gp->row[r]) : 0;
+      const bool active = r < nrows;
+      const int row = active ? us->row[r] : 0;
       int rb = 0, re = 0;
       float tauf = 0.f;
       float* srow = nullptr;
@@ -346,20 +417,22 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
 #pragma unroll
       for (int m = 0; m < 8; ++m) w2[m] = 0;
       if (active) {
-        const float qsc = __ldg(&p.q_scale[row]) * RELU_SAT_WEIGHT_SCALE;
-        const float* wr = p.w + (int64_t)row * H + 2 * (lane & 3);
+        const float qsc = us->qsc[r] * RELU_SAT_WEIGHT_SCALE;
+        const float* wr = &us->w[r][2 * (lane & 3)];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) w2[m] = pack2(__ldg(&wr[8 * m]) * qsc, __ldg(&wr[8 * m + 1]) * qsc);
-        rb = __ldg(&p.rb[row]);
-        re = __ldg(&p.re[row]);
+        for (int m = 0; m < 8; ++m) w2[m] = pack2(wr[8 * m] * qsc, wr[8 * m + 1] * qsc);
+        rb = us->rb[r];
+        re = us->re[r];
         if (filter) {
-          tauf = key_threshold_float(__ldg(&p.tau[row]));
+          tauf = key_threshold_float(us->tau[r]);
         } else {
-          srow = p.scores + (int64_t)__ldg(&gp->slot[r]) * p.ld;
+          srow = p.scores + (int64_t)us->slot[r] * p.ld;
           store_lim = min((int64_t)p.rs.N, p.ld);
         }
       }
-      for (int t = un.t0; t < un.t1 && ok; ++t, ++ait) {
+      __syncwarp();
+      mbar_arrive_warp(q_empty(qs));
+      for (int t = t0; t < t1 && ok; ++t, ++ait) {
         if (split && (int)(ait & 1) != team) continue;  // the other team's tile
         // this thread's key scale, used at the end of the iteration (paged:
         // and the page holding the key, from the tile's key stage, which
