@@ -324,7 +324,30 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
     sp.tau = tau;
     sp.out = out;
     sp.stats = st;
+    // paged grids span up to 8 sample tiles: one CTA per (pair, tile), then
+    // one warp per row selects its threshold
+    sp.split = rs.paged;
+    sp.sscores = at<float>(a, L.sscores);
+    sp.sld = SAMPLE_LD;
+    sp.srb = at<int32_t>(a, L.srb);
+    sp.sre = at<int32_t>(a, L.sre);
     DSA_LAUNCH(launch_sample(tm_q, sp, n_pairs(rs), stream));
+    if (sp.split) {
+      SampleTauParams tp{};
+      tp.rs = rs;
+      tp.K = K;
+      tp.target16 = o.target16;
+      tp.tau_bias = o.bias;
+      tp.rb = pp.rb;
+      tp.re = pp.re;
+      tp.srb = sp.srb;
+      tp.sre = sp.sre;
+      tp.sscores = sp.sscores;
+      tp.sld = SAMPLE_LD;
+      tp.tau = tau;
+      tp.stats = st;
+      DSA_LAUNCH(launch_sample_tau(tp, stream));
+    }
   }
 
   ScoreParams cp{};

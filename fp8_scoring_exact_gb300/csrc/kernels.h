@@ -54,9 +54,16 @@ struct SampleParams {
   const float* w;
   const int32_t* rb;
   const int32_t* re;
-  uint32_t* tau;               // [R] threshold keys (written)
+  uint32_t* tau;               // [R] threshold keys (written; not in split mode)
   int32_t* out;                // [R, K] (trivial rows written here)
   Stats* stats;
+  // split mode: one CTA per (row pair, 128-key sample tile) writes the
+  // sample scores and each row's sample range; sample_tau then selects
+  int split;
+  float* sscores;              // [R, sld]: row r's score of pair-grid sample j at r * sld + j
+  int64_t sld;
+  int32_t* srb;                // [R] first / end pair-grid sample inside the row's range
+  int32_t* sre;
 };
 
 struct ScoreParams {

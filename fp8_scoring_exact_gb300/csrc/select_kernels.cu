@@ -191,6 +191,10 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
 // remapping path; the other rows score the keys on a 1-in-200 grid with
 // tcgen05 (keys gathered into a swizzled shared tile by the threads) and take
 // as threshold the sample of descending rank ceil(m * target / L).
+// Split mode (paged rows, whose grids span several tiles): one CTA per (pair,
+// 128-key sample tile), so the tiles' gathers run side by side; each writes
+// its fp32 sample scores (and the tile-0 CTA the rows' sample ranges and
+// the trivial rows), and sample_tau_kernel selects the thresholds.
 constexpr int SAMPLE_THREADS = 128;
 constexpr uint32_t SM_OFF_Q = 0;
 constexpr uint32_t SM_OFF_K = SM_OFF_Q + SAMPLE_ROWS * H * D;       // 16384
@@ -199,11 +203,12 @@ constexpr uint32_t SM_OFF_W = SM_OFF_SAMP + SAMPLE_ROWS * MAX_SAMPLES * 4;  // 4
 constexpr uint32_t SM_OFF_SC = SM_OFF_W + SAMPLE_ROWS * H * 4;
 constexpr uint32_t SM_OFF_HIST = SM_OFF_SC + TILE * 4;
 constexpr uint32_t SM_OFF_MISC = SM_OFF_HIST + 256 * 4;
-// 52 KB per CTA: 4 CTAs (4 x 128 TMEM columns, all 512) fit on an SM
+// 52 KB per CTA: 4 CTAs (4 x 128 TMEM columns, all 512) fit on an SM, and
+// the launch bounds hold the registers to 128 so that 4 CTAs fit there too
 constexpr uint32_t SAMPLE_SMEM = 52 * 1024;
 static_assert(SM_OFF_MISC + 64 + 1024 <= SAMPLE_SMEM, "sample smem");
 
-__global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 const SampleParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -220,11 +225,13 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
 
   int rows[SAMPLE_ROWS];
   const int nr = rows_of_group<SAMPLE_ROWS>(rs, blockIdx.x, rows);
+  const bool split = p.split != 0;
+  const int tile0 = split ? (int)blockIdx.y : 0;  // split: this CTA's sample tile
   int act[2], nact = 0, lo = 0x7fffffff, hi = 0, ntriv = 0;
   for (int i = 0; i < nr; ++i) {
     const int b = p.rb[rows[i]], e = p.re[rows[i]];
     if (e - b <= K) {
-      write_all_valid(rs, rows[i], b, e, K, p.out, tid, SAMPLE_THREADS);
+      if (tile0 == 0) write_all_valid(rs, rows[i], b, e, K, p.out, tid, SAMPLE_THREADS);
       ++ntriv;
     } else {
       act[nact++] = rows[i];
@@ -232,12 +239,21 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
       hi = max(hi, e);
     }
   }
-  if (tid == 0 && ntriv) atomicAdd(&p.stats->trivial, ntriv);
+  if (tid == 0 && ntriv && tile0 == 0) atomicAdd(&p.stats->trivial, ntriv);
   if (nact == 0) return;
   int first, m_u, S;
   sample_grid(lo, hi, &first, &m_u, &S);
   const int target = (int)(((int64_t)p.target16 * K) / 16);
-  if (m_u == 0) {
+  if (split) {
+    // each active row's samples: pair-grid indices [j0, j1) inside its range
+    if (tile0 == 0 && tid < nact) {
+      const int row = act[tid];
+      const int b = p.rb[row], e = p.re[row];
+      p.srb[row] = max(0, ceil_div(b - first, S));
+      p.sre[row] = min(m_u, max(0, ceil_div(e - first, S)));
+    }
+    if (tile0 * TILE >= m_u) return;
+  } else if (m_u == 0) {
     if (tid < nact) p.tau[act[tid]] = 0u;
     return;
   }
@@ -270,7 +286,10 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
   __syncthreads();
   bool ok = misc[6] != 0;
   const uint32_t idesc = idesc_e4m3_f32(TILE, H * nact);
-  const int ntiles = ceil_div(m_u, TILE);
+  // tiles [tt_begin, tt_end) of the pair's grid: all of them, or this
+  // CTA's one in split mode
+  const int tt_begin = tile0;
+  const int tt_end = split ? tile0 + 1 : ceil_div(m_u, TILE);
   // one sample key per thread: its 128 bytes and scale; the next tile's are
   // loaded while the current tile is multiplied and reduced
   uint4 chunk[8];
@@ -296,8 +315,8 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
       for (int c = 0; c < 8; ++c) chunk[c] = make_uint4(0, 0, 0, 0);
     }
   };
-  fetch(0);
-  for (int tt = 0; tt < ntiles && ok; ++tt) {
+  fetch(tt_begin);
+  for (int tt = tt_begin; tt < tt_end && ok; ++tt) {
     const int j = tt * TILE + tid;
     const bool vj = j < m_u;
     // the fetched key into the 128-byte-swizzled tile
@@ -315,8 +334,9 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
                  idesc, k > 0);
       mma_commit(bar);
     }
-    if (tt + 1 < ntiles) fetch(tt + 1);
-    if (tid == 0) misc[6] = mbar_wait(bar, (tt + 1) & 1, abort_flag, &p.stats->status) ? 1 : 0;
+    if (tt + 1 < tt_end) fetch(tt + 1);
+    // phase 0 was the q load; this CTA's i-th MMA commit completes phase i + 1
+    if (tid == 0) misc[6] = mbar_wait(bar, (tt - tt_begin + 1) & 1, abort_flag, &p.stats->status) ? 1 : 0;
     __syncwarp();
     __syncthreads();
     ok = misc[6] != 0;
@@ -331,14 +351,19 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
       float acc = 0.f;
 #pragma unroll
       for (int h = 0; h < H; ++h) acc = fmaf(wsm[a * H + h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
-      if (vj) samp[a * MAX_SAMPLES + j] = ordered_key(acc * scs[tid]);
+      if (vj) {
+        if (split)
+          p.sscores[(int64_t)act[a] * p.sld + j] = acc * scs[tid];
+        else
+          samp[a * MAX_SAMPLES + j] = ordered_key(acc * scs[tid]);
+      }
     }
     tc_fence_before();
     __syncthreads();
   }
 
   // threshold of each active row from the samples inside its own range
-  for (int a = 0; a < nact && ok; ++a) {
+  for (int a = 0; a < nact && ok && !split; ++a) {
     const int row = act[a];
     const int b = p.rb[row], e = p.re[row];
     const int j0 = max(0, ceil_div(b - first, S));
@@ -357,7 +382,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
     }
     if (tid == 0) p.tau[row] = tau;
   }
-  if (!ok && tid < nact) p.tau[act[tid]] = 0u;
+  if (!ok && !split && tid < nact) p.tau[act[tid]] = 0u;
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -367,6 +392,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const __grid_con
 }
 
 cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_pairs_, cudaStream_t s) {
+  const dim3 grid(n_pairs_, p.split ? ceil_div(MAX_SAMPLES, TILE) : 1);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SAMPLE_SMEM);
@@ -374,7 +400,7 @@ cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_
     attr_set = true;
   }
   if (n_pairs_ <= 0) return cudaSuccess;
-  sample_kernel<<<n_pairs_, SAMPLE_THREADS, SAMPLE_SMEM, s>>>(tm_q, p);
+  sample_kernel<<<grid, SAMPLE_THREADS, SAMPLE_SMEM, s>>>(tm_q, p);
   return cudaGetLastError();
 }
 
