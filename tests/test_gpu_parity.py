@@ -7,6 +7,8 @@ score within TOL * E of the oracle's K-th score; on the small cases the sorted
 selected scores equal the oracle's element-wise.  Large cases are checked on
 seeded row samples plus every row the device sent to repair.
 """
+import copy
+
 import numpy as np
 import pytest
 
@@ -280,3 +282,57 @@ def test_topk_from_scores_exact(B):
         want = np.sort(sc[t, rb[t]:re[t]])[::-1][:n]
         got = np.sort(sc[t, sel])[::-1]
         assert np.array_equal(got, want), t
+
+
+# ------------------------------------------------------------- CUDA graph ----
+def test_fused_call_replays_from_a_cuda_graph(B):
+    """The fused call enqueues kernels only (no host synchronisation, no
+    allocation once its scratch is sized), so it can be captured into a CUDA
+    graph; a replay reads the buffers' current contents: new inputs copied
+    into the captured buffers give those inputs' exact top-K.  Dense rows with
+    the shared sample grid, and paged rows with split sampling."""
+    import torch
+    a = S.make_dense(24, 60000, K=1024, seed=51, causal=True)
+    b = S.make_dense(24, 60000, K=1024, seed=52, causal=True)
+    pa = S.make_paged(5, 2, K=512, seed=53, len_lo=300, len_hi=40000, n_short=1, short_hi=500)
+    # same shapes and page layout, new contents: the cache pages reversed,
+    # the queries and weights moved one sequence on
+    pb = copy.deepcopy(pa)
+    pb.k_cache = np.ascontiguousarray(pa.k_cache[::-1])
+    pb.k_cache_scale = np.ascontiguousarray(pa.k_cache_scale[::-1])
+    pb.q = np.roll(pa.q, 1, axis=0)
+    pb.q_scale = np.roll(pa.q_scale, 1, axis=0)
+    pb.w = np.roll(pa.w, 1, axis=0)
+    dev_d, dev_p = dense_args(a), paged_args(pa)
+    out_d = torch.empty((a.Q, a.K), dtype=torch.int32, device="cuda")
+    out_p = torch.empty((pa.B, pa.next_n, pa.K), dtype=torch.int32, device="cuda")
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+
+    def calls():
+        B.indexer_topk(*dev_d, K=a.K, out=out_d)
+        B.indexer_topk_paged(*dev_p, K=pa.K, out=out_p)
+
+    with torch.cuda.stream(gs):
+        calls()  # sizes this stream's scratch
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        calls()
+    for dst, src in zip(dev_d, dense_args(b)):
+        dst.copy_(src)
+    for dst, src in zip(dev_p, paged_args(pb)):
+        dst.copy_(src)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    rc, _ = B.last_device_status(gs)
+    assert rc == 0
+    assert check_dense_rows(b, out_d.cpu().numpy(), range(b.Q)) == {}
+    outp = out_p.cpu().numpy()
+    po = indexer.PagedOracle.from_inputs(pb)
+    for bb in range(pb.B):
+        for i in range(pb.next_n):
+            slots, I, E = po.row_scores(bb, i)
+            pr = checks.check_row(outp[bb, i], slots, I, E, pb.K, order_key=np.arange(len(slots)))
+            assert not pr, (bb, i, pr)
