@@ -44,6 +44,7 @@ struct Layout {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+static_assert(MAX_K == DSA_MAX_K, "kernel K cap matches the public header");
 constexpr int64_t SAMPLE_LD = (MAX_SAMPLES + 2 + 3) / 4 * 4;  // sample-score row stride
 
 // cand_stride: candidate slots per row (0: no candidate buffers); max_units:
