@@ -48,6 +48,7 @@ constexpr int SAMPLE_OFFSET = 100; // samples at keys 100 mod 200
 constexpr int MAX_SAMPLES = 1024;  // per row; longer rows widen the stride
 constexpr int SELECT_THREADS = 512;
 constexpr int SELECT_CAP = 12288;  // candidates the standalone selector keeps in SMEM
+constexpr int SEL_UNROLL = 4;      // float4 loads in flight per thread in its filter pass
 
 // Which plan a kernel reads: every row, the rows queued for repair, or the
 // rows' sample grids.
@@ -300,6 +301,18 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 // generic-proxy writes to shared memory -> visible to the async proxy (MMA)
+// Programmatic dependent launch: the library launches every kernel with
+// programmatic stream serialisation.  A kernel first lets the next launch
+// begin (it starts once every CTA of this grid has reached this point, and
+// its CTAs take SM resources only as they free up), then waits until the
+// previous grid of the stream has completed and its memory is visible: the
+// launch latency between the call's kernels overlaps the previous kernel's
+// tail.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // 16 bytes global -> shared without registers (cp.async); n_src = 0 writes
 // zeros and reads nothing.  Both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int n_src) {

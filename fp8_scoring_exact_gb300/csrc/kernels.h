@@ -179,6 +179,24 @@ struct SampleTauParams {
   Stats* stats;
 };
 
+// A kernel launch with programmatic stream serialisation (the kernels open
+// with pdl_enter()); returns the launch's error.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // host launchers (return cudaGetLastError() of the launch)
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_pairs, cudaStream_t s);

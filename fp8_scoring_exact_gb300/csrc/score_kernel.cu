@@ -161,6 +161,7 @@ template <int MODE, bool PAGED>
 __global__ void __launch_bounds__(SCORE_THREADS, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const ScoreParams p) {
+  pdl_enter();
   const int n_groups = p.plan == PLAN_REPAIR   ? p.stats->r_groups
                        : p.plan == PLAN_SAMPLE ? p.stats->s_groups
                                                : p.stats->n_groups;
@@ -542,8 +543,7 @@ static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  score_kernel<MODE, PAGED><<<grid, SCORE_THREADS, SMEM_BYTES, s>>>(tm_q, tm_k, p);
-  return cudaGetLastError();
+  return launch_pdl(score_kernel<MODE, PAGED>, dim3(grid), dim3(SCORE_THREADS), SMEM_BYTES, s, tm_q, tm_k, p);
 }
 
 cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,

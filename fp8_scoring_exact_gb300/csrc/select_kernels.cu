@@ -53,6 +53,7 @@ __device__ __forceinline__ int group_units(int lo, int hi, int chunk) {
 }
 
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   __shared__ int s_carry;
   const RowSpace& rs = p.rs;
@@ -182,8 +183,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  plan_kernel<<<1, PLAN_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(PLAN_THREADS), 0, s, p);
 }
 
 // ================================================================== sample ==
@@ -210,6 +210,7 @@ static_assert(SM_OFF_MISC + 64 + 1024 <= SAMPLE_SMEM, "sample smem");
 
 __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 const SampleParams p) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
@@ -400,8 +401,7 @@ cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_
     attr_set = true;
   }
   if (n_pairs_ <= 0) return cudaSuccess;
-  sample_kernel<<<grid, SAMPLE_THREADS, SAMPLE_SMEM, s>>>(tm_q, p);
-  return cudaGetLastError();
+  return launch_pdl(sample_kernel, grid, dim3(SAMPLE_THREADS), SAMPLE_SMEM, s, tm_q, p);
 }
 
 // ============================================================ sample (dense) ==
@@ -413,6 +413,7 @@ cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_
 constexpr int PREP_THREADS = 256;
 
 __global__ void __launch_bounds__(PREP_THREADS) sample_prep_kernel(const SamplePrepParams p) {
+  pdl_enter();
   const int gt = blockIdx.x * PREP_THREADS + threadIdx.x;
   const int nthreads = gridDim.x * PREP_THREADS;
   // 8 threads per grid key: 16 bytes each
@@ -443,6 +444,7 @@ constexpr int TAU_THREADS = 256;
 constexpr int TAU_KEYS_PER_LANE = MAX_SAMPLES / 32;
 
 __global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTauParams p) {
+  pdl_enter();
   __shared__ int hist_all[TAU_THREADS / 32][256];
   __shared__ int pick_all[TAU_THREADS / 32][4];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -497,13 +499,11 @@ __global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTau
 }
 
 cudaError_t launch_sample_prep(const SamplePrepParams& p, cudaStream_t s) {
-  sample_prep_kernel<<<64, PREP_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(sample_prep_kernel, dim3(64), dim3(PREP_THREADS), 0, s, p);
 }
 cudaError_t launch_sample_tau(const SampleTauParams& p, cudaStream_t s) {
   const int blocks = max(1, min(1024, ceil_div(p.rs.R, TAU_THREADS / 32)));
-  sample_tau_kernel<<<blocks, TAU_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(sample_tau_kernel, dim3(blocks), dim3(TAU_THREADS), 0, s, p);
 }
 
 // ================================================================== select ==
@@ -523,6 +523,7 @@ constexpr uint32_t SEL_OFF_MISC = SEL_OFF_HIST + 256 * 4;
 constexpr uint32_t SELECT_SMEM = SEL_OFF_MISC + 64;
 
 __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectParams p) {
+  pdl_enter();
   extern __shared__ uint8_t smem[];
   uint32_t* ckey = (uint32_t*)(smem + SEL_OFF_KEY);
   int32_t* cidx = (int32_t*)(smem + SEL_OFF_IDX);
@@ -594,18 +595,74 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
     auto filter = [&](uint32_t tau) -> int {
       if (tid == 0) misc[4] = 0;
       __syncthreads();
-      visit_row([&](uint32_t k, int i, bool v) {
+      // the unaligned head and tail (at most 6 keys): warp 0
+      if (tid < 32) {
+        const bool v = lane < nh;
+        const int i = !v ? b : (lane < (a0 - b) ? b + lane : a1 + (lane - (a0 - b)));
+        const uint32_t k = v ? ordered_key(srow[i]) : 0u;
         const bool pass = v && k >= tau;
         const unsigned mp = __ballot_sync(0xffffffffu, pass);
-        if (!mp) return;
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&misc[4], __popc(mp));
-        base = __shfl_sync(0xffffffffu, base, 0) + __popc(mp & lt);
-        if (pass && base < SELECT_CAP) {
-          ckey[base] = k;
-          cidx[base] = i;
+        if (mp) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&misc[4], __popc(mp));
+          base = __shfl_sync(0xffffffffu, base, 0) + __popc(mp & lt);
+          if (pass && base < SELECT_CAP) {
+            ckey[base] = k;
+            cidx[base] = i;
+          }
         }
-      });
+      }
+      // the aligned body: SEL_UNROLL float4 loads in flight per thread, its
+      // passing keys counted, a warp scan, one reservation per warp and
+      // round (a ballot and a shared atomic per key slot serialised the
+      // warps on one counter)
+      for (int base4 = 0; base4 < nvec; base4 += SELECT_THREADS * SEL_UNROLL) {
+        uint32_t kk[4 * SEL_UNROLL];
+#pragma unroll
+        for (int u = 0; u < SEL_UNROLL; ++u) {
+          const int vi = base4 + u * SELECT_THREADS + tid;
+          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (vi < nvec) x = __ldcs(&v4[vi]);
+          kk[4 * u + 0] = vi < nvec ? ordered_key(x.x) : 0u;
+          kk[4 * u + 1] = vi < nvec ? ordered_key(x.y) : 0u;
+          kk[4 * u + 2] = vi < nvec ? ordered_key(x.z) : 0u;
+          kk[4 * u + 3] = vi < nvec ? ordered_key(x.w) : 0u;
+        }
+        // key 0 never passes a threshold above 0, and tau 0 admits every
+        // valid key: padding counts only when tau is 0, so test vi again
+        int c = 0;
+#pragma unroll
+        for (int u = 0; u < SEL_UNROLL; ++u) {
+          const bool vv = base4 + u * SELECT_THREADS + tid < nvec;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) c += vv && kk[4 * u + q] >= tau;
+        }
+        int incl = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += t;
+        }
+        int wb = 0;
+        if (lane == 31 && incl) wb = atomicAdd(&misc[4], incl);
+        int pos = __shfl_sync(0xffffffffu, wb, 31) + incl - c;
+        if (c) {
+#pragma unroll
+          for (int u = 0; u < SEL_UNROLL; ++u) {
+            const int vi = base4 + u * SELECT_THREADS + tid;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (vi < nvec && kk[4 * u + q] >= tau) {
+                if (pos < SELECT_CAP) {
+                  ckey[pos] = kk[4 * u + q];
+                  cidx[pos] = a0 + vi * 4 + q;
+                }
+                ++pos;
+              }
+            }
+          }
+        }
+      }
       __syncthreads();
       return misc[4];
     };
@@ -700,6 +757,7 @@ constexpr int CS_PER_THREAD = CAND_MAX_REGIONS / CAND_THREADS;  // regions scann
 static_assert(CAND_MAX_REGIONS % CAND_THREADS == 0, "region scan");
 
 __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const CandParams p) {
+  pdl_enter();
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* ckey = (uint32_t*)(smem + CS_OFF_KEY);
   int32_t* cidx = (int32_t*)(smem + CS_OFF_IDX);
@@ -831,8 +889,7 @@ cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cand_select_kernel<<<grid, CAND_THREADS, CAND_SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(cand_select_kernel, dim3(grid), dim3(CAND_THREADS), CAND_SMEM, s, p);
 }
 
 // ============================================================ wide select ==
@@ -879,6 +936,7 @@ __device__ __forceinline__ int ld_dsmem(const int* p, uint32_t rank) {
 
 __global__ void __cluster_dims__(WIDE_CLUSTER, 1, 1) __launch_bounds__(WIDE_THREADS)
     wide_cluster_kernel(const WideParams p) {
+  pdl_enter();
   __shared__ int hist[256];
   __shared__ int tot[256];
   __shared__ int ctl[4];  // rank 0: digit, remaining rank
@@ -969,8 +1027,7 @@ __global__ void __cluster_dims__(WIDE_CLUSTER, 1, 1) __launch_bounds__(WIDE_THRE
 }
 
 cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s) {
-  wide_cluster_kernel<<<clusters * WIDE_CLUSTER, WIDE_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(wide_cluster_kernel, dim3(clusters * WIDE_CLUSTER), dim3(WIDE_THREADS), 0, s, p);
 }
 
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s) {
@@ -980,8 +1037,7 @@ cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  select_kernel<<<grid, SELECT_THREADS, SELECT_SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(grid), dim3(SELECT_THREADS), SELECT_SMEM, s, p);
 }
 
 }  // namespace dsa
