@@ -36,7 +36,7 @@ std::atomic<int64_t> g_launches{0};
 
 // ----------------------------------------------------------------- arena ----
 struct Layout {
-  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, unit_count, failed, wide_state;
+  size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, unit_count, failed;
   size_t cand_key, cand_idx, scores;
   size_t srb, sre, sgroups, sunit_start, skeys, sks, sscores;  // dense sampled thresholds
   size_t total;
@@ -67,7 +67,6 @@ Layout make_layout(int64_t R, int64_t G, int64_t cand_stride, int64_t max_units,
   L.runit_start = take((R + 1) * 4);
   L.unit_count = take((size_t)R * max_units * UNIT_REGIONS * 4);
   L.failed = take(R * 4);
-  L.wide_state = cand_stride ? take((size_t)R * WIDE_STATE * 4) : 0;
   L.cand_key = take((size_t)R * cand_stride * 4);
   L.cand_idx = take((size_t)R * cand_stride * 4);
   L.scores = take((size_t)score_rows * ld * 4);
@@ -413,7 +412,6 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   wp.ld = ld;
   wp.rb = pp.rb;
   wp.re = pp.re;
-  wp.state = at<int32_t>(a, L.wide_state);
   wp.out = out;
   wp.stats = st;
   DSA_LAUNCH(launch_wide_select(wp, o.grid / 2 > 0 ? o.grid / 2 : 1, stream));  // 4 CTAs per SM

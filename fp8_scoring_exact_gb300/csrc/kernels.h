@@ -140,11 +140,9 @@ struct WideParams {
   int64_t ld;
   const int32_t* rb;
   const int32_t* re;
-  int32_t* state;              // [R, WIDE_STATE]: [3], [4] emission counters
   int32_t* out;                // [R, K]
   const Stats* stats;
 };
-constexpr int WIDE_STATE = 16;
 
 // Sampled thresholds of dense rows from the scorer: sample_prep gathers the
 // grid keys (SAMPLE_OFFSET + j * stride) into a contiguous key set and writes

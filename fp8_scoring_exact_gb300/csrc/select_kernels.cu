@@ -903,6 +903,7 @@ cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s) {
 // rows, which exits at once when no row failed.
 constexpr int WIDE_CLUSTER = 8;
 constexpr int WIDE_THREADS = 512;
+constexpr int WIDE_UNROLL = 4;  // float4 loads in flight per thread
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -939,13 +940,12 @@ __global__ void __cluster_dims__(WIDE_CLUSTER, 1, 1) __launch_bounds__(WIDE_THRE
   pdl_enter();
   __shared__ int hist[256];
   __shared__ int tot[256];
-  __shared__ int ctl[4];  // rank 0: digit, remaining rank
+  __shared__ int ctl[4];  // rank 0: digit, remaining rank; every rank: [2], [3] its emission totals
+  __shared__ int wsum[2][WIDE_THREADS / 32];
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const int nf = p.stats->fail_count;
   const int K = p.K;
-  uint32_t lt;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
   for (int f = (int)cluster_id_x(); f < nf; f += (int)cluster_count_x()) {
     const int row = p.list[f];
     const int b = p.rb[row], e = p.re[row];
@@ -956,16 +956,27 @@ __global__ void __cluster_dims__(WIDE_CLUSTER, 1, 1) __launch_bounds__(WIDE_THRE
     const int per = ceil_div(n4, WIDE_CLUSTER);
     const int v0 = (int)rank * per, v1 = min(n4, v0 + per);
     const float4* v4 = reinterpret_cast<const float4*>(srow + a);
-    auto visit = [&](auto&& fn) {  // fn(key, index, valid) on all lanes, 4 keys per float4
-      for (int base = v0; base < v1; base += WIDE_THREADS) {
-        const int vi = base + tid;
-        const bool in = vi < v1;
-        const float4 x = in ? __ldcg(&v4[vi]) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const int i0 = a + 4 * vi;
-        fn(ordered_key(x.x), i0 + 0, in && i0 + 0 >= b && i0 + 0 < e);
-        fn(ordered_key(x.y), i0 + 1, in && i0 + 1 >= b && i0 + 1 < e);
-        fn(ordered_key(x.z), i0 + 2, in && i0 + 2 >= b && i0 + 2 < e);
-        fn(ordered_key(x.w), i0 + 3, in && i0 + 3 >= b && i0 + 3 < e);
+    // fn(key, index, valid) on all lanes, 4 keys per float4, WIDE_UNROLL
+    // float4 loads in flight per thread (one at a time left every pass
+    // waiting on the L2 latency); the order of a thread's keys is fixed
+    auto visit = [&](auto&& fn) {
+      for (int base = v0; base < v1; base += WIDE_THREADS * WIDE_UNROLL) {
+        float4 x[WIDE_UNROLL];
+#pragma unroll
+        for (int u = 0; u < WIDE_UNROLL; ++u) {
+          const int vi = base + u * WIDE_THREADS + tid;
+          x[u] = vi < v1 ? __ldcg(&v4[vi]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < WIDE_UNROLL; ++u) {
+          const int vi = base + u * WIDE_THREADS + tid;
+          const bool in = vi < v1;
+          const int i0 = a + 4 * vi;
+          fn(ordered_key(x[u].x), i0 + 0, in && i0 + 0 >= b && i0 + 0 < e);
+          fn(ordered_key(x[u].y), i0 + 1, in && i0 + 1 >= b && i0 + 1 < e);
+          fn(ordered_key(x[u].z), i0 + 2, in && i0 + 2 >= b && i0 + 2 < e);
+          fn(ordered_key(x[u].w), i0 + 3, in && i0 + 3 >= b && i0 + 3 < e);
+        }
       }
     };
     uint32_t prefix = 0, mask = 0;
@@ -992,37 +1003,63 @@ __global__ void __cluster_dims__(WIDE_CLUSTER, 1, 1) __launch_bounds__(WIDE_THRE
       rem = ld_dsmem(&ctl[1], 0);
       prefix |= digit << shift;
       mask |= 0xFFu << shift;
-      if (pass == 3 && rank == 0 && tid == 0) {
-        p.state[(int64_t)f * WIDE_STATE + 3] = 0;  // emission counters
-        p.state[(int64_t)f * WIDE_STATE + 4] = 0;
-      }
       cluster_sync_all();  // everyone read the digit before the next pass rewrites it
     }
-    // every key above the K-th key and the first `rem` keys equal to it,
-    // slots reserved once per warp
+    // every key above the K-th key and the first `rem` keys equal to it, in
+    // the cluster's slice order: each thread counts its keys, a CTA scan
+    // gives its offsets, the 8 CTA totals are exchanged through distributed
+    // shared memory, then every thread writes its keys (no global atomics:
+    // reservations on two counters shared by the cluster serialised it)
     const uint32_t theta = prefix;
     const int rr = rem;
-    int32_t* cnt = p.state + (int64_t)f * WIDE_STATE;
     int32_t* o = p.out + (int64_t)row * K;
-    visit([&](uint32_t k, int i, bool v) {
-      const bool gt = v && k > theta, eq = v && k == theta;
-      const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
-      if (!(mg | me)) return;
-      int bg = 0, be = 0;
-      if (lane == 0) {
-        if (mg) bg = atomicAdd(&cnt[3], __popc(mg));
-        if (me) be = atomicAdd(&cnt[4], __popc(me));
+    int cg = 0, ce = 0;
+    visit([&](uint32_t k, int, bool v) {
+      cg += v && k > theta;
+      ce += v && k == theta;
+    });
+    int ig = cg, ie = ce;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int tg = __shfl_up_sync(0xffffffffu, ig, d), te = __shfl_up_sync(0xffffffffu, ie, d);
+      if (lane >= d) {
+        ig += tg;
+        ie += te;
       }
-      bg = __shfl_sync(0xffffffffu, bg, 0);
-      be = __shfl_sync(0xffffffffu, be, 0);
-      const int qg = bg + __popc(mg & lt);
-      if (gt && qg < K - rr) o[qg] = p.rs.paged ? out_index(p.rs, row, i) : i;
-      if (eq) {
-        const int q = be + __popc(me & lt);
-        if (q < rr) o[K - rr + q] = p.rs.paged ? out_index(p.rs, row, i) : i;
+    }
+    const int warp = tid >> 5;
+    if (lane == 31) {
+      wsum[0][warp] = ig;
+      wsum[1][warp] = ie;
+    }
+    __syncthreads();
+    int og = ig - cg, oe = ie - ce, cta_g = 0, cta_e = 0;
+#pragma unroll
+    for (int w = 0; w < WIDE_THREADS / 32; ++w) {
+      og += w < warp ? wsum[0][w] : 0;
+      oe += w < warp ? wsum[1][w] : 0;
+      cta_g += wsum[0][w];
+      cta_e += wsum[1][w];
+    }
+    if (tid == 0) {
+      ctl[2] = cta_g;
+      ctl[3] = cta_e;
+    }
+    cluster_sync_all();  // every CTA's totals are published
+    for (uint32_t r = 0; r < rank; ++r) {
+      og += ld_dsmem(&ctl[2], r);
+      oe += ld_dsmem(&ctl[3], r);
+    }
+    visit([&](uint32_t k, int i, bool v) {
+      if (v && k > theta) {
+        if (og < K - rr) o[og] = p.rs.paged ? out_index(p.rs, row, i) : i;
+        ++og;
+      } else if (v && k == theta) {
+        if (oe < rr) o[K - rr + oe] = p.rs.paged ? out_index(p.rs, row, i) : i;
+        ++oe;
       }
     });
-    cluster_sync_all();  // the row is done before the cluster moves on
+    cluster_sync_all();  // the row is done (and ctl read) before the cluster moves on
   }
 }
 
