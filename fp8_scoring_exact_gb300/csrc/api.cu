@@ -510,6 +510,76 @@ int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uin
   return run_fused(rs, K, tq, tk, k_cache, k_cache_scale, q_scale, w, nullptr, nullptr, out_idx, stream);
 }
 
+// Exact top-K over a given fp32 score matrix [R, ld] (the standalone
+// selector and the unfused pipeline's second stage), after a main plan `pp`
+// (trivial_len = K) on the same arena: one threshold per row from its own
+// sample grid in the matrix (rows with L <= K get every valid index there),
+// the compare-and-append filter over the matrix into the rows' candidate
+// regions, the candidate selector with its certificate, and exact repair of
+// the rows that fail it straight from their matrix rows.
+int enqueue_matrix_select(Arena* a, const RowSpace& rs, int K, const Opts& o, const float* scores, int64_t ld,
+                          const PlanParams& pp, int max_units, int32_t* out, cudaStream_t stream) {
+  const Layout& L = a->L;
+  Stats* st = pp.stats;
+  uint32_t* tau = at<uint32_t>(a, L.tau);
+  SampleTauParams tp{};
+  tp.rs = rs;
+  tp.K = K;
+  tp.target16 = o.target16;
+  tp.tau_bias = o.bias;
+  tp.rb = pp.rb;
+  tp.re = pp.re;
+  tp.sscores = scores;
+  tp.sld = ld;
+  tp.tau = tau;
+  tp.stats = st;
+  tp.from_matrix = 1;
+  tp.out = out;
+  DSA_LAUNCH(launch_sample_tau(tp, stream));
+  MatrixFilterParams mf{};
+  mf.rs = rs;
+  mf.chunk_tiles = pp.chunk_tiles;
+  mf.scores = scores;
+  mf.ld = ld;
+  mf.rb = pp.rb;
+  mf.re = pp.re;
+  mf.groups = pp.groups;
+  mf.unit_start = pp.unit_start;
+  mf.tau = tau;
+  mf.cand_key = at<uint32_t>(a, L.cand_key);
+  mf.cand_idx = at<int32_t>(a, L.cand_idx);
+  mf.unit_count = at<int32_t>(a, L.unit_count);
+  mf.max_units = max_units;
+  mf.stats = st;
+  DSA_LAUNCH(launch_matrix_filter(mf, 2 * o.grid, stream));  // one wave: 2 CTAs of 512 threads per SM
+  CandParams cs{};
+  cs.rs = rs;
+  cs.K = K;
+  cs.groups = pp.groups;
+  cs.unit_start = pp.unit_start;
+  cs.unit_count = mf.unit_count;
+  cs.cand_key = mf.cand_key;
+  cs.cand_idx = mf.cand_idx;
+  cs.max_units = max_units;
+  cs.failed_rows = at<int32_t>(a, L.failed);
+  cs.out = out;
+  cs.stats = st;
+  DSA_LAUNCH(launch_cand_select(cs, 3 * o.grid, stream));
+  WideParams wp{};
+  wp.rs = rs;
+  wp.K = K;
+  wp.list = cs.failed_rows;
+  wp.scores = scores;
+  wp.ld = ld;
+  wp.by_row = 1;
+  wp.rb = pp.rb;
+  wp.re = pp.re;
+  wp.out = out;
+  wp.stats = st;
+  DSA_LAUNCH(launch_wide_select(wp, o.grid / 2 > 0 ? o.grid / 2 : 1, stream));
+  return DSA_OK;
+}
+
 static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
                        const float* w, const int32_t* row_begin, const int32_t* row_end, int Q, int N, int K,
                        float* scores, int64_t ld, int32_t* out_idx, cudaStream_t stream) {
@@ -522,9 +592,13 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   rs.N = N;
   const int G = n_groups(rs);
   const int64_t own_ld = align_up((size_t)N, 4);
+  const int chunk = chunk_for(o, rs);
+  const int max_units = ceil_div(ceil_div(N, TILE), chunk);
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
-  Arena* a = get_arena(stream, make_layout(Q, G, 0, 0, scores ? 0 : Q, own_ld), &err);
+  Arena* a = get_arena(stream,
+                       make_layout(Q, G, out_idx ? ROW_SLOTS : 0, out_idx ? max_units : 0, scores ? 0 : Q, own_ld),
+                       &err);
   if (!a) return err;
   const Layout& L = a->L;
   Stats* st = at<Stats>(a, L.stats);
@@ -535,7 +609,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   pp.rs = rs;
   pp.K = K;
   pp.trivial_len = out_idx ? K : 0;
-  pp.chunk_tiles = chunk_for(o, rs);
+  pp.chunk_tiles = chunk;
   pp.row_begin_in = row_begin;
   pp.row_end_in = row_end;
   pp.rb = at<int32_t>(a, L.rb);
@@ -565,19 +639,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   DSA_LAUNCH(launch_score(tq, tk, cp, o.grid, stream));
   if (o.profile) cudaEventRecord(a->ev1, stream);
   if (!out_idx) return DSA_OK;
-
-  SelectParams sel{};
-  sel.rs = rs;
-  sel.K = K;
-  sel.target16 = o.target16;
-  sel.scores = sbuf;
-  sel.ld = sld;
-  sel.rb = pp.rb;
-  sel.re = pp.re;
-  sel.out = out_idx;
-  sel.stats = st;
-  DSA_LAUNCH(launch_select(sel, 2 * o.grid, stream));
-  return DSA_OK;
+  return enqueue_matrix_select(a, rs, K, o, sbuf, sld, pp, max_units, out_idx, stream);
 }
 
 int dsa_indexer_topk_unfused(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
@@ -609,16 +671,18 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   RowSpace rs{};
   rs.R = Q;
   rs.N = N;
+  const int chunk = chunk_for(o, rs);
+  const int max_units = ceil_div(ceil_div(N, TILE), chunk);
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
-  Arena* a = get_arena(stream, make_layout(Q, n_groups(rs), 0, 0, 0, 0), &err);
+  Arena* a = get_arena(stream, make_layout(Q, n_groups(rs), ROW_SLOTS, max_units, 0, 0), &err);
   if (!a) return err;
   const Layout& L = a->L;
   PlanParams pp{};
   pp.rs = rs;
   pp.K = K;
-  pp.trivial_len = 0x7fffffff;  // no scoring work: ranges and counters only
-  pp.chunk_tiles = 64;
+  pp.trivial_len = K;
+  pp.chunk_tiles = chunk;
   pp.row_begin_in = row_begin;
   pp.row_end_in = row_end;
   pp.rb = at<int32_t>(a, L.rb);
@@ -628,19 +692,8 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = at<Stats>(a, L.stats);
   DSA_LAUNCH(launch_plan(pp, stream));
-  SelectParams sel{};
-  sel.rs = rs;
-  sel.K = K;
-  sel.target16 = o.target16;
-  sel.scores = scores;
-  sel.ld = ld;
-  sel.rb = pp.rb;
-  sel.re = pp.re;
-  sel.out = out_idx;
-  sel.stats = pp.stats;
   a->profiled = false;
-  DSA_LAUNCH(launch_select(sel, 2 * o.grid, stream));
-  return DSA_OK;
+  return enqueue_matrix_select(a, rs, K, o, scores, ld, pp, max_units, out_idx, stream);
 }
 
 int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const int32_t* row_begin,

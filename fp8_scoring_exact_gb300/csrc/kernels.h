@@ -136,7 +136,8 @@ struct WideParams {
   RowSpace rs;
   int K;
   const int32_t* list;         // repair rows; count in stats->fail_count
-  const float* scores;         // score row of list entry f at f * ld
+  const float* scores;         // score row of list entry f at f * ld (by_row: at row * ld)
+  int by_row;
   int64_t ld;
   const int32_t* rb;
   const int32_t* re;
@@ -175,6 +176,33 @@ struct SampleTauParams {
   int64_t sld;
   uint32_t* tau;               // [R] (written for rows with L > K)
   Stats* stats;
+  // from_matrix: sscores is a full fp32 score matrix [R, sld]; a row's
+  // samples are its own 1-in-200 grid inside [rb, re) (srb / sre unused),
+  // and rows with L <= K get every valid index in out (trivial path)
+  int from_matrix;
+  int32_t* out;
+};
+
+// Candidate filter over a given fp32 score matrix (the standalone top-K):
+// the work units of a main plan, each warp (row slot r, key quarter q) of a
+// 512-thread CTA appending the scores of its row that reach the row's
+// threshold to region (c, q) of the row, like the scorer's filter epilogue
+// (the candidate selector then takes over unchanged).
+struct MatrixFilterParams {
+  RowSpace rs;
+  int chunk_tiles;
+  const float* scores;         // [R, ld]
+  int64_t ld;
+  const int32_t* rb;
+  const int32_t* re;
+  const Group* groups;
+  const int32_t* unit_start;
+  const uint32_t* tau;
+  uint32_t* cand_key;          // [R, ROW_SLOTS]
+  int32_t* cand_idx;
+  int32_t* unit_count;         // [R, max_units, 4]
+  int max_units;
+  Stats* stats;
 };
 
 // A kernel launch with programmatic stream serialisation (the kernels open
@@ -205,6 +233,7 @@ cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
 cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s);
+cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStream_t s);
 
 // number of work groups of G query rows for a row space
 template <int G>

@@ -452,20 +452,38 @@ __global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTau
   int* pick = pick_all[wid];
   const int warp = blockIdx.x * (TAU_THREADS / 32) + wid, nwarps = gridDim.x * (TAU_THREADS / 32);
   const int target = (int)(((int64_t)p.target16 * p.K) / 16);
+  int ntriv = 0;
   for (int row = warp; row < p.rs.R; row += nwarps) {
-    const int L = p.re[row] - p.rb[row];
-    if (L <= p.K) continue;
-    const int j0 = p.srb[row];
-    const int m = min(p.sre[row] - j0, MAX_SAMPLES);
+    const int b = p.rb[row], L = p.re[row] - b;
+    if (L <= p.K) {
+      if (p.from_matrix) {  // trivial path: every valid index, then -1
+        int32_t* o = p.out + (int64_t)row * p.K;
+        for (int i = lane; i < p.K; i += 32) o[i] = i < L ? b + i : -1;
+        ++ntriv;
+      }
+      continue;
+    }
+    int j0, m, stride = 1;
+    const float* sr;
+    if (p.from_matrix) {  // the row's own grid keys in the score matrix
+      int first;
+      sample_grid(b, b + L, &first, &m, &stride);
+      j0 = 0;
+      sr = p.sscores + (int64_t)row * p.sld + first;
+    } else {
+      j0 = p.srb[row];
+      m = p.sre[row] - j0;
+      sr = p.sscores + (int64_t)row * p.sld + j0;
+    }
+    m = min(m, MAX_SAMPLES);
     const int rank = sample_rank(m, L, target);
     uint32_t tau = 0u;
     if (m > 0 && rank >= 1 && rank <= m) {
       uint32_t key[TAU_KEYS_PER_LANE];
-      const float* sr = p.sscores + (int64_t)row * p.sld + j0;
 #pragma unroll
       for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
         const int i = q * 32 + lane;
-        key[q] = i < m ? ordered_key(__ldcg(&sr[i])) : 0u;
+        key[q] = i < m ? ordered_key(__ldcg(&sr[(int64_t)i * stride])) : 0u;
       }
       uint32_t prefix = 0, mask = 0;
       int rem = rank;
@@ -496,6 +514,7 @@ __global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTau
     }
     if (lane == 0) p.tau[row] = tau;
   }
+  if (lane == 0 && ntriv) atomicAdd(&p.stats->trivial, ntriv);
 }
 
 cudaError_t launch_sample_prep(const SamplePrepParams& p, cudaStream_t s) {
@@ -949,7 +968,7 @@ __global__ void __cluster_dims__(WIDE_CLUSTER, 1, 1) __launch_bounds__(WIDE_THRE
   for (int f = (int)cluster_id_x(); f < nf; f += (int)cluster_count_x()) {
     const int row = p.list[f];
     const int b = p.rb[row], e = p.re[row];
-    const float* srow = p.scores + (int64_t)f * p.ld;
+    const float* srow = p.scores + (int64_t)(p.by_row ? row : f) * p.ld;
     // this CTA's slice: float4s covering [a, e) split in WIDE_CLUSTER parts
     const int a = b & ~3;
     const int n4 = ((e + 3) >> 2) - (a >> 2);
@@ -1075,6 +1094,106 @@ cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s) {
     attr_set = true;
   }
   return launch_pdl(select_kernel, dim3(grid), dim3(SELECT_THREADS), SELECT_SMEM, s, p);
+}
+
+// ======================================================== matrix filter ==
+// Compare-and-append over a given fp32 score matrix ("Fusing Indexer Scoring
+// and Exact Top-k for DeepSeek-V3.2", section 3.2, applied to a stored
+// matrix): warp w of a 512-thread CTA takes row slot w / 4 of the unit's
+// group and every 4th 128-key tile of the unit from tile w % 4 on, reading
+// each tile as one float4 per lane, MF_UNROLL tiles in flight (the HBM
+// latency needs about 64 KB in flight per SM, and two CTAs fit one); the
+// scores that reach the row's threshold go to the warp's region of the row
+// with a ballot and a register counter, and the count to unit_count at the
+// end of the unit: the layout the candidate selector reads after the
+// scorer's filter epilogue (any split of a unit's keys over its 4 regions
+// serves it).
+constexpr int MF_THREADS = 512;
+constexpr int MF_UNROLL = 4;
+
+__global__ void __launch_bounds__(MF_THREADS) matrix_filter_kernel(const MatrixFilterParams p) {
+  pdl_enter();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = warp >> 2, quarter = warp & 3;
+  const int n_groups = p.stats->n_groups, total = p.stats->total_units;
+  const uint32_t lt = lanemask_lt();
+  // a contiguous range of units per CTA: the group is found once by binary
+  // search and then advanced (a search per unit left the loads idle for as
+  // long as the unit's own streaming took)
+  const int per = ceil_div(total, (int)gridDim.x);
+  const int u_begin = (int)blockIdx.x * per, u_end = min(total, u_begin + per);
+  int g = 0;
+  if (u_begin < u_end) {
+    int lo = 0, hi = n_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(&p.unit_start[mid]) <= u_begin)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    g = lo;
+  }
+  int g_start = u_begin < u_end ? __ldg(&p.unit_start[g]) : 0;
+  int g_next = u_begin < u_end ? __ldg(&p.unit_start[g + 1]) : 0;
+  for (int u = u_begin; u < u_end; ++u) {
+    while (u >= g_next) {
+      ++g;
+      g_start = g_next;
+      g_next = __ldg(&p.unit_start[g + 1]);
+    }
+    const int c = u - g_start;
+    const int nunits = g_next - g_start;
+    const Group* gp = p.groups + g;
+    if (r >= gp->nrows) continue;  // uniform over the warp
+    const int t0 = gp->lo / TILE + c * p.chunk_tiles;
+    const int t1 = (int)min((int64_t)t0 + p.chunk_tiles, (int64_t)ceil_div(gp->hi, TILE));
+    const int row = gp->row[r];
+    const int b = p.rb[row], e = p.re[row];
+    const uint32_t tau = p.tau[row];
+    const int wcap = region_cap(nunits);
+    const int64_t region = (int64_t)row * ROW_SLOTS + (int64_t)(c * UNIT_REGIONS + quarter) * wcap;
+    uint32_t* ck = p.cand_key + region;
+    int32_t* ci = p.cand_idx + region;
+    const float* srow = p.scores + (int64_t)row * p.ld;
+    int wcnt = 0;
+    for (int t = t0 + quarter; t < t1; t += 4 * MF_UNROLL) {
+      float4 x[MF_UNROLL];
+#pragma unroll
+      for (int v = 0; v < MF_UNROLL; ++v) {
+        const int s = (t + 4 * v) * TILE + 4 * lane;  // first of the lane's 4 keys
+        // a float4 wholly inside [b, e) (ld is a multiple of 4 and the row
+        // range lies in [0, N]: a float4 that reaches into it stays inside
+        // the row), zero when none of its keys is in range
+        x[v] = (t + 4 * v < t1 && s + 3 >= b && s < e) ? __ldcs(reinterpret_cast<const float4*>(srow + s))
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int v = 0; v < MF_UNROLL; ++v) {
+        const int s0 = (t + 4 * v) * TILE + 4 * lane;
+        const bool tile_in = t + 4 * v < t1;
+        const float xs[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int s = s0 + j;
+          const uint32_t key = ordered_key(xs[j]);
+          const bool pred = tile_in && s >= b && s < e && key >= tau;
+          const uint32_t m = __ballot_sync(0xffffffffu, pred);
+          const int pos = wcnt + __popc(m & lt);
+          wcnt += __popc(m);
+          if (pred && pos < wcap) {
+            ck[pos] = key;
+            ci[pos] = s;
+          }
+        }
+      }
+    }
+    if (lane == 0) p.unit_count[(int64_t)row * p.max_units * UNIT_REGIONS + c * UNIT_REGIONS + quarter] = min(wcnt, wcap + 1);
+  }
+}
+
+cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStream_t s) {
+  return launch_pdl(matrix_filter_kernel, dim3(grid), dim3(MF_THREADS), 0, s, p);
 }
 
 }  // namespace dsa
