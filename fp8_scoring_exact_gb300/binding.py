@@ -215,7 +215,7 @@ def last_device_status(stream=None):
 
 
 def last_repaired_rows(stream=None, cap=1 << 20):
-    """Row ids the last fused call on the stream sent to exact repair."""
+    """Row ids the last selecting call on the stream sent to exact repair."""
     buf = (ctypes.c_int32 * cap)()
     n = lib().dsa_indexer_last_repaired_rows(_stream_ptr(stream), buf, cap)
     if n < 0:

@@ -187,9 +187,10 @@ DSA_API int dsa_indexer_last_device_status(dsa_stream_t stream, int32_t* failure
 
 /*
  * Synchronises `stream` and copies the ids of the rows that the most recent
- * fused call on it sent to exact repair (certificate failed) into rows_out
- * (at most `cap` of them, in no particular order).  Returns their number
- * (>= 0) or a negative dsa_status.
+ * selecting call on it (fused, unfused or dsa_indexer_topk_from_scores) sent
+ * to exact repair (certificate failed) into rows_out (at most `cap` of them,
+ * in no particular order).  Returns their number (>= 0) or a negative
+ * dsa_status.
  */
 DSA_API int dsa_indexer_last_repaired_rows(dsa_stream_t stream, int32_t* rows_out, int cap);
 

@@ -284,6 +284,46 @@ def test_topk_from_scores_exact(B):
         assert np.array_equal(got, want), t
 
 
+@pytest.mark.parametrize("bias,kind", [(0, None), (1 << 31, "underflow"), (-(1 << 33), "overflow")])
+def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind):
+    """A padded row stride (ld > N, N not a multiple of 4), ranges that end at
+    N or start off a 4-key boundary, rows with ties; with the threshold pushed
+    to either end every row longer than K fails the certificate and is
+    selected again from its own matrix row, exactly."""
+    import torch
+    rng = np.random.default_rng(77)
+    Q, N, K, ld = 14, 20001, 1024, 20008
+    sc = np.full((Q, ld), np.nan, np.float32)   # the padding is never read
+    sc[:, :N] = rng.standard_normal((Q, N)).astype(np.float32)
+    sc[2, :N] = np.round(sc[2, :N] * 2) / 2     # heavy ties
+    rb = rng.integers(0, 3000, Q).astype(np.int32)
+    re = np.full(Q, N, np.int32)
+    re[1::2] = (rb[1::2] + rng.integers(K + 1, N - 3000, Q // 2)).astype(np.int32)
+    rb[3] = 4097                                # off a 4-key boundary
+    re[5] = rb[5] + K                           # exactly K: trivial path
+    re[6] = rb[6] + 3                           # fewer than K
+    d = to_dev(sc, rb, re)
+    B.set_option("tau_bias", bias)
+    try:
+        out = B.topk_from_scores(d[0], d[1], d[2], K=K, N=N).cpu().numpy()
+        counters = _status_ok(B)
+    finally:
+        B.set_option("tau_bias", 0)
+    long_rows = int(((re - rb) > K).sum())
+    if kind:
+        assert counters[kind] == long_rows
+        assert sorted(B.last_repaired_rows()) == sorted(np.nonzero((re - rb) > K)[0].tolist())
+    for t in range(Q):
+        L = int(re[t] - rb[t])
+        n = min(L, K)
+        sel = out[t, :n]
+        assert (out[t, n:] == -1).all()
+        assert len(np.unique(sel)) == n and np.all((sel >= rb[t]) & (sel < re[t]))
+        want = np.sort(sc[t, rb[t]:re[t]])[::-1][:n]
+        got = np.sort(sc[t, sel])[::-1]
+        assert np.array_equal(got, want), t
+
+
 # ------------------------------------------------------------- CUDA graph ----
 def test_fused_call_replays_from_a_cuda_graph(B):
     """The fused call enqueues kernels only (no host synchronisation, no
