@@ -283,23 +283,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* m, int x, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(bar)
-      : "memory");
-}
-// contiguous global -> shared copy by the TMA engine (16-byte aligned
-// addresses, size a multiple of 16), completing on an mbarrier
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-// order generic-proxy global accesses before later async-proxy (TMA) ones
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 // generic-proxy writes to shared memory -> visible to the async proxy (MMA)
 // Programmatic dependent launch: the library launches every kernel with
 // programmatic stream serialisation.  A kernel first lets the next launch
@@ -392,23 +375,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-// 16 lanes x 64 columns: thread t receives, for each block m of 8 columns,
-// columns 8m + 2(t % 4) + {0, 1} of lanes base + t / 4 (r[4m], r[4m+1]) and
-// base + 8 + t / 4 (r[4m+2], r[4m+3]).
-__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-// 16 lanes x 32 columns: the first four 8-column blocks of the .x8 layout
-// above (r[4m .. 4m+3] for m = 0..3).
+// 16 lanes x 32 columns: thread t receives, for each block m (0..3) of 8
+// columns, columns 8m + 2(t % 4) + {0, 1} of lanes base + t / 4 (r[4m],
+// r[4m+1]) and base + 8 + t / 4 (r[4m+2], r[4m+3]).
 __device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
@@ -424,20 +393,6 @@ __device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t* r) {
 __device__ __forceinline__ float ldg_pinned_f32(const float* p) {
   float v;
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ int ldg_pinned_s32(const int32_t* p) {
-  int v;
-  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-// release / acquire at GPU scope on a global counter
-__device__ __forceinline__ void red_release_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -473,10 +428,6 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
 // acc += a * b on two fp32 lanes (sm_100+ packed FMA)
 __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
   asm volatile("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-// 16 bytes of shared memory as two packed float pairs
-__device__ __forceinline__ void lds_2x64(uint32_t addr, uint64_t& a, uint64_t& b) {
-  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
 }
 
 // ------------------------------------------------- radix select (shared) ----

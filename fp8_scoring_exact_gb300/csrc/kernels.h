@@ -112,8 +112,6 @@ struct SelectParams {
   RowSpace rs;
   int K;
   int target16;
-  int list_mode;               // 1: rows = failed_rows[0 .. stats->fail_count), score row f
-  const int32_t* list;
   const float* scores;
   int64_t ld;
   const int32_t* rb;

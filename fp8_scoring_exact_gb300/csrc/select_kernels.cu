@@ -553,11 +553,11 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
   const RowSpace& rs = p.rs;
   const int tid = threadIdx.x, lane = tid & 31;
   const int K = p.K;
-  const int count = p.list_mode ? p.stats->fail_count : rs.R;
+  const int count = rs.R;
   const int target = (int)(((int64_t)p.target16 * K) / 16);
 
   for (int f = blockIdx.x; f < count; f += gridDim.x) {
-    const int row = p.list_mode ? p.list[f] : f;
+    const int row = f;
     const int b = p.rb[row], e = p.re[row];
     const int L = e - b;
     int32_t* o = p.out + (int64_t)row * K;
@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
       write_all_valid(rs, row, b, e, K, p.out, tid, SELECT_THREADS);
       continue;
     }
-    const float* srow = p.scores + (int64_t)(p.list_mode ? f : row) * p.ld;
+    const float* srow = p.scores + (int64_t)row * p.ld;
 
     // sampled threshold: the sample of descending rank `rk` (0 = every key)
     int first, m, S;
