@@ -154,9 +154,11 @@ DSA_API int dsa_indexer_topk_from_scores(const float* scores, int64_t ld,
 
 /*
  * Same operation and result as dsa_indexer_topk_from_scores, but this entry
- * point allocates no memory at all, for callers that cannot call cudaMalloc
- * (for example code running while a CUDA graph is being captured, or an
- * embedding runtime that owns every device allocation and forbids others).
+ * point allocates no memory at all, for callers that cannot call cudaMalloc:
+ * an embedding runtime that owns every device allocation and forbids others
+ * (a serving engine that reserves all free memory for its KV cache at start-up
+ * and accounts for every byte), or a plugin host whose memory budget is fixed
+ * before this library is loaded.
  * The paper has no counterpart; it is a deployment convenience.
  *
  * Its scratch is one fixed device array of 512 KiB compiled into this

@@ -2,8 +2,9 @@
 must return what the allocating entry point (dsa_indexer_topk_from_scores)
 returns, call after call.
 
-It exists for callers that cannot call cudaMalloc (code running during CUDA
-graph capture, or runtimes that own all device memory); its scratch is a fixed
+It exists for callers that cannot call cudaMalloc (runtimes that own all
+device memory, such as a serving engine that reserves the free memory for its
+KV cache at start-up, or plugin hosts with a fixed budget); its scratch is a fixed
 array in device memory shared by every call, so two calls in a row also check
 that each call resets what it reads.  Selection from given fp32 scores is
 exact: up to ties, the sorted selected scores must be identical.
