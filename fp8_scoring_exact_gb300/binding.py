@@ -3,7 +3,8 @@
 Argument marshalling only: every step of the operator runs in the library's
 CUDA kernels.  Tensors are torch CUDA tensors (FP8 data as uint8 or
 torch.float8_e4m3fn); they are passed to the C ABI as raw device pointers
-together with the current (or given) CUDA stream.  There is no CPU fallback:
+together with the current (or given) CUDA stream.  indexer_topk_host takes
+CPU tensors instead (the library does the copies).  There is no CPU fallback:
 if the library is missing or a call fails, an exception is raised.
 """
 from __future__ import annotations
@@ -21,7 +22,8 @@ _LIB = None
 DSA_OK, DSA_ERR_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_RANGE = 0, -1, -2, -3, -4, -5
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_UNSUPPORTED", -3: "DSA_ERR_CUDA",
                 -4: "DSA_ERR_TIMEOUT", -5: "DSA_ERR_RANGE"}
-OPTIONS = {"chunk_tiles": 1, "tau_bias": 2, "profile": 3, "grid_ctas": 4, "sample_target": 5}
+OPTIONS = {"chunk_tiles": 1, "tau_bias": 2, "profile": 3, "grid_ctas": 4, "sample_target": 5,
+           "host_chunk_rows": 6}
 HEADS, HEAD_DIM, MAX_K = 64, 128, 2048
 
 _P = ctypes.c_void_p
@@ -31,6 +33,7 @@ _I64 = ctypes.c_int64
 # C ABI signatures, name -> (restype, argtypes)
 SIGNATURES = {
     "dsa_indexer_topk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "dsa_indexer_topk_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_topk_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "dsa_indexer_topk_unfused": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_scores": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I64, _P]),
@@ -128,6 +131,40 @@ def indexer_topk(q, q_scale, k, k_scale, w, row_begin, row_end, K=2048, out=None
     rc = getattr(lib(), fn)(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(row_begin),
                             _ptr(row_end), Q, N, K, _ptr(out), _stream_ptr(stream))
     _check(fn, rc)
+    return out
+
+
+def _host(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a CPU tensor")
+    if t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def indexer_topk_host(q, q_scale, k, k_scale, w, row_begin, row_end, K=2048, out=None, stream=None):
+    """dsa_indexer_topk_host: the fused operator on CPU tensors (pinned memory lets the
+    library overlap its copies with the scoring); returns int32 [Q,K] on the CPU.
+    Synchronous."""
+    q, k = _host(q, "q", torch.uint8), _host(k, "k", torch.uint8)
+    q_scale = _host(q_scale, "q_scale", torch.float32)
+    k_scale = _host(k_scale, "k_scale", torch.float32)
+    w = _host(w, "w", torch.float32)
+    row_begin = _host(row_begin, "row_begin", torch.int32)
+    row_end = _host(row_end, "row_end", torch.int32)
+    Q, N = q.shape[0], k.shape[0]
+    if tuple(q.shape[1:]) != (HEADS, HEAD_DIM) or tuple(k.shape[1:]) != (HEAD_DIM,):
+        raise ValueError("q must be [Q,64,128] and k [N,128]")
+    if out is None:
+        out = torch.empty((Q, K), dtype=torch.int32, pin_memory=q.is_pinned())
+    _host(out, "out", torch.int32)
+    rc = lib().dsa_indexer_topk_host(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(row_begin),
+                                     _ptr(row_end), Q, N, K, _ptr(out), _stream_ptr(stream))
+    _check("dsa_indexer_topk_host", rc)
     return out
 
 

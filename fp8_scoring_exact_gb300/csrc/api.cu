@@ -10,6 +10,7 @@
 //   -> standalone exact select of those rows.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -32,6 +33,7 @@ int64_t g_tau_bias = 0;
 int64_t g_profile = 0;
 int64_t g_grid = 0;
 int64_t g_target16 = 32;
+int64_t g_host_chunk_rows = 0;  // 0: chosen per call (host_chunk_rows)
 std::atomic<int64_t> g_launches{0};
 
 // ----------------------------------------------------------------- arena ----
@@ -474,6 +476,102 @@ void* noalloc_scratch(int* err) {
   return p;
 }
 
+// ----------------------------------------------------- host-buffer entry --
+// Device staging of dsa_indexer_topk_host per (device, stream): two row-chunk
+// slots (q, q scales, weights, ranges, indices) and the keys with their
+// scales.  While one chunk is scored on the caller's stream, a copy stream
+// owned by the stage brings in the next chunk's rows and takes out the
+// previous chunk's indices.
+constexpr int HOST_MAX_CHUNKS = 64;
+
+struct HostLayout {
+  size_t q, qs, w, rb, re, out, slot;  // offsets inside a slot, slot size
+  size_t k, ks, total;                 // keys and key scales after the two slots
+};
+
+HostLayout host_layout(int64_t N, int64_t C, int K) {
+  HostLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.q = take((size_t)C * H * D);
+  L.qs = take((size_t)C * 4);
+  L.w = take((size_t)C * H * 4);
+  L.rb = take((size_t)C * 4);
+  L.re = take((size_t)C * 4);
+  L.out = take((size_t)C * K * 4);
+  L.slot = off;
+  off = 2 * L.slot;
+  L.k = take((size_t)N * D);
+  L.ks = take((size_t)N * 4);
+  L.total = off;
+  return L;
+}
+
+struct HostStage {
+  uint8_t* base = nullptr;
+  size_t cap = 0;
+  cudaStream_t copy = nullptr;
+  cudaEvent_t entry = nullptr, copies_done = nullptr, in_ready[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr};
+  Stats* stats_h = nullptr;  // pinned: the status block of each chunk
+};
+
+std::mutex g_host_mu;  // one host-buffer call at a time (it synchronises before returning)
+std::map<std::pair<int, cudaStream_t>, HostStage> g_host;
+
+// Rows per chunk: the option when set, else half of the rows but at least
+// 2048 (every chunk pays the fused call's fixed launch sequence and its
+// scorer's tail again; measured at Q = 4096 x N = 131072 from pinned host
+// memory: 1 chunk 4.84 ms, 2 chunks 4.77, 4 chunks 4.88, 8 chunks 5.22);
+// at most HOST_MAX_CHUNKS chunks; a multiple of the 4-row groups.
+int host_chunk_rows(int Q) {
+  int64_t c;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    c = g_host_chunk_rows;
+  }
+  if (c <= 0) c = std::max<int64_t>(2048, ((int64_t)Q + 1) / 2);
+  c = std::max<int64_t>(c, ((int64_t)Q + HOST_MAX_CHUNKS - 1) / HOST_MAX_CHUNKS);
+  c = (c + GROUP_ROWS - 1) / GROUP_ROWS * GROUP_ROWS;
+  return (int)std::min<int64_t>(c, Q);
+}
+
+// Device address of the status block the last call on `stream` wrote.
+Stats* arena_stats(cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_arenas.find({dev, stream});
+  if (it == g_arenas.end() || !it->second.base) return nullptr;
+  return reinterpret_cast<Stats*>(it->second.base + it->second.L.stats);
+}
+
+int host_stage_init(HostStage& hs, const HostLayout& L, cudaStream_t stream) {
+  if (!hs.copy) {
+    if (cudaStreamCreateWithFlags(&hs.copy, cudaStreamNonBlocking) != cudaSuccess) return DSA_ERR_CUDA;
+    cudaEvent_t* evs[] = {&hs.entry, &hs.copies_done, &hs.in_ready[0], &hs.in_ready[1], &hs.done[0], &hs.done[1]};
+    for (cudaEvent_t* e : evs)
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return DSA_ERR_CUDA;
+    if (cudaMallocHost(&hs.stats_h, HOST_MAX_CHUNKS * sizeof(Stats)) != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  if (hs.cap < L.total) {
+    if (hs.base) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess || cudaStreamSynchronize(hs.copy) != cudaSuccess)
+        return DSA_ERR_CUDA;
+      cudaFree(hs.base);
+      hs.base = nullptr;
+      hs.cap = 0;
+    }
+    const size_t want = align_up(L.total + L.total / 8, 1 << 20);
+    if (cudaMalloc(&hs.base, want) != cudaSuccess) return DSA_ERR_CUDA;
+    hs.cap = want;
+  }
+  return DSA_OK;
+}
+
 }  // namespace
 
 // =================================================================== C ABI ==
@@ -492,6 +590,91 @@ int dsa_indexer_topk(const uint8_t* q_fp8, const float* q_scale, const uint8_t* 
   rs.R = Q;
   rs.N = N;
   return run_fused(rs, K, tq, tk, k_fp8, k_scale, q_scale, w, row_begin, row_end, out_idx, stream);
+}
+
+int dsa_indexer_topk_host(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
+                          const float* w, const int32_t* row_begin, const int32_t* row_end, int Q, int N, int K,
+                          int32_t* out_idx, dsa_stream_t stream_) {
+  if (!q_fp8 || !q_scale || !k_fp8 || !k_scale || !w || !row_begin || !row_end || !out_idx) return DSA_ERR_ARG;
+  if (Q <= 0 || N <= 0 || K < 1 || K > DSA_MAX_K) return DSA_ERR_ARG;
+  if ((int64_t)Q * H >= (1ll << 31) || (int64_t)N >= (1ll << 31) - TILE) return DSA_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const int C = host_chunk_rows(Q);
+  const int nch = ceil_div(Q, C);
+  const HostLayout L = host_layout(N, C, K);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> hl(g_host_mu);
+  HostStage& hs = g_host[{dev, stream}];
+  int rc = host_stage_init(hs, L, stream);
+  if (rc != DSA_OK) {
+    cudaGetLastError();
+    return rc;
+  }
+#define DSA_HOST_CK(expr)           \
+  do {                              \
+    if ((expr) != cudaSuccess) {    \
+      cudaGetLastError();           \
+      return DSA_ERR_CUDA;          \
+    }                               \
+  } while (0)
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  auto slot = [&](int c) { return hs.base + (size_t)(c & 1) * L.slot; };
+  // the copy stream starts behind the work already on the caller's stream
+  // (an earlier call may still be reading the staging)
+  DSA_HOST_CK(cudaEventRecord(hs.entry, stream));
+  DSA_HOST_CK(cudaStreamWaitEvent(hs.copy, hs.entry, 0));
+  DSA_HOST_CK(cudaMemcpyAsync(hs.base + L.k, k_fp8, (size_t)N * D, h2d, hs.copy));
+  DSA_HOST_CK(cudaMemcpyAsync(hs.base + L.ks, k_scale, (size_t)N * 4, h2d, hs.copy));
+  auto h2d_chunk = [&](int c) -> cudaError_t {
+    const int64_t r0 = (int64_t)c * C;
+    const size_t n = (size_t)std::min<int64_t>(C, Q - r0);
+    uint8_t* s = slot(c);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(s + L.q, q_fp8 + r0 * H * D, n * H * D, h2d, hs.copy)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(s + L.qs, q_scale + r0, n * 4, h2d, hs.copy)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(s + L.w, w + r0 * H, n * H * 4, h2d, hs.copy)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(s + L.rb, row_begin + r0, n * 4, h2d, hs.copy)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(s + L.re, row_end + r0, n * 4, h2d, hs.copy)) != cudaSuccess) return e;
+    return cudaEventRecord(hs.in_ready[c & 1], hs.copy);
+  };
+  DSA_HOST_CK(h2d_chunk(0));
+  if (nch > 1) DSA_HOST_CK(h2d_chunk(1));
+  CUtensorMap tk;
+  if (!tmap_rows_u8(&tk, hs.base + L.k, N, TILE)) return DSA_ERR_CUDA;
+  for (int c = 0; c < nch; ++c) {
+    const int64_t r0 = (int64_t)c * C;
+    const int n = (int)std::min<int64_t>(C, Q - r0);
+    uint8_t* s = slot(c);
+    DSA_HOST_CK(cudaStreamWaitEvent(stream, hs.in_ready[c & 1], 0));
+    CUtensorMap tq;
+    if (!tmap_rows_u8(&tq, s + L.q, (uint64_t)n * H, H)) return DSA_ERR_CUDA;
+    RowSpace rs{};
+    rs.R = n;
+    rs.N = N;
+    rc = run_fused(rs, K, tq, tk, hs.base + L.k, reinterpret_cast<const float*>(hs.base + L.ks),
+                   reinterpret_cast<const float*>(s + L.qs), reinterpret_cast<const float*>(s + L.w),
+                   reinterpret_cast<const int32_t*>(s + L.rb), reinterpret_cast<const int32_t*>(s + L.re),
+                   reinterpret_cast<int32_t*>(s + L.out), stream);
+    if (rc != DSA_OK) return rc;
+    // this chunk's status block, taken before the next chunk's plan resets it
+    Stats* st = arena_stats(stream);
+    if (!st) return DSA_ERR_CUDA;
+    DSA_HOST_CK(cudaMemcpyAsync(&hs.stats_h[c], st, sizeof(Stats), d2h, stream));
+    DSA_HOST_CK(cudaEventRecord(hs.done[c & 1], stream));
+    DSA_HOST_CK(cudaStreamWaitEvent(hs.copy, hs.done[c & 1], 0));
+    DSA_HOST_CK(cudaMemcpyAsync(out_idx + r0 * K, s + L.out, (size_t)n * K * 4, d2h, hs.copy));
+    if (c + 2 < nch) DSA_HOST_CK(h2d_chunk(c + 2));
+  }
+  DSA_HOST_CK(cudaEventRecord(hs.copies_done, hs.copy));
+  DSA_HOST_CK(cudaStreamWaitEvent(stream, hs.copies_done, 0));
+  DSA_HOST_CK(cudaStreamSynchronize(stream));
+#undef DSA_HOST_CK
+  int status = 0;
+  for (int c = 0; c < nch; ++c) status |= hs.stats_h[c].status;
+  if (status & ST_TIMEOUT) return DSA_ERR_TIMEOUT;
+  if (status & ST_RANGE) return DSA_ERR_RANGE;
+  return DSA_OK;
 }
 
 int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_cache,
@@ -821,6 +1004,10 @@ int dsa_indexer_set_option(int option, int64_t value) {
       if (value < 1 || value > 256) return DSA_ERR_ARG;
       g_target16 = value;
       return DSA_OK;
+    case DSA_OPT_HOST_CHUNK_ROWS:
+      if (value < 0 || value > (1 << 30)) return DSA_ERR_ARG;
+      g_host_chunk_rows = value;
+      return DSA_OK;
 
     default:
       return DSA_ERR_ARG;
@@ -840,6 +1027,8 @@ int64_t dsa_indexer_get_option(int option) {
       return g_grid;
     case DSA_OPT_SAMPLE_TARGET:
       return g_target16;
+    case DSA_OPT_HOST_CHUNK_ROWS:
+      return g_host_chunk_rows;
 
     default:
       return DSA_ERR_ARG;
@@ -864,6 +1053,23 @@ int64_t dsa_indexer_launch_count(void) { return g_launches.load(); }
 const char* dsa_indexer_version(void) { return "dsa_indexer 0.1 (sm_103a, tcgen05 + TMA)"; }
 
 int dsa_indexer_release(void) {
+  // lock order of the library: g_host_mu before g_mu
+  std::lock_guard<std::mutex> hl(g_host_mu);
+  for (auto& kv : g_host) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(kv.first.first);
+    HostStage& hs = kv.second;
+    if (hs.copy) cudaStreamSynchronize(hs.copy);
+    if (hs.base) cudaFree(hs.base);
+    cudaEvent_t evs[] = {hs.entry, hs.copies_done, hs.in_ready[0], hs.in_ready[1], hs.done[0], hs.done[1]};
+    for (cudaEvent_t e : evs)
+      if (e) cudaEventDestroy(e);
+    if (hs.copy) cudaStreamDestroy(hs.copy);
+    if (hs.stats_h) cudaFreeHost(hs.stats_h);
+    cudaSetDevice(cur);
+  }
+  g_host.clear();
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_arenas.empty()) cudaDeviceSynchronize();
   for (auto& kv : g_arenas) {

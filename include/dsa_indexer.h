@@ -92,6 +92,33 @@ DSA_API int dsa_indexer_topk(const uint8_t* q_fp8, const float* q_scale,
                      int32_t* out_idx, dsa_stream_t stream);
 
 /*
+ * The fused operator of dsa_indexer_topk on HOST buffers (every array
+ * argument is host memory, same layouts and meaning): the library copies the
+ * inputs to device staging it owns, runs the fused operator over chunks of
+ * rows, and copies the indices back into out_idx.  Rows are independent, so
+ * the chunks give the same result as one call; while one chunk is scored on
+ * `stream`, an internal copy stream brings in the next chunk's rows and takes
+ * out the previous chunk's indices.  Rows per chunk: DSA_OPT_HOST_CHUNK_ROWS,
+ * by default half of Q but at least 2048 rows.
+ *
+ * Synchronous: returns when out_idx holds the result.  Return value: DSA_OK,
+ * an argument error (nothing enqueued), DSA_ERR_CUDA, or the device status of
+ * the call (DSA_ERR_RANGE or DSA_ERR_TIMEOUT, combined over all chunks).
+ * Host buffers in page-locked memory (cudaHostAlloc / pinned) let the copies
+ * overlap the scoring; pageable buffers work but serialise them.  The device
+ * staging (keys, two row chunks) is allocated on the first call and grown on
+ * demand, per (device, stream).  Host-buffer calls are serialised within a
+ * process.  dsa_indexer_last_device_status and dsa_indexer_last_repaired_rows
+ * describe the last chunk only (repaired row ids relative to that chunk).
+ */
+DSA_API int dsa_indexer_topk_host(const uint8_t* q_fp8, const float* q_scale,
+                          const uint8_t* k_fp8, const float* k_scale,
+                          const float* w,
+                          const int32_t* row_begin, const int32_t* row_end,
+                          int Q, int N, int K,
+                          int32_t* out_idx, dsa_stream_t stream);
+
+/*
  * Paged variant (contest write-up, "DSA TopK Indexer"): keys in a cache of
  * 64-token pages with one fp32 scale per token; logical token s of sequence b
  * lives in physical slot block_table[b][s / 64] * 64 + s % 64.  Query row i of
@@ -206,7 +233,8 @@ typedef enum {
   DSA_OPT_TAU_BIAS = 2,       /* added to every sampled threshold key: >0 forces underflow, <0 overflow (test knob; default 0) */
   DSA_OPT_PROFILE = 3,        /* 1: time the main kernel of each call with CUDA events (default 0) */
   DSA_OPT_GRID_CTAS = 4,      /* CTAs of the persistent kernels (default: SM count) */
-  DSA_OPT_SAMPLE_TARGET = 5   /* candidates the threshold aims at, in units of K/16 (default 32 = 2K) */
+  DSA_OPT_SAMPLE_TARGET = 5,  /* candidates the threshold aims at, in units of K/16 (default 32 = 2K) */
+  DSA_OPT_HOST_CHUNK_ROWS = 6 /* rows per chunk of dsa_indexer_topk_host (default 0: chosen per call) */
 } dsa_option;
 DSA_API int dsa_indexer_set_option(int option, int64_t value);
 DSA_API int64_t dsa_indexer_get_option(int option);

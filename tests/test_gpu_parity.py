@@ -170,6 +170,51 @@ def test_forced_repair_paged_is_exact(B, bias, kind):
             assert not pr, (b, i, pr)
 
 
+# ---------------------------------------------------- host-buffer entry ----
+@pytest.mark.parametrize("chunk_rows,pinned", [(0, True), (16, True), (12, False)])
+def test_host_buffer_entry_matches_device_entry(B, chunk_rows, pinned):
+    """dsa_indexer_topk_host (host arrays in and out, row chunks pipelined over
+    the library's copy stream) returns what the device entry returns: the
+    chunks (16 or 12 rows of 45, a ragged last chunk; one chunk by default)
+    are independent rows, and the selection is exact."""
+    import torch
+    inp = S.make_dense(45, 9000, K=512, seed=21, causal=True)
+    host = [torch.from_numpy(np.ascontiguousarray(a)) for a in
+            (inp.q, inp.q_scale, inp.k, inp.k_scale, inp.w, inp.row_begin, inp.row_end)]
+    if pinned:
+        host = [t.pin_memory() for t in host]
+    B.set_option("host_chunk_rows", chunk_rows)
+    try:
+        for _ in range(2):  # the staging is reused on the second call
+            out = B.indexer_topk_host(*host, K=inp.K).numpy()
+            assert check_dense_rows(inp, out, range(inp.Q)) == {}
+    finally:
+        B.set_option("host_chunk_rows", 0)
+    ref = B.indexer_topk(*dense_args(inp), K=inp.K).cpu().numpy()
+    o = indexer.DenseOracle.from_inputs(inp)
+    for t in range(inp.Q):
+        ids, I, _ = o.row_scores(t)
+        pos = {int(s): i for i, s in enumerate(ids)}
+        a = np.sort([I[pos[int(s)]] for s in out[t] if s >= 0])
+        b = np.sort([I[pos[int(s)]] for s in ref[t] if s >= 0])
+        assert np.array_equal(a, b), t
+
+
+def test_host_buffer_entry_reports_bad_ranges(B):
+    import torch
+    inp = S.make_dense(20, 700, K=16, seed=22, causal=False)
+    inp.row_begin[13], inp.row_end[13] = 10, 701     # end past N, in the second chunk
+    host = [torch.from_numpy(np.ascontiguousarray(a)) for a in
+            (inp.q, inp.q_scale, inp.k, inp.k_scale, inp.w, inp.row_begin, inp.row_end)]
+    B.set_option("host_chunk_rows", 8)
+    try:
+        with pytest.raises(B.IndexerError) as e:
+            B.indexer_topk_host(*host, K=16)
+    finally:
+        B.set_option("host_chunk_rows", 0)
+    assert e.value.code == B.DSA_ERR_RANGE
+
+
 # ------------------------------------------------------------- edge cases ----
 def test_edge_ranges(B):
     """Empty rows, L = K, L = K + 1, offset ranges, a single key."""

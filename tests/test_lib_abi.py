@@ -49,6 +49,10 @@ def test_null_and_size_arguments_rejected_without_gpu():
                                     None) == binding.DSA_ERR_ARG
     assert L.dsa_indexer_scores(fake, fake, fake, fake, fake, fake, fake, 4, 8, fake, 6, None) == binding.DSA_ERR_ARG
     assert L.dsa_indexer_topk_from_scores(fake, 7, fake, fake, 4, 7, 16, fake, None) == binding.DSA_ERR_ARG
+    assert L.dsa_indexer_topk_host(None, None, None, None, None, None, None, 1, 1, 1, None, None) == binding.DSA_ERR_ARG
+    assert L.dsa_indexer_topk_host(fake, fake, fake, fake, fake, fake, fake, 4, 8, 0, fake, None) == binding.DSA_ERR_ARG
+    assert L.dsa_indexer_topk_host(fake, fake, fake, fake, fake, fake, fake, 1 << 25, 8, 16, fake,
+                                   None) == binding.DSA_ERR_UNSUPPORTED
 
 
 def test_options_roundtrip_and_validate():
@@ -56,6 +60,11 @@ def test_options_roundtrip_and_validate():
     binding.set_option("chunk_tiles", 32)
     assert binding.get_option("chunk_tiles") == 32
     binding.set_option("chunk_tiles", old)
+    binding.set_option("host_chunk_rows", 256)
+    assert binding.get_option("host_chunk_rows") == 256
+    binding.set_option("host_chunk_rows", 0)
+    with pytest.raises(binding.IndexerError):
+        binding.set_option("host_chunk_rows", -1)
     with pytest.raises(binding.IndexerError):
         binding.set_option("chunk_tiles", 0)
     assert binding.lib().dsa_indexer_set_option(999, 1) == binding.DSA_ERR_ARG
