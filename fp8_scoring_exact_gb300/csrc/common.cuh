@@ -76,7 +76,8 @@ struct Stats {
   int r_units;
   int s_groups;      // sample plan
   int s_units;
-  int pad[4];
+  int next_unit[3];  // per plan (PLAN_*): the next work unit a scorer CTA takes
+  int pad[1];
 };
 
 // A work group: up to 2 query rows that stream the same keys.  Key range is

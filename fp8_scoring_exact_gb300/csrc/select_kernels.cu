@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
   }
   if (tid == 0) {
     p.unit_start[0] = 0;
+    p.stats->next_unit[p.plan] = 0;
     if (p.plan == PLAN_MAIN) {
       p.stats->n_groups = G;
       p.stats->total_units = s_carry;
