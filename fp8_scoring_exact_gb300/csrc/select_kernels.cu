@@ -481,15 +481,28 @@ __global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTau
     uint32_t tau = 0u;
     if (m > 0 && rank >= 1 && rank <= m) {
       uint32_t key[TAU_KEYS_PER_LANE];
+      uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
       for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
         const int i = q * 32 + lane;
         key[q] = i < m ? ordered_key(__ldcg(&sr[(int64_t)i * stride])) : 0u;
+        if (i < m) {
+          kmin = min(kmin, key[q]);
+          kmax = max(kmax, key[q]);
+        }
       }
-      uint32_t prefix = 0, mask = 0;
+      // the leading bytes every sample shares are the threshold's too (the
+      // samples of a row have similar magnitudes, so the first byte or two
+      // usually are): the radix passes start below them
+      kmin = __reduce_min_sync(0xffffffffu, kmin);
+      kmax = __reduce_max_sync(0xffffffffu, kmax);
+      const uint32_t diff = kmin ^ kmax;
+      const int shared_bytes = diff ? (int)(__clz(diff) >> 3) : 4;
+      uint32_t mask = shared_bytes ? (0xffffffffu << (32 - 8 * shared_bytes)) : 0u;
+      uint32_t prefix = kmin & mask;
       int rem = rank;
 #pragma unroll 1
-      for (int pass = 0; pass < 4; ++pass) {
+      for (int pass = shared_bytes; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
 #pragma unroll
         for (int i = lane; i < 256; i += 32) hist[i] = 0;
@@ -505,7 +518,25 @@ __global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTau
         prefix |= (uint32_t)pick[0] << shift;
         mask |= 0xFFu << shift;
         rem = pick[1];
+        const int cnt = pick[2];
         __syncwarp();
+        if (cnt == 1) {
+          // the threshold is the only sample in its bucket: read it whole
+          // instead of running the remaining passes
+          uint32_t found = 0u;
+          bool have = false;
+#pragma unroll
+          for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
+            const int i = q * 32 + lane;
+            if (i < m && (key[q] & mask) == prefix) {
+              found = key[q];
+              have = true;
+            }
+          }
+          const unsigned b = __ballot_sync(0xffffffffu, have);
+          prefix = __shfl_sync(0xffffffffu, found, __ffs(b) - 1);
+          break;
+        }
       }
       tau = prefix;
       if (p.tau_bias != 0) {
