@@ -3,11 +3,14 @@
 // launch sequences of the fused, paged, unfused and standalone operators.
 //
 // Launch sequence of the fused operator (all on the caller's stream, no host
-// synchronisation):
-//   plan (ranges, pairs, work units) -> sample (thresholds, remapping path)
-//   -> persistent scorer in filter mode with TopK warps
-//   -> repair plan -> persistent scorer in store mode over the queued rows
-//   -> standalone exact select of those rows.
+// synchronisation; every kernel launched with programmatic dependent launch):
+//   plan (ranges, 4-row groups, work units) -> sampled thresholds (dense: the
+//   shared grid gathered once, scored by the scorer in store mode, one
+//   threshold per row; paged and short rows: the per-pair sampling kernel)
+//   -> persistent scorer in filter mode (candidates to per-row regions)
+//   -> candidate selector (certificate, radix select, emission)
+//   -> repair plan -> scorer in store mode over the failed rows
+//   -> cluster radix select of those rows.
 #include <cudaTypedefs.h>
 
 #include <algorithm>

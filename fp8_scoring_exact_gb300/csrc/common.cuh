@@ -80,7 +80,7 @@ struct Stats {
   int pad[1];
 };
 
-// A work group: up to 2 query rows that stream the same keys.  Key range is
+// A work group: up to GROUP_ROWS (4) query rows that stream the same keys.  Key range is
 // the union of the rows' valid ranges, in logical key coordinates.
 struct Group {
   int nrows;
