@@ -554,11 +554,22 @@ Stats* arena_stats(cudaStream_t stream) {
 
 int host_stage_init(HostStage& hs, const HostLayout& L, cudaStream_t stream) {
   if (!hs.copy) {
-    if (cudaStreamCreateWithFlags(&hs.copy, cudaStreamNonBlocking) != cudaSuccess) return DSA_ERR_CUDA;
-    cudaEvent_t* evs[] = {&hs.entry, &hs.copies_done, &hs.in_ready[0], &hs.in_ready[1], &hs.done[0], &hs.done[1]};
-    for (cudaEvent_t* e : evs)
-      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return DSA_ERR_CUDA;
-    if (cudaMallocHost(&hs.stats_h, HOST_MAX_CHUNKS * sizeof(Stats)) != cudaSuccess) return DSA_ERR_CUDA;
+    // built in a local first: the stage takes it only once every part exists
+    HostStage n;
+    bool ok = cudaStreamCreateWithFlags(&n.copy, cudaStreamNonBlocking) == cudaSuccess;
+    cudaEvent_t* evs[] = {&n.entry, &n.copies_done, &n.in_ready[0], &n.in_ready[1], &n.done[0], &n.done[1]};
+    for (cudaEvent_t* e : evs) ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaMallocHost(&n.stats_h, HOST_MAX_CHUNKS * sizeof(Stats)) == cudaSuccess;
+    if (!ok) {
+      for (cudaEvent_t* e : evs)
+        if (*e) cudaEventDestroy(*e);
+      if (n.copy) cudaStreamDestroy(n.copy);
+      if (n.stats_h) cudaFreeHost(n.stats_h);
+      return DSA_ERR_CUDA;
+    }
+    n.base = hs.base;
+    n.cap = hs.cap;
+    hs = n;
   }
   if (hs.cap < L.total) {
     if (hs.base) {
@@ -614,12 +625,18 @@ int dsa_indexer_topk_host(const uint8_t* q_fp8, const float* q_scale, const uint
     cudaGetLastError();
     return rc;
   }
-#define DSA_HOST_CK(expr)           \
-  do {                              \
-    if ((expr) != cudaSuccess) {    \
-      cudaGetLastError();           \
-      return DSA_ERR_CUDA;          \
-    }                               \
+  // on an error, the copies already enqueued may still write out_idx or read
+  // the caller's buffers: they are waited for before returning
+  auto fail = [&](int code) {
+    cudaGetLastError();
+    cudaStreamSynchronize(hs.copy);
+    cudaStreamSynchronize(stream);
+    cudaGetLastError();
+    return code;
+  };
+#define DSA_HOST_CK(expr)                                 \
+  do {                                                    \
+    if ((expr) != cudaSuccess) return fail(DSA_ERR_CUDA); \
   } while (0)
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
   auto slot = [&](int c) { return hs.base + (size_t)(c & 1) * L.slot; };
@@ -644,14 +661,14 @@ int dsa_indexer_topk_host(const uint8_t* q_fp8, const float* q_scale, const uint
   DSA_HOST_CK(h2d_chunk(0));
   if (nch > 1) DSA_HOST_CK(h2d_chunk(1));
   CUtensorMap tk;
-  if (!tmap_rows_u8(&tk, hs.base + L.k, N, TILE)) return DSA_ERR_CUDA;
+  if (!tmap_rows_u8(&tk, hs.base + L.k, N, TILE)) return fail(DSA_ERR_CUDA);
   for (int c = 0; c < nch; ++c) {
     const int64_t r0 = (int64_t)c * C;
     const int n = (int)std::min<int64_t>(C, Q - r0);
     uint8_t* s = slot(c);
     DSA_HOST_CK(cudaStreamWaitEvent(stream, hs.in_ready[c & 1], 0));
     CUtensorMap tq;
-    if (!tmap_rows_u8(&tq, s + L.q, (uint64_t)n * H, H)) return DSA_ERR_CUDA;
+    if (!tmap_rows_u8(&tq, s + L.q, (uint64_t)n * H, H)) return fail(DSA_ERR_CUDA);
     RowSpace rs{};
     rs.R = n;
     rs.N = N;
@@ -659,10 +676,10 @@ int dsa_indexer_topk_host(const uint8_t* q_fp8, const float* q_scale, const uint
                    reinterpret_cast<const float*>(s + L.qs), reinterpret_cast<const float*>(s + L.w),
                    reinterpret_cast<const int32_t*>(s + L.rb), reinterpret_cast<const int32_t*>(s + L.re),
                    reinterpret_cast<int32_t*>(s + L.out), stream);
-    if (rc != DSA_OK) return rc;
+    if (rc != DSA_OK) return fail(rc);
     // this chunk's status block, taken before the next chunk's plan resets it
     Stats* st = arena_stats(stream);
-    if (!st) return DSA_ERR_CUDA;
+    if (!st) return fail(DSA_ERR_CUDA);
     DSA_HOST_CK(cudaMemcpyAsync(&hs.stats_h[c], st, sizeof(Stats), d2h, stream));
     DSA_HOST_CK(cudaEventRecord(hs.done[c & 1], stream));
     DSA_HOST_CK(cudaStreamWaitEvent(hs.copy, hs.done[c & 1], 0));
