@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
   float* wsm = (float*)(smem + SM_OFF_W);
   float* scs = (float*)(smem + SM_OFF_SC);
   int* hist = (int*)(smem + SM_OFF_HIST);
-  int* misc = (int*)(smem + SM_OFF_MISC);  // [0] tmem base, [1..4] digit block, [5] abort, [6] wait verdict
+  int* misc = (int*)(smem + SM_OFF_MISC);  // [0] tmem base, [1..4] digit block, [5] abort, [6] wait result
   const uint32_t bar = sbase + SM_OFF_MISC + 32;
   const RowSpace& rs = p.rs;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     mbar_arrive_expect_tx(bar, nact * H * D);
     for (int a = 0; a < nact; ++a) tma_load_2d(sbase + SM_OFF_Q + a * H * D, &tm_q, 0, act[a] * H, bar);
   }
-  // thread 0 waits (bounded) and the CTA follows its verdict
+  // thread 0 waits (bounded) and the CTA follows its result
   if (tid == 0) misc[6] = mbar_wait(bar, 0, abort_flag, &p.stats->status) ? 1 : 0;
   __syncwarp();
   __syncthreads();
