@@ -164,6 +164,50 @@ def test_relu_per_head_not_after_sum():
     assert I[0] == 1.0 and E[0] == 2.0
 
 
+def test_worked_example_offset_range_by_hand():
+    # A row whose valid range starts past key 0 (section 2.3: each row has its
+    # own [k_start, k_end)).  Keys are one-hot on dim 0 with distinct values
+    # c_s, q has a single non-zero element q[0, 0] = 1 and the only weight is
+    # w[0] = 2, so I[s] = 2 * ReLU(c_s) * q_scale * k_scale[s].
+    #   s     :  0    1    2    3     4     5    6    7
+    #   c_s   :  1   -1    2    3   -0.5   0.25  4   1.5
+    #   k_sc  :  1    1    1    1     1    0.5   2    1
+    # Row 0 sees [3, 7): I = 2*3*1, 0, 2*0.25*0.5, 2*4*2 = 6, 0, 0.25, 16
+    # (q_scale 1); its top 2 are keys 6 and 3, labelled by their absolute
+    # positions.
+    c = [1, -1, 2, 3, -0.5, 0.25, 4, 1.5]
+    keys = np.zeros((8, 4))
+    keys[:, 0] = c
+    q = np.zeros((2, 4))
+    q[0, 0] = 1.0
+    ks = np.array([1, 1, 1, 1, 1, 0.5, 2, 1], np.float32)
+    o = indexer.DenseOracle(_codes(q)[None], np.ones(1, np.float32), _codes(keys), ks,
+                            np.array([[2.0, 0.0]], np.float32), np.array([3]), np.array([7]), 2)
+    ids, I, E = o.row_scores(0)
+    assert ids.tolist() == [3, 4, 5, 6]
+    assert I.tolist() == [6.0, 0.0, 0.25, 16.0]
+    assert E.tolist() == [6.0, 1.0, 0.25, 16.0]
+    out, *_ = o.topk(0)
+    assert sorted(out.tolist()) == [3, 6]
+
+
+def test_offset_range_is_the_full_row_restricted():
+    # the same keys scored over [b, e) and over [0, N): the scores of the
+    # offset row are the full row's entries b..e-1, under the same labels
+    # (the float64 head combination may sum in another order for another
+    # length, so equal to within 1e-12 E rather than bit for bit)
+    q, qs, k, ks, w, _, _, K = _tiny_dense(12, Q=1)
+    N = k.shape[0]
+    full = indexer.DenseOracle(q, qs, k, ks, w, np.array([0]), np.array([N]), K)
+    ids_f, I_f, E_f = full.row_scores(0)
+    for b, e in [(37, 211), (1, N), (N - 17, N), (150, 151)]:
+        part = indexer.DenseOracle(q, qs, k, ks, w, np.array([b]), np.array([e]), K)
+        ids, I, E = part.row_scores(0)
+        assert ids.tolist() == list(range(b, e))
+        assert np.all(np.abs(I - I_f[b:e]) <= 1e-12 * E_f[b:e])
+        assert np.all(np.abs(E - E_f[b:e]) <= 1e-12 * E_f[b:e])
+
+
 # ------------------------------------------------------------- selection ----
 def test_topk_is_maximal_by_subset_enumeration():
     rng = np.random.default_rng(5)
@@ -287,6 +331,26 @@ def test_checker_accepts_oracle_and_catches_planted_mistakes():
     assert checks.check_row(bad, ids, I, E, K)                    # missing entry
 
 
+def test_checker_elementwise_criterion_catches_a_swapped_tie():
+    # Scores with a three-way tie at the K-th value (theta = 3, K = 4): the
+    # exact top-4 is {5, 4, 3, 3}.  Swapping the key scoring 5 for the
+    # unselected theta-tied key keeps every index valid and unique (i) and
+    # every selected score at or above theta (ii), so only the element-wise
+    # comparison of the sorted scores (iii) can see that 5 is missing.
+    ids = np.arange(10, 20)
+    I = np.array([5.0, 4.0, 3.0, 3.0, 3.0, 2.0, 1.0, 0.0, 0.0, 0.0])
+    E = np.abs(I) + 1.0
+    K = 4
+    good = np.array([10, 11, 12, 13])
+    assert checks.check_row(good, ids, I, E, K) == []
+    swapped = np.array([14, 11, 12, 13])                          # 5 -> a theta tie
+    assert checks.check_row(swapped, ids, I, E, K, elementwise=False) == []
+    probs = checks.check_row(swapped, ids, I, E, K)
+    assert len(probs) == 1 and "sorted scores differ" in probs[0]
+    # a different theta-tied key in place of a tied one is a correct answer
+    assert checks.check_row(np.array([10, 11, 12, 14]), ids, I, E, K) == []
+
+
 # ------------------------------------------------------------- mutation ----
 MUTANTS = {
     "no_relu": lambda d, w, qs, ks: (w.astype(np.float64) @ d.astype(np.float64)) * float(qs) * ks * indexer.DOT_UNIT,
@@ -315,6 +379,39 @@ def test_pins_catch_planted_oracle_mistakes(name, monkeypatch):
         except AssertionError:
             caught += 1
     assert caught >= 1, f"mutation {name} escaped every pin"
+
+
+def _row_scores_keys_from_zero(self, t):
+    # planted slip: the row's keys taken from position 0 instead of row_begin
+    b, e = int(self.row_begin[t]), int(self.row_end[t])
+    ids = np.arange(b, e, dtype=np.int64)
+    dots = indexer.exact_dots(self.qu[t], self.ku[:e - b])
+    I, E = indexer.combine_heads(dots, self.w[t], self.q_scale[t], self.k_scale[:e - b])
+    return ids, I, E
+
+
+def _row_scores_labels_from_zero(self, t):
+    # planted slip: the right keys, labelled 0..L-1 instead of b..e-1
+    b, e = int(self.row_begin[t]), int(self.row_end[t])
+    dots = indexer.exact_dots(self.qu[t], self.ku[b:e])
+    I, E = indexer.combine_heads(dots, self.w[t], self.q_scale[t], self.k_scale[b:e])
+    return np.arange(e - b, dtype=np.int64), I, E
+
+
+@pytest.mark.parametrize("mutant", [_row_scores_keys_from_zero, _row_scores_labels_from_zero])
+def test_pins_catch_planted_offset_range_mistakes(mutant, monkeypatch):
+    monkeypatch.setattr(indexer.DenseOracle, "row_scores", mutant)
+    for pin in (test_worked_example_offset_range_by_hand, test_offset_range_is_the_full_row_restricted):
+        with pytest.raises(AssertionError):
+            pin()
+
+
+def test_pins_catch_a_vacuous_elementwise_criterion(monkeypatch):
+    # the checker with criterion (iii) switched off must fail its pin
+    real = checks.check_row
+    monkeypatch.setattr(checks, "check_row", lambda *a, **kw: real(*a, **{**kw, "elementwise": False}))
+    with pytest.raises(AssertionError):
+        test_checker_elementwise_criterion_catches_a_swapped_tie()
 
 
 def test_pins_catch_transposed_dot(monkeypatch):
