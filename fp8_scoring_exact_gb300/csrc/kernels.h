@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace dsa {
@@ -219,6 +221,27 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// One bit per device (0..63) for a per-device, once-only host action.
+struct DeviceFlags {
+  std::atomic<uint64_t> bits{0};
+};
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once
+// per device: the attribute belongs to the device's context, so a process
+// that calls the library on several GPUs sets it on each (devices past 63
+// set it on every launch).  Two threads setting it at once is harmless.
+template <typename... KArgs>
+inline cudaError_t set_smem_attr_once(void (*kernel)(KArgs...), int bytes, DeviceFlags& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.bits.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.bits.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 // host launchers (return cudaGetLastError() of the launch)

@@ -555,13 +555,9 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
 template <int MODE, bool PAGED>
 static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
                                   cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(score_kernel<MODE, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_attr_once(score_kernel<MODE, PAGED>, SMEM_BYTES, attr_set);
+  if (e != cudaSuccess) return e;
   return launch_pdl(score_kernel<MODE, PAGED>, dim3(grid), dim3(SCORE_THREADS), SMEM_BYTES, s, tm_q, tm_k, p);
 }
 

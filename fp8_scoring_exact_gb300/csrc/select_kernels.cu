@@ -395,12 +395,9 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
 
 cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_pairs_, cudaStream_t s) {
   const dim3 grid(n_pairs_, p.split ? ceil_div(MAX_SAMPLES, TILE) : 1);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SAMPLE_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_attr_once(sample_kernel, SAMPLE_SMEM, attr_set);
+  if (e != cudaSuccess) return e;
   if (n_pairs_ <= 0) return cudaSuccess;
   return launch_pdl(sample_kernel, grid, dim3(SAMPLE_THREADS), SAMPLE_SMEM, s, tm_q, p);
 }
@@ -714,8 +711,12 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
           }
         }
       }
+      // every thread reads the count before the barrier that lets the next
+      // filter (after a threshold lookup that may take no barrier) reset it
       __syncthreads();
-      return misc[4];
+      const int count = misc[4];
+      __syncthreads();
+      return count;
     };
 
     // the certificate holds for any threshold: retry with a relaxed one when
@@ -934,12 +935,9 @@ __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const Cand
 }
 
 cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(cand_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CAND_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_attr_once(cand_select_kernel, CAND_SMEM, attr_set);
+  if (e != cudaSuccess) return e;
   return launch_pdl(cand_select_kernel, dim3(grid), dim3(CAND_THREADS), CAND_SMEM, s, p);
 }
 
@@ -1119,12 +1117,9 @@ cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s
 }
 
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SELECT_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_attr_once(select_kernel, SELECT_SMEM, attr_set);
+  if (e != cudaSuccess) return e;
   return launch_pdl(select_kernel, dim3(grid), dim3(SELECT_THREADS), SELECT_SMEM, s, p);
 }
 

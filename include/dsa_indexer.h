@@ -197,7 +197,10 @@ DSA_API int dsa_indexer_topk_from_scores(const float* scores, int64_t ld,
  * array it reads, but all calls share the one array: calls that may overlap
  * on the GPU (on different streams, or from different threads without
  * ordering) race and must be serialised by the caller.  Calls to this entry
- * point are not reported by dsa_indexer_last_device_status().
+ * point are not reported by dsa_indexer_last_device_status(): a row whose
+ * range lies outside [0, N] (or has begin > end) comes back as K entries of
+ * -1, exactly like an empty row, and nothing else signals it; callers that
+ * cannot vouch for their ranges validate them before the call.
  */
 DSA_API int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld,
                                                  const int32_t* row_begin, const int32_t* row_end,

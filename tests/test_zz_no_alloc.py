@@ -1,13 +1,21 @@
 """The entry point that allocates nothing (dsa_indexer_topk_from_scores_noalloc)
-must return what the allocating entry point (dsa_indexer_topk_from_scores)
-returns, call after call.
+must return the exact top-K of each score row, and what the allocating entry
+point (dsa_indexer_topk_from_scores) returns, call after call.
 
 It exists for callers that cannot call cudaMalloc (runtimes that own all
 device memory, such as a serving engine that reserves the free memory for its
 KV cache at start-up, or plugin hosts with a fixed budget); its scratch is a fixed
 array in device memory shared by every call, so two calls in a row also check
 that each call resets what it reads.  Selection from given fp32 scores is
-exact: up to ties, the sorted selected scores must be identical.
+exact: up to ties, the sorted selected scores must equal a full sort of the
+row bit for bit.
+
+Besides random rows, each case holds rows built to take every branch of the
+kernel behind this entry point: a threshold that leaves fewer than K
+candidates and whose relaxed retry falls outside the sample (every key then
+passes), rows where every threshold admits more candidates than fit (massive
+ties: the full-row radix select), rows of exactly K and fewer than K keys, an
+empty row, and -0 / +0 ties.
 """
 import numpy as np
 import pytest
@@ -15,6 +23,14 @@ import pytest
 from helpers import to_dev
 
 pytestmark = pytest.mark.gpu
+
+SAMPLE_STRIDE, SAMPLE_OFFSET = 200, 100   # the sampled-threshold grid (one key in 200)
+
+
+def _grid(b, e):
+    """Positions of the sample grid inside [b, e) (keys 100 mod 200)."""
+    first = b + (SAMPLE_OFFSET - b) % SAMPLE_STRIDE
+    return np.arange(first, e, SAMPLE_STRIDE)
 
 
 def _case(seed, Q, N, K):
@@ -28,20 +44,38 @@ def _case(seed, Q, N, K):
     re[3] = rb[3] + K                         # exactly K valid keys
     re[4] = rb[4] + 7                         # fewer than K
     re[5] = rb[5]                             # empty
+    # underflow, then a relaxed rank past the sample: the grid keys outscore
+    # every other key, so the first threshold (a grid key of rank about
+    # m * 2K / L) admits only that many keys; four times that rank exceeds
+    # the m grid keys, so the retry threshold is "every key" (L = 4K: m = 40
+    # grid keys, rank 21 then 84 > 40)
+    rb[6], re[6] = 123, 123 + 4 * K
+    sc[6, _grid(rb[6], re[6])] = 100.0 + np.arange(len(_grid(rb[6], re[6])), dtype=np.float32)
+    # every key equal: each threshold admits the whole row, which is longer
+    # than the selector keeps (overflow at every retry, then the full-row
+    # radix select); and a two-valued row
+    rb[7], re[7] = 0, N
+    sc[7] = 1.5
+    rb[8], re[8] = 11, N - 3
+    sc[8] = rng.choice(np.float32([-1.0, 2.0]), N)
     return sc, rb, re
 
 
-def _same_selection(sc, rb, re, K, a, b):
+def _check_exact(sc, rb, re, K, out):
+    """Valid, distinct, min(L, K) indices then -1 padding; the sorted selected
+    scores equal the full sort of the row's valid scores, bit for bit."""
     for t in range(sc.shape[0]):
-        n = min(max(int(re[t] - rb[t]), 0), K)
-        assert (a[t, n:] == -1).all() and (b[t, n:] == -1).all(), t
-        for out in (a, b):
-            sel = out[t, :n]
-            assert len(np.unique(sel)) == n and np.all((sel >= rb[t]) & (sel < re[t])), t
-        assert np.array_equal(np.sort(sc[t, a[t, :n]]), np.sort(sc[t, b[t, :n]])), t
+        L = max(int(re[t] - rb[t]), 0)
+        n = min(L, K)
+        assert (out[t, n:] == -1).all(), t
+        sel = out[t, :n]
+        assert len(np.unique(sel)) == n and np.all((sel >= rb[t]) & (sel < re[t])), t
+        want = np.sort(sc[t, rb[t]:re[t]])[::-1][:n]
+        got = np.sort(sc[t, sel])[::-1]
+        assert np.array_equal(got, want), t
 
 
-def test_noalloc_matches_allocating_entry_on_two_calls_in_a_row():
+def test_noalloc_is_exact_and_matches_allocating_entry_on_two_calls_in_a_row():
     import torch
 
     from fp8_scoring_exact_gb300 import binding as B
@@ -53,7 +87,9 @@ def test_noalloc_matches_allocating_entry_on_two_calls_in_a_row():
         out = torch.full((Q, K), -7, dtype=torch.int32, device="cuda")
         B.topk_from_scores_noalloc(d_sc, d_rb, d_re, K=K, out=out)
         torch.cuda.synchronize()
-        _same_selection(sc, rb, re, K, out.cpu().numpy(), ref)
+        got = out.cpu().numpy()
+        _check_exact(sc, rb, re, K, got)
+        _check_exact(sc, rb, re, K, ref)
 
 
 def test_noalloc_rejects_more_rows_than_its_scratch_holds():
