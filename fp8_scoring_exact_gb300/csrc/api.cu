@@ -37,6 +37,9 @@ int64_t g_profile = 0;
 int64_t g_grid = 0;
 int64_t g_target16 = 32;
 int64_t g_host_chunk_rows = 0;  // 0: chosen per call (host_chunk_rows)
+int64_t g_unit_order = 0;       // 1: scorer units handed out last first (test option)
+int64_t g_wait_us = WAIT_LIMIT_NS / 1000;  // limit of every pipeline wait
+int64_t g_withhold = 0;         // 1: the main scorer never signals its first accumulator (test option)
 std::atomic<int64_t> g_launches{0};
 
 // ----------------------------------------------------------------- arena ----
@@ -184,6 +187,9 @@ struct Opts {
   int chunk, grid, target16;
   int64_t bias;
   bool profile;
+  int reverse_units;
+  int withhold;
+  uint64_t wait_ns;
 };
 
 // Tiles per work unit: the option when set, else 64 for dense rows and 32
@@ -218,6 +224,9 @@ Opts read_opts() {
   o.bias = g_tau_bias;
   o.profile = g_profile != 0;
   o.target16 = (int)g_target16;
+  o.reverse_units = g_unit_order != 0;
+  o.withhold = g_withhold != 0;
+  o.wait_ns = (uint64_t)g_wait_us * 1000ull;
   const int sms = sm_count();
   o.grid = g_grid > 0 ? (int)g_grid : (sms > 0 ? sms : 1);
   return o;
@@ -225,23 +234,25 @@ Opts read_opts() {
 
 // ------------------------------------------------- shared launch sequence --
 // Fused pipeline over a row space whose keys are described by tm_k.
-int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensorMap& tm_k, const uint8_t* k_raw,
+int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUtensorMap& tm_k, const uint8_t* k_raw,
               const float* ks_raw, const float* q_scale,
               const float* w, const int32_t* row_begin, const int32_t* row_end, int32_t* out, cudaStream_t stream) {
   const Opts o = read_opts();
-  const int chunk = chunk_for(o, rs);
-  const int G = n_groups(rs);
-  const int64_t ld = align_up((size_t)rs.N, 4);
+  const int chunk = chunk_for(o, rs_in);
+  const int G = n_groups(rs_in);
+  const int64_t ld = align_up((size_t)rs_in.N, 4);
   // candidate-region units per row: paged, twice the work units (a group of
   // at most two rows runs two epilogue teams per unit)
-  const int max_units = (rs.paged ? 2 : 1) * ceil_div(ceil_div(rs.N, TILE), chunk);
+  const int max_units = (rs_in.paged ? 2 : 1) * ceil_div(ceil_div(rs_in.N, TILE), chunk);
   const int64_t cand_stride = ROW_SLOTS;
   std::lock_guard<std::mutex> lk(g_mu);
   int err = DSA_OK;
-  Arena* a = get_arena(stream, make_layout(rs.R, G, cand_stride, max_units, rs.R, ld), &err);
+  Arena* a = get_arena(stream, make_layout(rs_in.R, G, cand_stride, max_units, rs_in.R, ld), &err);
   if (!a) return err;
   const Layout& L = a->L;
   Stats* st = at<Stats>(a, L.stats);
+  RowSpace rs = rs_in;
+  if (rs.paged) rs.status = &st->status;
 
   PlanParams pp{};
   pp.rs = rs;
@@ -301,6 +312,8 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
       scp.mode = MODE_STORE;
       scp.chunk_tiles = WHOLE_PAIR_TILES;
       scp.plan = PLAN_SAMPLE;
+      scp.reverse_units = o.reverse_units;
+      scp.wait_ns = o.wait_ns;
       scp.k_scale = sx.sks;
       scp.q_scale = q_scale;
       scp.w = w;
@@ -349,6 +362,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
     sp.sld = SAMPLE_LD;
     sp.srb = at<int32_t>(a, L.srb);
     sp.sre = at<int32_t>(a, L.sre);
+    sp.wait_ns = o.wait_ns;
     DSA_LAUNCH(launch_sample(tm_q, sp, n_pairs(rs), stream));
     if (sp.split) {
       SampleTauParams tp{};
@@ -373,6 +387,9 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   cp.mode = MODE_FILTER;
   cp.chunk_tiles = chunk;
   cp.plan = PLAN_MAIN;
+  cp.reverse_units = o.reverse_units;
+  cp.withhold_first_acc = o.withhold;
+  cp.wait_ns = o.wait_ns;
   cp.k_scale = ks_raw;
   cp.q_scale = q_scale;
   cp.w = w;
@@ -413,6 +430,7 @@ int run_fused(const RowSpace& rs, int K, const CUtensorMap& tm_q, const CUtensor
   DSA_LAUNCH(launch_plan(rp, stream));
 
   ScoreParams rcp = cp;
+  rcp.withhold_first_acc = 0;
   rcp.mode = MODE_STORE;
   rcp.plan = PLAN_REPAIR;
   rcp.groups = rp.groups;
@@ -841,6 +859,8 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   cp.rs = rs;
   cp.mode = MODE_STORE;
   cp.chunk_tiles = pp.chunk_tiles;
+  cp.reverse_units = o.reverse_units;
+  cp.wait_ns = o.wait_ns;
   cp.k_scale = k_scale;
   cp.q_scale = q_scale;
   cp.w = w;
@@ -1028,6 +1048,18 @@ int dsa_indexer_set_option(int option, int64_t value) {
       if (value < 0 || value > (1 << 30)) return DSA_ERR_ARG;
       g_host_chunk_rows = value;
       return DSA_OK;
+    case DSA_OPT_UNIT_ORDER:
+      if (value != 0 && value != 1) return DSA_ERR_ARG;
+      g_unit_order = value;
+      return DSA_OK;
+    case DSA_OPT_WAIT_LIMIT_US:
+      if (value < 1 || value > 60000000) return DSA_ERR_ARG;
+      g_wait_us = value;
+      return DSA_OK;
+    case DSA_OPT_TEST_WITHHOLD:
+      if (value != 0 && value != 1) return DSA_ERR_ARG;
+      g_withhold = value;
+      return DSA_OK;
 
     default:
       return DSA_ERR_ARG;
@@ -1049,6 +1081,12 @@ int64_t dsa_indexer_get_option(int option) {
       return g_target16;
     case DSA_OPT_HOST_CHUNK_ROWS:
       return g_host_chunk_rows;
+    case DSA_OPT_UNIT_ORDER:
+      return g_unit_order;
+    case DSA_OPT_WAIT_LIMIT_US:
+      return g_wait_us;
+    case DSA_OPT_TEST_WITHHOLD:
+      return g_withhold;
 
     default:
       return DSA_ERR_ARG;

@@ -159,22 +159,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Pipeline waits give up after this long (the kernel then records
-// ST_TIMEOUT, drains and returns instead of hanging the GPU).
+// Pipeline waits give up after a limit passed in by the host (by default
+// WAIT_LIMIT_NS; the kernel then records ST_TIMEOUT, lets what it already
+// issued land and returns instead of hanging the GPU).
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+// Waits of the abort path, for copies and MMAs issued before the abort
+// (they complete within microseconds; the bound only guarantees an end).
+constexpr uint64_t DRAIN_LIMIT_NS = 2000000000ull;
 
 // Bounded wait: true when the phase with `parity` completed; false when the
 // CTA-wide abort flag is set or the time limit passed (then it sets both the
 // abort flag and the status bit).  The polling loop is out of line: the hot
 // loops only pay for one test when the phase has already completed.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                            int* status) {
+                                            int* status, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 7u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, ST_TIMEOUT);
         return false;
@@ -183,16 +187,26 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, status);
+  return mbar_wait_slow(bar, parity, abort_flag, status, limit_ns);
+}
+
+// Abort path: wait, bounded by DRAIN_LIMIT_NS and regardless of the abort
+// flag, for the phase with `parity` of a barrier that copies or MMAs issued
+// before the abort arrive on; false if the bound passed.
+static __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > DRAIN_LIMIT_NS) return false;
+  return true;
 }
 
 // Warp-uniform bounded wait: every lane polls (so every lane acquires the
 // phase) and every lane returns the same value, so code after it that needs
 // a converged warp (tcgen05.ld .sync.aligned, shuffles) never diverges.
 static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                 int* status) {
+                                                 int* status, uint64_t limit_ns) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     const bool done = mbar_try_wait(bar, parity);
@@ -206,7 +220,7 @@ static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t bar, uint32_t p
           const uint64_t now = globaltimer_ns();
           if (t0 == 0) {
             t0 = now;
-          } else if (now - t0 > WAIT_LIMIT_NS) {
+          } else if (now - t0 > limit_ns) {
             *abort_flag = 1;
             atomicOr(status, ST_TIMEOUT);
             give_up = 1;
@@ -218,9 +232,9 @@ static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t bar, uint32_t p
   }
 }
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               int* status) {
+                                               int* status, uint64_t limit_ns) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  return mbar_wait_warp_slow(bar, parity, abort_flag, status);
+  return mbar_wait_warp_slow(bar, parity, abort_flag, status, limit_ns);
 }
 
 // Warp-uniform bounded wait for a warp whose wake-up latency has slack (the
@@ -228,7 +242,8 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
 // takes no issue slots from the epilogue warps that share its SM
 // sub-partition (measured: 1% on the dense scorer).
 static __device__ __noinline__ bool mbar_wait_warp_backoff_slow(uint32_t bar, uint32_t parity,
-                                                         volatile int* abort_flag, int* status) {
+                                                         volatile int* abort_flag, int* status,
+                                                         uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     __nanosleep(128);
@@ -237,7 +252,7 @@ static __device__ __noinline__ bool mbar_wait_warp_backoff_slow(uint32_t bar, ui
     if ((threadIdx.x & 31) == 0) {
       if (*abort_flag) {
         give_up = 1;
-      } else if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      } else if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, ST_TIMEOUT);
         give_up = 1;
@@ -247,9 +262,9 @@ static __device__ __noinline__ bool mbar_wait_warp_backoff_slow(uint32_t bar, ui
   }
 }
 __device__ __forceinline__ bool mbar_wait_warp_backoff(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                       int* status) {
+                                                       int* status, uint64_t limit_ns) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  return mbar_wait_warp_backoff_slow(bar, parity, abort_flag, status);
+  return mbar_wait_warp_backoff_slow(bar, parity, abort_flag, status, limit_ns);
 }
 
 // n arrivals (a warp arriving for itself and n - 1 others), from the lane
@@ -306,6 +321,8 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int n
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+// Waits until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // The mbarrier tracks this thread's earlier cp.async copies: its pending
 // count rises by one now and falls by one when they have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {

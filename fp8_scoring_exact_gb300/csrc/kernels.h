@@ -23,6 +23,7 @@ struct RowSpace {
   int max_pages;
   int next_n;
   int num_pages;
+  int* status;                 // paged: the call's status word (a used block-table entry outside [0, num_pages))
 };
 
 // chunk size that makes every work unit a whole row pair (tiles per row < 2^24)
@@ -66,6 +67,7 @@ struct SampleParams {
   int64_t sld;
   int32_t* srb;                // [R] first / end pair-grid sample inside the row's range
   int32_t* sre;
+  uint64_t wait_ns;            // limit of every pipeline wait
 };
 
 struct ScoreParams {
@@ -73,6 +75,9 @@ struct ScoreParams {
   int mode;                    // MODE_STORE or MODE_FILTER
   int chunk_tiles;
   int plan;                    // which plan to read (PLAN_*)
+  int reverse_units;           // 1: the counter hands the plan's units out last first (a test of order independence)
+  int withhold_first_acc;      // test option: the MMA never signals its first accumulator (a wait must run out)
+  uint64_t wait_ns;            // limit of every pipeline wait
   const float* k_scale;        // dense [N] or paged [P * 64]
   const float* q_scale;
   const float* w;

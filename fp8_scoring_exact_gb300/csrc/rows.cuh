@@ -28,11 +28,16 @@ __device__ __forceinline__ int rows_of_group(const RowSpace& rs, int g, int* row
 
 __device__ __forceinline__ int row_seq(const RowSpace& rs, int row) { return rs.paged ? row / rs.next_n : -1; }
 
-// Output index of logical key s of `row`: dense s; paged physical slot.
+// Output index of logical key s of `row`: dense s; paged physical slot.  A
+// block-table entry outside [0, num_pages) gives -1 and sets ST_RANGE.
 __device__ __forceinline__ int32_t out_index(const RowSpace& rs, int row, int s) {
   if (!rs.paged) return s;
   const int b = row / rs.next_n;
   const int page = __ldg(&rs.block_table[(int64_t)b * rs.max_pages + (s >> 6)]);
+  if (page < 0 || page >= rs.num_pages) {
+    if (rs.status) atomicOr(rs.status, ST_RANGE);
+    return -1;
+  }
   return page * PAGE + (s & (PAGE - 1));
 }
 

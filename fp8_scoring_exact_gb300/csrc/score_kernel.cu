@@ -84,7 +84,7 @@ struct UnitSlot {
 static_assert(sizeof(UnitSlot) % 16 == 0 && offsetof(UnitSlot, w) % 16 == 0, "unit slot layout");
 constexpr uint32_t OFF_UNIT = OFF_PAGE + 128;
 constexpr uint32_t OFF_BAR = OFF_UNIT + 2 * sizeof(UnitSlot);
-constexpr int N_BARS = 2 * STAGES + 4 + 2 * ACC_BUFS;
+constexpr int N_BARS = 2 * STAGES + 4 + 2 * ACC_BUFS + 1;  // + the MMA's drain barrier (abort path)
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr uint32_t MISC_BYTES = 64;
 constexpr uint32_t SMEM_USED = OFF_MISC + MISC_BYTES;
@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
   auto q_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
   auto acc_full = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + i); };
   auto acc_empty = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + ACC_BUFS + i); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4 + 2 * ACC_BUFS);
   const float* stage_scales = (const float*)(smem + OFF_SCALE);
   UnitSlot* unit_slots = (UnitSlot*)(smem + OFF_UNIT);
   int* stage_pages = (int*)(smem + OFF_PAGE);
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       mbar_init(acc_full(i), 1);
       mbar_init(acc_empty(i), EPI_THREADS / 32);
     }
+    mbar_init(drain_bar, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -223,6 +225,10 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc->tmem_base;
+  const uint64_t wait_ns = p.wait_ns;
+  // producer: key tiles issued and q slots armed (the abort path waits for
+  // the last copy of each stage and slot)
+  uint32_t kit = 0, q_armed = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer --
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       tma_prefetch_desc(&tm_k);
     }
     const int num_pages = p.rs.num_pages;
-    uint32_t kit = 0, ui = 0;
+    uint32_t ui = 0;
     bool ok = true;
     int* next_unit = &p.stats->next_unit[p.plan];
     for (; ok; ++ui) {
@@ -248,7 +254,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       if (lane == 0) u = atomicAdd(next_unit, 1);
       u = __shfl_sync(0xffffffffu, u, 0);
       const int qs = ui & 1;
-      if (!(ok = mbar_wait_warp_backoff(q_empty(qs), ((ui >> 1) & 1) ^ 1, abort_flag, status))) break;
+      if (!(ok = mbar_wait_warp_backoff(q_empty(qs), ((ui >> 1) & 1) ^ 1, abort_flag, status, wait_ns))) break;
+      ++q_armed;
       if (u >= total) {
         // no unit left: the slot says so to the MMA and epilogue warps
         if (lane == 0) {
@@ -257,6 +264,10 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         }
         break;
       }
+      // every unit writes only its own candidate regions and count, so the
+      // order they are handed out in cannot change the result (a test
+      // option hands them out last first)
+      if (p.reverse_units) u = total - 1 - u;
       Group G;
       const Unit un = decode_unit(p, n_groups, u, G);
       {
@@ -320,16 +331,20 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         const int st = kit % STAGES;
         if (paged && ((t - un.t0) & 15) == 0) {
           // a page id outside the cache is clamped to the first row past
-          // it (TMA then reads zeros there instead of foreign memory); -1:
-          // the entry is past the sequence
+          // it (TMA then reads zeros there instead of foreign memory) and
+          // reported (ST_RANGE); -1: the entry is past the sequence
           const int j = 2 * t + lane;
           btv = -1;
+          bool bad = false;
           if ((int64_t)j * PAGE < G.hi) {
             btv = __ldg(&bt[j]);
-            if (btv < 0 || btv >= num_pages) btv = num_pages;
+            bad = btv < 0 || btv >= num_pages;
+            if (bad) btv = num_pages;
           }
+          if (__ballot_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, ST_RANGE);
         }
-        if (!(ok = mbar_wait_warp_backoff(key_empty(st), ((kit / STAGES) & 1) ^ 1, abort_flag, status))) break;
+        if (!(ok = mbar_wait_warp_backoff(key_empty(st), ((kit / STAGES) & 1) ^ 1, abort_flag, status, wait_ns)))
+          break;
         const uint32_t kdst = sbase + OFF_KEYS + st * KEY_STAGE_BYTES;
         if (!paged) {
           if (lane == 0) {
@@ -365,21 +380,21 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      uint32_t kit = 0, ait = 0, ui = 0;
+      uint32_t mit = 0, ait = 0, ui = 0;
       bool ok = true;
       for (; ok; ++ui) {
         const int qs = ui & 1;
-        if (!(ok = mbar_wait(q_full(qs), (ui >> 1) & 1, abort_flag, status))) break;
+        if (!(ok = mbar_wait(q_full(qs), (ui >> 1) & 1, abort_flag, status, wait_ns))) break;
         const UnitSlot* us = unit_slots + qs;
         if (us->nunits < 0) break;  // no unit left
         const int t0 = us->t0, t1 = us->t1;
         const uint32_t idesc = idesc_e4m3_f32(TILE, H * us->nrows);
         const uint64_t qdesc = sw128_kmajor_desc(sbase + OFF_Q + qs * Q_SLOT_BYTES);
-        for (int t = t0; t < t1; ++t, ++kit, ++ait) {
-          const int st = kit % STAGES;
-          if (!(ok = mbar_wait(key_full(st), (kit / STAGES) & 1, abort_flag, status))) break;
+        for (int t = t0; t < t1; ++t, ++mit, ++ait) {
+          const int st = mit % STAGES;
+          if (!(ok = mbar_wait(key_full(st), (mit / STAGES) & 1, abort_flag, status, wait_ns))) break;
           const int ab = ait % ACC_BUFS;
-          if (!(ok = mbar_wait(acc_empty(ab), ((ait / ACC_BUFS) & 1) ^ 1, abort_flag, status))) break;
+          if (!(ok = mbar_wait(acc_empty(ab), ((ait / ACC_BUFS) & 1) ^ 1, abort_flag, status, wait_ns))) break;
           tc_fence_after();
           const uint64_t kdesc = sw128_kmajor_desc(sbase + OFF_KEYS + st * KEY_STAGE_BYTES);
           const uint32_t d = tmem_base + ab * ACC_COLS;
@@ -387,7 +402,9 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) mma_e4m3(d, kdesc + 2 * k, qdesc + 2 * k, idesc, k > 0);
           mma_commit(key_empty(st));
-          mma_commit(acc_full(ab));
+          // (test option: the first accumulator is never signalled, so the
+          // epilogue's bounded wait for it runs out)
+          if (!(p.withhold_first_acc && ait == 0)) mma_commit(acc_full(ab));
         }
         if (ok) mma_commit(q_empty(qs));
       }
@@ -405,7 +422,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       // the unit as the producer staged it beside its q rows; the slot is
       // released as soon as this warp holds what it needs in registers
       const int qs = ui & 1;
-      if (!(ok = mbar_wait_warp(q_full(qs), (ui >> 1) & 1, abort_flag, status))) break;
+      if (!(ok = mbar_wait_warp(q_full(qs), (ui >> 1) & 1, abort_flag, status, wait_ns))) break;
       const UnitSlot* us = unit_slots + qs;
       if (us->nunits < 0) break;  // no unit left
       const int t0 = us->t0, t1 = us->t1, nrows = us->nrows;
@@ -462,7 +479,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         float ks;
         int page = 0;
         if constexpr (paged) {
-          if (!(ok = mbar_wait_warp(key_full(kst), (ait / STAGES) & 1, abort_flag, status))) break;
+          if (!(ok = mbar_wait_warp(key_full(kst), (ait / STAGES) & 1, abort_flag, status, wait_ns))) break;
           ks = stage_scales[kst * TILE + kt];
           page = stage_pages[2 * kst + (kt >> 6)];
         } else {
@@ -470,7 +487,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           ks = s < p.rs.N ? ldg_pinned_f32(&p.k_scale[s]) : 0.f;
         }
         const int ab = ait & (ACC_BUFS - 1);
-        if (!(ok = mbar_wait_warp(acc_full(ab), (ait / ACC_BUFS) & 1, abort_flag, status))) break;
+        if (!(ok = mbar_wait_warp(acc_full(ab), (ait / ACC_BUFS) & 1, abort_flag, status, wait_ns))) break;
         tc_fence_after();
         float part[4] = {0.f, 0.f, 0.f, 0.f};
         if (active) {
@@ -538,11 +555,28 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
 
   __syncthreads();
   if (misc->abort_flag) {
-    // a wait gave up: let copies and MMAs already issued land before the
-    // shared memory and TMEM are released
-    if (threadIdx.x == 0) {
-      const uint64_t t0 = globaltimer_ns();
-      while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+    // a wait gave up: before the shared memory and TMEM are released, the
+    // copies and MMAs already issued land.  A stage or q slot has at most
+    // one copy outstanding, the last one armed on it, so waiting for that
+    // phase of its barrier covers it (the TMA bytes and the cp.async
+    // arrivals of the same phase); a last commit tracks every MMA issued.
+    if (warp == 0) {
+      cp_async_wait_all();
+      if (lane == 0) {
+        for (uint32_t st = 0; st < (uint32_t)STAGES; ++st)
+          if (kit > st) {
+            const uint32_t last = st + STAGES * ((kit - 1 - st) / STAGES);
+            mbar_drain(key_full(st), (last / STAGES) & 1);
+          }
+        for (uint32_t qs = 0; qs < 2; ++qs)
+          if (q_armed > qs) {
+            const uint32_t last = qs + 2 * ((q_armed - 1 - qs) / 2);
+            mbar_drain(q_full(qs), (last >> 1) & 1);
+          }
+      }
+    } else if (warp == 1 && lane == 0) {
+      mma_commit(drain_bar);
+      mbar_drain(drain_bar, 0);
     }
     __syncthreads();
   }

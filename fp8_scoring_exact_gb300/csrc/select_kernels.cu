@@ -282,8 +282,10 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     mbar_arrive_expect_tx(bar, nact * H * D);
     for (int a = 0; a < nact; ++a) tma_load_2d(sbase + SM_OFF_Q + a * H * D, &tm_q, 0, act[a] * H, bar);
   }
-  // thread 0 waits (bounded) and the CTA follows its result
-  if (tid == 0) misc[6] = mbar_wait(bar, 0, abort_flag, &p.stats->status) ? 1 : 0;
+  // thread 0 waits (bounded) and the CTA follows its result; pend = the
+  // parity of the phase whose copy or MMA is outstanding (at most one)
+  uint32_t pend = 0;
+  if (tid == 0) misc[6] = mbar_wait(bar, 0, abort_flag, &p.stats->status, p.wait_ns) ? 1 : 0;
   __syncwarp();
   __syncthreads();
   bool ok = misc[6] != 0;
@@ -338,7 +340,8 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     }
     if (tt + 1 < tt_end) fetch(tt + 1);
     // phase 0 was the q load; this CTA's i-th MMA commit completes phase i + 1
-    if (tid == 0) misc[6] = mbar_wait(bar, (tt - tt_begin + 1) & 1, abort_flag, &p.stats->status) ? 1 : 0;
+    pend = (tt - tt_begin + 1) & 1;
+    if (tid == 0) misc[6] = mbar_wait(bar, pend, abort_flag, &p.stats->status, p.wait_ns) ? 1 : 0;
     __syncwarp();
     __syncthreads();
     ok = misc[6] != 0;
@@ -385,6 +388,9 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     if (tid == 0) p.tau[row] = tau;
   }
   if (!ok && !split && tid < nact) p.tau[act[tid]] = 0u;
+  // a wait gave up: the copy or MMA it waited for lands before the shared
+  // memory and TMEM are released
+  if (!ok && tid == 0) mbar_drain(bar, pend);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -841,7 +847,10 @@ __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const Cand
 #pragma unroll
     for (int i = 0; i < CS_PER_THREAD; ++i) {
       const int j = tid * CS_PER_THREAD + i;
-      const int x = j < nreg && j < CAND_MAX_REGIONS ? __ldcg(&cnt[j]) : 0;
+      // (a count is in [0, wcap + 1] unless the scorer gave up before
+      // writing it: clamped, so a stale word cannot move a gather out of
+      // the row's slots)
+      const int x = j < nreg && j < CAND_MAX_REGIONS ? max(__ldcg(&cnt[j]), 0) : 0;
       lost |= x > wcap;
       c[i] = min(x, wcap);
       tsum += c[i];

@@ -63,7 +63,9 @@ typedef enum {
   DSA_ERR_UNSUPPORTED = -2,  /* a size beyond what the kernels address (e.g. N >= 2^31 / 128) */
   DSA_ERR_CUDA = -3,         /* a CUDA runtime call failed (no device, launch failure, out of memory) */
   DSA_ERR_TIMEOUT = -4,      /* device status: a bounded pipeline wait gave up (kernel returned early) */
-  DSA_ERR_RANGE = -5         /* device status: some row range was outside [0, N]; that row got all -1 */
+  DSA_ERR_RANGE = -5         /* device status: some row range was outside [0, N] (that row got all -1), or a
+                                used block-table entry was outside [0, num_pages) (that sequence's rows are
+                                undefined: the bad page reads as zeros, its slots as -1 or out of range) */
 } dsa_status;
 
 #define DSA_HEADS 64
@@ -133,6 +135,11 @@ DSA_API int dsa_indexer_topk_host(const uint8_t* q_fp8, const float* q_scale,
  *   seq_lens      [B] int32, 0 <= seq_lens[b] <= max_pages * 64
  *   num_pages     P (bounds every block_table entry that is used)
  *   out_idx       [B, next_n, K] int32 (written)
+ *
+ * A used block_table entry (entry s / 64 of a key s the sequence's rows see)
+ * outside [0, P) is never followed: the page reads as zeros and the call's
+ * device status reports DSA_ERR_RANGE; that sequence's rows are undefined,
+ * every other sequence is unaffected.
  */
 DSA_API int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale,
                            const uint8_t* k_cache, const float* k_cache_scale,
@@ -237,7 +244,15 @@ typedef enum {
   DSA_OPT_PROFILE = 3,        /* 1: time the main kernel of each call with CUDA events (default 0) */
   DSA_OPT_GRID_CTAS = 4,      /* CTAs of the persistent kernels (default: SM count) */
   DSA_OPT_SAMPLE_TARGET = 5,  /* candidates the threshold aims at, in units of K/16 (default 32 = 2K) */
-  DSA_OPT_HOST_CHUNK_ROWS = 6 /* rows per chunk of dsa_indexer_topk_host (default 0: chosen per call) */
+  DSA_OPT_HOST_CHUNK_ROWS = 6, /* rows per chunk of dsa_indexer_topk_host (default 0: chosen per call) */
+  DSA_OPT_UNIT_ORDER = 7,      /* order the scorer's work units are handed out in: 0 plan order (default),
+                                  1 last first; the result does not depend on it (test option) */
+  DSA_OPT_WAIT_LIMIT_US = 8,   /* microseconds after which a pipeline wait inside a kernel gives up (default
+                                  2000000, range 1..60000000): the kernel then lets the copies and MMAs it
+                                  already issued land, returns early, and the call reports DSA_ERR_TIMEOUT */
+  DSA_OPT_TEST_WITHHOLD = 9    /* test option: 1 makes the fused operator's main scorer never signal its first
+                                  accumulator, so that its epilogue's wait runs out after DSA_OPT_WAIT_LIMIT_US
+                                  and the call reports DSA_ERR_TIMEOUT (its output is then undefined); default 0 */
 } dsa_option;
 DSA_API int dsa_indexer_set_option(int option, int64_t value);
 DSA_API int64_t dsa_indexer_get_option(int option);

@@ -77,6 +77,41 @@ def test_causal_q2048_n16k_all_rows(B):
     assert bad == {}, list(bad.items())[:3]
 
 
+def test_causal_q2048_n16k_units_last_first(B):
+    """The persistent scorer hands its work units out from a counter; each
+    unit writes only its own candidate regions and count, so handing them out
+    in reverse order must give an exact result too (every row)."""
+    inp = S.make_config(1)
+    B.set_option("unit_order", 1)
+    try:
+        out = B.indexer_topk(*dense_args(inp), K=inp.K).cpu().numpy()
+        counters = _status_ok(B)
+    finally:
+        B.set_option("unit_order", 0)
+    assert counters["underflow"] + counters["overflow"] <= 8
+    bad = check_rows_parallel(inp, out, range(inp.Q))
+    assert bad == {}, list(bad.items())[:3]
+
+
+@pytest.mark.parametrize("next_n", [2, 5])
+def test_paged_units_last_first(B, next_n):
+    """The same for paged rows: groups of at most two rows (two epilogue teams,
+    virtual units 2c and 2c + 1) and of four and one rows."""
+    inp = S.make_paged(9, next_n, K=512, seed=40 + next_n, len_lo=600, len_hi=30000, n_short=2, short_hi=700)
+    B.set_option("unit_order", 1)
+    try:
+        out = B.indexer_topk_paged(*paged_args(inp), K=inp.K).cpu().numpy()
+        _status_ok(B)
+    finally:
+        B.set_option("unit_order", 0)
+    po = indexer.PagedOracle.from_inputs(inp)
+    for b in range(inp.B):
+        for i in range(inp.next_n):
+            slots, I, E = po.row_scores(b, i)
+            pr = checks.check_row(out[b, i], slots, I, E, inp.K, order_key=np.arange(len(slots)))
+            assert not pr, (b, i, pr)
+
+
 # ------------------------------------------------- full-size sampled rows ----
 def _sampled_rows(Q, n, seed):
     rng = np.random.default_rng(seed)
@@ -129,6 +164,55 @@ def test_paged_small_all_rows(B, next_n):
             slots, I, E = po.row_scores(b, i)
             pr = checks.check_row(out[b, i], slots, I, E, inp.K, order_key=np.arange(len(slots)))
             assert not pr, (b, i, pr)
+
+
+def test_paged_bad_block_table_entries_report_range(B):
+    """A used block-table entry outside [0, num_pages) is reported through the
+    device status (DSA_ERR_RANGE) and never followed: one negative entry in
+    a sequence whose rows are scored, one past the cache in a sequence whose
+    rows take the remapping path (L <= K).  The other sequences stay exact."""
+    inp = S.make_paged(6, 2, K=512, seed=71, len_lo=3000, len_hi=9000, n_short=0)
+    P = inp.k_cache.shape[0]
+    inp.seq_lens[1] = 300                        # remapping path (L <= K)
+    inp.block_table[0, 3] = -5                   # inside sequence 0's 3000+ keys
+    inp.block_table[1, 2] = P + 7                # inside sequence 1's 300 keys
+    out = B.indexer_topk_paged(*paged_args(inp), K=inp.K).cpu().numpy()
+    rc, _ = B.last_device_status()
+    assert rc == B.DSA_ERR_RANGE
+    po = indexer.PagedOracle.from_inputs(inp)
+    for b in range(2, inp.B):
+        for i in range(inp.next_n):
+            slots, I, E = po.row_scores(b, i)
+            pr = checks.check_row(out[b, i], slots, I, E, inp.K, order_key=np.arange(len(slots)))
+            assert not pr, (b, i, pr)
+    # the same batch with a valid table is clean
+    good = S.make_paged(6, 2, K=512, seed=71, len_lo=3000, len_hi=9000, n_short=0)
+    good.seq_lens[1] = 300
+    B.indexer_topk_paged(*paged_args(good), K=good.K)
+    _status_ok(B)
+
+
+# ------------------------------------------------------- bounded waits ----
+def test_bounded_wait_runs_out_and_the_next_call_is_exact(B):
+    """Every pipeline wait inside the kernels is bounded.  With a test option
+    the main scorer never signals its first accumulator, so its epilogue's
+    wait (limit 50 ms here) runs out: the kernel lets the copies and MMAs it
+    issued land, returns early, and the call reports DSA_ERR_TIMEOUT.  The
+    context stays usable: the next call is exact."""
+    inp = S.make_dense(16, 20000, K=512, seed=61, causal=True)
+    args = dense_args(inp)
+    B.set_option("wait_limit_us", 50000)
+    B.set_option("test_withhold", 1)
+    try:
+        B.indexer_topk(*args, K=inp.K)
+        rc, _ = B.last_device_status()
+    finally:
+        B.set_option("test_withhold", 0)
+        B.set_option("wait_limit_us", 2000000)
+    assert rc == B.DSA_ERR_TIMEOUT
+    out = B.indexer_topk(*args, K=inp.K).cpu().numpy()
+    _status_ok(B)
+    assert check_dense_rows(inp, out, range(inp.Q)) == {}
 
 
 # ----------------------------------------------------------------- repair ----
