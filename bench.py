@@ -244,6 +244,51 @@ def time_oracle(inp, n_rows, procs, reps=1):
     return rk * reps / dt, dt, list(rows)
 
 
+# --------------------------------------------------------- FP8 peak probe --
+def fp8_peak_probe(device, seconds=2.0, n=8192):
+    """Dense e4m3 x e4m3 GEMM throughput of the library GEMM (torch._scaled_mm,
+    cuBLASLt), n^3 with fp32 accumulation, bf16 output: best of 10 (burst) and
+    back to back for `seconds` (sustained), with the SM clock sampled during
+    the sustained loop.  Evidence for the FP8 roofline denominator, which stays
+    the measured bf16 peak times the nominal fp8/bf16 ratio."""
+    import torch
+    try:
+        a = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=device, dtype=torch.float32)
+
+        def mm():
+            return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+        for _ in range(3):
+            mm()
+        torch.cuda.synchronize(device)
+        flop = 2.0 * n ** 3
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mm()
+            e1.record()
+            torch.cuda.synchronize(device)
+            best = min(best, e0.elapsed_time(e1))
+        with ClockSampler(device.index) as clk:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(1, int(seconds * 1e3 / best))
+            e0.record()
+            for _ in range(reps):
+                mm()
+            e1.record()
+            torch.cuda.synchronize(device)
+        sus_ms = e0.elapsed_time(e1) / reps
+        return {"burst_tflops": flop / (best * 1e-3) / 1e12, "sustained_tflops": flop / (sus_ms * 1e-3) / 1e12,
+                "sustained_clocks": clk.summary(), "n": n,
+                "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, per-tensor scales 1: best of 10 and back to back "
+                       f"for {seconds:.0f} s"}
+    except Exception as e:  # the probe is evidence only; the bench line stands without it
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
 # ------------------------------------------------------------ GPU arm -------
 def _e2e(args, dev, host, out, stream, world, device, call, R, host_call=None):
     """Same metric through the public API with host buffers: every step copies
@@ -423,6 +468,38 @@ def run_ours(args, rank, world, device):
                           "matrix; bytes = every valid score once + output; L2 flushed before each step"}
         del scores
 
+    # the math-only control ("Fusing Indexer Scoring and Exact Top-k for
+    # DeepSeek-V3.2", section 5.2): the main scorer with its score reduction
+    # and candidate filter removed, timed alternately with the real call in
+    # the same rounds; exposed = the share of the main kernel's time they add
+    control = None
+    if "control" in legs and call_unfused is not None:
+        checksum = torch.zeros(1, dtype=torch.float32, device=device)
+        binding.set_option("profile", 1)
+        ctl_args = (*dev[:7],)
+        for _ in range(max(1, args.warmup)):
+            binding.math_control(*ctl_args, K=inp.K, checksum=checksum)
+        torch.cuda.synchronize(device)
+        f_ms, c_ms = [], []
+        for i in range(args.steps):
+            flush.zero_()
+            step()
+            f_ms.append(binding.profiled_main_ms())
+            flush.zero_()
+            binding.math_control(*ctl_args, K=inp.K, checksum=checksum)
+            c_ms.append(binding.profiled_main_ms())
+        binding.set_option("profile", 0)
+        fm, cm = statistics.mean(f_ms), statistics.mean(c_ms)
+        control = {"main_kernel_ms": fm, "control_kernel_ms": cm, "exposed_frac": (fm - cm) / fm,
+                   "control_tflops": FLOP_PER_ROW_KEY * R / (cm * 1e-3) / 1e12,
+                   "call_ms": ms_per_step, "exposed_call_frac": (ms_per_step - cm) / ms_per_step,
+                   "note": "math-only control (dsa_indexer_math_control): same units, TMA loads, tcgen05 MMAs and "
+                           "barriers; the epilogue folds one accumulator column per warp and tile into a checksum. "
+                           "exposed_frac = (main - control) / main, alternating rounds; exposed_call_frac = "
+                           "(whole call - control) / whole call"}
+
+    fp8_probe = fp8_peak_probe(device) if "fp8peak" in legs else None
+
     # end to end through the public API from pinned host buffers
     e2e = None
     if "e2e" in legs:
@@ -450,6 +527,8 @@ def run_ours(args, rank, world, device):
         roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                     "frac": achieved / fp8_peak, "traffic": measured_traffic(args.config, args.rows, args.keys),
                     "kernel": kernel_name, "kernel_ms": main_avg, "peak_source": peak_note}
+        if fp8_probe is not None:
+            roofline["fp8_probe"] = fp8_probe
 
     res = {
         "metric": METRIC,
@@ -476,6 +555,7 @@ def run_ours(args, rank, world, device):
         "unfused": ({"ms_per_step": unf_ms, "fused_speedup": unf_ms / ms_per_step} if unf_ms else None),
         "graph": graph,
         "select": select,
+        "math_control": control,
         "failures": counters,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -586,8 +666,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override: causal workload with this many query rows")
     ap.add_argument("--keys", type=int, default=0, help="override: causal workload with this many keys")
-    ap.add_argument("--legs", default="fused,unfused,graph,select,e2e",
-                    help="comma list of legs to run besides the timed fused leg (unfused, graph, select, e2e)")
+    ap.add_argument("--legs", default="fused,unfused,graph,select,control,fp8peak,e2e",
+                    help="comma list of legs to run besides the timed fused leg "
+                         "(unfused, graph, select, control, fp8peak, e2e)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

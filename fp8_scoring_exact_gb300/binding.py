@@ -39,6 +39,7 @@ SIGNATURES = {
     "dsa_indexer_scores": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I64, _P]),
     "dsa_indexer_topk_from_scores": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_topk_from_scores_noalloc": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
+    "dsa_indexer_math_control": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_last_device_status": (_I, [_P, _P]),
     "dsa_indexer_last_repaired_rows": (_I, [_P, _P, _I]),
     "dsa_indexer_set_option": (_I, [_I, _I64]),
@@ -242,6 +243,23 @@ def topk_from_scores_noalloc(scores, row_begin, row_end, K=2048, N=None, out=Non
                                                     _ptr(_dev(out, "out", torch.int32)), _stream_ptr(stream))
     _check("dsa_indexer_topk_from_scores_noalloc", rc)
     return out
+
+
+def math_control(q, q_scale, k, k_scale, w, row_begin, row_end, K=2048, checksum=None, stream=None):
+    """The math-only control (a measurement): the fused call's main scorer with its
+    score reduction and candidate filter removed.  Returns the checksum tensor
+    (one device float, added to)."""
+    q, k = _u8(q, "q"), _u8(k, "k")
+    if checksum is None:
+        checksum = torch.zeros(1, dtype=torch.float32, device=q.device)
+    rc = lib().dsa_indexer_math_control(_ptr(q), _ptr(_dev(q_scale, "q_scale", torch.float32)), _ptr(k),
+                                        _ptr(_dev(k_scale, "k_scale", torch.float32)),
+                                        _ptr(_dev(w, "w", torch.float32)),
+                                        _ptr(_dev(row_begin, "row_begin", torch.int32)),
+                                        _ptr(_dev(row_end, "row_end", torch.int32)), q.shape[0], k.shape[0], K,
+                                        _ptr(_dev(checksum, "checksum", torch.float32)), _stream_ptr(stream))
+    _check("dsa_indexer_math_control", rc)
+    return checksum
 
 
 def last_device_status(stream=None):

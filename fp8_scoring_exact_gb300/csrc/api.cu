@@ -268,6 +268,7 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
   pp.unit_start = at<int32_t>(a, L.unit_start);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = st;
+  pp.wait_ns = o.wait_ns;
   DSA_LAUNCH(launch_plan(pp, stream));
 
   uint32_t* tau = at<uint32_t>(a, L.tau);
@@ -313,7 +314,6 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
       scp.chunk_tiles = WHOLE_PAIR_TILES;
       scp.plan = PLAN_SAMPLE;
       scp.reverse_units = o.reverse_units;
-      scp.wait_ns = o.wait_ns;
       scp.k_scale = sx.sks;
       scp.q_scale = q_scale;
       scp.w = w;
@@ -362,7 +362,6 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
     sp.sld = SAMPLE_LD;
     sp.srb = at<int32_t>(a, L.srb);
     sp.sre = at<int32_t>(a, L.sre);
-    sp.wait_ns = o.wait_ns;
     DSA_LAUNCH(launch_sample(tm_q, sp, n_pairs(rs), stream));
     if (sp.split) {
       SampleTauParams tp{};
@@ -389,7 +388,6 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
   cp.plan = PLAN_MAIN;
   cp.reverse_units = o.reverse_units;
   cp.withhold_first_acc = o.withhold;
-  cp.wait_ns = o.wait_ns;
   cp.k_scale = ks_raw;
   cp.q_scale = q_scale;
   cp.w = w;
@@ -853,6 +851,7 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   pp.unit_start = at<int32_t>(a, L.unit_start);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = st;
+  pp.wait_ns = o.wait_ns;
   DSA_LAUNCH(launch_plan(pp, stream));
 
   ScoreParams cp{};
@@ -860,7 +859,6 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   cp.mode = MODE_STORE;
   cp.chunk_tiles = pp.chunk_tiles;
   cp.reverse_units = o.reverse_units;
-  cp.wait_ns = o.wait_ns;
   cp.k_scale = k_scale;
   cp.q_scale = q_scale;
   cp.w = w;
@@ -928,6 +926,7 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   pp.unit_start = at<int32_t>(a, L.unit_start);
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = at<Stats>(a, L.stats);
+  pp.wait_ns = o.wait_ns;
   DSA_LAUNCH(launch_plan(pp, stream));
   a->profiled = false;
   return enqueue_matrix_select(a, rs, K, o, scores, ld, pp, max_units, out_idx, stream);
@@ -964,6 +963,7 @@ int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const 
   pp.unit_start = reinterpret_cast<int32_t*>(base + L.unit_start);
   pp.failed_rows = reinterpret_cast<int32_t*>(base + L.failed);
   pp.stats = reinterpret_cast<Stats*>(base + L.stats);
+  pp.wait_ns = o.wait_ns;
   DSA_LAUNCH(launch_plan(pp, stream));
   SelectParams sel{};
   sel.rs = rs;
@@ -976,6 +976,63 @@ int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld, const 
   sel.out = out_idx;
   sel.stats = pp.stats;
   DSA_LAUNCH(launch_select(sel, 2 * o.grid, stream));
+  return DSA_OK;
+}
+
+int dsa_indexer_math_control(const uint8_t* q_fp8, const float* q_scale, const uint8_t* k_fp8, const float* k_scale,
+                             const float* w, const int32_t* row_begin, const int32_t* row_end, int Q, int N, int K,
+                             float* checksum, dsa_stream_t stream_) {
+  int rc = check_dense(q_fp8, q_scale, k_fp8, k_scale, w, row_begin, row_end, Q, N);
+  if (rc != DSA_OK) return rc;
+  if (!checksum || K < 1 || K > DSA_MAX_K) return DSA_ERR_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  CUtensorMap tq, tk;
+  if (!tmap_rows_u8(&tq, q_fp8, (uint64_t)Q * H, H) || !tmap_rows_u8(&tk, k_fp8, N, TILE)) return DSA_ERR_CUDA;
+  const Opts o = read_opts();
+  RowSpace rs{};
+  rs.R = Q;
+  rs.N = N;
+  // the fused call's main plan: the same rows (L > K), groups and units
+  const int chunk = chunk_for(o, rs);
+  std::lock_guard<std::mutex> lk(g_mu);
+  int err = DSA_OK;
+  Arena* a = get_arena(stream, make_layout(Q, n_groups(rs), 0, 0, 0, 0), &err);
+  if (!a) return err;
+  const Layout& L = a->L;
+  PlanParams pp{};
+  pp.rs = rs;
+  pp.plan = PLAN_MAIN;
+  pp.K = K;
+  pp.trivial_len = K;
+  pp.chunk_tiles = chunk;
+  pp.row_begin_in = row_begin;
+  pp.row_end_in = row_end;
+  pp.rb = at<int32_t>(a, L.rb);
+  pp.re = at<int32_t>(a, L.re);
+  pp.groups = at<Group>(a, L.groups);
+  pp.unit_start = at<int32_t>(a, L.unit_start);
+  pp.failed_rows = at<int32_t>(a, L.failed);
+  pp.stats = at<Stats>(a, L.stats);
+  pp.wait_ns = o.wait_ns;
+  DSA_LAUNCH(launch_plan(pp, stream));
+  ScoreParams cp{};
+  cp.rs = rs;
+  cp.mode = MODE_CONTROL;
+  cp.chunk_tiles = chunk;
+  cp.plan = PLAN_MAIN;
+  cp.k_scale = k_scale;
+  cp.q_scale = q_scale;
+  cp.w = w;
+  cp.rb = pp.rb;
+  cp.re = pp.re;
+  cp.groups = pp.groups;
+  cp.unit_start = pp.unit_start;
+  cp.scores = checksum;
+  cp.stats = pp.stats;
+  a->profiled = o.profile;
+  if (o.profile) cudaEventRecord(a->ev0, stream);
+  DSA_LAUNCH(launch_score(tq, tk, cp, o.grid, stream));
+  if (o.profile) cudaEventRecord(a->ev1, stream);
   return DSA_OK;
 }
 

@@ -56,7 +56,11 @@ enum Plan : int { PLAN_MAIN = 0, PLAN_REPAIR = 1, PLAN_SAMPLE = 2 };
 
 // MODE_STORE: fp32 scores to a matrix.  MODE_FILTER: scores at or above the
 // row's threshold become candidates for the candidate selector.
-enum Mode : int { MODE_STORE = 0, MODE_FILTER = 1 };
+// MODE_CONTROL: the math-only control (a measurement, never part of an
+// operator): the same loads, MMAs and barriers, but the epilogue only reads
+// one accumulator column per warp and tile into a checksum and releases the
+// accumulator (no ReLU, head reduction or candidates).
+enum Mode : int { MODE_STORE = 0, MODE_FILTER = 1, MODE_CONTROL = 2 };
 
 // status word bits (per call)
 constexpr int ST_TIMEOUT = 1;
@@ -78,6 +82,7 @@ struct Stats {
   int s_units;
   int next_unit[3];  // per plan (PLAN_*): the next work unit a scorer CTA takes
   int pad[1];
+  unsigned long long wait_ns;  // limit of the call's pipeline waits (read only by a wait that stalls)
 };
 
 // A work group: up to GROUP_ROWS (4) query rows that stream the same keys.  Key range is
@@ -159,7 +164,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Pipeline waits give up after a limit passed in by the host (by default
+// Pipeline waits give up after the call's limit (Stats::wait_ns, by default
 // WAIT_LIMIT_NS; the kernel then records ST_TIMEOUT, lets what it already
 // issued land and returns instead of hanging the GPU).
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
@@ -167,29 +172,35 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 // (they complete within microseconds; the bound only guarantees an end).
 constexpr uint64_t DRAIN_LIMIT_NS = 2000000000ull;
 
+// The call's wait limit, from its status block (the plan kernel stores it).
+__device__ __forceinline__ uint64_t wait_limit(const Stats* st) {
+  const uint64_t l = *(volatile const unsigned long long*)&st->wait_ns;
+  return l ? l : WAIT_LIMIT_NS;
+}
+
 // Bounded wait: true when the phase with `parity` completed; false when the
 // CTA-wide abort flag is set or the time limit passed (then it sets both the
 // abort flag and the status bit).  The polling loop is out of line: the hot
 // loops only pay for one test when the phase has already completed.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                            int* status, uint64_t limit_ns) {
+                                            Stats* st) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 7u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
+      if (globaltimer_ns() - t0 > wait_limit(st)) {
         *abort_flag = 1;
-        atomicOr(status, ST_TIMEOUT);
+        atomicOr(&st->status, ST_TIMEOUT);
         return false;
       }
     }
   }
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, uint64_t limit_ns) {
+                                          Stats* st) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, status, limit_ns);
+  return mbar_wait_slow(bar, parity, abort_flag, st);
 }
 
 // Abort path: wait, bounded by DRAIN_LIMIT_NS and regardless of the abort
@@ -206,7 +217,7 @@ static __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
 // phase) and every lane returns the same value, so code after it that needs
 // a converged warp (tcgen05.ld .sync.aligned, shuffles) never diverges.
 static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                 int* status, uint64_t limit_ns) {
+                                                 Stats* st) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     const bool done = mbar_try_wait(bar, parity);
@@ -220,9 +231,9 @@ static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t bar, uint32_t p
           const uint64_t now = globaltimer_ns();
           if (t0 == 0) {
             t0 = now;
-          } else if (now - t0 > limit_ns) {
+          } else if (now - t0 > wait_limit(st)) {
             *abort_flag = 1;
-            atomicOr(status, ST_TIMEOUT);
+            atomicOr(&st->status, ST_TIMEOUT);
             give_up = 1;
           }
         }
@@ -232,9 +243,9 @@ static __device__ __noinline__ bool mbar_wait_warp_slow(uint32_t bar, uint32_t p
   }
 }
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               int* status, uint64_t limit_ns) {
+                                               Stats* st) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  return mbar_wait_warp_slow(bar, parity, abort_flag, status, limit_ns);
+  return mbar_wait_warp_slow(bar, parity, abort_flag, st);
 }
 
 // Warp-uniform bounded wait for a warp whose wake-up latency has slack (the
@@ -242,8 +253,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
 // takes no issue slots from the epilogue warps that share its SM
 // sub-partition (measured: 1% on the dense scorer).
 static __device__ __noinline__ bool mbar_wait_warp_backoff_slow(uint32_t bar, uint32_t parity,
-                                                         volatile int* abort_flag, int* status,
-                                                         uint64_t limit_ns) {
+                                                         volatile int* abort_flag, Stats* st) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     __nanosleep(128);
@@ -252,9 +262,9 @@ static __device__ __noinline__ bool mbar_wait_warp_backoff_slow(uint32_t bar, ui
     if ((threadIdx.x & 31) == 0) {
       if (*abort_flag) {
         give_up = 1;
-      } else if (globaltimer_ns() - t0 > limit_ns) {
+      } else if (globaltimer_ns() - t0 > wait_limit(st)) {
         *abort_flag = 1;
-        atomicOr(status, ST_TIMEOUT);
+        atomicOr(&st->status, ST_TIMEOUT);
         give_up = 1;
       }
     }
@@ -262,9 +272,9 @@ static __device__ __noinline__ bool mbar_wait_warp_backoff_slow(uint32_t bar, ui
   }
 }
 __device__ __forceinline__ bool mbar_wait_warp_backoff(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                       int* status, uint64_t limit_ns) {
+                                                       Stats* st) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  return mbar_wait_warp_backoff_slow(bar, parity, abort_flag, status, limit_ns);
+  return mbar_wait_warp_backoff_slow(bar, parity, abort_flag, st);
 }
 
 // n arrivals (a warp arriving for itself and n - 1 others), from the lane
@@ -391,6 +401,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+// 32 lanes x 1 column: thread i gets lane (base + i).
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+  return r;
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // 16 lanes x 32 columns: thread t receives, for each block m (0..3) of 8

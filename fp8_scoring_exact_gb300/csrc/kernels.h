@@ -44,6 +44,7 @@ struct PlanParams {
   int32_t* unit_start;         // [G + 1]
   const int32_t* failed_rows;  // repair mode input
   Stats* stats;
+  uint64_t wait_ns;            // main plan: the call's pipeline wait limit (stored in the status block)
 };
 
 struct SampleParams {
@@ -67,7 +68,6 @@ struct SampleParams {
   int64_t sld;
   int32_t* srb;                // [R] first / end pair-grid sample inside the row's range
   int32_t* sre;
-  uint64_t wait_ns;            // limit of every pipeline wait
 };
 
 struct ScoreParams {
@@ -77,7 +77,6 @@ struct ScoreParams {
   int plan;                    // which plan to read (PLAN_*)
   int reverse_units;           // 1: the counter hands the plan's units out last first (a test of order independence)
   int withhold_first_acc;      // test option: the MMA never signals its first accumulator (a wait must run out)
-  uint64_t wait_ns;            // limit of every pipeline wait
   const float* k_scale;        // dense [N] or paged [P * 64]
   const float* q_scale;
   const float* w;
@@ -92,7 +91,7 @@ struct ScoreParams {
   int32_t* cand_idx;           // [R, ROW_SLOTS]
   int32_t* unit_count;         // [R, max_units, 4]: candidates region (c, q) holds (cap + 1: lost some)
   int max_units;               // candidate-region units per row, at most (2 x work units)
-  // MODE_STORE
+  // MODE_STORE (MODE_CONTROL: the checksum word, added to)
   float* scores;               // [slots, ld]
   int64_t ld;
   Stats* stats;

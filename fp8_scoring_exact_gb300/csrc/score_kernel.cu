@@ -62,15 +62,22 @@ constexpr int KEY_STAGE_BYTES = TILE * D;            // 16384
 constexpr int Q_ROW_BYTES = H * D;                   // 8192
 constexpr int Q_SLOT_BYTES = GROUP_ROWS * Q_ROW_BYTES;  // 32768
 
-// paged keys: each key stage also holds the tile's 128 key scales (two pages
-// of 64) and its two page ids.  (Dense keys load their scales directly: the
-// extra barrier work per tile cost more epilogue issue slots, measured 6%.)
+// Key scales in shared memory: paged keys, one block of the tile's 128
+// scales (two pages of 64) per key stage, beside its two page ids; dense
+// keys, a ring of SCALE_RING blocks indexed by the tile count.  A dense
+// block needs no barrier of its own: it lands with the stage's keys (same
+// barrier), and the producer runs at most STAGES + ACC_BUFS - 1 = 7 tiles
+// ahead of the slowest epilogue warp, which reads the scales of a tile
+// before it releases that tile's accumulator, so a block is not refilled
+// while it can still be read.
 constexpr int SCALE_STAGE_BYTES = TILE * 4;
+constexpr int SCALE_RING = 16;
+static_assert(SCALE_RING >= STAGES + ACC_BUFS, "dense scale ring depth");
 
 constexpr uint32_t OFF_KEYS = 0;
 constexpr uint32_t OFF_Q = OFF_KEYS + STAGES * KEY_STAGE_BYTES;
 constexpr uint32_t OFF_SCALE = OFF_Q + 2 * Q_SLOT_BYTES;
-constexpr uint32_t OFF_PAGE = OFF_SCALE + STAGES * SCALE_STAGE_BYTES;  // paged: [STAGES][2] page ids
+constexpr uint32_t OFF_PAGE = OFF_SCALE + SCALE_RING * SCALE_STAGE_BYTES;  // paged: [STAGES][2] page ids
 // per q slot: the unit those q rows belong to, as the MMA and epilogue
 // warps need it (producer-written)
 struct UnitSlot {
@@ -225,7 +232,6 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc->tmem_base;
-  const uint64_t wait_ns = p.wait_ns;
   // producer: key tiles issued and q slots armed (the abort path waits for
   // the last copy of each stage and slot)
   uint32_t kit = 0, q_armed = 0;
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       if (lane == 0) u = atomicAdd(next_unit, 1);
       u = __shfl_sync(0xffffffffu, u, 0);
       const int qs = ui & 1;
-      if (!(ok = mbar_wait_warp_backoff(q_empty(qs), ((ui >> 1) & 1) ^ 1, abort_flag, status, wait_ns))) break;
+      if (!(ok = mbar_wait_warp_backoff(q_empty(qs), ((ui >> 1) & 1) ^ 1, abort_flag, p.stats))) break;
       ++q_armed;
       if (u >= total) {
         // no unit left: the slot says so to the MMA and epilogue warps
@@ -343,10 +349,18 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
           }
           if (__ballot_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, ST_RANGE);
         }
-        if (!(ok = mbar_wait_warp_backoff(key_empty(st), ((kit / STAGES) & 1) ^ 1, abort_flag, status, wait_ns)))
+        if (!(ok = mbar_wait_warp_backoff(key_empty(st), ((kit / STAGES) & 1) ^ 1, abort_flag, p.stats)))
           break;
         const uint32_t kdst = sbase + OFF_KEYS + st * KEY_STAGE_BYTES;
         if (!paged) {
+          // the tile's key scales, 16 bytes per lane into ring block
+          // kit % SCALE_RING (zeros past N), tracked by the stage's barrier
+          const int s0 = t * TILE + 4 * lane;
+          const int nb = max(0, min(16, 4 * (p.rs.N - s0)));
+          cp_async_16(sbase + OFF_SCALE + (kit % SCALE_RING) * SCALE_STAGE_BYTES + lane * 16,
+                      p.k_scale + (nb ? s0 : 0), nb);
+          cp_async_mbar_arrive(key_full(st));
+          __syncwarp();
           if (lane == 0) {
             mbar_arrive_expect_tx(key_full(st), KEY_STAGE_BYTES);
             tma_load_2d(kdst, &tm_k, 0, t * TILE, key_full(st));
@@ -384,7 +398,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       bool ok = true;
       for (; ok; ++ui) {
         const int qs = ui & 1;
-        if (!(ok = mbar_wait(q_full(qs), (ui >> 1) & 1, abort_flag, status, wait_ns))) break;
+        if (!(ok = mbar_wait(q_full(qs), (ui >> 1) & 1, abort_flag, p.stats))) break;
         const UnitSlot* us = unit_slots + qs;
         if (us->nunits < 0) break;  // no unit left
         const int t0 = us->t0, t1 = us->t1;
@@ -392,9 +406,9 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         const uint64_t qdesc = sw128_kmajor_desc(sbase + OFF_Q + qs * Q_SLOT_BYTES);
         for (int t = t0; t < t1; ++t, ++mit, ++ait) {
           const int st = mit % STAGES;
-          if (!(ok = mbar_wait(key_full(st), (mit / STAGES) & 1, abort_flag, status, wait_ns))) break;
+          if (!(ok = mbar_wait(key_full(st), (mit / STAGES) & 1, abort_flag, p.stats))) break;
           const int ab = ait % ACC_BUFS;
-          if (!(ok = mbar_wait(acc_empty(ab), ((ait / ACC_BUFS) & 1) ^ 1, abort_flag, status, wait_ns))) break;
+          if (!(ok = mbar_wait(acc_empty(ab), ((ait / ACC_BUFS) & 1) ^ 1, abort_flag, p.stats))) break;
           tc_fence_after();
           const uint64_t kdesc = sw128_kmajor_desc(sbase + OFF_KEYS + st * KEY_STAGE_BYTES);
           const uint32_t d = tmem_base + ab * ACC_COLS;
@@ -418,11 +432,12 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
     const int kt = quarter * 32 + (lane >> 2) + 8 * (lane & 3);
     uint32_t ait = 0, ui = 0;
     bool ok = true;
+    float checksum = 0.f;  // MODE_CONTROL
     for (; ok; ++ui) {
       // the unit as the producer staged it beside its q rows; the slot is
       // released as soon as this warp holds what it needs in registers
       const int qs = ui & 1;
-      if (!(ok = mbar_wait_warp(q_full(qs), (ui >> 1) & 1, abort_flag, status, wait_ns))) break;
+      if (!(ok = mbar_wait_warp(q_full(qs), (ui >> 1) & 1, abort_flag, p.stats))) break;
       const UnitSlot* us = unit_slots + qs;
       if (us->nunits < 0) break;  // no unit left
       const int t0 = us->t0, t1 = us->t1, nrows = us->nrows;
@@ -469,6 +484,21 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       }
       __syncwarp();
       mbar_arrive_warp(q_empty(qs));
+      if constexpr (MODE == MODE_CONTROL) {
+        // math-only control: wait for each accumulator, fold one of its
+        // columns into the checksum, release it
+        for (int t = t0; t < t1 && ok; ++t, ++ait) {
+          const int ab = ait & (ACC_BUFS - 1);
+          if (!(ok = mbar_wait_warp(acc_full(ab), (ait / ACC_BUFS) & 1, abort_flag, p.stats))) break;
+          tc_fence_after();
+          const uint32_t v = tmem_ld1(tmem_base + ab * ACC_COLS + r * H + ((uint32_t)(quarter * 32) << 16));
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive_warp(acc_empty(ab));
+          checksum += __uint_as_float(v);
+        }
+        continue;
+      }
       for (int t = t0; t < t1 && ok; ++t, ++ait) {
         if (split && (int)(ait & 1) != team) continue;  // the other team's tile
         // this thread's key scale, used at the end of the iteration (paged:
@@ -476,19 +506,18 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
         // this warp then releases with the accumulator; the stage cannot be
         // refilled before that, so its full phase is still this tile's)
         const int kst = ait % STAGES;
-        float ks;
+        float ks = 0.f;
         int page = 0;
         if constexpr (paged) {
-          if (!(ok = mbar_wait_warp(key_full(kst), (ait / STAGES) & 1, abort_flag, status, wait_ns))) break;
+          if (!(ok = mbar_wait_warp(key_full(kst), (ait / STAGES) & 1, abort_flag, p.stats))) break;
           ks = stage_scales[kst * TILE + kt];
           page = stage_pages[2 * kst + (kt >> 6)];
-        } else {
-          const int s = t * TILE + kt;
-          ks = s < p.rs.N ? ldg_pinned_f32(&p.k_scale[s]) : 0.f;
         }
         const int ab = ait & (ACC_BUFS - 1);
-        if (!(ok = mbar_wait_warp(acc_full(ab), (ait / ACC_BUFS) & 1, abort_flag, status, wait_ns))) break;
+        if (!(ok = mbar_wait_warp(acc_full(ab), (ait / ACC_BUFS) & 1, abort_flag, p.stats))) break;
         tc_fence_after();
+        // dense: the scales landed with the tile's keys, before its MMA
+        if constexpr (!paged) ks = stage_scales[(ait % SCALE_RING) * TILE + kt];
         float part[4] = {0.f, 0.f, 0.f, 0.f};
         if (active) {
           // four 16x256b.x4 chunks (lanes +0 / +16 x heads 0-31 / 32-63)
@@ -551,6 +580,11 @@ __global__ void __launch_bounds__(SCORE_THREADS, 1)
       if (filter && active && ok && lane == 0)
         p.unit_count[(int64_t)row * p.max_units * UNIT_REGIONS + vc * UNIT_REGIONS + quarter] = min(wcnt, wcap + 1);
     }
+    if constexpr (MODE == MODE_CONTROL) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) checksum += __shfl_xor_sync(0xffffffffu, checksum, o);
+      if (lane == 0) atomicAdd(p.scores, checksum);
+    }
   }
 
   __syncthreads();
@@ -598,6 +632,7 @@ static cudaError_t launch_variant(const CUtensorMap& tm_q, const CUtensorMap& tm
 cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
                          cudaStream_t s) {
   const bool paged = p.rs.paged != 0;
+  if (p.mode == MODE_CONTROL) return paged ? cudaErrorInvalidValue : launch_variant<MODE_CONTROL, false>(tm_q, tm_k, p, grid, s);
   if (p.mode == MODE_FILTER)
     return paged ? launch_variant<MODE_FILTER, true>(tm_q, tm_k, p, grid, s)
                  : launch_variant<MODE_FILTER, false>(tm_q, tm_k, p, grid, s);

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
   } else if (p.plan == PLAN_MAIN) {
     if (tid == 0) {
       Stats z = {};
+      z.wait_ns = p.wait_ns;
       *p.stats = z;
     }
     __syncthreads();
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
   // thread 0 waits (bounded) and the CTA follows its result; pend = the
   // parity of the phase whose copy or MMA is outstanding (at most one)
   uint32_t pend = 0;
-  if (tid == 0) misc[6] = mbar_wait(bar, 0, abort_flag, &p.stats->status, p.wait_ns) ? 1 : 0;
+  if (tid == 0) misc[6] = mbar_wait(bar, 0, abort_flag, p.stats) ? 1 : 0;
   __syncwarp();
   __syncthreads();
   bool ok = misc[6] != 0;
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     if (tt + 1 < tt_end) fetch(tt + 1);
     // phase 0 was the q load; this CTA's i-th MMA commit completes phase i + 1
     pend = (tt - tt_begin + 1) & 1;
-    if (tid == 0) misc[6] = mbar_wait(bar, pend, abort_flag, &p.stats->status, p.wait_ns) ? 1 : 0;
+    if (tid == 0) misc[6] = mbar_wait(bar, pend, abort_flag, p.stats) ? 1 : 0;
     __syncwarp();
     __syncthreads();
     ok = misc[6] != 0;

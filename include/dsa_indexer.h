@@ -215,6 +215,26 @@ DSA_API int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld
                                                  int32_t* out_idx, dsa_stream_t stream);
 
 /*
+ * Math-only control (a measurement, not an operator; section 5.2 of the
+ * indexer study, "Math-only control"): the fused operator's plan and its main
+ * scorer with the same work units, tile loads, tcgen05 MMAs and barriers, but
+ * an epilogue that only reads one accumulator column per warp and tile, adds
+ * it to a checksum and releases the accumulator: no ReLU, head reduction,
+ * threshold, candidates or selection, and no sampled threshold before it.
+ * Timing it against dsa_indexer_topk on the same inputs shows how much of
+ * the main kernel's time the score reduction and candidate filter still
+ * add.  Same arguments as dsa_indexer_topk; instead of indices it adds the
+ * checksum (meaningless as a value) to *checksum (one device float).  With
+ * DSA_OPT_PROFILE set, dsa_indexer_profiled_main_ms reports its scorer.
+ */
+DSA_API int dsa_indexer_math_control(const uint8_t* q_fp8, const float* q_scale,
+                                     const uint8_t* k_fp8, const float* k_scale,
+                                     const float* w,
+                                     const int32_t* row_begin, const int32_t* row_end,
+                                     int Q, int N, int K,
+                                     float* checksum, dsa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports the device status of the most recent
  * call enqueued on it: DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_RANGE (or
  * DSA_ERR_CUDA if synchronising failed).  failures_out (may be NULL) receives

@@ -215,6 +215,22 @@ def test_bounded_wait_runs_out_and_the_next_call_is_exact(B):
     assert check_dense_rows(inp, out, range(inp.Q)) == {}
 
 
+def test_math_control_runs_the_main_plan(B):
+    """The math-only control (a measurement entry point) runs the fused call's
+    main scorer without its score reduction and filter: it completes with a
+    clean status and a finite checksum, and leaves the fused call exact."""
+    import torch
+    inp = S.make_dense(16, 20000, K=512, seed=62, causal=True)
+    args = dense_args(inp)
+    cs = B.math_control(*args, K=inp.K)
+    torch.cuda.synchronize()
+    _status_ok(B)
+    assert np.isfinite(cs.item())
+    out = B.indexer_topk(*args, K=inp.K).cpu().numpy()
+    _status_ok(B)
+    assert check_dense_rows(inp, out, range(inp.Q)) == {}
+
+
 # ----------------------------------------------------------------- repair ----
 @pytest.mark.parametrize("bias,kind", [(1 << 31, "underflow"), (-(1 << 33), "overflow")])
 def test_forced_repair_is_exact(B, bias, kind):
