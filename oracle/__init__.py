@@ -26,9 +26,15 @@ How (plain, slow, exact):
 compare-and-append, four-pass radix select, certificate; section 3.2) in plain
 Python for unit tests of that logic.  `checks.py` holds the parity criteria.
 
+`sparse_attention.py` is the oracle of the step downstream of the indexer
+(contest write-up, "DSA Sparse Attention"): attention of each query token
+over the KV entries its top-K indices name, base-2 softmax, 512-dim output
+and log-sum-exp, in float64.
+
 Pins: tests/test_oracle_*.py check every function here against the format
 definition, torch's independent float8 decoder, Python-integer brute force,
-hand-computed worked examples, subset enumeration and invariants.
+hand-computed worked examples, closed-form special cases, subset enumeration
+and invariants.
 """
 
-from . import e4m3, indexer, select, checks  # noqa: F401
+from . import e4m3, indexer, select, checks, sparse_attention  # noqa: F401
