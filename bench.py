@@ -289,6 +289,64 @@ def fp8_peak_probe(device, seconds=2.0, n=8192):
         return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
 
 
+# ------------------------------------------------ sparse-attention decode --
+def sparse_attention_leg(args, binding, device, flush, heads=16):
+    """The step downstream of the indexer (contest write-up, "DSA Sparse
+    Attention"): the paged decode batch's top-2048 slots (the paged indexer's
+    own result on that workload) feed the sparse-attention decode over a bf16
+    latent cache (512 + 64 dims per slot) with the same page layout, `heads`
+    heads per token.  The cache and queries are seeded Gaussian values drawn
+    on the device.  Bytes = every valid slot's 1152-byte row once per token
+    (tokens do not share their gathers) + queries + output."""
+    import torch
+    from fp8_scoring_exact_gb300 import synthetic
+    ip = synthetic.make_config(4)
+    host = [np.ascontiguousarray(a) for a in (ip.q, ip.q_scale, ip.k_cache, ip.k_cache_scale, ip.w,
+                                              ip.block_table, ip.seq_lens)]
+    dev = [torch.from_numpy(a).to(device) for a in host]
+    idx = binding.indexer_topk_paged(*dev, K=ip.K).reshape(-1, ip.K)
+    rc, _ = binding.last_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} from the indexer feeding the sparse attention")
+    del dev
+    T, slots = idx.shape[0], ip.k_cache.shape[0] * 64
+    g = torch.Generator(device=device)
+    g.manual_seed(4)
+    ckv = torch.randn((slots, 512), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    kpe = torch.randn((slots, 64), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    qn = torch.randn((T, heads, 512), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    qp = torch.randn((T, heads, 64), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    out = torch.empty((T, heads, 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((T, heads), dtype=torch.float32, device=device)
+    scale = synthetic.sm_scale_default()
+    for _ in range(max(1, args.warmup)):
+        binding.sparse_attention(qn, qp, ckv, kpe, idx, scale, out=out, lse=lse)
+    torch.cuda.synchronize(device)
+    if binding.sparse_attention_last_status() != 0:
+        raise RuntimeError("sparse attention status")
+    stream = torch.cuda.current_stream(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        binding.sparse_attention(qn, qp, ckv, kpe, idx, scale, out=out, lse=lse)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    ms = statistics.mean([a.elapsed_time(b) for a, b in ev])
+    valid = int((idx >= 0).sum().item())
+    nbytes = valid * (512 + 64) * 2 + T * heads * 576 * 2 + T * heads * (512 * 2 + 4) + T * ip.K * 4
+    flop = valid * heads * 2 * (576 + 512)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm = load_peaks()["hbm_gbs"]
+    del ckv, kpe
+    return {"ms_per_step": ms, "tokens": T, "heads": heads, "K": ip.K, "valid_slots": valid,
+            "bytes_per_step": nbytes, "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm,
+            "tflops": flop / (ms * 1e-3) / 1e12,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm},
+            "note": "dsa_sparse_attention over the paged decode batch's own top-2048 slots (64 sequences x 2 "
+                    "tokens), bf16 latent cache 512+64 per slot, L2 flushed before each step"}
+
+
 # ------------------------------------------------------------ GPU arm -------
 def _e2e(args, dev, host, out, stream, world, device, call, R, host_call=None):
     """Same metric through the public API with host buffers: every step copies
@@ -499,6 +557,7 @@ def run_ours(args, rank, world, device):
                            "(whole call - control) / whole call"}
 
     fp8_probe = fp8_peak_probe(device) if "fp8peak" in legs else None
+    sparse = sparse_attention_leg(args, binding, device, flush) if "sparse" in legs else None
 
     # end to end through the public API from pinned host buffers
     e2e = None
@@ -556,6 +615,7 @@ def run_ours(args, rank, world, device):
         "graph": graph,
         "select": select,
         "math_control": control,
+        "sparse_attention": sparse,
         "failures": counters,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -666,9 +726,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override: causal workload with this many query rows")
     ap.add_argument("--keys", type=int, default=0, help="override: causal workload with this many keys")
-    ap.add_argument("--legs", default="fused,unfused,graph,select,control,fp8peak,e2e",
+    ap.add_argument("--legs", default="fused,unfused,graph,select,control,fp8peak,sparse,e2e",
                     help="comma list of legs to run besides the timed fused leg "
-                         "(unfused, graph, select, control, fp8peak, e2e)")
+                         "(unfused, graph, select, control, fp8peak, sparse, e2e)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -40,6 +40,8 @@ SIGNATURES = {
     "dsa_indexer_topk_from_scores": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_topk_from_scores_noalloc": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _P]),
     "dsa_indexer_math_control": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "dsa_sparse_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P]),
+    "dsa_sparse_attention_last_status": (_I, [_P]),
     "dsa_indexer_last_device_status": (_I, [_P, _P]),
     "dsa_indexer_last_repaired_rows": (_I, [_P, _P, _I]),
     "dsa_indexer_set_option": (_I, [_I, _I64]),
@@ -260,6 +262,37 @@ def math_control(q, q_scale, k, k_scale, w, row_begin, row_end, K=2048, checksum
                                         _ptr(_dev(checksum, "checksum", torch.float32)), _stream_ptr(stream))
     _check("dsa_indexer_math_control", rc)
     return checksum
+
+
+def sparse_attention(q_nope, q_pe, ckv, kpe, indices, sm_scale, out=None, lse=None, stream=None):
+    """Sparse-attention decode over top-K slots: q_nope [T,H,512], q_pe [T,H,64] bf16,
+    ckv [S,512], kpe [S,64] bf16 (slot-major cache), indices [T,K] int32 (-1: padding).
+    Returns (out [T,H,512] bf16, lse [T,H] fp32, base 2)."""
+    q_nope = _dev(q_nope, "q_nope", torch.bfloat16)
+    q_pe = _dev(q_pe, "q_pe", torch.bfloat16)
+    ckv = _dev(ckv, "ckv", torch.bfloat16)
+    kpe = _dev(kpe, "kpe", torch.bfloat16)
+    indices = _dev(indices, "indices", torch.int32)
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    if tuple(q_nope.shape[2:]) != (512,) or tuple(q_pe.shape) != (T, H, 64):
+        raise ValueError("q_nope must be [T,H,512] and q_pe [T,H,64]")
+    ckv2, kpe2 = ckv.reshape(-1, 512), kpe.reshape(-1, 64)
+    if ckv2.shape[0] != kpe2.shape[0]:
+        raise ValueError("ckv and kpe must hold the same slots")
+    K = indices.shape[-1]
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q_nope.device)
+    rc = lib().dsa_sparse_attention(_ptr(q_nope), _ptr(q_pe), _ptr(ckv2), _ptr(kpe2), _ptr(indices), T, H, K,
+                                    ckv2.shape[0], float(sm_scale), _ptr(_dev(out, "out", torch.bfloat16)),
+                                    _ptr(_dev(lse, "lse", torch.float32)), _stream_ptr(stream))
+    _check("dsa_sparse_attention", rc)
+    return out, lse
+
+
+def sparse_attention_last_status(stream=None) -> int:
+    return int(lib().dsa_sparse_attention_last_status(_stream_ptr(stream)))
 
 
 def last_device_status(stream=None):

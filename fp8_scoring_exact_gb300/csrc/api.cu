@@ -194,14 +194,24 @@ struct Opts {
 
 // Tiles per work unit: the option when set, else 64 for dense rows and 32
 // for paged ones (decode batches mix very short and very long sequences:
-// smaller units balance the long tail), halved (down to 16) while the row
-// groups would give fewer than 4 units per CTA.  Measured on GB300.
+// smaller units balance the long tail), halved (down to 8) while the row
+// groups would give fewer than 4 units per CTA (few rows with long
+// histories: the key dimension supplies the parallelism).  Measured on
+// GB300.  Never so small that a row's candidate regions (4 per unit, twice
+// that for paged rows) exceed what the candidate selector reads: such rows
+// would all fail their certificate and go to repair.
+constexpr int REPAIR_CHUNK = 8;  // tiles per unit of the repair scorer
+int min_chunk_for(const RowSpace& rs) {
+  const int tiles = ceil_div(rs.N, TILE);
+  const int per_unit = UNIT_REGIONS * (rs.paged ? 2 : 1);
+  return ceil_div(tiles * per_unit, CAND_MAX_REGIONS);
+}
 int chunk_for(const Opts& o, const RowSpace& rs) {
   if (o.chunk > 0) return o.chunk;
   const int64_t tiles = (int64_t)n_groups(rs) * ceil_div(rs.N, TILE);
   int c = rs.paged ? 32 : 64;
-  while (c > 16 && tiles / c < 4LL * o.grid) c >>= 1;
-  return c;
+  while (c > 8 && tiles / c < 4LL * o.grid) c >>= 1;
+  return std::max(c, min_chunk_for(rs));
 }
 
 // Tiles per work unit of the selection over a stored score matrix: 256
@@ -214,7 +224,7 @@ int matrix_chunk_for(const Opts& o, const RowSpace& rs) {
   const int64_t tiles = (int64_t)n_groups(rs) * ceil_div(rs.N, TILE);
   int c = 256;
   while (c > 16 && tiles / c < 8LL * o.grid) c >>= 1;
-  return c;
+  return std::max(c, min_chunk_for(rs));
 }
 
 Opts read_opts() {
@@ -420,15 +430,19 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
   cs.stats = st;
   DSA_LAUNCH(launch_cand_select(cs, 3 * o.grid, stream));  // 3 CTAs per SM (shared memory)
 
-  // exact repair of rows whose certificate failed
+  // exact repair of rows whose certificate failed: a store-mode scorer has
+  // no candidate regions, so its units are short (REPAIR_CHUNK tiles) and
+  // even a single failed long row is spread over many SMs
   PlanParams rp = pp;
   rp.plan = PLAN_REPAIR;
+  rp.chunk_tiles = REPAIR_CHUNK;
   rp.groups = at<Group>(a, L.rgroups);
   rp.unit_start = at<int32_t>(a, L.runit_start);
   DSA_LAUNCH(launch_plan(rp, stream));
 
   ScoreParams rcp = cp;
   rcp.withhold_first_acc = 0;
+  rcp.chunk_tiles = REPAIR_CHUNK;
   rcp.mode = MODE_STORE;
   rcp.plan = PLAN_REPAIR;
   rcp.groups = rp.groups;
@@ -493,6 +507,40 @@ void* noalloc_scratch(int* err) {
   }
   g_noalloc_addr[dev] = p;
   return p;
+}
+
+// ------------------------------------------------- sparse-attention scratch --
+// Per (device, stream): the status word and the split partials of
+// dsa_sparse_attention, grown on demand (growing synchronises the device).
+struct AuxScratch {
+  uint8_t* base = nullptr;
+  size_t cap = 0;
+};
+std::map<std::pair<int, cudaStream_t>, AuxScratch> g_aux;  // guarded by g_mu
+
+uint8_t* aux_scratch(cudaStream_t stream, size_t need, int* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    *err = DSA_ERR_CUDA;
+    return nullptr;
+  }
+  AuxScratch& a = g_aux[{dev, stream}];
+  if (a.cap < need) {
+    if (a.base) {
+      cudaDeviceSynchronize();
+      cudaFree(a.base);
+      a.base = nullptr;
+      a.cap = 0;
+    }
+    const size_t want = align_up(need + need / 8, 1 << 20);
+    if (cudaMalloc(&a.base, want) != cudaSuccess) {
+      cudaGetLastError();
+      *err = DSA_ERR_CUDA;
+      return nullptr;
+    }
+    a.cap = want;
+  }
+  return a.base;
 }
 
 // ----------------------------------------------------- host-buffer entry --
@@ -1036,6 +1084,65 @@ int dsa_indexer_math_control(const uint8_t* q_fp8, const float* q_scale, const u
   return DSA_OK;
 }
 
+int dsa_sparse_attention(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* ckv, const uint16_t* kpe,
+                         const int32_t* indices, int T, int H, int K, int num_slots, float sm_scale, uint16_t* out,
+                         float* lse, dsa_stream_t stream_) {
+  if (!q_nope || !q_pe || !ckv || !kpe || !indices || !out || !lse) return DSA_ERR_ARG;
+  if (T <= 0 || H <= 0 || (H % 16) || K < 1 || num_slots <= 0 || !(sm_scale > 0.f)) return DSA_ERR_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv) || !aligned16(kpe) || !aligned16(out))
+    return DSA_ERR_ARG;
+  if ((int64_t)T * H >= (1ll << 31) / 512 || (int64_t)T * K >= (1ll << 31) || T > 65535) return DSA_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const Opts o = read_opts();
+  // splits of each token's key list: about two CTAs per SM in one wave, at
+  // least 64 keys per split
+  const int ctas = T * (H / 16);
+  int splits = std::max(1, std::min(2 * o.grid / std::max(ctas, 1), K / 64));
+  int per = ceil_div(ceil_div(K, splits), 32) * 32;
+  splits = ceil_div(K, per);
+  const int64_t rows = (int64_t)T * H;
+  const size_t off_ml = 256, off_o = align_up(off_ml + (size_t)splits * rows * 8, 256);
+  const size_t need = splits > 1 ? off_o + (size_t)splits * rows * 512 * 4 : 256;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int err = DSA_OK;
+  uint8_t* base = aux_scratch(stream, need, &err);
+  if (!base) return err;
+  SparseAttnParams p{};
+  p.q_nope = reinterpret_cast<const __nv_bfloat16*>(q_nope);
+  p.q_pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
+  p.ckv = reinterpret_cast<const __nv_bfloat16*>(ckv);
+  p.kpe = reinterpret_cast<const __nv_bfloat16*>(kpe);
+  p.idx = indices;
+  p.T = T;
+  p.H = H;
+  p.K = K;
+  p.num_slots = num_slots;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.splits = splits;
+  p.keys_per_split = per;
+  p.part_ml = reinterpret_cast<float2*>(base + off_ml);
+  p.part_o = reinterpret_cast<float*>(base + off_o);
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = reinterpret_cast<int*>(base);
+  if (cudaMemsetAsync(p.status, 0, sizeof(int), stream) != cudaSuccess) return DSA_ERR_CUDA;
+  DSA_LAUNCH(launch_sparse_attn(p, stream));
+  return DSA_OK;
+}
+
+int dsa_sparse_attention_last_status(dsa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_aux.find({dev, stream});
+  if (it == g_aux.end() || !it->second.base) return DSA_OK;
+  int st = 0;
+  if (cudaMemcpy(&st, it->second.base, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  return (st & ST_RANGE) ? DSA_ERR_RANGE : DSA_OK;
+}
+
 int dsa_indexer_last_device_status(dsa_stream_t stream_, int32_t* failures_out) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
@@ -1186,7 +1293,7 @@ int dsa_indexer_release(void) {
   }
   g_host.clear();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_arenas.empty()) cudaDeviceSynchronize();
+  if (!g_arenas.empty() || !g_aux.empty()) cudaDeviceSynchronize();
   for (auto& kv : g_arenas) {
     int cur = 0;
     cudaGetDevice(&cur);
@@ -1197,6 +1304,14 @@ int dsa_indexer_release(void) {
     cudaSetDevice(cur);
   }
   g_arenas.clear();
+  for (auto& kv : g_aux) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(kv.first.first);
+    if (kv.second.base) cudaFree(kv.second.base);
+    cudaSetDevice(cur);
+  }
+  g_aux.clear();
   return DSA_OK;
 }
 

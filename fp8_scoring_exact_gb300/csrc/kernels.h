@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -227,6 +228,26 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// Sparse-attention decode over the indexer's slots (sparse_attn.cu): grid
+// (H / 16, T, splits); each split of a token's key list leaves an
+// unnormalised partial output and its (max, sum) for the merge kernel, or,
+// with one split, the result.
+struct SparseAttnParams {
+  const __nv_bfloat16* q_nope;  // [T, H, 512]
+  const __nv_bfloat16* q_pe;    // [T, H, 64]
+  const __nv_bfloat16* ckv;     // [num_slots, 512]
+  const __nv_bfloat16* kpe;     // [num_slots, 64]
+  const int32_t* idx;           // [T, K] slots (-1: padding)
+  int T, H, K, num_slots;
+  float scale_log2;             // sm_scale * log2(e)
+  int splits, keys_per_split;
+  float* part_o;                // [splits, T, H, 512]
+  float2* part_ml;              // [splits, T, H]: running max (base-2 units) and sum
+  __nv_bfloat16* out;           // [T, H, 512]
+  float* lse;                   // [T, H]
+  int* status;                  // ST_RANGE: a slot >= num_slots was named (read as padding)
+};
+
 // One bit per device (0..63) for a per-device, once-only host action.
 struct DeviceFlags {
   std::atomic<uint64_t> bits{0};
@@ -259,6 +280,7 @@ cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
 cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s);
 cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStream_t s);
+cudaError_t launch_sparse_attn(const SparseAttnParams& p, cudaStream_t s);
 
 // number of work groups of G query rows for a row space
 template <int G>

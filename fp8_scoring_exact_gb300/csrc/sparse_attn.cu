@@ -1,0 +1,377 @@
+// sparse_attn.cu -- sparse-attention decode over the indexer's top-K slots.
+//
+// For each query token t and head h (contest write-up, "DSA Sparse
+// Attention"): gather the KV entries the token's index list names, logits
+// z_j = q_nope . ckv[i_j] + q_pe . kpe[i_j], a base-2 softmax of
+// u_j = z_j * sm_scale * log2(e), out = sum_j p_j ckv[i_j] (512 dims) and
+// lse = log2(sum_j 2^u_j).
+//
+// The step is bound by the gather (2048 rows x 1152 bytes per token, read
+// once for all of the token's heads: ~30 FLOP per byte), so the contraction
+// runs on warp-level bf16 tensor-core MMAs (m16n8k16, fp32 accumulation),
+// which keep the arithmetic well below the gather time, with the token's 16
+// heads as the MMA's M dimension.
+//
+// One CTA (4 warps) per (token, block of 16 heads, split of the key list):
+//   - the 16 query rows (q_nope | q_pe, 576 dims) are loaded once; warp w
+//     keeps the A fragments of dims [144 w, 144 w + 144) in registers;
+//   - key tiles of 32 slots are gathered (cp.async, 16 bytes per copy, one
+//     1152-byte row per slot; padding slots read as zeros) into a ring of
+//     SA_STAGES shared tiles, SA_STAGES - 1 gathers in flight while a tile
+//     is processed (measured: 32-key tiles in a 2-deep ring beat 16-key
+//     tiles in a 4-deep one, whose per-tile barriers and latency chains
+//     doubled per key);
+//   - QK: warp w multiplies its 144 dims for all 32 keys (partial logits to
+//     shared memory), then all 128 threads sum the 4 partials, apply the
+//     running (online) max and sums of the base-2 softmax per head, and
+//     write the tile's weights as bf16;
+//   - PV: warp w owns output dims [128 w, 128 w + 128): its accumulators are
+//     rescaled by 2^(m_old - m_new) and take the tile's weights times the
+//     tile's ckv rows (ldmatrix.trans).
+// Splits of one token's key list are merged by a second kernel (running max,
+// rescaled sums); a single split writes the result directly.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dsa {
+
+namespace {
+
+constexpr int SA_DC = 512;                 // compressed KV dims (output)
+constexpr int SA_DP = 64;                  // rope dims
+constexpr int SA_DQ = SA_DC + SA_DP;       // 576
+constexpr int SA_HB = 16;                  // heads per CTA (MMA M)
+constexpr int SA_TK = 32;                  // keys per tile
+constexpr int SA_STAGES = 2;               // gathered tiles in the ring
+constexpr int SA_NB = SA_TK / 8;           // key n-blocks of the logit MMAs
+constexpr int SA_KPT = SA_TK / 8;          // keys per thread in the softmax (16 heads x SA_TK keys / 128)
+static_assert(SA_TK % 16 == 0 && SA_KPT % 2 == 0, "tile of whole 16-key k-steps");
+constexpr int SA_THREADS = 128;
+constexpr int SA_ROW = SA_DQ + 8;          // shared row stride (bf16): 1168 bytes, ldmatrix without conflicts
+constexpr int SA_CHUNKS = SA_DQ * 2 / 16;  // 16-byte copies per row: 72
+constexpr int SA_SROW = SA_TK + 8;         // partial-logit row stride (floats): float2 stores without conflicts
+constexpr int SA_PROW = SA_TK + 8;         // weight row stride (bf16): 48 bytes, ldmatrix without conflicts
+
+constexpr uint32_t SA_OFF_Q = 0;
+constexpr uint32_t SA_OFF_KV = SA_OFF_Q + SA_HB * SA_ROW * 2;               // 18688
+constexpr uint32_t SA_KV_BYTES = SA_TK * SA_ROW * 2;                        // 18688
+constexpr uint32_t SA_OFF_S = SA_OFF_KV + SA_STAGES * SA_KV_BYTES;
+constexpr uint32_t SA_OFF_P = SA_OFF_S + 4 * SA_HB * SA_SROW * 4;
+constexpr uint32_t SA_OFF_STAT = SA_OFF_P + SA_HB * SA_PROW * 2;
+constexpr uint32_t SA_OFF_IDX = SA_OFF_STAT + 3 * SA_HB * 4;                // m, l, alpha per head
+constexpr uint32_t SA_SMEM = SA_OFF_IDX + SA_STAGES * SA_TK * 4;
+static_assert(SA_OFF_KV % 16 == 0 && SA_OFF_S % 16 == 0 && SA_OFF_P % 16 == 0, "sparse attention layout");
+static_assert(SA_SMEM <= 113 * 1024, "two CTAs per SM");
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float exp2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+}  // namespace
+
+__global__ void __launch_bounds__(SA_THREADS, 2) sparse_attn_kernel(const SparseAttnParams p) {
+  pdl_enter();
+  extern __shared__ __align__(16) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  float* sS = reinterpret_cast<float*>(smem + SA_OFF_S);
+  __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(smem + SA_OFF_P);
+  float* sM = reinterpret_cast<float*>(smem + SA_OFF_STAT);
+  float* sL = sM + SA_HB;
+  float* sA = sL + SA_HB;
+  int* sIdx = reinterpret_cast<int*>(smem + SA_OFF_IDX);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hb = blockIdx.x, t = blockIdx.y, split = blockIdx.z;
+  const int H = p.H, K = p.K;
+  const int j_begin = split * p.keys_per_split;
+  const int j_end = min(K, j_begin + p.keys_per_split);
+  const int n_tiles = j_end > j_begin ? ceil_div(j_end - j_begin, SA_TK) : 0;
+  const int32_t* idx_row = p.idx + (int64_t)t * K;
+  const int64_t qrow0 = (int64_t)t * H + hb * SA_HB;  // first (token, head) row of this CTA
+
+  // query rows: 16 x (512 + 64) bf16
+  for (int c = tid; c < SA_HB * SA_CHUNKS; c += SA_THREADS) {
+    const int r = c / SA_CHUNKS, k = c % SA_CHUNKS;
+    const void* src = k < SA_DC / 8 ? (const void*)(p.q_nope + (qrow0 + r) * SA_DC + 8 * k)
+                                    : (const void*)(p.q_pe + (qrow0 + r) * SA_DP + 8 * (k - SA_DC / 8));
+    cp_async_16(sbase + SA_OFF_Q + (r * SA_ROW + 8 * k) * 2, src, 16);
+  }
+  // the key tile starting at list position j0 into buffer b: the slots of the
+  // tile (-1: padding or past the list; a slot outside the cache is
+  // reported and read as padding), then one 1152-byte row per slot
+  // (every copying thread reads its row's slot itself: no barrier between
+  // the slot list and the copies)
+  auto gather = [&](int j0, int b) {
+    if (tid < SA_TK) {
+      const int j = j0 + tid;
+      int s = j < j_end ? __ldg(&idx_row[j]) : -1;
+      if (s >= p.num_slots) {
+        atomicOr(p.status, ST_RANGE);
+        s = -1;
+      }
+      sIdx[b * SA_TK + tid] = s;
+    }
+    const uint32_t dst0 = sbase + SA_OFF_KV + b * SA_KV_BYTES;
+    for (int c = tid; c < SA_TK * SA_CHUNKS; c += SA_THREADS) {
+      const int r = c / SA_CHUNKS, k = c % SA_CHUNKS;
+      const int j = j0 + r;
+      int s = j < j_end ? __ldg(&idx_row[j]) : -1;
+      if (s >= p.num_slots) s = -1;
+      const int64_t slot = s < 0 ? 0 : s;
+      const void* src = k < SA_DC / 8 ? (const void*)(p.ckv + slot * SA_DC + 8 * k)
+                                      : (const void*)(p.kpe + slot * SA_DP + 8 * (k - SA_DC / 8));
+      cp_async_16(dst0 + (r * SA_ROW + 8 * k) * 2, src, s < 0 ? 0 : 16);
+    }
+  };
+  if (tid < SA_HB) {
+    sM[tid] = -__int_as_float(0x7f800000);
+    sL[tid] = 0.f;
+  }
+  // prologue: the first SA_STAGES - 1 tiles (one commit group each, empty
+  // groups past the end keep the group count uniform)
+#pragma unroll
+  for (int i = 0; i < SA_STAGES - 1; ++i) {
+    if (i < n_tiles) gather(j_begin + i * SA_TK, i);
+    cp_async_commit();
+  }
+
+  // output accumulators: 16 heads x 128 dims per warp = 16 n-blocks
+  float acc[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  uint32_t qa[9][4];  // this warp's 9 k-steps of the query rows (A fragments)
+  const int kd0 = warp * 144;  // this warp's logit dims
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int b = it % SA_STAGES;
+    cp_async_wait<SA_STAGES - 2>();
+    __syncthreads();  // tile `it` landed for every thread; the previous tile's readers are done
+    if (it == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 9; ++ks) {
+        const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int col = kd0 + 16 * ks + 8 * (lane >> 4);
+        ldsm_x4(sbase + SA_OFF_Q + (row * SA_ROW + col) * 2, qa[ks]);
+      }
+    }
+    // refill the buffer the previous tile used
+    if (it + SA_STAGES - 1 < n_tiles) gather(j_begin + (it + SA_STAGES - 1) * SA_TK, (it + SA_STAGES - 1) % SA_STAGES);
+    cp_async_commit();
+
+    // ---- partial logits over this warp's 144 dims: 16 heads x SA_TK keys
+    const uint32_t kv = sbase + SA_OFF_KV + b * SA_KV_BYTES;
+    float s[SA_NB][4];
+#pragma unroll
+    for (int nb = 0; nb < SA_NB; ++nb) {
+      s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
+      const int krow = 8 * nb + (lane & 7);
+#pragma unroll
+      for (int ks2 = 0; ks2 < 4; ++ks2) {  // k-steps 2 ks2, 2 ks2 + 1
+        uint32_t bf[4];
+        ldsm_x4(kv + (krow * SA_ROW + kd0 + 32 * ks2 + 8 * (lane >> 3)) * 2, bf);
+        mma_bf16(s[nb], qa[2 * ks2], bf[0], bf[1]);
+        mma_bf16(s[nb], qa[2 * ks2 + 1], bf[2], bf[3]);
+      }
+      uint32_t bf[2];
+      ldsm_x2(kv + (krow * SA_ROW + kd0 + 128 + 8 * ((lane >> 3) & 1)) * 2, bf);
+      mma_bf16(s[nb], qa[8], bf[0], bf[1]);
+    }
+    {
+      float* sw = sS + warp * SA_HB * SA_SROW;
+      const int r0 = lane >> 2, c0 = 2 * (lane & 3);
+#pragma unroll
+      for (int nb = 0; nb < SA_NB; ++nb) {
+        *reinterpret_cast<float2*>(&sw[r0 * SA_SROW + 8 * nb + c0]) = make_float2(s[nb][0], s[nb][1]);
+        *reinterpret_cast<float2*>(&sw[(r0 + 8) * SA_SROW + 8 * nb + c0]) = make_float2(s[nb][2], s[nb][3]);
+      }
+    }
+    __syncthreads();
+
+    // ---- online base-2 softmax: thread (head h, keys SA_KPT kq .. + SA_KPT - 1)
+    {
+      const int h = tid >> 3, kq = tid & 7;
+      float u[SA_KPT];
+      {
+        const int* si = sIdx + b * SA_TK + SA_KPT * kq;
+#pragma unroll
+        for (int i = 0; i < SA_KPT; i += 2) {
+          float2 a = *reinterpret_cast<const float2*>(&sS[(0 * SA_HB + h) * SA_SROW + SA_KPT * kq + i]);
+#pragma unroll
+          for (int w = 1; w < 4; ++w) {
+            const float2 x = *reinterpret_cast<const float2*>(&sS[(w * SA_HB + h) * SA_SROW + SA_KPT * kq + i]);
+            a.x += x.x;
+            a.y += x.y;
+          }
+          u[i] = si[i] >= 0 ? a.x * p.scale_log2 : -__int_as_float(0x7f800000);
+          u[i + 1] = si[i + 1] >= 0 ? a.y * p.scale_log2 : -__int_as_float(0x7f800000);
+        }
+      }
+      float tmax = u[0];
+#pragma unroll
+      for (int i = 1; i < SA_KPT; ++i) tmax = fmaxf(tmax, u[i]);
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+      const float m_old = sM[h];
+      const float m_new = fmaxf(m_old, tmax);
+      const float m_use = m_new == -__int_as_float(0x7f800000) ? 0.f : m_new;
+      // weights rounded to bf16 for the PV product; the sums use the
+      // rounded values, so the normalisation matches what is accumulated
+      float psum = 0.f;
+      __nv_bfloat162* pp = reinterpret_cast<__nv_bfloat162*>(sP + h * SA_PROW + SA_KPT * kq);
+#pragma unroll
+      for (int i = 0; i < SA_KPT; i += 2) {
+        const __nv_bfloat162 w2 = __floats2bfloat162_rn(exp2_approx(u[i] - m_use), exp2_approx(u[i + 1] - m_use));
+        const float2 f2 = __bfloat1622float2(w2);
+        psum += f2.x + f2.y;
+        pp[i / 2] = w2;
+      }
+      psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+      psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+      psum += __shfl_xor_sync(0xffffffffu, psum, 4);
+      __syncwarp();
+      if (kq == 0) {
+        const float alpha = exp2_approx(m_old - m_use);  // 0 when m_old is -inf
+        sA[h] = alpha;
+        sL[h] = sL[h] * alpha + psum;
+        sM[h] = m_new;
+      }
+    }
+    __syncthreads();
+
+    // ---- PV: this warp's 128 output dims, SA_TK / 16 key k-steps
+    {
+      const float a_lo = sA[lane >> 2], a_hi = sA[(lane >> 2) + 8];
+#pragma unroll
+      for (int nb = 0; nb < 16; ++nb) {
+        acc[nb][0] *= a_lo;
+        acc[nb][1] *= a_lo;
+        acc[nb][2] *= a_hi;
+        acc[nb][3] *= a_hi;
+      }
+      const int d0 = warp * 128;
+#pragma unroll
+      for (int ks = 0; ks < SA_TK / 16; ++ks) {
+        uint32_t pa[4];
+        const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
+        ldsm_x4(sbase + SA_OFF_P + (row * SA_PROW + 16 * ks + 8 * (lane >> 4)) * 2, pa);
+        const int krow = 16 * ks + row;
+#pragma unroll
+        for (int nb2 = 0; nb2 < 8; ++nb2) {
+          uint32_t bf[4];
+          ldsm_x4_t(kv + (krow * SA_ROW + d0 + 16 * nb2 + 8 * (lane >> 4)) * 2, bf);
+          mma_bf16(acc[2 * nb2], pa, bf[0], bf[1]);
+          mma_bf16(acc[2 * nb2 + 1], pa, bf[2], bf[3]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- this split's result: rows r0 = lane / 4 and r0 + 8, dims
+  // 128 warp + 8 nb + 2 (lane % 4) + {0, 1}
+  const int r0 = lane >> 2;
+  const int64_t ro0 = qrow0 + r0, ro1 = ro0 + 8;
+  const int dbase = warp * 128 + 2 * (lane & 3);
+  if (p.splits == 1) {
+    const float l0 = sL[r0], l1 = sL[r0 + 8];
+    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+    for (int nb = 0; nb < 16; ++nb) {
+      *reinterpret_cast<__nv_bfloat162*>(p.out + ro0 * SA_DC + dbase + 8 * nb) =
+          __floats2bfloat162_rn(acc[nb][0] * i0, acc[nb][1] * i0);
+      *reinterpret_cast<__nv_bfloat162*>(p.out + ro1 * SA_DC + dbase + 8 * nb) =
+          __floats2bfloat162_rn(acc[nb][2] * i1, acc[nb][3] * i1);
+    }
+    if (tid < SA_HB) {
+      const float l = sL[tid];
+      p.lse[qrow0 + tid] = l > 0.f ? sM[tid] + __log2f(l) : -__int_as_float(0x7f800000);
+    }
+    return;
+  }
+  float* po = p.part_o + ((int64_t)split * p.T * H) * SA_DC;
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) {
+    *reinterpret_cast<float2*>(po + ro0 * SA_DC + dbase + 8 * nb) = make_float2(acc[nb][0], acc[nb][1]);
+    *reinterpret_cast<float2*>(po + ro1 * SA_DC + dbase + 8 * nb) = make_float2(acc[nb][2], acc[nb][3]);
+  }
+  if (tid < SA_HB) p.part_ml[(int64_t)split * p.T * H + qrow0 + tid] = make_float2(sM[tid], sL[tid]);
+}
+
+// Merge of the splits of one (token, head): one warp, 16 dims per lane.
+constexpr int SM_THREADS = 256;
+__global__ void __launch_bounds__(SM_THREADS) sparse_attn_merge_kernel(const SparseAttnParams p) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (SM_THREADS / 32) + (threadIdx.x >> 5);
+  const int64_t rows = (int64_t)p.T * p.H;
+  if (row >= rows) return;
+  float M = -__int_as_float(0x7f800000);
+  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, p.part_ml[s * rows + row].x);
+  const float m_use = M == -__int_as_float(0x7f800000) ? 0.f : M;
+  float L = 0.f;
+  float o[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = 0.f;
+  for (int s = 0; s < p.splits; ++s) {
+    const float2 ml = p.part_ml[s * rows + row];
+    const float w = exp2_approx(ml.x - m_use);  // 0 for a split with no valid key
+    L += w * ml.y;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + (s * rows + row) * SA_DC + 16 * lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 x = __ldcs(src + i);
+      o[4 * i] += w * x.x;
+      o[4 * i + 1] += w * x.y;
+      o[4 * i + 2] += w * x.z;
+      o[4 * i + 3] += w * x.w;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(p.out + row * SA_DC + 16 * lane);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) dst[i] = __floats2bfloat162_rn(o[2 * i] * inv, o[2 * i + 1] * inv);
+  if (lane == 0) p.lse[row] = L > 0.f ? M + __log2f(L) : -__int_as_float(0x7f800000);
+}
+
+cudaError_t launch_sparse_attn(const SparseAttnParams& p, cudaStream_t s) {
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_attr_once(sparse_attn_kernel, SA_SMEM, attr_set);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(sparse_attn_kernel, dim3(p.H / SA_HB, p.T, p.splits), dim3(SA_THREADS), SA_SMEM, s, p);
+  if (e != cudaSuccess || p.splits == 1) return e;
+  const int64_t rows = (int64_t)p.T * p.H;
+  return launch_pdl(sparse_attn_merge_kernel, dim3((unsigned)ceil_div((int)rows, SM_THREADS / 32)),
+                    dim3(SM_THREADS), 0, s, p);
+}
+
+}  // namespace dsa

@@ -210,3 +210,63 @@ def make_config(cid: int, seed: int | None = None):
     if cid == 4:
         return make_paged(64, 2, seed=seed, name=CONFIG_NAMES[4])
     raise ValueError(cid)
+
+
+# --------------------------------------------------- sparse-attention decode --
+# DeepSeek-V3.2 latent attention geometry: a 512-dim compressed KV entry and a
+# 64-dim rope part per cache slot, bf16; 16 heads (one tensor-parallel shard
+# of 128).  The contest write-up's sparse-attention step names only the shape
+# of the computation; these sizes are the model's.
+SA_DC, SA_DP = 512, 64
+
+
+@dataclass
+class SparseAttnInputs:
+    """One sparse-attention decode problem: bf16 tensors (torch, CPU) and the
+    int32 slot lists (numpy, -1 = padding)."""
+    q_nope: "torch.Tensor"   # bf16 [T, H, 512]
+    q_pe: "torch.Tensor"     # bf16 [T, H, 64]
+    ckv: "torch.Tensor"      # bf16 [S, 512]
+    kpe: "torch.Tensor"      # bf16 [S, 64]
+    indices: np.ndarray      # int32 [T, K]
+    sm_scale: float
+
+    @property
+    def T(self):
+        return self.q_nope.shape[0]
+
+    @property
+    def H(self):
+        return self.q_nope.shape[1]
+
+    @property
+    def K(self):
+        return self.indices.shape[1]
+
+    def valid_indices(self) -> int:
+        return int((self.indices >= 0).sum())
+
+
+def sm_scale_default() -> float:
+    """1 / sqrt(192): the softmax scale of a 128 + 64 dim query-key head."""
+    return 1.0 / float(np.sqrt(192.0))
+
+
+def make_sparse_attention(T: int, H: int, S: int, K: int, *, seed: int = 0, n_valid=None,
+                          indices: np.ndarray | None = None) -> SparseAttnInputs:
+    """q, cache ~ N(0, 1) rounded to bf16; token t gets n_valid[t] distinct
+    random slots of [0, S) (default min(K, S)) then -1 padding, unless
+    `indices` ([T, K] int32) is given."""
+    rng = np.random.default_rng(seed)
+
+    def bf16(shape):
+        return torch.from_numpy(_gauss(rng, shape)).to(torch.bfloat16)
+
+    q_nope, q_pe = bf16((T, H, SA_DC)), bf16((T, H, SA_DP))
+    ckv, kpe = bf16((S, SA_DC)), bf16((S, SA_DP))
+    if indices is None:
+        indices = np.full((T, K), -1, np.int32)
+        for t in range(T):
+            n = min(K, S) if n_valid is None else int(n_valid[t])
+            indices[t, :n] = rng.choice(S, size=n, replace=False)
+    return SparseAttnInputs(q_nope, q_pe, ckv, kpe, np.ascontiguousarray(indices, np.int32), sm_scale_default())

@@ -215,6 +215,39 @@ DSA_API int dsa_indexer_topk_from_scores_noalloc(const float* scores, int64_t ld
                                                  int32_t* out_idx, dsa_stream_t stream);
 
 /*
+ * Sparse-attention decode over the indexer's result (contest write-up, "DSA
+ * Sparse Attention"), the step that consumes the top-K slots: for every query
+ * token t and head h, with u_j = sm_scale * log2(e) * (q_nope[t, h] .
+ * ckv[i_j] + q_pe[t, h] . kpe[i_j]) over the slots i_j listed in
+ * indices[t, :] (negative entries are padding),
+ *
+ *     out[t, h] = sum_j 2^(u_j) ckv[i_j] / sum_j 2^(u_j)       (base-2 softmax)
+ *     lse[t, h] = log2(sum_j 2^(u_j))                       (-inf: no valid slot)
+ *
+ *   q_nope   [T, H, 512] bf16       q_pe [T, H, 64] bf16    (H a multiple of 16)
+ *   ckv      [num_slots, 512] bf16  kpe  [num_slots, 64] bf16 (the compressed KV
+ *            cache and its rope part, slot-major: for a paged cache of
+ *            64-token pages, slot = page * 64 + offset, as the paged indexer
+ *            returns it)
+ *   indices  [T, K] int32           out [T, H, 512] bf16    lse [T, H] fp32
+ *
+ * bf16 arrays are passed as their 16-bit patterns; they must be 16-byte
+ * aligned.  Arithmetic: bf16 products accumulated in fp32, weights rounded
+ * to bf16 for the weighted sum, output rounded to bf16.  A slot >= num_slots
+ * is read as padding and reported by dsa_sparse_attention_last_status
+ * (DSA_ERR_RANGE).  Scratch (split partials) is owned by the library per
+ * (device, stream), grown on demand.
+ */
+DSA_API int dsa_sparse_attention(const uint16_t* q_nope, const uint16_t* q_pe,
+                                 const uint16_t* ckv, const uint16_t* kpe,
+                                 const int32_t* indices, int T, int H, int K, int num_slots,
+                                 float sm_scale, uint16_t* out, float* lse, dsa_stream_t stream);
+
+/* Synchronises `stream`; DSA_OK, or DSA_ERR_RANGE if the most recent
+ * dsa_sparse_attention call on it met a slot outside [0, num_slots). */
+DSA_API int dsa_sparse_attention_last_status(dsa_stream_t stream);
+
+/*
  * Math-only control (a measurement, not an operator; section 5.2 of the
  * indexer study, "Math-only control"): the fused operator's plan and its main
  * scorer with the same work units, tile loads, tcgen05 MMAs and barriers, but

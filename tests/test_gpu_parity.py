@@ -112,6 +112,32 @@ def test_paged_units_last_first(B, next_n):
             assert not pr, (b, i, pr)
 
 
+# ------------------------------------------- small Q, long history; Q8192 ----
+@pytest.mark.parametrize("Q", [8, 64, 152])
+def test_small_q_long_history_all_rows(B, Q):
+    """Fewer query rows than SMs (or about as many) over a 128K-key causal
+    history: the key dimension is split into work units that all SMs share,
+    and every row is exact."""
+    inp = S.make_dense(Q, 131072, K=2048, seed=80 + Q)
+    out = B.indexer_topk(*dense_args(inp), K=inp.K).cpu().numpy()
+    _status_ok(B)
+    bad = check_rows_parallel(inp, out, range(Q))
+    assert bad == {}, list(bad.items())[:3]
+
+
+def test_q8192_chunk_sampled_and_repaired_rows(B):
+    """An 8192-row prefill chunk over 128K keys (twice the headline rows):
+    64 seeded rows, the first, middle and last rows, and every repaired row."""
+    inp = S.make_dense(8192, 131072, K=2048, seed=88)
+    out = B.indexer_topk(*dense_args(inp), K=inp.K).cpu().numpy()
+    counters = _status_ok(B)
+    repaired = B.last_repaired_rows()
+    assert len(repaired) == counters["underflow"] + counters["overflow"]
+    rows = sorted(set(_sampled_rows(inp.Q, 64, 188)) | set(repaired))
+    bad = check_rows_parallel(inp, out, rows)
+    assert bad == {}, list(bad.items())[:3]
+
+
 # ------------------------------------------------- full-size sampled rows ----
 def _sampled_rows(Q, n, seed):
     rng = np.random.default_rng(seed)
