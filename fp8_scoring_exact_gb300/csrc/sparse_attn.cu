@@ -52,11 +52,11 @@ constexpr int SA_THREADS = 128;
 constexpr int SA_ROW = SA_DQ + 8;          // shared row stride (bf16): 1168 bytes, ldmatrix without conflicts
 constexpr int SA_CHUNKS = SA_DQ * 2 / 16;  // 16-byte copies per row: 72
 constexpr int SA_SROW = SA_TK + 8;         // partial-logit row stride (floats): float2 stores without conflicts
-constexpr int SA_PROW = SA_TK + 8;         // weight row stride (bf16): 48 bytes, ldmatrix without conflicts
+constexpr int SA_PROW = SA_TK + 8;         // weight row stride (bf16): 80 bytes, ldmatrix without conflicts
 
 constexpr uint32_t SA_OFF_Q = 0;
 constexpr uint32_t SA_OFF_KV = SA_OFF_Q + SA_HB * SA_ROW * 2;               // 18688
-constexpr uint32_t SA_KV_BYTES = SA_TK * SA_ROW * 2;                        // 18688
+constexpr uint32_t SA_KV_BYTES = SA_TK * SA_ROW * 2;                        // 37376
 constexpr uint32_t SA_OFF_S = SA_OFF_KV + SA_STAGES * SA_KV_BYTES;
 constexpr uint32_t SA_OFF_P = SA_OFF_S + 4 * SA_HB * SA_SROW * 4;
 constexpr uint32_t SA_OFF_STAT = SA_OFF_P + SA_HB * SA_PROW * 2;
