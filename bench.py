@@ -244,6 +244,60 @@ def time_oracle(inp, n_rows, procs, reps=1):
     return rk * reps / dt, dt, list(rows)
 
 
+# ------------------------------------------------------ other workloads --
+def other_configs_leg(args, binding, device, flush, skip):
+    """The fused call on the indexed workloads other than the timed one (same
+    protocol: warm-up, L2 flushed before every step, CUDA events; the main
+    kernel timed by the library's events), so that every workload has a
+    number measured in the same run."""
+    import torch
+    from fp8_scoring_exact_gb300 import synthetic
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    out_rec = {}
+    for cid in range(len(synthetic.CONFIG_NAMES)):
+        if cid == skip:
+            continue
+        inp = synthetic.make_config(cid)
+        host, shape, call, _ = problem(inp, binding)
+        dev = [torch.from_numpy(a).to(device) for a in host]
+        out = torch.empty(shape, dtype=torch.int32, device=device)
+        binding.set_option("profile", 1)
+        for _ in range(max(3, args.warmup)):
+            call(dev, out)
+        torch.cuda.synchronize(device)
+        stream = torch.cuda.current_stream(device)
+        ms, main = [], []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(dev, out)
+            e1.record(stream)
+            main.append(binding.profiled_main_ms())
+            torch.cuda.synchronize(device)
+            ms.append(e0.elapsed_time(e1))
+        binding.set_option("profile", 0)
+        rc, counters = binding.last_device_status()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} on workload {cid}")
+        R = inp.row_keys()
+        m, k = statistics.mean(ms), statistics.mean(main)
+        t_tensor = FLOP_PER_ROW_KEY * R / (fp8_peak * 1e12) * 1e3
+        t_core = CORE_OPS_PER_ROW_KEY * R / (sms * 128 * peaks["sm_max_mhz"] * 1e6) * 1e3
+        t_hbm = algorithmic_bytes_of(inp) / (peaks["hbm_gbs"] * 1e9) * 1e3
+        rec = {"workload": inp.name, "ms_per_call": m, "row_keys_per_s": R / (m * 1e-3), "main_kernel_ms": k,
+               "call_frac_of_roofline": max(t_tensor, t_core, t_hbm) / m, "failures": counters}
+        if t_hbm > t_tensor:
+            rec["main_kernel_frac_of_hbm"] = algorithmic_bytes_of(inp) / (k * 1e-3) / 1e9 / peaks["hbm_gbs"]
+        else:
+            rec["main_kernel_frac_of_fp8_peak"] = FLOP_PER_ROW_KEY * R / (k * 1e-3) / 1e12 / fp8_peak
+        out_rec[synthetic.CONFIG_NAMES[cid]] = rec
+        del dev, out
+    return out_rec
+
+
 # --------------------------------------------------------- FP8 peak probe --
 def fp8_peak_probe(device, seconds=2.0, n=8192):
     """Dense e4m3 x e4m3 GEMM throughput of the library GEMM (torch._scaled_mm,
@@ -378,7 +432,23 @@ def _e2e(args, dev, host, out, stream, world, device, call, R, host_call=None):
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / args.steps
-    return {"value": world * R / (e2e_ms * 1e-3), "unit": "row-keys/s", "h2d_bytes_per_step": h2d,
+    # the host link alone: one plain 64 MiB copy each way between pinned host
+    # memory and the device (torch issues a cudaMemcpyAsync), best of 5
+    probe_h = torch.empty(64 << 20, dtype=torch.uint8).pin_memory()
+    probe_d = torch.empty(64 << 20, dtype=torch.uint8, device=device)
+    link = {}
+    for name, dst, src in (("h2d_gbs", probe_d, probe_h), ("d2h_gbs", probe_h, probe_d)):
+        best = float("inf")
+        for _ in range(5):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            c1.record(stream)
+            torch.cuda.synchronize(device)
+            best = min(best, c0.elapsed_time(c1))
+        link[name] = (64 << 20) / (best * 1e-3) / 1e9
+    return {"value": world * R / (e2e_ms * 1e-3), "unit": "row-keys/s", "pinned_copy_64mib": link,
+            "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
             "api": ("dsa_indexer_topk_host (host buffers; copies inside the library)" if host_call is not None
                     else "torch copies + dsa_indexer_topk_paged")}
@@ -557,6 +627,8 @@ def run_ours(args, rank, world, device):
                            "(whole call - control) / whole call"}
 
     fp8_probe = fp8_peak_probe(device) if "fp8peak" in legs else None
+    others = (other_configs_leg(args, binding, device, flush, args.config)
+              if "configs" in legs and not (args.rows or args.keys) else None)
     sparse = sparse_attention_leg(args, binding, device, flush) if "sparse" in legs else None
 
     # end to end through the public API from pinned host buffers
@@ -616,6 +688,7 @@ def run_ours(args, rank, world, device):
         "select": select,
         "math_control": control,
         "sparse_attention": sparse,
+        "other_workloads": others,
         "failures": counters,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -726,9 +799,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override: causal workload with this many query rows")
     ap.add_argument("--keys", type=int, default=0, help="override: causal workload with this many keys")
-    ap.add_argument("--legs", default="fused,unfused,graph,select,control,fp8peak,sparse,e2e",
+    ap.add_argument("--legs", default="fused,unfused,graph,select,control,fp8peak,sparse,configs,e2e",
                     help="comma list of legs to run besides the timed fused leg "
-                         "(unfused, graph, select, control, fp8peak, sparse, e2e)")
+                         "(unfused, graph, select, control, fp8peak, sparse, configs, e2e)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -1187,7 +1187,9 @@ __global__ void __launch_bounds__(MF_THREADS) matrix_filter_kernel(const MatrixF
     const int t1 = (int)min((int64_t)t0 + p.chunk_tiles, (int64_t)ceil_div(gp->hi, TILE));
     const int row = gp->row[r];
     const int b = p.rb[row], e = p.re[row];
-    const uint32_t tau = p.tau[row];
+    // the threshold as a float: score >= tauf <=> its key >= the threshold
+    // key (non-NaN scores), so a key is formed only for the scores that pass
+    const float tauf = key_threshold_float(p.tau[row]);
     const int wcap = region_cap(nunits);
     const int64_t region = (int64_t)row * ROW_SLOTS + (int64_t)(c * UNIT_REGIONS + quarter) * wcap;
     uint32_t* ck = p.cand_key + region;
@@ -1210,17 +1212,24 @@ __global__ void __launch_bounds__(MF_THREADS) matrix_filter_kernel(const MatrixF
         const int s0 = (t + 4 * v) * TILE + 4 * lane;
         const bool tile_in = t + 4 * v < t1;
         const float xs[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
+        bool pr[4];
+        if (tile_in && s0 >= b && s0 + 4 <= e) {  // the common case: the whole float4 in range
+#pragma unroll
+          for (int j = 0; j < 4; ++j) pr[j] = xs[j] >= tauf;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) pr[j] = tile_in && s0 + j >= b && s0 + j < e && xs[j] >= tauf;
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int s = s0 + j;
-          const uint32_t key = ordered_key(xs[j]);
-          const bool pred = tile_in && s >= b && s < e && key >= tau;
-          const uint32_t m = __ballot_sync(0xffffffffu, pred);
-          const int pos = wcnt + __popc(m & lt);
-          wcnt += __popc(m);
-          if (pred && pos < wcap) {
-            ck[pos] = key;
-            ci[pos] = s;
+          const uint32_t m = __ballot_sync(0xffffffffu, pr[j]);
+          if (m) {  // warp-uniform: nothing to do when no lane keeps a score
+            const int pos = wcnt + __popc(m & lt);
+            if (pr[j] && pos < wcap) {
+              ck[pos] = ordered_key(xs[j]);
+              ci[pos] = s0 + j;
+            }
+            wcnt += __popc(m);
           }
         }
       }
