@@ -53,6 +53,17 @@ def test_null_and_size_arguments_rejected_without_gpu():
     assert L.dsa_indexer_topk_host(fake, fake, fake, fake, fake, fake, fake, 4, 8, 0, fake, None) == binding.DSA_ERR_ARG
     assert L.dsa_indexer_topk_host(fake, fake, fake, fake, fake, fake, fake, 1 << 25, 8, 16, fake,
                                    None) == binding.DSA_ERR_UNSUPPORTED
+    # sparse attention: heads must be a multiple of 16, a positive scale, aligned bf16 arrays
+    assert L.dsa_sparse_attention(fake, fake, fake, fake, fake, 4, 8, 64, 100, 0.1, fake, fake,
+                                  None) == binding.DSA_ERR_ARG
+    assert L.dsa_sparse_attention(fake, fake, fake, fake, fake, 4, 16, 64, 100, 0.0, fake, fake,
+                                  None) == binding.DSA_ERR_ARG
+    assert L.dsa_sparse_attention(mis, fake, fake, fake, fake, 4, 16, 64, 100, 0.1, fake, fake,
+                                  None) == binding.DSA_ERR_ARG
+    assert L.dsa_sparse_attention(None, fake, fake, fake, fake, 4, 16, 64, 100, 0.1, fake, fake,
+                                  None) == binding.DSA_ERR_ARG
+    assert L.dsa_indexer_math_control(None, None, None, None, None, None, None, 1, 1, 1, None,
+                                      None) == binding.DSA_ERR_ARG
 
 
 def test_options_roundtrip_and_validate():
@@ -69,6 +80,18 @@ def test_options_roundtrip_and_validate():
         binding.set_option("chunk_tiles", 0)
     assert binding.lib().dsa_indexer_set_option(999, 1) == binding.DSA_ERR_ARG
     assert "sm_103a" in binding.version()
+    # the pipeline wait limit and the test options
+    assert binding.get_option("wait_limit_us") == 2000000
+    binding.set_option("wait_limit_us", 50000)
+    assert binding.get_option("wait_limit_us") == 50000
+    binding.set_option("wait_limit_us", 2000000)
+    for name, bad in (("wait_limit_us", 0), ("wait_limit_us", 60000001), ("unit_order", 2), ("test_withhold", 3)):
+        with pytest.raises(binding.IndexerError):
+            binding.set_option(name, bad)
+    for name in ("unit_order", "test_withhold"):
+        binding.set_option(name, 1)
+        assert binding.get_option(name) == 1
+        binding.set_option(name, 0)
 
 
 def test_product_path_has_no_cpu_fallback():
