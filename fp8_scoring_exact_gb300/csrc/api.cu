@@ -1094,10 +1094,10 @@ int dsa_sparse_attention(const uint16_t* q_nope, const uint16_t* q_pe, const uin
   if ((int64_t)T * H >= (1ll << 31) / 512 || (int64_t)T * K >= (1ll << 31) || T > 65535) return DSA_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const Opts o = read_opts();
-  // splits of each token's key list: about two CTAs per SM in one wave, at
+  // splits of each token's key list: about one wave of resident CTAs, at
   // least 64 keys per split
   const int ctas = T * (H / 16);
-  int splits = std::max(1, std::min(2 * o.grid / std::max(ctas, 1), K / 64));
+  int splits = std::max(1, std::min(sparse_attn_ctas_per_sm() * o.grid / std::max(ctas, 1), K / 64));
   int per = ceil_div(ceil_div(K, splits), 32) * 32;
   splits = ceil_div(K, per);
   const int64_t rows = (int64_t)T * H;

@@ -281,6 +281,7 @@ cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s);
 cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStream_t s);
 cudaError_t launch_sparse_attn(const SparseAttnParams& p, cudaStream_t s);
+int sparse_attn_ctas_per_sm();  // CTAs of the sparse-attention kernel resident per SM
 
 // number of work groups of G query rows for a row space
 template <int G>
