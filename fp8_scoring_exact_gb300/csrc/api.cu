@@ -1098,7 +1098,8 @@ int dsa_sparse_attention(const uint16_t* q_nope, const uint16_t* q_pe, const uin
   // least 64 keys per split
   const int ctas = T * (H / 16);
   int splits = std::max(1, std::min(sparse_attn_ctas_per_sm() * o.grid / std::max(ctas, 1), K / 64));
-  int per = ceil_div(ceil_div(K, splits), 32) * 32;
+  // (a split's slots, at most SA_MAX_PER = 2048, are staged in shared memory)
+  int per = std::min(ceil_div(ceil_div(K, splits), 32) * 32, 2048);
   splits = ceil_div(K, per);
   const int64_t rows = (int64_t)T * H;
   const size_t off_ml = 256, off_o = align_up(off_ml + (size_t)splits * rows * 8, 256);

@@ -70,7 +70,8 @@ constexpr uint32_t SA_OFF_S = SA_OFF_KV + SA_STAGES * SA_KV_BYTES;
 constexpr uint32_t SA_OFF_P = SA_OFF_S + 4 * SA_HB * SA_SROW * 4;
 constexpr uint32_t SA_OFF_STAT = SA_OFF_P + SA_HB * SA_PROW * 2;
 constexpr uint32_t SA_OFF_IDX = SA_OFF_STAT + 3 * SA_HB * 4;                // m, l, alpha per head
-constexpr uint32_t SA_SMEM = SA_OFF_IDX + SA_STAGES * SA_TK * 4;
+constexpr int SA_MAX_PER = 2048;           // slots of one split, loaded into shared memory at the start
+constexpr uint32_t SA_SMEM = SA_OFF_IDX + SA_MAX_PER * 4;
 static_assert((SA_ROW * 2) % 16 == 0 && SA_TK == 4 * SA_WARPS, "rows aligned; 4 rows per warp");
 static_assert(SA_OFF_KV % 16 == 0 && SA_OFF_S % 16 == 0 && SA_OFF_P % 16 == 0, "sparse attention layout");
 static_assert(SA_SMEM * SA_CTAS_PER_SM <= 226 * 1024, "shared memory per SM");
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(SA_THREADS, SA_CTAS_PER_SM) sparse_attn_kernel
   float* sM = reinterpret_cast<float*>(smem + SA_OFF_STAT);
   float* sL = sM + SA_HB;
   float* sA = sL + SA_HB;
-  int* sIdx = reinterpret_cast<int*>(smem + SA_OFF_IDX);
+  int* sSlot = reinterpret_cast<int*>(smem + SA_OFF_IDX);  // this split's slots, -1 past its end
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hb = blockIdx.x, t = blockIdx.y, split = blockIdx.z;
@@ -133,23 +134,25 @@ __global__ void __launch_bounds__(SA_THREADS, SA_CTAS_PER_SM) sparse_attn_kernel
                                     : (const void*)(p.q_pe + (qrow0 + r) * SA_DP + 8 * (k - SA_DC / 8));
     cp_async_16(sbase + SA_OFF_Q + (r * SA_ROW + 8 * k) * 2, src, 16);
   }
-  // the key tile starting at list position j0 into buffer b: warp w copies
-  // rows 4w .. 4w + 3 (slot -1: padding or past the list, zero-filled; a
-  // slot outside the cache is reported and treated as padding)
-  auto gather = [&](int j0, int b) {
-    int s = -1;
-    if (lane < 4) {
-      const int j = j0 + 4 * warp + lane;
-      s = j < j_end ? __ldg(&idx_row[j]) : -1;
-      if (s >= p.num_slots) {
-        atomicOr(p.status, ST_RANGE);
-        s = -1;
-      }
-      sIdx[b * SA_TK + 4 * warp + lane] = s;
+  // this split's slots into shared memory once (-1: padding, past the list,
+  // or a slot outside the cache, which is reported): the gathers then take
+  // their rows' slots from there instead of waiting on global loads
+  for (int i = tid; i < n_tiles * SA_TK; i += SA_THREADS) {
+    const int j = j_begin + i;
+    int sl = j < j_end ? __ldg(&idx_row[j]) : -1;
+    if (sl >= p.num_slots) {
+      atomicOr(p.status, ST_RANGE);
+      sl = -1;
     }
+    sSlot[i] = sl;
+  }
+  __syncthreads();
+  // tile i into buffer b: warp w copies rows 4w .. 4w + 3 (a padding slot's
+  // row zero-filled), its lanes consecutive 16-byte chunks of each row
+  auto gather = [&](int i, int b) {
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
-      const int sr = __shfl_sync(0xffffffffu, s, rr);
+      const int sr = sSlot[i * SA_TK + 4 * warp + rr];
       const int64_t slot = sr < 0 ? 0 : sr;
       const int n = sr < 0 ? 0 : 16;
       const uint32_t dst = sbase + SA_OFF_KV + b * SA_KV_BYTES + (4 * warp + rr) * SA_ROW * 2 + 16 * lane;
@@ -159,13 +162,6 @@ __global__ void __launch_bounds__(SA_THREADS, SA_CTAS_PER_SM) sparse_attn_kernel
       if (lane < 8) cp_async_16(dst + 1024, reinterpret_cast<const uint8_t*>(p.kpe + slot * SA_DP) + 16 * lane, n);
     }
   };
-  // query rows: 16 x (512 + 64) bf16
-  for (int c = tid; c < SA_HB * SA_CHUNKS; c += SA_THREADS) {
-    const int r = c / SA_CHUNKS, k = c % SA_CHUNKS;
-    const void* src = k < SA_DC / 8 ? (const void*)(p.q_nope + (qrow0 + r) * SA_DC + 8 * k)
-                                    : (const void*)(p.q_pe + (qrow0 + r) * SA_DP + 8 * (k - SA_DC / 8));
-    cp_async_16(sbase + SA_OFF_Q + (r * SA_ROW + 8 * k) * 2, src, 16);
-  }
   if (tid < SA_HB) {
     sM[tid] = -__int_as_float(0x7f800000);
     sL[tid] = 0.f;
@@ -174,7 +170,7 @@ __global__ void __launch_bounds__(SA_THREADS, SA_CTAS_PER_SM) sparse_attn_kernel
   // query rows in the first; empty groups past the end keep the count uniform)
 #pragma unroll
   for (int i = 0; i < SA_STAGES - 1; ++i) {
-    if (i < n_tiles) gather(j_begin + i * SA_TK, i);
+    if (i < n_tiles) gather(i, i);
     cp_async_commit();
   }
 
@@ -200,7 +196,7 @@ __global__ void __launch_bounds__(SA_THREADS, SA_CTAS_PER_SM) sparse_attn_kernel
       }
     }
     // refill the buffer the previous tile used
-    if (it + SA_STAGES - 1 < n_tiles) gather(j_begin + (it + SA_STAGES - 1) * SA_TK, (it + SA_STAGES - 1) % SA_STAGES);
+    if (it + SA_STAGES - 1 < n_tiles) gather(it + SA_STAGES - 1, (it + SA_STAGES - 1) % SA_STAGES);
     cp_async_commit();
 
     // ---- partial logits over this warp's 144 dims: 16 heads x its 16 keys
@@ -244,7 +240,7 @@ __global__ void __launch_bounds__(SA_THREADS, SA_CTAS_PER_SM) sparse_attn_kernel
           a.x += x.x;
           a.y += x.y;
         }
-        const int* si = sIdx + b * SA_TK + 2 * kq;
+        const int* si = sSlot + it * SA_TK + 2 * kq;
         u[0] = si[0] >= 0 ? a.x * p.scale_log2 : -__int_as_float(0x7f800000);
         u[1] = si[1] >= 0 ? a.y * p.scale_log2 : -__int_as_float(0x7f800000);
       }
