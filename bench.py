@@ -354,18 +354,24 @@ def sparse_attention_leg(args, binding, device, flush, heads=16):
     (tokens do not share their gathers) + queries + output."""
     import torch
     from fp8_scoring_exact_gb300 import synthetic
-    ip = synthetic.make_config(4)
-    host = [np.ascontiguousarray(a) for a in (ip.q, ip.q_scale, ip.k_cache, ip.k_cache_scale, ip.w,
-                                              ip.block_table, ip.seq_lens)]
-    dev = [torch.from_numpy(a).to(device) for a in host]
-    idx = binding.indexer_topk_paged(*dev, K=ip.K).reshape(-1, ip.K)
-    rc, _ = binding.last_device_status()
-    if rc != 0:
-        raise RuntimeError(f"device status {rc} from the indexer feeding the sparse attention")
-    del dev
-    T, slots = idx.shape[0], ip.k_cache.shape[0] * 64
     g = torch.Generator(device=device)
     g.manual_seed(4)
+    if args.sparse_slots > 0:
+        # a smaller case of the same kernel for profiling: 128 tokens x 2048
+        # uniformly random slots of a cache of `sparse_slots` slots
+        K, T, slots = 2048, 128, args.sparse_slots
+        idx = torch.randint(0, slots, (T, K), generator=g, device=device, dtype=torch.int32)
+    else:
+        ip = synthetic.make_config(4)
+        host = [np.ascontiguousarray(a) for a in (ip.q, ip.q_scale, ip.k_cache, ip.k_cache_scale, ip.w,
+                                                  ip.block_table, ip.seq_lens)]
+        dev = [torch.from_numpy(a).to(device) for a in host]
+        idx = binding.indexer_topk_paged(*dev, K=ip.K).reshape(-1, ip.K)
+        rc, _ = binding.last_device_status()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} from the indexer feeding the sparse attention")
+        del dev
+        K, T, slots = ip.K, idx.shape[0], ip.k_cache.shape[0] * 64
     ckv = torch.randn((slots, 512), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
     kpe = torch.randn((slots, 64), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
     qn = torch.randn((T, heads, 512), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
@@ -388,17 +394,19 @@ def sparse_attention_leg(args, binding, device, flush, heads=16):
     torch.cuda.synchronize(device)
     ms = statistics.mean([a.elapsed_time(b) for a, b in ev])
     valid = int((idx >= 0).sum().item())
-    nbytes = valid * (512 + 64) * 2 + T * heads * 576 * 2 + T * heads * (512 * 2 + 4) + T * ip.K * 4
+    nbytes = valid * (512 + 64) * 2 + T * heads * 576 * 2 + T * heads * (512 * 2 + 4) + T * K * 4
     flop = valid * heads * 2 * (576 + 512)
     gbs = nbytes / (ms * 1e-3) / 1e9
     hbm = load_peaks()["hbm_gbs"]
     del ckv, kpe
-    return {"ms_per_step": ms, "tokens": T, "heads": heads, "K": ip.K, "valid_slots": valid,
+    return {"ms_per_step": ms, "tokens": T, "heads": heads, "K": K, "valid_slots": valid, "cache_slots": slots,
             "bytes_per_step": nbytes, "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm,
             "tflops": flop / (ms * 1e-3) / 1e12,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm},
-            "note": "dsa_sparse_attention over the paged decode batch's own top-2048 slots (64 sequences x 2 "
-                    "tokens), bf16 latent cache 512+64 per slot, L2 flushed before each step"}
+            "note": ("dsa_sparse_attention over " + (f"uniformly random slots of a {slots}-slot cache"
+                                                     if args.sparse_slots > 0 else
+                                                     "the paged decode batch's own top-2048 slots (64 sequences x 2 tokens)")
+                     + ", bf16 latent cache 512+64 per slot, L2 flushed before each step")}
 
 
 # ------------------------------------------------------------ GPU arm -------
@@ -799,6 +807,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override: causal workload with this many query rows")
     ap.add_argument("--keys", type=int, default=0, help="override: causal workload with this many keys")
+    ap.add_argument("--sparse-slots", type=int, default=0,
+                    help="sparse leg on random slots of a cache of this many slots (a smaller profiling case) "
+                         "instead of the paged decode batch's own top-2048 result")
     ap.add_argument("--legs", default="fused,unfused,graph,select,control,fp8peak,sparse,configs,e2e",
                     help="comma list of legs to run besides the timed fused leg "
                          "(unfused, graph, select, control, fp8peak, sparse, configs, e2e)")
