@@ -92,3 +92,32 @@ def test_sparse_attention_reports_slots_outside_the_cache(B):
     assert B.sparse_attention_last_status() == B.DSA_ERR_RANGE
     inp.indices[1, 5] = -1
     _check(inp, out, lse)
+
+
+def test_sparse_attention_replays_from_a_cuda_graph(B):
+    """The call enqueues a status reset and kernels only (its scratch sized by
+    a first call), so it can be captured once and replayed on new inputs
+    copied into the captured buffers."""
+    import torch
+    a = S.make_sparse_attention(6, 16, 3000, 512, seed=94)
+    b = S.make_sparse_attention(6, 16, 3000, 512, seed=95)
+    dev = [x.cuda() for x in (a.q_nope, a.q_pe, a.ckv, a.kpe)]
+    idx = torch.from_numpy(a.indices).cuda()
+    out = torch.empty((a.T, a.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((a.T, a.H), dtype=torch.float32, device="cuda")
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        B.sparse_attention(*dev, idx, a.sm_scale, out=out, lse=lse)  # sizes this stream's scratch
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        B.sparse_attention(*dev, idx, a.sm_scale, out=out, lse=lse)
+    for d, h in zip(dev, (b.q_nope, b.q_pe, b.ckv, b.kpe)):
+        d.copy_(h.cuda())
+    idx.copy_(torch.from_numpy(b.indices).cuda())
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert B.sparse_attention_last_status(gs) == 0
+    _check(b, out.float().cpu().numpy(), lse.cpu().numpy())
