@@ -426,19 +426,21 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
   cs.cand_idx = cp.cand_idx;
   cs.max_units = max_units;
   cs.failed_rows = at<int32_t>(a, L.failed);
+  cs.tau = tau;
   cs.out = out;
   cs.stats = st;
-  DSA_LAUNCH(launch_cand_select(cs, 3 * o.grid, stream));  // 3 CTAs per SM (shared memory)
-
   // exact repair of rows whose certificate failed: a store-mode scorer has
   // no candidate regions, so its units are short (REPAIR_CHUNK tiles) and
-  // even a single failed long row is spread over many SMs
+  // even a single failed long row is spread over many SMs; the selector's
+  // last CTA writes this plan
   PlanParams rp = pp;
   rp.plan = PLAN_REPAIR;
   rp.chunk_tiles = REPAIR_CHUNK;
   rp.groups = at<Group>(a, L.rgroups);
   rp.unit_start = at<int32_t>(a, L.runit_start);
-  DSA_LAUNCH(launch_plan(rp, stream));
+  cs.plan_repair = 1;
+  cs.repair = rp;
+  DSA_LAUNCH(launch_cand_select(cs, cand_select_ctas_per_sm() * o.grid, stream));
 
   ScoreParams rcp = cp;
   rcp.withhold_first_acc = 0;
@@ -842,9 +844,10 @@ int enqueue_matrix_select(Arena* a, const RowSpace& rs, int K, const Opts& o, co
   cs.cand_idx = mf.cand_idx;
   cs.max_units = max_units;
   cs.failed_rows = at<int32_t>(a, L.failed);
+  cs.tau = tau;
   cs.out = out;
   cs.stats = st;
-  DSA_LAUNCH(launch_cand_select(cs, 3 * o.grid, stream));
+  DSA_LAUNCH(launch_cand_select(cs, cand_select_ctas_per_sm() * o.grid, stream));
   WideParams wp{};
   wp.rs = rs;
   wp.K = K;

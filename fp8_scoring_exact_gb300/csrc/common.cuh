@@ -81,7 +81,8 @@ struct Stats {
   int s_groups;      // sample plan
   int s_units;
   int next_unit[3];  // per plan (PLAN_*): the next work unit a scorer CTA takes
-  int pad[1];
+  int cs_done;       // candidate-selector CTAs finished (the last one plans the repair)
+  int cs_next;       // candidate selector: items handed out past each CTA's first
   unsigned long long wait_ns;  // limit of the call's pipeline waits (read only by a wait that stalls)
 };
 

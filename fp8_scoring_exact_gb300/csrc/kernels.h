@@ -109,10 +109,13 @@ struct CandParams {
   const int32_t* unit_count;
   const uint32_t* cand_key;     // [R, ROW_SLOTS]
   const int32_t* cand_idx;
+  const uint32_t* tau;         // [R] threshold keys (every candidate is at or above its row's)
   int max_units;
   int32_t* failed_rows;        // [R] (appended, count in stats->fail_count)
   int32_t* out;                // [R, K]
   Stats* stats;
+  int plan_repair;             // 1: the CTA that finishes last writes the repair plan below
+  PlanParams repair;           // (plan PLAN_REPAIR)
 };
 
 struct SelectParams {
@@ -278,6 +281,7 @@ cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
                          cudaStream_t s);
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
 cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s);
+int cand_select_ctas_per_sm();  // the selector's CTAs resident per SM (its grid: this x SMs)
 cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s);
 cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStream_t s);
 cudaError_t launch_sparse_attn(const SparseAttnParams& p, cudaStream_t s);

@@ -195,199 +195,44 @@ __device__ __forceinline__ int sample_rank(int m, int L, int target) {
 }
 
 // ------------------------------------------- whole-CTA selection (256 threads)
-// Exact K-th largest of n keys in shared memory (n a multiple of 4, pad keys
-// 0, every real key non-zero), by the whole CTA of 256 threads: bytes every
-// real key shares are skipped; each remaining byte is one histogram pass into
-// 4 sub-histograms (warp % 4: little atomic contention) and a one-bin-per-
-// thread scan from the top; once the bucket holding the K-th key fits in
-// `cbuf` (ccap keys) it is compacted there and the later passes scan only it.
-// Returns theta = the K-th largest key and rr = how many keys equal to theta
-// belong to the top K.  sc: >= 24 ints of shared scratch.
-__device__ __forceinline__ void block_select_kth(const uint32_t* keys, int n, int K, int* shist, uint32_t* cbuf,
-                                                 int ccap, int* sc, uint32_t& theta, int& rr) {
+// Descending scan of nb (<= 1024) bin counts by 256 threads (4 bins each,
+// thread t owns bins nb-1-4t .. nb-4-4t): the bin that holds the rem-th
+// largest key goes to sc[2], the rank inside it to sc[3], its count to
+// sc[4]; with `slots`, every bin's count is replaced by the number of keys
+// in the bins above it (its first slot in a descending counting sort).
+// sc[8..15]: warp sums.  Ends with a CTA barrier.
+__device__ __forceinline__ void desc_scan_pick(int* hist, int nb, int rem, int* sc, bool slots) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-  if (tid == 0) {
-    sc[0] = -1;
-    sc[1] = 0;
+  int c[4], s = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int b = nb - 1 - 4 * tid - j;
+    c[j] = b >= 0 ? hist[b] : 0;
+    s += c[j];
+  }
+  int incl = s;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) sc[8 + warp] = incl;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) incl += w < warp ? sc[8 + w] : 0;
+  int e = incl - s;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int b = nb - 1 - 4 * tid - j;
+    if (e < rem && rem <= e + c[j]) {
+      sc[2] = b;
+      sc[3] = rem - e;
+      sc[4] = c[j];
+    }
+    if (slots && b >= 0) hist[b] = e;
+    e += c[j];
   }
   __syncthreads();
-  uint32_t a = 0xffffffffu, o = 0u;
-  for (int i = tid; i < (n >> 2); i += 256) {
-    const uint4 v = k4[i];
-    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (x[c]) {
-        a &= x[c];
-        o |= x[c];
-      }
-  }
-  a = __reduce_and_sync(0xffffffffu, a);
-  o = __reduce_or_sync(0xffffffffu, o);
-  if (lane == 0) {
-    atomicAnd((unsigned*)&sc[0], a);
-    atomicOr((unsigned*)&sc[1], o);
-  }
-  __syncthreads();
-  const uint32_t diff = (uint32_t)sc[0] ^ (uint32_t)sc[1];
-  int pass = 0;
-  uint32_t mask = 0;
-  while (pass < 3 && ((diff >> (24 - 8 * pass)) & 0xFFu) == 0) {
-    mask |= 0xFFu << (24 - 8 * pass);
-    ++pass;
-  }
-  uint32_t prefix = (uint32_t)sc[1] & mask;
-  int rem = K;
-  const uint32_t* src = keys;
-  int nsrc = n;
-  bool compact = false;
-  int* h = shist + (warp & 3) * 256;
-#pragma unroll 1
-  for (; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int b = tid; b < 4 * 256; b += 256) shist[b] = 0;
-    __syncthreads();
-    if (!compact) {
-      for (int i = tid; i < (nsrc >> 2); i += 256) {
-        const uint4 v = reinterpret_cast<const uint4*>(src)[i];
-        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if ((x[c] & mask) == prefix) atomicAdd(&h[(x[c] >> shift) & 0xFFu], 1);
-      }
-    } else {
-      for (int i = tid; i < nsrc; i += 256) {
-        const uint32_t x = src[i];
-        if ((x & mask) == prefix) atomicAdd(&h[(x >> shift) & 0xFFu], 1);
-      }
-    }
-    __syncthreads();
-    // thread t owns bin 255 - t: a descending scan finds the bin of the rem-th key
-    const int bin = 255 - tid;
-    const int c = shist[bin] + shist[256 + bin] + shist[512 + bin] + shist[768 + bin];
-    int incl = c;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    if (lane == 31) sc[8 + warp] = incl;
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < 8; ++w) incl += w < warp ? sc[8 + w] : 0;
-    const int excl = incl - c;
-    if (excl < rem && rem <= incl) {
-      sc[2] = bin;
-      sc[3] = rem - excl;
-      sc[4] = c;
-    }
-    __syncthreads();
-    prefix |= (uint32_t)sc[2] << shift;
-    mask |= 0xFFu << shift;
-    rem = sc[3];
-    const int cnt = sc[4];
-    if (!compact && pass < 3 && cnt <= ccap) {
-      // the K-th key's bucket into cbuf: each thread counts its hits, an
-      // exclusive scan over the CTA gives its first slot, then it writes
-      // them (no shared counter: one atomic per warp and ballot serialised
-      // the warps, measured 2.5-4.9K cycles per row, this ~1K)
-      const int n4s = nsrc >> 2;
-      int mine = 0;
-      for (int i = tid; i < n4s; i += 256) {
-        const uint4 v = reinterpret_cast<const uint4*>(src)[i];
-        mine += ((v.x & mask) == prefix) + ((v.y & mask) == prefix) + ((v.z & mask) == prefix) +
-                ((v.w & mask) == prefix);
-      }
-      int incl2 = mine;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl2, d);
-        if (lane >= d) incl2 += v;
-      }
-      if (lane == 31) sc[16 + warp] = incl2;
-      __syncthreads();
-      int pos = incl2 - mine;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) pos += w < warp ? sc[16 + w] : 0;
-      for (int i = tid; i < n4s; i += 256) {
-        const uint4 v = reinterpret_cast<const uint4*>(src)[i];
-        if ((v.x & mask) == prefix) cbuf[pos++] = v.x;
-        if ((v.y & mask) == prefix) cbuf[pos++] = v.y;
-        if ((v.z & mask) == prefix) cbuf[pos++] = v.z;
-        if ((v.w & mask) == prefix) cbuf[pos++] = v.w;
-      }
-      src = cbuf;
-      nsrc = cnt;
-      compact = true;
-    }
-    __syncthreads();
-  }
-  theta = prefix;
-  rr = rem;
-}
-
-// Emission by the whole CTA of 256 threads: every key above theta and the
-// first rr keys equal to it (keys/ids in shared memory, n a multiple of 4):
-// each thread counts its keys, one reservation per warp, then writes (the
-// stores are fire-and-forget: staging the row in shared memory for
-// coalesced stores was measured slower).  counters[0..1]: shared, zero on
-// entry.
-__device__ __forceinline__ void block_emit(const uint32_t* keys, const int32_t* ids, int n, uint32_t theta, int rr,
-                                           int K, int32_t* o, int* counters) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int n4 = n >> 2;
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-  const int4* i4 = reinterpret_cast<const int4*>(ids);
-  for (int base = 0; base < n4; base += 256 * 4) {
-    // this thread's up to 4 quads: i = base + tid + 256 j
-    int cg = 0, ce = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = base + tid + 256 * j;
-      if (i < n4) {
-        const uint4 v = k4[i];
-        cg += (v.x > theta) + (v.y > theta) + (v.z > theta) + (v.w > theta);
-        ce += (v.x == theta) + (v.y == theta) + (v.z == theta) + (v.w == theta);
-      }
-    }
-    int ig = cg, ie = ce;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int vg = __shfl_up_sync(0xffffffffu, ig, d), ve = __shfl_up_sync(0xffffffffu, ie, d);
-      if (lane >= d) {
-        ig += vg;
-        ie += ve;
-      }
-    }
-    int bg = 0, be = 0;
-    if (lane == 31) {
-      if (ig) bg = atomicAdd(&counters[0], ig);
-      if (ie) be = atomicAdd(&counters[1], ie);
-    }
-    bg = __shfl_sync(0xffffffffu, bg, 31) + ig - cg;
-    be = __shfl_sync(0xffffffffu, be, 31) + ie - ce;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = base + tid + 256 * j;
-      if (i < n4) {
-        const uint4 v = k4[i];
-        const int4 d = i4[i];
-        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-        const int32_t id[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (x[q] > theta) {
-            if (bg < K - rr) o[bg] = id[q];
-            ++bg;
-          } else if (x[q] == theta) {
-            if (be < rr) o[K - rr + be] = id[q];
-            ++be;
-          }
-        }
-      }
-    }
-  }
 }
 
 }  // namespace dsa

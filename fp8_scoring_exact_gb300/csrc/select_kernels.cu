@@ -52,6 +52,97 @@ __device__ __forceinline__ int group_units(int lo, int hi, int chunk) {
   return ceil_div(tiles, chunk);
 }
 
+// Groups of a plan and their work-unit prefix (unit_start), by every thread
+// of the calling CTA (any multiple of 32 threads); G groups.  warp_sums: 32
+// ints and s_carry: one int of shared memory.  Failed-row entries are read
+// through L2: the repair plan may run in the CTA that finishes the
+// candidate selection, whose other CTAs queued them.
+__device__ void plan_groups(const PlanParams& p, int G, int* warp_sums, int* s_carry) {
+  const RowSpace& rs = p.rs;
+  const int tid = threadIdx.x;
+  if (tid == 0) *s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < G; base += (int)blockDim.x) {
+    const int g = base + tid;
+    int units = 0;
+    if (g < G) {
+      Group grp;
+      grp.nrows = 0;
+      grp.lo = 0x7fffffff;
+      grp.hi = 0;
+      for (int i = 0; i < GROUP_ROWS; ++i) grp.row[i] = grp.slot[i] = 0;
+      if (p.plan != PLAN_REPAIR) {
+        int rows[GROUP_ROWS];
+        const int nr = rows_of_group<GROUP_ROWS>(rs, g, rows);
+        grp.seq = rs.paged ? rows[0] / rs.next_n : -1;
+        for (int i = 0; i < nr; ++i) {
+          const int b = p.rb[rows[i]], e = p.re[rows[i]];
+          // the sample plan leaves out the rows the main plan calls trivial
+          const int len = p.plan == PLAN_SAMPLE ? p.row_end_in[rows[i]] - p.row_begin_in[rows[i]] : e - b;
+          if (len > p.trivial_len && e > b) {
+            grp.row[grp.nrows] = rows[i];
+            grp.slot[grp.nrows] = rows[i];
+            ++grp.nrows;
+            grp.lo = min(grp.lo, b);
+            grp.hi = max(grp.hi, e);
+          }
+        }
+      } else if (rs.paged) {
+        const int row = __ldcg(&p.failed_rows[g]);
+        grp.nrows = 1;
+        grp.row[0] = row;
+        grp.slot[0] = g;
+        grp.seq = row / rs.next_n;
+        grp.lo = p.rb[row];
+        grp.hi = p.re[row];
+      } else {
+        // failed-list entries 4g .. 4g + 3; slot = the entry (its score row)
+        const int nf = __ldcg(&p.stats->fail_count);
+        grp.seq = -1;
+        for (int i = 0; i < GROUP_ROWS && GROUP_ROWS * g + i < nf; ++i) {
+          const int f = GROUP_ROWS * g + i, row = __ldcg(&p.failed_rows[f]);
+          grp.row[grp.nrows] = row;
+          grp.slot[grp.nrows] = f;
+          ++grp.nrows;
+          grp.lo = min(grp.lo, p.rb[row]);
+          grp.hi = max(grp.hi, p.re[row]);
+        }
+      }
+      if (grp.nrows == 0) grp.lo = grp.hi = 0;
+      units = group_units(grp.lo, grp.hi, p.chunk_tiles);
+      p.groups[g] = grp;
+    }
+    const int incl = block_inclusive_scan(units, warp_sums);
+    const int carry = *s_carry;
+    if (g < G) p.unit_start[g + 1] = carry + incl;
+    __syncthreads();
+    if (tid == (int)blockDim.x - 1) *s_carry = carry + incl;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.unit_start[0] = 0;
+    p.stats->next_unit[p.plan] = 0;
+    if (p.plan == PLAN_MAIN) {
+      p.stats->n_groups = G;
+      p.stats->total_units = *s_carry;
+    } else if (p.plan == PLAN_REPAIR) {
+      p.stats->r_groups = G;
+      p.stats->r_units = *s_carry;
+    } else {
+      p.stats->s_groups = G;
+      p.stats->s_units = *s_carry;
+    }
+  }
+}
+
+// Groups of the repair plan: dense rows all read one key array, so four
+// failed rows share a group (scored over the union of their ranges); paged
+// rows, one per group.
+__device__ __forceinline__ int repair_groups(const PlanParams& p) {
+  const int nf = __ldcg(&p.stats->fail_count);
+  return p.rs.paged ? nf : ceil_div(nf, GROUP_ROWS);
+}
+
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) {
   pdl_enter();
   __shared__ int warp_sums[32];
@@ -104,84 +195,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
     __syncthreads();
     G = n_groups(rs);
   } else {
-    // dense rows all read one key array: four failed rows share a group
-    // (scored over the union of their ranges); paged rows, one per group
-    G = rs.paged ? p.stats->fail_count : ceil_div(p.stats->fail_count, GROUP_ROWS);
+    G = repair_groups(p);
   }
 
-  if (tid == 0) s_carry = 0;
-  __syncthreads();
-  for (int base = 0; base < G; base += PLAN_THREADS) {
-    const int g = base + tid;
-    int units = 0;
-    if (g < G) {
-      Group grp;
-      grp.nrows = 0;
-      grp.lo = 0x7fffffff;
-      grp.hi = 0;
-      for (int i = 0; i < GROUP_ROWS; ++i) grp.row[i] = grp.slot[i] = 0;
-      if (p.plan != PLAN_REPAIR) {
-        int rows[GROUP_ROWS];
-        const int nr = rows_of_group<GROUP_ROWS>(rs, g, rows);
-        grp.seq = rs.paged ? rows[0] / rs.next_n : -1;
-        for (int i = 0; i < nr; ++i) {
-          const int b = p.rb[rows[i]], e = p.re[rows[i]];
-          // the sample plan leaves out the rows the main plan calls trivial
-          const int len = p.plan == PLAN_SAMPLE ? p.row_end_in[rows[i]] - p.row_begin_in[rows[i]] : e - b;
-          if (len > p.trivial_len && e > b) {
-            grp.row[grp.nrows] = rows[i];
-            grp.slot[grp.nrows] = rows[i];
-            ++grp.nrows;
-            grp.lo = min(grp.lo, b);
-            grp.hi = max(grp.hi, e);
-          }
-        }
-      } else if (rs.paged) {
-        const int row = p.failed_rows[g];
-        grp.nrows = 1;
-        grp.row[0] = row;
-        grp.slot[0] = g;
-        grp.seq = row / rs.next_n;
-        grp.lo = p.rb[row];
-        grp.hi = p.re[row];
-      } else {
-        // failed-list entries 4g .. 4g + 3; slot = the entry (its score row)
-        const int nf = p.stats->fail_count;
-        grp.seq = -1;
-        for (int i = 0; i < GROUP_ROWS && GROUP_ROWS * g + i < nf; ++i) {
-          const int f = GROUP_ROWS * g + i, row = p.failed_rows[f];
-          grp.row[grp.nrows] = row;
-          grp.slot[grp.nrows] = f;
-          ++grp.nrows;
-          grp.lo = min(grp.lo, p.rb[row]);
-          grp.hi = max(grp.hi, p.re[row]);
-        }
-      }
-      if (grp.nrows == 0) grp.lo = grp.hi = 0;
-      units = group_units(grp.lo, grp.hi, p.chunk_tiles);
-      p.groups[g] = grp;
-    }
-    const int incl = block_inclusive_scan(units, warp_sums);
-    const int carry = s_carry;
-    if (g < G) p.unit_start[g + 1] = carry + incl;
-    __syncthreads();
-    if (tid == PLAN_THREADS - 1) s_carry = carry + incl;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    p.unit_start[0] = 0;
-    p.stats->next_unit[p.plan] = 0;
-    if (p.plan == PLAN_MAIN) {
-      p.stats->n_groups = G;
-      p.stats->total_units = s_carry;
-    } else if (p.plan == PLAN_REPAIR) {
-      p.stats->r_groups = G;
-      p.stats->r_units = s_carry;
-    } else {
-      p.stats->s_groups = G;
-      p.stats->s_units = s_carry;
-    }
-  }
+  plan_groups(p, G, warp_sums, &s_carry);
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
@@ -799,37 +816,71 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
 // ("Fusing Indexer Scoring and Exact Top-k for DeepSeek-V3.2", section 3.2:
 // every key at or above the threshold is a candidate, and when there are at
 // least K of them the top K of the candidates are the top K of the row).
-// One CTA per (group, row) item at a time: certificate over the region
-// counts, gather of the regions into shared memory, radix select, emission.
-constexpr uint32_t cs_align16(uint32_t x) { return (x + 15u) & ~15u; }
-constexpr uint32_t CS_OFF_KEY = 0;
-constexpr uint32_t CS_OFF_IDX = CS_OFF_KEY + CAND_CAP * 4;
-constexpr uint32_t CS_OFF_OFF = CS_OFF_IDX + CAND_CAP * 4;  // region offsets, then the compaction buffer
-constexpr uint32_t CS_OFF_HIST = cs_align16(CS_OFF_OFF + CAND_MAX_REGIONS * 4);
-constexpr uint32_t CS_OFF_MISC = cs_align16(CS_OFF_HIST + 4 * 256 * 4);
+// The candidates stay in their regions in global memory (the scorer has
+// just written them, mostly to L2) and each row reads them twice instead of
+// staging them in shared memory.  Every candidate is at or above the row's
+// threshold key tau, so the first pass histograms (key - tau) in CS_BINS
+// bins of 2^CS_SHIFT0 key units (1/512 of a binade for normal floats; the
+// last bin takes everything beyond) and places the K-th key in one bin b0;
+// the histogram's descending exclusive prefix gives each bin above b0 its
+// first output slot (a counting sort of those bins).  A bin b0 holding more
+// than CS_STAGE keys is narrowed to a sub-interval by further CS_BINS-bin
+// passes over its key interval (each divides the interval by CS_BINS, down
+// to a single key value).  The last pass writes every key of the bins above
+// b0 to its bin's next slot and the keys of b0 above the interval after
+// them, and stages the interval's keys, whose rank-rem key (theta) is found
+// by counting ranks.  One CTA per (group, row) item at a time with ~14 KB
+// of shared memory, so many rows are in flight per SM.
+#ifndef DSA_CS_CTAS
+#define DSA_CS_CTAS 6
+#endif
+#ifndef DSA_CS_UNROLL
+#define DSA_CS_UNROLL 2
+#endif
+constexpr int CS_BINS = 1024;
+constexpr int CS_SHIFT0 = 14;
+constexpr int CS_STAGE = 128;
+constexpr int CAND_CTAS_PER_SM = DSA_CS_CTAS;
+constexpr int CS_UNROLL = DSA_CS_UNROLL;  // 16-byte loads per thread in flight in a pass
+constexpr uint32_t CS_OFF_HIST = 0;                                  // level-0 histogram, then slots
+constexpr uint32_t CS_OFF_HIST2 = CS_OFF_HIST + CS_BINS * 4;         // narrowing passes
+constexpr uint32_t CS_OFF_CNT = CS_OFF_HIST2 + CS_BINS * 4;          // per-region candidate counts
+constexpr uint32_t CS_OFF_SKEY = CS_OFF_CNT + CAND_MAX_REGIONS * 4;  // the interval's keys
+constexpr uint32_t CS_OFF_SIDX = CS_OFF_SKEY + CS_STAGE * 4;         // and ids
+constexpr uint32_t CS_OFF_MISC = CS_OFF_SIDX + CS_STAGE * 4;
 constexpr uint32_t CAND_SMEM = CS_OFF_MISC + 32 * 4;
-static_assert(CS_OFF_IDX % 16 == 0 && CS_OFF_OFF % 16 == 0 && CS_OFF_HIST % 16 == 0 && CS_OFF_MISC % 16 == 0,
-              "candidate selector layout");
-static_assert(CAND_THREADS == 256, "block_select_kth / block_emit are written for 256 threads");
-static_assert(3 * (CAND_SMEM + 1024) <= 228 * 1024, "three candidate-selector CTAs per SM");
+static_assert(CAND_THREADS == 256 && CS_BINS == 4 * CAND_THREADS, "desc_scan_pick: 4 bins per thread");
+static_assert(CS_STAGE <= CAND_THREADS, "one staged key per thread");
+static_assert(CAND_CTAS_PER_SM * (CAND_SMEM + 1024) <= 228 * 1024, "candidate-selector CTAs per SM");
 constexpr int CS_PER_THREAD = CAND_MAX_REGIONS / CAND_THREADS;  // regions scanned per thread
 static_assert(CAND_MAX_REGIONS % CAND_THREADS == 0, "region scan");
 
-__global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const CandParams p) {
+__global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_kernel(const CandParams p) {
   pdl_enter();
   extern __shared__ __align__(16) uint8_t smem[];
-  uint32_t* ckey = (uint32_t*)(smem + CS_OFF_KEY);
-  int32_t* cidx = (int32_t*)(smem + CS_OFF_IDX);
-  int* off = (int*)(smem + CS_OFF_OFF);
-  int* shist = (int*)(smem + CS_OFF_HIST);
-  // [0..5] selection scratch, [6] failed-row slot, [8..15] warp sums, [16..23] warp real counts,
-  // [24..25] emission counters
+  int* hist = (int*)(smem + CS_OFF_HIST);
+  int* hist2 = (int*)(smem + CS_OFF_HIST2);
+  int* cnts = (int*)(smem + CS_OFF_CNT);
+  uint32_t* skey = (uint32_t*)(smem + CS_OFF_SKEY);
+  int32_t* sidx = (int32_t*)(smem + CS_OFF_SIDX);
+  // [0..7] bin pick, [8..15] warp sums, [17] staged count, [21] theta,
+  // [22] rr, [23..25] emission counters (staged above / staged equal /
+  // single-value equal), [26] last-CTA flag, [27] next item
   int* misc = (int*)(smem + CS_OFF_MISC);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWARPS = CAND_THREADS / 32;
   const int K = p.K;
   const int items = p.stats->n_groups * GROUP_ROWS;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+  // items: the CTA's own first, then the next from a counter (rows differ
+  // in cost, and a static split left SMs idle at the end)
+  auto next_item = [&]() {
+    if (tid == 0) misc[27] = (int)gridDim.x + atomicAdd(&p.stats->cs_next, 1);
+    __syncthreads();
+    const int v = misc[27];
+    __syncthreads();
+    return v;
+  };
+  for (int it = blockIdx.x; it < items; it = next_item()) {
     const int g = it / GROUP_ROWS, r = it % GROUP_ROWS;
     const Group* gp = p.groups + g;
     if (r >= gp->nrows) continue;  // uniform over the CTA
@@ -840,49 +891,30 @@ __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const Cand
     const int nreg = nu * UNIT_REGIONS;
     const int wcap = region_cap(max(nu, 1));
     const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * UNIT_REGIONS;
-    // certificate over the region counts (wcap + 1 = candidates were lost),
-    // and an exclusive scan of the counts
-    int c[CS_PER_THREAD];
+    // certificate over the region counts (wcap + 1 = candidates were lost)
     int tsum = 0;
     bool lost = nreg > CAND_MAX_REGIONS;
 #pragma unroll
     for (int i = 0; i < CS_PER_THREAD; ++i) {
       const int j = tid * CS_PER_THREAD + i;
       // (a count is in [0, wcap + 1] unless the scorer gave up before
-      // writing it: clamped, so a stale word cannot move a gather out of
+      // writing it: clamped, so a stale word cannot move a read out of
       // the row's slots)
-      const int x = j < nreg && j < CAND_MAX_REGIONS ? max(__ldcg(&cnt[j]), 0) : 0;
+      const int x = j < nreg ? max(__ldcg(&cnt[j]), 0) : 0;
       lost |= x > wcap;
-      c[i] = min(x, wcap);
-      tsum += c[i];
+      const int c = min(x, wcap);
+      cnts[j] = c;
+      tsum += c;
     }
-    int incl = tsum;
+    tsum = __reduce_add_sync(0xffffffffu, tsum);
+    if (lane == 0) misc[8 + warp] = tsum;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
+    for (int j = 0; j < 4; ++j) hist[tid + CAND_THREADS * j] = 0;
+    if (tid == 0) misc[17] = misc[23] = misc[24] = misc[25] = 0;
     const bool any_lost = __syncthreads_or(lost);
-    if (lane == 31) misc[8 + warp] = incl;
-    if (tid == 0) {
-      misc[24] = 0;
-      misc[25] = 0;
-    }
-    __syncthreads();
-    int wbase = 0, n = 0;
+    int n = 0;
 #pragma unroll
-    for (int w = 0; w < NWARPS; ++w) {
-      const int ws = misc[8 + w];
-      wbase += w < warp ? ws : 0;
-      n += ws;
-    }
-    int run = wbase + incl - tsum;
-#pragma unroll
-    for (int i = 0; i < CS_PER_THREAD; ++i) {
-      const int j = tid * CS_PER_THREAD + i;
-      if (j < CAND_MAX_REGIONS) off[j] = run;
-      run += c[i];
-    }
+    for (int w = 0; w < NWARPS; ++w) n += misc[8 + w];
     if (n < K || any_lost || n > CAND_CAP) {
       if (tid == 0) {
         const int f = atomicAdd(&p.stats->fail_count, 1);
@@ -892,55 +924,189 @@ __global__ void __launch_bounds__(CAND_THREADS, 3) cand_select_kernel(const Cand
       __syncthreads();
       continue;
     }
-    __syncthreads();
-    // gather: tpr threads per region (more when regions are few), 16-byte
-    // loads (a region starts on a 4-entry boundary and holds a multiple of
-    // 4 slots, so the last load stays inside it), up to 4 of each array in
-    // flight per thread; region sizes from the offsets (no count reload)
+    if (tid == 0) atomicAdd(&p.stats->cand_total, n);
+    const uint32_t tau = __ldcg(&p.tau[row]);
     const uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
     const int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
+    // tpr threads per region (more when regions are few), two 16-byte loads
+    // each in flight; a region starts on a 4-entry boundary and holds a
+    // multiple of 4 slots, so its last load stays inside it
     int tpr = 4;
     while (tpr < 32 && tpr * 2 * nreg <= CAND_THREADS) tpr *= 2;
-    for (int j = tid / tpr; j < nreg; j += CAND_THREADS / tpr) {
-      const int o = off[j];
-      const int x = (j + 1 < nreg ? off[j + 1] : n) - o;
-      const uint32_t* sk = ck + (int64_t)j * wcap;
-      const int32_t* si = ci + (int64_t)j * wcap;
-      const uint4* sk4 = reinterpret_cast<const uint4*>(sk);
-      const int4* si4 = reinterpret_cast<const int4*>(si);
+    const int rstep = CAND_THREADS / tpr, sub = tid % tpr;
+
+    // pass 1: histogram of (key - tau) >> CS_SHIFT0, and a check that no
+    // candidate is below tau
+    bool below = false;
+    for (int jb = 0; jb < nreg; jb += rstep) {
+      const int j = jb + tid / tpr;
+      const int x = j < nreg ? cnts[j] : 0;
+      const uint4* sk4 = reinterpret_cast<const uint4*>(ck + (int64_t)j * wcap);
       const int x4 = (x + 3) >> 2;
-      for (int i = tid % tpr; i < x4; i += 4 * tpr) {
-        uint4 kv[4];
-        int4 iv[4];
+      for (int e = sub; e < x4; e += CS_UNROLL * tpr) {
+        uint4 v[CS_UNROLL];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int e = i + tpr * q;
-          kv[q] = e < x4 ? __ldcg(&sk4[e]) : make_uint4(0, 0, 0, 0);
-          iv[q] = e < x4 ? __ldcg(&si4[e]) : make_int4(0, 0, 0, 0);
+        for (int u = 0; u < CS_UNROLL; ++u) {
+          const int eu = e + u * tpr;
+          v[u] = eu < x4 ? __ldcg(&sk4[eu]) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int e = 4 * (i + tpr * q);
-          if (e < x) { ckey[o + e] = kv[q].x; cidx[o + e] = iv[q].x; }
-          if (e + 1 < x) { ckey[o + e + 1] = kv[q].y; cidx[o + e + 1] = iv[q].y; }
-          if (e + 2 < x) { ckey[o + e + 2] = kv[q].z; cidx[o + e + 2] = iv[q].z; }
-          if (e + 3 < x) { ckey[o + e + 3] = kv[q].w; cidx[o + e + 3] = iv[q].w; }
+        for (int u = 0; u < CS_UNROLL; ++u) {
+          const uint32_t kk[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (4 * (e + u * tpr) + c < x) {
+              below |= kk[c] < tau;
+              atomicAdd(&hist[min((kk[c] - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1))], 1);
+            }
+          }
         }
       }
     }
-    // key 0 pads the list to a multiple of 4 (every real key is non-zero)
-    const int n4 = (n + 3) & ~3;
-    if (tid < n4 - n) {
-      ckey[n + tid] = 0u;
-      cidx[n + tid] = -1;
+    if (__syncthreads_or(below)) {
+      // (the filter keeps keys at or above tau only: never taken; a row
+      // that broke it is rescored exactly)
+      if (tid == 0) {
+        const int f = atomicAdd(&p.stats->fail_count, 1);
+        p.failed_rows[f] = row;
+        atomicAdd(&p.stats->overflow, 1);
+      }
+      __syncthreads();
+      continue;
     }
-    if (tid == 0) atomicAdd(&p.stats->cand_total, n);
+    desc_scan_pick(hist, CS_BINS, K, misc, true);  // hist now holds each bin's first slot
+    const uint32_t b0 = (uint32_t)misc[2];
+    int rem = misc[3], bc = misc[4];
+    // the K-th key's interval [lo, hi)
+    unsigned long long lo = (unsigned long long)tau + ((unsigned long long)b0 << CS_SHIFT0);
+    unsigned long long hi = 1ull << 32;
+    if (b0 < CS_BINS - 1) hi = min(hi, lo + (1ull << CS_SHIFT0));
+    // narrowing passes while the interval holds more keys than the stage
+#pragma unroll 1
+    while (bc > CS_STAGE && hi - lo > 1) {
+      const int s = max(0, 64 - __clzll((long long)(hi - lo - 1)) - 10);
+      const uint32_t lo32 = (uint32_t)lo, hin = (uint32_t)(hi - 1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) hist2[tid + CAND_THREADS * j] = 0;
+      __syncthreads();
+      for (int jb = 0; jb < nreg; jb += rstep) {
+        const int j = jb + tid / tpr;
+        const int x = j < nreg ? cnts[j] : 0;
+        const uint4* sk4 = reinterpret_cast<const uint4*>(ck + (int64_t)j * wcap);
+        const int x4 = (x + 3) >> 2;
+        for (int e = sub; e < x4; e += tpr) {
+          const uint4 v = __ldcg(&sk4[e]);
+          const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (4 * e + c < x && kk[c] >= lo32 && kk[c] <= hin) atomicAdd(&hist2[(kk[c] - lo32) >> s], 1);
+        }
+      }
+      __syncthreads();
+      desc_scan_pick(hist2, CS_BINS, rem, misc, false);
+      rem = misc[3];
+      bc = misc[4];
+      lo += (unsigned long long)misc[2] << s;
+      hi = min(hi, lo + (1ull << s));
+    }
+    const bool single = hi - lo == 1;  // the interval is one key value: theta
+    const uint32_t lo32 = (uint32_t)lo, hin = (uint32_t)(hi - 1);
+    int32_t* o = p.out + (int64_t)row * K;
+
+    // last pass: the bins above b0 to their slots (o[0, A0)), the keys of
+    // b0 above the interval next (to o[K - rem)), the interval's keys
+    // staged (or, for a single value, its first rem keys to o[K - rem, K))
+    for (int jb = 0; jb < nreg; jb += rstep) {
+      const int j = jb + tid / tpr;
+      const int x = j < nreg ? cnts[j] : 0;
+      const uint4* sk4 = reinterpret_cast<const uint4*>(ck + (int64_t)j * wcap);
+      const int4* si4 = reinterpret_cast<const int4*>(ci + (int64_t)j * wcap);
+      const int x4 = (x + 3) >> 2;
+      for (int e = sub; e < x4; e += CS_UNROLL * tpr) {
+        uint4 v[CS_UNROLL];
+        int4 d[CS_UNROLL];
+#pragma unroll
+        for (int u = 0; u < CS_UNROLL; ++u) {
+          const int eu = e + u * tpr;
+          v[u] = eu < x4 ? __ldcg(&sk4[eu]) : make_uint4(0, 0, 0, 0);
+          d[u] = eu < x4 ? __ldcg(&si4[eu]) : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int c = 0; c < 4 * CS_UNROLL; ++c) {
+          const uint4 vu = v[c >> 2];
+          const int4 du = d[c >> 2];
+          const uint32_t kq[4] = {vu.x, vu.y, vu.z, vu.w};
+          const int32_t iq[4] = {du.x, du.y, du.z, du.w};
+          if (4 * (e + (c >> 2) * tpr) + (c & 3) < x) {
+            const uint32_t k = kq[c & 3];
+            const int32_t idc = iq[c & 3];
+            const uint32_t bin = min((k - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1));
+            if (bin > b0) {
+              o[atomicAdd(&hist[bin], 1)] = idc;
+            } else if (bin == b0) {
+              if (k > hin) {
+                o[atomicAdd(&hist[b0], 1)] = idc;
+              } else if (k >= lo32) {
+                if (single) {
+                  const int q = atomicAdd(&misc[25], 1);
+                  if (q < rem) o[K - rem + q] = idc;
+                } else {
+                  const int q = atomicAdd(&misc[17], 1);
+                  skey[q] = k;
+                  sidx[q] = idc;
+                }
+              }
+            }
+          }
+        }
+      }
+    }
     __syncthreads();
-    uint32_t theta;
-    int rr;
-    block_select_kth(ckey, n4, K, shist, (uint32_t*)off, CAND_MAX_REGIONS, misc, theta, rr);
-    block_emit(ckey, cidx, n4, theta, rr, K, p.out + (int64_t)row * K, misc + 24);
+    if (!single) {
+      // the rem-th largest of the bc staged keys: the first of its equal
+      // keys whose count of larger keys is below rem and reaches rem with
+      // its equals
+      const bool mine = tid < bc;
+      const uint32_t me = mine ? skey[tid] : 0u;
+      if (mine) {
+        int gt = 0, eq = 0, eqb = 0;
+        for (int j = 0; j < bc; ++j) {
+          const uint32_t y = skey[j];
+          gt += y > me;
+          eq += y == me;
+          eqb += (y == me) & (j < tid);
+        }
+        if (eqb == 0 && gt < rem && rem <= gt + eq) {
+          misc[21] = (int)me;
+          misc[22] = rem - gt;
+        }
+      }
+      __syncthreads();
+      const uint32_t theta = (uint32_t)misc[21];
+      const int rr = misc[22];
+      if (mine) {
+        if (me > theta) {
+          o[K - rem + atomicAdd(&misc[23], 1)] = sidx[tid];
+        } else if (me == theta) {
+          const int q = atomicAdd(&misc[24], 1);
+          if (q < rr) o[K - rr + q] = sidx[tid];
+        }
+      }
+    }
     __syncthreads();
+  }
+  // the CTA that finishes last writes the repair plan (the rows queued
+  // above), which the repair scorer launched next reads
+  if (p.plan_repair) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) misc[26] = atomicAdd(&p.stats->cs_done, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    const bool last = misc[26] != 0;
+    if (last) {
+      __threadfence();
+      plan_groups(p.repair, repair_groups(p.repair), misc, hist);
+    }
   }
 }
 
@@ -950,6 +1116,8 @@ cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   return launch_pdl(cand_select_kernel, dim3(grid), dim3(CAND_THREADS), CAND_SMEM, s, p);
 }
+
+int cand_select_ctas_per_sm() { return CAND_CTAS_PER_SM; }
 
 // ============================================================ wide select ==
 // The rows whose certificate failed are few and long: each is selected by a
