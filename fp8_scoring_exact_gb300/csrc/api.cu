@@ -440,7 +440,7 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
   rp.unit_start = at<int32_t>(a, L.runit_start);
   cs.plan_repair = 1;
   cs.repair = rp;
-  DSA_LAUNCH(launch_cand_select(cs, cand_select_ctas_per_sm() * o.grid, stream));
+  DSA_LAUNCH(launch_cand_select(cs, o.grid, stream));
 
   ScoreParams rcp = cp;
   rcp.withhold_first_acc = 0;
@@ -847,7 +847,7 @@ int enqueue_matrix_select(Arena* a, const RowSpace& rs, int K, const Opts& o, co
   cs.tau = tau;
   cs.out = out;
   cs.stats = st;
-  DSA_LAUNCH(launch_cand_select(cs, cand_select_ctas_per_sm() * o.grid, stream));
+  DSA_LAUNCH(launch_cand_select(cs, o.grid, stream));
   WideParams wp{};
   wp.rs = rs;
   wp.K = K;

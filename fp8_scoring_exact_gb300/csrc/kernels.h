@@ -280,8 +280,7 @@ cudaError_t launch_sample_tau(const SampleTauParams& p, cudaStream_t s);
 cudaError_t launch_score(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const ScoreParams& p, int grid,
                          cudaStream_t s);
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
-cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s);
-int cand_select_ctas_per_sm();  // the selector's CTAs resident per SM (its grid: this x SMs)
+cudaError_t launch_cand_select(const CandParams& p, int sms, cudaStream_t s);  // grid: a few CTAs per SM
 cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s);
 cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStream_t s);
 cudaError_t launch_sparse_attn(const SparseAttnParams& p, cudaStream_t s);

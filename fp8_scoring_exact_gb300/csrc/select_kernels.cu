@@ -205,11 +205,78 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   return launch_pdl(plan_kernel, dim3(1), dim3(PLAN_THREADS), 0, s, p);
 }
 
+// The rank-th largest (1 <= rank <= m) of a warp's m keys, key[q] of lane l
+// being key q * 32 + l (positions >= m ignored): 8-bit radix passes in a
+// per-warp histogram (hist: 256 ints, pick: 4 ints of shared memory), with
+// no CTA barrier.  The leading bytes every key shares are the answer's too
+// (a row's samples have similar magnitudes, so the first byte or two
+// usually are): the passes start below them.
+template <int KPL>
+__device__ __forceinline__ uint32_t warp_select_rank(const uint32_t (&key)[KPL], int m, int rank, int* hist,
+                                                     int* pick) {
+  const int lane = threadIdx.x & 31;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int q = 0; q < KPL; ++q) {
+    if (q * 32 + lane < m) {
+      kmin = min(kmin, key[q]);
+      kmax = max(kmax, key[q]);
+    }
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  const uint32_t diff = kmin ^ kmax;
+  const int shared_bytes = diff ? (int)(__clz(diff) >> 3) : 4;
+  uint32_t mask = shared_bytes ? (0xffffffffu << (32 - 8 * shared_bytes)) : 0u;
+  uint32_t prefix = kmin & mask;
+  int rem = rank;
+#pragma unroll 1
+  for (int pass = shared_bytes; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+#pragma unroll
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < KPL; ++q) {
+      const int i = q * 32 + lane;
+      if (i < m && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & 0xFFu], 1);
+    }
+    __syncwarp();
+    radix_pick_digit(hist, rem, pick);
+    __syncwarp();
+    prefix |= (uint32_t)pick[0] << shift;
+    mask |= 0xFFu << shift;
+    rem = pick[1];
+    const int cnt = pick[2];
+    __syncwarp();
+    if (cnt == 1) {
+      // the answer is the only key in its bucket: read it whole instead of
+      // running the remaining passes
+      uint32_t found = 0u;
+      bool have = false;
+#pragma unroll
+      for (int q = 0; q < KPL; ++q) {
+        const int i = q * 32 + lane;
+        if (i < m && (key[q] & mask) == prefix) {
+          found = key[q];
+          have = true;
+        }
+      }
+      const unsigned b = __ballot_sync(0xffffffffu, have);
+      prefix = __shfl_sync(0xffffffffu, found, __ffs(b) - 1);
+      break;
+    }
+  }
+  return prefix;
+}
+
 // ================================================================== sample ==
 // One CTA (4 warps) per query-row pair: rows with at most K keys take the
 // remapping path; the other rows score the keys on a 1-in-200 grid with
 // tcgen05 (keys gathered into a swizzled shared tile by the threads) and take
-// as threshold the sample of descending rank ceil(m * target / L).
+// as threshold the sample of descending rank ceil(m * target / L), one warp
+// per row once the scores are out of tensor memory (which is released first,
+// so the next CTA on the SM can start its MMA).
 // Split mode (paged rows, whose grids span several tiles): one CTA per (pair,
 // 128-key sample tile), so the tiles' gathers run side by side; each writes
 // its fp32 sample scores (and the tile-0 CTA the rows' sample ranges and
@@ -220,8 +287,9 @@ constexpr uint32_t SM_OFF_K = SM_OFF_Q + SAMPLE_ROWS * H * D;       // 16384
 constexpr uint32_t SM_OFF_SAMP = SM_OFF_K + TILE * D;               // 32768
 constexpr uint32_t SM_OFF_W = SM_OFF_SAMP + SAMPLE_ROWS * MAX_SAMPLES * 4;  // 40960
 constexpr uint32_t SM_OFF_SC = SM_OFF_W + SAMPLE_ROWS * H * 4;
-constexpr uint32_t SM_OFF_HIST = SM_OFF_SC + TILE * 4;
-constexpr uint32_t SM_OFF_MISC = SM_OFF_HIST + 256 * 4;
+constexpr uint32_t SM_OFF_HIST = SM_OFF_SC + TILE * 4;                   // a 256-bin histogram per warp
+constexpr uint32_t SM_OFF_PICK = SM_OFF_HIST + (SAMPLE_THREADS / 32) * 256 * 4;  // and its pick words
+constexpr uint32_t SM_OFF_MISC = SM_OFF_PICK + (SAMPLE_THREADS / 32) * 4 * 4;
 // 52 KB per CTA: 4 CTAs (4 x 128 TMEM columns, all 512) fit on an SM, and
 // the launch bounds hold the registers to 128 so that 4 CTAs fit there too
 constexpr uint32_t SAMPLE_SMEM = 52 * 1024;
@@ -236,11 +304,10 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
   uint32_t* samp = (uint32_t*)(smem + SM_OFF_SAMP);
   float* wsm = (float*)(smem + SM_OFF_W);
   float* scs = (float*)(smem + SM_OFF_SC);
-  int* hist = (int*)(smem + SM_OFF_HIST);
-  int* misc = (int*)(smem + SM_OFF_MISC);  // [0] tmem base, [1..4] digit block, [5] abort, [6] wait result
+  int* misc = (int*)(smem + SM_OFF_MISC);  // [0] tmem base, [5] abort, [6] wait result
   const uint32_t bar = sbase + SM_OFF_MISC + 32;
   const RowSpace& rs = p.rs;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = p.K;
 
   int rows[SAMPLE_ROWS];
@@ -300,14 +367,6 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     mbar_arrive_expect_tx(bar, nact * H * D);
     for (int a = 0; a < nact; ++a) tma_load_2d(sbase + SM_OFF_Q + a * H * D, &tm_q, 0, act[a] * H, bar);
   }
-  // thread 0 waits (bounded) and the CTA follows its result; pend = the
-  // parity of the phase whose copy or MMA is outstanding (at most one)
-  uint32_t pend = 0;
-  if (tid == 0) misc[6] = mbar_wait(bar, 0, abort_flag, p.stats) ? 1 : 0;
-  __syncwarp();
-  __syncthreads();
-  bool ok = misc[6] != 0;
-  const uint32_t idesc = idesc_e4m3_f32(TILE, H * nact);
   // tiles [tt_begin, tt_end) of the pair's grid: all of them, or this
   // CTA's one in split mode
   const int tt_begin = tile0;
@@ -338,6 +397,14 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     }
   };
   fetch(tt_begin);
+  // thread 0 waits (bounded) and the CTA follows its result; pend = the
+  // parity of the phase whose copy or MMA is outstanding (at most one)
+  uint32_t pend = 0;
+  if (tid == 0) misc[6] = mbar_wait(bar, 0, abort_flag, p.stats) ? 1 : 0;
+  __syncwarp();
+  __syncthreads();
+  bool ok = misc[6] != 0;
+  const uint32_t idesc = idesc_e4m3_f32(TILE, H * nact);
   for (int tt = tt_begin; tt < tt_end && ok; ++tt) {
     const int j = tt * TILE + tid;
     const bool vj = j < m_u;
@@ -366,14 +433,20 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     if (!ok) break;
     tc_fence_after();
     for (int a = 0; a < nact; ++a) {
-      uint32_t v[H];
       const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + a * H;
-      tmem_ld32(ta, v);
-      tmem_ld32(ta + 32, v + 32);
-      tmem_wait_ld();
-      float acc = 0.f;
+      // four interleaved sums (a 64-long chain of dependent FMAs would set
+      // the epilogue's latency), 32 heads per TMEM load
+      float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int h = 0; h < H; ++h) acc = fmaf(wsm[a * H + h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
+      for (int hh = 0; hh < H; hh += 32) {
+        uint32_t v[32];
+        tmem_ld32(ta + hh, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          a4[h & 3] = fmaf(wsm[a * H + hh + h], fmaxf(__uint_as_float(v[h]), 0.f), a4[h & 3]);
+      }
+      const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
       if (vj) {
         if (split)
           p.sscores[(int64_t)act[a] * p.sld + j] = acc * scs[tid];
@@ -385,27 +458,6 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     __syncthreads();
   }
 
-  // threshold of each active row from the samples inside its own range
-  for (int a = 0; a < nact && ok && !split; ++a) {
-    const int row = act[a];
-    const int b = p.rb[row], e = p.re[row];
-    const int j0 = max(0, ceil_div(b - first, S));
-    const int j1 = min(m_u, ceil_div(e - first, S));
-    const int m = max(0, j1 - j0);
-    const int rank = sample_rank(m, e - b, target);
-    uint32_t tau = 0u;
-    if (m > 0 && rank >= 1 && rank <= m) {
-      const uint32_t* sa = samp + a * MAX_SAMPLES + j0;
-      int rr;
-      group_radix_select([&](int i) { return sa[i]; }, m, rank, hist, misc + 1, tid, SAMPLE_THREADS, 0, tau, rr);
-      if (p.tau_bias != 0) {
-        const int64_t t = (int64_t)tau + p.tau_bias;
-        tau = (uint32_t)(t < 0 ? 0 : (t > 0xffffffffll ? 0xffffffffll : t));
-      }
-    }
-    if (tid == 0) p.tau[row] = tau;
-  }
-  if (!ok && !split && tid < nact) p.tau[act[tid]] = 0u;
   // a wait gave up: the copy or MMA it waited for lands before the shared
   // memory and TMEM are released
   if (!ok && tid == 0) mbar_drain(bar, pend);
@@ -414,6 +466,37 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, TILE);
+  }
+  if (split) return;
+  // threshold of active row a (by warp a) from the samples inside its own
+  // range (at most one tile of them: a grid of more takes the shared-grid
+  // path; a larger m would leave the threshold at 0, every key a candidate,
+  // and the certificate would send the row to repair)
+  if (warp < nact) {
+    const int row = act[warp];
+    uint32_t tau = 0u;
+    if (ok) {
+      const int b = p.rb[row], e = p.re[row];
+      const int j0 = max(0, ceil_div(b - first, S));
+      const int j1 = min(m_u, ceil_div(e - first, S));
+      const int m = max(0, j1 - j0);
+      const int rank = sample_rank(m, e - b, target);
+      if (m > 0 && m <= 4 * 32 && rank >= 1 && rank <= m) {
+        uint32_t key[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = q * 32 + lane;
+          key[q] = i < m ? samp[warp * MAX_SAMPLES + j0 + i] : 0u;
+        }
+        tau = warp_select_rank<4>(key, m, rank, (int*)(smem + SM_OFF_HIST) + warp * 256,
+                                  (int*)(smem + SM_OFF_PICK) + warp * 4);
+        if (p.tau_bias != 0) {
+          const int64_t t = (int64_t)tau + p.tau_bias;
+          tau = (uint32_t)(t < 0 ? 0 : (t > 0xffffffffll ? 0xffffffffll : t));
+        }
+      }
+    }
+    if (lane == 0) p.tau[row] = tau;
   }
 }
 
@@ -502,63 +585,12 @@ __global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTau
     uint32_t tau = 0u;
     if (m > 0 && rank >= 1 && rank <= m) {
       uint32_t key[TAU_KEYS_PER_LANE];
-      uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
       for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
         const int i = q * 32 + lane;
         key[q] = i < m ? ordered_key(__ldcg(&sr[(int64_t)i * stride])) : 0u;
-        if (i < m) {
-          kmin = min(kmin, key[q]);
-          kmax = max(kmax, key[q]);
-        }
       }
-      // the leading bytes every sample shares are the threshold's too (the
-      // samples of a row have similar magnitudes, so the first byte or two
-      // usually are): the radix passes start below them
-      kmin = __reduce_min_sync(0xffffffffu, kmin);
-      kmax = __reduce_max_sync(0xffffffffu, kmax);
-      const uint32_t diff = kmin ^ kmax;
-      const int shared_bytes = diff ? (int)(__clz(diff) >> 3) : 4;
-      uint32_t mask = shared_bytes ? (0xffffffffu << (32 - 8 * shared_bytes)) : 0u;
-      uint32_t prefix = kmin & mask;
-      int rem = rank;
-#pragma unroll 1
-      for (int pass = shared_bytes; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-#pragma unroll
-        for (int i = lane; i < 256; i += 32) hist[i] = 0;
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
-          const int i = q * 32 + lane;
-          if (i < m && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & 0xFFu], 1);
-        }
-        __syncwarp();
-        radix_pick_digit(hist, rem, pick);
-        __syncwarp();
-        prefix |= (uint32_t)pick[0] << shift;
-        mask |= 0xFFu << shift;
-        rem = pick[1];
-        const int cnt = pick[2];
-        __syncwarp();
-        if (cnt == 1) {
-          // the threshold is the only sample in its bucket: read it whole
-          // instead of running the remaining passes
-          uint32_t found = 0u;
-          bool have = false;
-#pragma unroll
-          for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
-            const int i = q * 32 + lane;
-            if (i < m && (key[q] & mask) == prefix) {
-              found = key[q];
-              have = true;
-            }
-          }
-          const unsigned b = __ballot_sync(0xffffffffu, have);
-          prefix = __shfl_sync(0xffffffffu, found, __ffs(b) - 1);
-          break;
-        }
-      }
+      const uint32_t prefix = warp_select_rank<TAU_KEYS_PER_LANE>(key, m, rank, hist, pick);
       tau = prefix;
       if (p.tau_bias != 0) {
         const int64_t t = (int64_t)tau + p.tau_bias;
@@ -831,31 +863,31 @@ __global__ void __launch_bounds__(SELECT_THREADS) select_kernel(const SelectPara
 // them, and stages the interval's keys, whose rank-rem key (theta) is found
 // by counting ranks.  One CTA per (group, row) item at a time with ~14 KB
 // of shared memory, so many rows are in flight per SM.
-#ifndef DSA_CS_CTAS
-#define DSA_CS_CTAS 6
-#endif
-#ifndef DSA_CS_UNROLL
-#define DSA_CS_UNROLL 2
-#endif
 constexpr int CS_BINS = 1024;
 constexpr int CS_SHIFT0 = 14;
 constexpr int CS_STAGE = 128;
-constexpr int CAND_CTAS_PER_SM = DSA_CS_CTAS;
-constexpr int CS_UNROLL = DSA_CS_UNROLL;  // 16-byte loads per thread in flight in a pass
+// Two builds of the selector (measured on GB300): many rows (more than
+// CS_FEW_PER_SM per SM), 6 CTAs per SM with two 16-byte loads in flight per
+// thread and pass (throughput); few rows, 4 CTAs per SM (more registers)
+// with four (a row's latency: its loads take fewer rounds).
+constexpr int CS_MANY_CTAS = 6, CS_MANY_UNROLL = 2;
+constexpr int CS_FEW_CTAS = 4, CS_FEW_UNROLL = 4, CS_FEW_PER_SM = 4;
 constexpr uint32_t CS_OFF_HIST = 0;                                  // level-0 histogram, then slots
 constexpr uint32_t CS_OFF_HIST2 = CS_OFF_HIST + CS_BINS * 4;         // narrowing passes
 constexpr uint32_t CS_OFF_CNT = CS_OFF_HIST2 + CS_BINS * 4;          // per-region candidate counts
 constexpr uint32_t CS_OFF_SKEY = CS_OFF_CNT + CAND_MAX_REGIONS * 4;  // the interval's keys
 constexpr uint32_t CS_OFF_SIDX = CS_OFF_SKEY + CS_STAGE * 4;         // and ids
-constexpr uint32_t CS_OFF_MISC = CS_OFF_SIDX + CS_STAGE * 4;
+constexpr uint32_t CS_OFF_OUT = CS_OFF_SIDX + CS_STAGE * 4;          // the row's output, written out at the end
+constexpr uint32_t CS_OFF_MISC = CS_OFF_OUT + MAX_K * 4;
 constexpr uint32_t CAND_SMEM = CS_OFF_MISC + 32 * 4;
 static_assert(CAND_THREADS == 256 && CS_BINS == 4 * CAND_THREADS, "desc_scan_pick: 4 bins per thread");
 static_assert(CS_STAGE <= CAND_THREADS, "one staged key per thread");
-static_assert(CAND_CTAS_PER_SM * (CAND_SMEM + 1024) <= 228 * 1024, "candidate-selector CTAs per SM");
+static_assert(CS_MANY_CTAS * (CAND_SMEM + 1024) <= 228 * 1024, "candidate-selector CTAs per SM");
 constexpr int CS_PER_THREAD = CAND_MAX_REGIONS / CAND_THREADS;  // regions scanned per thread
 static_assert(CAND_MAX_REGIONS % CAND_THREADS == 0, "region scan");
 
-__global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_kernel(const CandParams p) {
+template <int CTAS, int CS_UNROLL>
+__global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const CandParams p) {
   pdl_enter();
   extern __shared__ __align__(16) uint8_t smem[];
   int* hist = (int*)(smem + CS_OFF_HIST);
@@ -863,6 +895,7 @@ __global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_ke
   int* cnts = (int*)(smem + CS_OFF_CNT);
   uint32_t* skey = (uint32_t*)(smem + CS_OFF_SKEY);
   int32_t* sidx = (int32_t*)(smem + CS_OFF_SIDX);
+  int32_t* so = (int32_t*)(smem + CS_OFF_OUT);
   // [0..7] bin pick, [8..15] warp sums, [17] staged count, [21] theta,
   // [22] rr, [23..25] emission counters (staged above / staged equal /
   // single-value equal), [26] last-CTA flag, [27] next item
@@ -871,16 +904,19 @@ __global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_ke
   constexpr int NWARPS = CAND_THREADS / 32;
   const int K = p.K;
   const int items = p.stats->n_groups * GROUP_ROWS;
-  // items: the CTA's own first, then the next from a counter (rows differ
-  // in cost, and a static split left SMs idle at the end)
-  auto next_item = [&]() {
+  // items: the CTA's own first, then (the many-row build) the next from a
+  // counter: rows differ in cost, and a static split left SMs idle at the
+  // end; the few-row build has at most one item per CTA
+  constexpr bool dynamic = CTAS == CS_MANY_CTAS;
+  auto next_item = [&](int cur) {
+    if (!dynamic) return cur + (int)gridDim.x;
     if (tid == 0) misc[27] = (int)gridDim.x + atomicAdd(&p.stats->cs_next, 1);
     __syncthreads();
     const int v = misc[27];
     __syncthreads();
     return v;
   };
-  for (int it = blockIdx.x; it < items; it = next_item()) {
+  for (int it = blockIdx.x; it < items; it = next_item(it)) {
     const int g = it / GROUP_ROWS, r = it % GROUP_ROWS;
     const Group* gp = p.groups + g;
     if (r >= gp->nrows) continue;  // uniform over the CTA
@@ -891,6 +927,7 @@ __global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_ke
     const int nreg = nu * UNIT_REGIONS;
     const int wcap = region_cap(max(nu, 1));
     const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * UNIT_REGIONS;
+    const uint32_t tau = __ldcg(&p.tau[row]);
     // certificate over the region counts (wcap + 1 = candidates were lost)
     int tsum = 0;
     bool lost = nreg > CAND_MAX_REGIONS;
@@ -925,14 +962,16 @@ __global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_ke
       continue;
     }
     if (tid == 0) atomicAdd(&p.stats->cand_total, n);
-    const uint32_t tau = __ldcg(&p.tau[row]);
     const uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
     const int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
-    // tpr threads per region (more when regions are few), two 16-byte loads
-    // each in flight; a region starts on a 4-entry boundary and holds a
-    // multiple of 4 slots, so its last load stays inside it
-    int tpr = 4;
-    while (tpr < 32 && tpr * 2 * nreg <= CAND_THREADS) tpr *= 2;
+    // tpr threads per region, enough for one round of CS_UNROLL 16-byte
+    // loads each over an average region (many short regions: one thread
+    // each, so that all of a row's loads are in flight at once); a region
+    // starts on a 4-entry boundary and holds a multiple of 4 slots, so its
+    // last load stays inside it
+    const int avg4 = ceil_div(n, 4 * nreg);
+    int tpr = 1;
+    while (tpr < 32 && tpr * CS_UNROLL < avg4) tpr *= 2;
     const int rstep = CAND_THREADS / tpr, sub = tid % tpr;
 
     // pass 1: histogram of (key - tau) >> CS_SHIFT0, and a check that no
@@ -1013,9 +1052,10 @@ __global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_ke
     const uint32_t lo32 = (uint32_t)lo, hin = (uint32_t)(hi - 1);
     int32_t* o = p.out + (int64_t)row * K;
 
-    // last pass: the bins above b0 to their slots (o[0, A0)), the keys of
-    // b0 above the interval next (to o[K - rem)), the interval's keys
-    // staged (or, for a single value, its first rem keys to o[K - rem, K))
+    // last pass (slots in the shared copy of the row's output): the bins
+    // above b0 to their slots ([0, A0)), the keys of b0 above the interval
+    // next (to K - rem), the interval's keys staged (or, for a single value,
+    // its first rem keys to [K - rem, K))
     for (int jb = 0; jb < nreg; jb += rstep) {
       const int j = jb + tid / tpr;
       const int x = j < nreg ? cnts[j] : 0;
@@ -1042,14 +1082,14 @@ __global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_ke
             const int32_t idc = iq[c & 3];
             const uint32_t bin = min((k - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1));
             if (bin > b0) {
-              o[atomicAdd(&hist[bin], 1)] = idc;
+              so[atomicAdd(&hist[bin], 1)] = idc;
             } else if (bin == b0) {
               if (k > hin) {
-                o[atomicAdd(&hist[b0], 1)] = idc;
+                so[atomicAdd(&hist[b0], 1)] = idc;
               } else if (k >= lo32) {
                 if (single) {
                   const int q = atomicAdd(&misc[25], 1);
-                  if (q < rem) o[K - rem + q] = idc;
+                  if (q < rem) so[K - rem + q] = idc;
                 } else {
                   const int q = atomicAdd(&misc[17], 1);
                   skey[q] = k;
@@ -1086,21 +1126,28 @@ __global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_ke
       const int rr = misc[22];
       if (mine) {
         if (me > theta) {
-          o[K - rem + atomicAdd(&misc[23], 1)] = sidx[tid];
+          so[K - rem + atomicAdd(&misc[23], 1)] = sidx[tid];
         } else if (me == theta) {
           const int q = atomicAdd(&misc[24], 1);
-          if (q < rr) o[K - rr + q] = sidx[tid];
+          if (q < rr) so[K - rr + q] = sidx[tid];
         }
       }
     }
+    // the row out, coalesced (the slots above scatter)
+    __syncthreads();
+    for (int i = tid; i < K; i += CAND_THREADS) o[i] = so[i];
     __syncthreads();
   }
   // the CTA that finishes last writes the repair plan (the rows queued
   // above), which the repair scorer launched next reads
   if (p.plan_repair) {
-    __threadfence();
+    // (thread 0 wrote this CTA's failed-row entries: its fence orders them
+    // before its ticket)
     __syncthreads();
-    if (tid == 0) misc[26] = atomicAdd(&p.stats->cs_done, 1) == (int)gridDim.x - 1;
+    if (tid == 0) {
+      __threadfence();
+      misc[26] = atomicAdd(&p.stats->cs_done, 1) == (int)gridDim.x - 1;
+    }
     __syncthreads();
     const bool last = misc[26] != 0;
     if (last) {
@@ -1110,14 +1157,19 @@ __global__ void __launch_bounds__(CAND_THREADS, CAND_CTAS_PER_SM) cand_select_ke
   }
 }
 
-cudaError_t launch_cand_select(const CandParams& p, int grid, cudaStream_t s) {
-  static DeviceFlags attr_set;
-  cudaError_t e = set_smem_attr_once(cand_select_kernel, CAND_SMEM, attr_set);
+cudaError_t launch_cand_select(const CandParams& p, int sms, cudaStream_t s) {
+  static DeviceFlags attr_many, attr_few;
+  if (p.rs.R > CS_FEW_PER_SM * sms) {
+    auto k = cand_select_kernel<CS_MANY_CTAS, CS_MANY_UNROLL>;
+    cudaError_t e = set_smem_attr_once(k, CAND_SMEM, attr_many);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k, dim3(CS_MANY_CTAS * sms), dim3(CAND_THREADS), CAND_SMEM, s, p);
+  }
+  auto k = cand_select_kernel<CS_FEW_CTAS, CS_FEW_UNROLL>;
+  cudaError_t e = set_smem_attr_once(k, CAND_SMEM, attr_few);
   if (e != cudaSuccess) return e;
-  return launch_pdl(cand_select_kernel, dim3(grid), dim3(CAND_THREADS), CAND_SMEM, s, p);
+  return launch_pdl(k, dim3(CS_FEW_CTAS * sms), dim3(CAND_THREADS), CAND_SMEM, s, p);
 }
-
-int cand_select_ctas_per_sm() { return CAND_CTAS_PER_SM; }
 
 // ============================================================ wide select ==
 // The rows whose certificate failed are few and long: each is selected by a
