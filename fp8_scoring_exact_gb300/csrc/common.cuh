@@ -41,7 +41,6 @@ __host__ __device__ constexpr int region_cap(int nunits) {
 // -------------------------------------------------------------- selection --
 constexpr int MAX_K = 2048;        // largest K (the public header's DSA_MAX_K)
 constexpr int CAND_CAP = 8192;     // candidates selected per row (certificate capacity)
-constexpr int CAND_THREADS = 256;  // candidate selector: threads per CTA
 constexpr int CAND_MAX_REGIONS = 1024;  // regions (units x 4) one row may have
 constexpr int SAMPLE_STRIDE = 200; // one sample per 200 keys: ~0.5% of the row
 constexpr int SAMPLE_OFFSET = 100; // samples at keys 100 mod 200

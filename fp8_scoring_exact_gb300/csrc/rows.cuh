@@ -195,18 +195,21 @@ __device__ __forceinline__ int sample_rank(int m, int L, int target) {
 }
 
 // ------------------------------------------- whole-CTA selection (256 threads)
-// Descending scan of nb (<= 1024) bin counts by 256 threads (4 bins each,
-// thread t owns bins nb-1-4t .. nb-4-4t): the bin that holds the rem-th
-// largest key goes to sc[2], the rank inside it to sc[3], its count to
-// sc[4]; with `slots`, every bin's count is replaced by the number of keys
-// in the bins above it (its first slot in a descending counting sort).
-// sc[8..15]: warp sums.  Ends with a CTA barrier.
+// Descending scan of nb (<= 1024) bin counts by the NT threads of a CTA
+// (1024 / NT bins each, thread t owning the t-th run from the top): the
+// bin that holds the rem-th largest key goes to sc[2], the rank inside it
+// to sc[3], its count to sc[4]; with `slots`, every bin's count is
+// replaced by the number of keys in the bins above it (its first slot in a
+// descending counting sort).  sc[32..63]: warp sums.  Ends with a CTA
+// barrier.
+template <int NT>
 __device__ __forceinline__ void desc_scan_pick(int* hist, int nb, int rem, int* sc, bool slots) {
+  constexpr int BPT = 1024 / NT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int c[4], s = 0;
+  int c[BPT], s = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int b = nb - 1 - 4 * tid - j;
+  for (int j = 0; j < BPT; ++j) {
+    const int b = nb - 1 - BPT * tid - j;
     c[j] = b >= 0 ? hist[b] : 0;
     s += c[j];
   }
@@ -216,14 +219,14 @@ __device__ __forceinline__ void desc_scan_pick(int* hist, int nb, int rem, int* 
     const int v = __shfl_up_sync(0xffffffffu, incl, d);
     if (lane >= d) incl += v;
   }
-  if (lane == 31) sc[8 + warp] = incl;
+  if (lane == 31) sc[32 + warp] = incl;
   __syncthreads();
 #pragma unroll
-  for (int w = 0; w < 8; ++w) incl += w < warp ? sc[8 + w] : 0;
+  for (int w = 0; w < NT / 32; ++w) incl += w < warp ? sc[32 + w] : 0;
   int e = incl - s;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int b = nb - 1 - 4 * tid - j;
+  for (int j = 0; j < BPT; ++j) {
+    const int b = nb - 1 - BPT * tid - j;
     if (e < rem && rem <= e + c[j]) {
       sc[2] = b;
       sc[3] = rem - e;

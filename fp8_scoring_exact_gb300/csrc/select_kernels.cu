@@ -867,11 +867,21 @@ constexpr int CS_BINS = 1024;
 constexpr int CS_SHIFT0 = 14;
 constexpr int CS_STAGE = 128;
 // Two builds of the selector (measured on GB300): many rows (more than
-// CS_FEW_PER_SM per SM), 6 CTAs per SM with two 16-byte loads in flight per
-// thread and pass (throughput); few rows, 4 CTAs per SM (more registers)
-// with four (a row's latency: its loads take fewer rounds).
-constexpr int CS_MANY_CTAS = 6, CS_MANY_UNROLL = 2;
-constexpr int CS_FEW_CTAS = 4, CS_FEW_UNROLL = 4, CS_FEW_PER_SM = 4;
+// CS_FEW_PER_SM per SM), CTAs of 256 threads, 6 per SM, two 16-byte loads
+// in flight per thread and pass (throughput); few rows, larger CTAs so that
+// a row's loads take fewer rounds (its latency is the kernel's).
+#ifndef DSA_CS_FEW_NT
+#define DSA_CS_FEW_NT 512
+#endif
+#ifndef DSA_CS_FEW_CTAS
+#define DSA_CS_FEW_CTAS 2
+#endif
+#ifndef DSA_CS_FEW_UNROLL
+#define DSA_CS_FEW_UNROLL 4
+#endif
+constexpr int CS_MANY_NT = 256, CS_MANY_CTAS = 6, CS_MANY_UNROLL = 2;
+constexpr int CS_FEW_NT = DSA_CS_FEW_NT, CS_FEW_CTAS = DSA_CS_FEW_CTAS, CS_FEW_UNROLL = DSA_CS_FEW_UNROLL;
+constexpr int CS_FEW_PER_SM = 4;
 constexpr uint32_t CS_OFF_HIST = 0;                                  // level-0 histogram, then slots
 constexpr uint32_t CS_OFF_HIST2 = CS_OFF_HIST + CS_BINS * 4;         // narrowing passes
 constexpr uint32_t CS_OFF_CNT = CS_OFF_HIST2 + CS_BINS * 4;          // per-region candidate counts
@@ -879,15 +889,16 @@ constexpr uint32_t CS_OFF_SKEY = CS_OFF_CNT + CAND_MAX_REGIONS * 4;  // the inte
 constexpr uint32_t CS_OFF_SIDX = CS_OFF_SKEY + CS_STAGE * 4;         // and ids
 constexpr uint32_t CS_OFF_OUT = CS_OFF_SIDX + CS_STAGE * 4;          // the row's output, written out at the end
 constexpr uint32_t CS_OFF_MISC = CS_OFF_OUT + MAX_K * 4;
-constexpr uint32_t CAND_SMEM = CS_OFF_MISC + 32 * 4;
-static_assert(CAND_THREADS == 256 && CS_BINS == 4 * CAND_THREADS, "desc_scan_pick: 4 bins per thread");
-static_assert(CS_STAGE <= CAND_THREADS, "one staged key per thread");
-static_assert(CS_MANY_CTAS * (CAND_SMEM + 1024) <= 228 * 1024, "candidate-selector CTAs per SM");
-constexpr int CS_PER_THREAD = CAND_MAX_REGIONS / CAND_THREADS;  // regions scanned per thread
-static_assert(CAND_MAX_REGIONS % CAND_THREADS == 0, "region scan");
+constexpr uint32_t CAND_SMEM = CS_OFF_MISC + 64 * 4;
+static_assert(CS_STAGE <= CS_MANY_NT && CS_STAGE <= CS_FEW_NT, "one staged key per thread");
+static_assert(CS_MANY_CTAS * (CAND_SMEM + 1024) <= 228 * 1024 && CS_FEW_CTAS * (CAND_SMEM + 1024) <= 228 * 1024,
+              "candidate-selector CTAs per SM");
+static_assert(CS_MANY_CTAS * CS_MANY_NT <= 2048 && CS_FEW_CTAS * CS_FEW_NT <= 2048, "threads per SM");
 
-template <int CTAS, int CS_UNROLL>
-__global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const CandParams p) {
+template <int NT, int CTAS, int CS_UNROLL>
+__global__ void __launch_bounds__(NT, CTAS) cand_select_kernel(const CandParams p) {
+  constexpr int CS_PER_THREAD = CAND_MAX_REGIONS / NT;  // regions scanned per thread
+  static_assert(CAND_MAX_REGIONS % NT == 0 && CS_BINS % NT == 0, "region scan, bins per thread");
   pdl_enter();
   extern __shared__ __align__(16) uint8_t smem[];
   int* hist = (int*)(smem + CS_OFF_HIST);
@@ -896,18 +907,18 @@ __global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const C
   uint32_t* skey = (uint32_t*)(smem + CS_OFF_SKEY);
   int32_t* sidx = (int32_t*)(smem + CS_OFF_SIDX);
   int32_t* so = (int32_t*)(smem + CS_OFF_OUT);
-  // [0..7] bin pick, [8..15] warp sums, [17] staged count, [21] theta,
-  // [22] rr, [23..25] emission counters (staged above / staged equal /
-  // single-value equal), [26] last-CTA flag, [27] next item
+  // [0..7] bin pick, [17] staged count, [21] theta, [22] rr, [23..25]
+  // emission counters (staged above / staged equal / single-value equal),
+  // [26] last-CTA flag, [27] next item, [32..63] warp sums
   int* misc = (int*)(smem + CS_OFF_MISC);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int NWARPS = CAND_THREADS / 32;
+  constexpr int NWARPS = NT / 32;
   const int K = p.K;
   const int items = p.stats->n_groups * GROUP_ROWS;
   // items: the CTA's own first, then (the many-row build) the next from a
   // counter: rows differ in cost, and a static split left SMs idle at the
   // end; the few-row build has at most one item per CTA
-  constexpr bool dynamic = CTAS == CS_MANY_CTAS;
+  constexpr bool dynamic = NT == CS_MANY_NT && CTAS == CS_MANY_CTAS;
   auto next_item = [&](int cur) {
     if (!dynamic) return cur + (int)gridDim.x;
     if (tid == 0) misc[27] = (int)gridDim.x + atomicAdd(&p.stats->cs_next, 1);
@@ -944,14 +955,14 @@ __global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const C
       tsum += c;
     }
     tsum = __reduce_add_sync(0xffffffffu, tsum);
-    if (lane == 0) misc[8 + warp] = tsum;
+    if (lane == 0) misc[32 + warp] = tsum;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) hist[tid + CAND_THREADS * j] = 0;
+    for (int j = 0; j < CS_BINS / NT; ++j) hist[tid + NT * j] = 0;
     if (tid == 0) misc[17] = misc[23] = misc[24] = misc[25] = 0;
     const bool any_lost = __syncthreads_or(lost);
     int n = 0;
 #pragma unroll
-    for (int w = 0; w < NWARPS; ++w) n += misc[8 + w];
+    for (int w = 0; w < NWARPS; ++w) n += misc[32 + w];
     if (n < K || any_lost || n > CAND_CAP) {
       if (tid == 0) {
         const int f = atomicAdd(&p.stats->fail_count, 1);
@@ -972,7 +983,7 @@ __global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const C
     const int avg4 = ceil_div(n, 4 * nreg);
     int tpr = 1;
     while (tpr < 32 && tpr * CS_UNROLL < avg4) tpr *= 2;
-    const int rstep = CAND_THREADS / tpr, sub = tid % tpr;
+    const int rstep = NT / tpr, sub = tid % tpr;
 
     // pass 1: histogram of (key - tau) >> CS_SHIFT0, and a check that no
     // candidate is below tau
@@ -1013,7 +1024,7 @@ __global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const C
       __syncthreads();
       continue;
     }
-    desc_scan_pick(hist, CS_BINS, K, misc, true);  // hist now holds each bin's first slot
+    desc_scan_pick<NT>(hist, CS_BINS, K, misc, true);  // hist now holds each bin's first slot
     const uint32_t b0 = (uint32_t)misc[2];
     int rem = misc[3], bc = misc[4];
     // the K-th key's interval [lo, hi)
@@ -1026,7 +1037,7 @@ __global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const C
       const int s = max(0, 64 - __clzll((long long)(hi - lo - 1)) - 10);
       const uint32_t lo32 = (uint32_t)lo, hin = (uint32_t)(hi - 1);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) hist2[tid + CAND_THREADS * j] = 0;
+      for (int j = 0; j < CS_BINS / NT; ++j) hist2[tid + NT * j] = 0;
       __syncthreads();
       for (int jb = 0; jb < nreg; jb += rstep) {
         const int j = jb + tid / tpr;
@@ -1042,7 +1053,7 @@ __global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const C
         }
       }
       __syncthreads();
-      desc_scan_pick(hist2, CS_BINS, rem, misc, false);
+      desc_scan_pick<NT>(hist2, CS_BINS, rem, misc, false);
       rem = misc[3];
       bc = misc[4];
       lo += (unsigned long long)misc[2] << s;
@@ -1135,7 +1146,7 @@ __global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const C
     }
     // the row out, coalesced (the slots above scatter)
     __syncthreads();
-    for (int i = tid; i < K; i += CAND_THREADS) o[i] = so[i];
+    for (int i = tid; i < K; i += NT) o[i] = so[i];
     __syncthreads();
   }
   // the CTA that finishes last writes the repair plan (the rows queued
@@ -1160,15 +1171,15 @@ __global__ void __launch_bounds__(CAND_THREADS, CTAS) cand_select_kernel(const C
 cudaError_t launch_cand_select(const CandParams& p, int sms, cudaStream_t s) {
   static DeviceFlags attr_many, attr_few;
   if (p.rs.R > CS_FEW_PER_SM * sms) {
-    auto k = cand_select_kernel<CS_MANY_CTAS, CS_MANY_UNROLL>;
+    auto k = cand_select_kernel<CS_MANY_NT, CS_MANY_CTAS, CS_MANY_UNROLL>;
     cudaError_t e = set_smem_attr_once(k, CAND_SMEM, attr_many);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, dim3(CS_MANY_CTAS * sms), dim3(CAND_THREADS), CAND_SMEM, s, p);
+    return launch_pdl(k, dim3(CS_MANY_CTAS * sms), dim3(CS_MANY_NT), CAND_SMEM, s, p);
   }
-  auto k = cand_select_kernel<CS_FEW_CTAS, CS_FEW_UNROLL>;
+  auto k = cand_select_kernel<CS_FEW_NT, CS_FEW_CTAS, CS_FEW_UNROLL>;
   cudaError_t e = set_smem_attr_once(k, CAND_SMEM, attr_few);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(CS_FEW_CTAS * sms), dim3(CAND_THREADS), CAND_SMEM, s, p);
+  return launch_pdl(k, dim3(CS_FEW_CTAS * sms), dim3(CS_FEW_NT), CAND_SMEM, s, p);
 }
 
 // ============================================================ wide select ==
