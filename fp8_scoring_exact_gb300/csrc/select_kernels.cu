@@ -1378,6 +1378,15 @@ cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s) {
 // serves it).
 constexpr int MF_THREADS = 512;
 constexpr int MF_UNROLL = 4;
+// Compaction of the kept scores (measured on the standalone top-K): rows
+// shorter than MF_SHORT_ROW keep a large share (~K of L) and use a ballot per
+// score; in longer rows a warp step keeping at most MF_SCAN_MAX of its 512
+// scores uses per-lane masks and one warp scan (4096 x 131072, ~3% kept:
+// 0.773 -> 0.647 ms), a step keeping more (ties at the threshold) ballots
+// over the mask bits.
+constexpr int MF_SHORT_ROW = 32768;
+constexpr int MF_SCAN_MAX = 48;
+static_assert(MF_UNROLL == 4, "the kept-score mask and its selects are written for four float4s");
 
 __global__ void __launch_bounds__(MF_THREADS) matrix_filter_kernel(const MatrixFilterParams p) {
   pdl_enter();
@@ -1426,6 +1435,7 @@ __global__ void __launch_bounds__(MF_THREADS) matrix_filter_kernel(const MatrixF
     uint32_t* ck = p.cand_key + region;
     int32_t* ci = p.cand_idx + region;
     const float* srow = p.scores + (int64_t)row * p.ld;
+    const bool short_row = e - b < MF_SHORT_ROW;
     int wcnt = 0;
     for (int t = t0 + quarter; t < t1; t += 4 * MF_UNROLL) {
       float4 x[MF_UNROLL];
@@ -1438,32 +1448,100 @@ __global__ void __launch_bounds__(MF_THREADS) matrix_filter_kernel(const MatrixF
         x[v] = (t + 4 * v < t1 && s + 3 >= b && s < e) ? __ldcs(reinterpret_cast<const float4*>(srow + s))
                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      if (short_row) {
+        // short rows keep a large share (~K of L): a ballot per score and
+        // key position keeps the warp's stores in runs
+#pragma unroll
+        for (int v = 0; v < MF_UNROLL; ++v) {
+          const int s0 = (t + 4 * v) * TILE + 4 * lane;
+          const bool tile_in = t + 4 * v < t1;
+          const float xs[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
+          bool pr[4];
+          if (tile_in && s0 >= b && s0 + 4 <= e) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pr[j] = xs[j] >= tauf;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pr[j] = tile_in && s0 + j >= b && s0 + j < e && xs[j] >= tauf;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t m = __ballot_sync(0xffffffffu, pr[j]);
+            if (m) {  // warp-uniform: nothing to do when no lane keeps a score
+              const int pos = wcnt + __popc(m & lt);
+              if (pr[j] && pos < wcap) {
+                ck[pos] = ordered_key(xs[j]);
+                ci[pos] = s0 + j;
+              }
+              wcnt += __popc(m);
+            }
+          }
+        }
+        continue;
+      }
+      // long rows: the lane's kept scores as a 16-bit mask
+      uint32_t mask = 0u;
 #pragma unroll
       for (int v = 0; v < MF_UNROLL; ++v) {
         const int s0 = (t + 4 * v) * TILE + 4 * lane;
         const bool tile_in = t + 4 * v < t1;
         const float xs[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
-        bool pr[4];
         if (tile_in && s0 >= b && s0 + 4 <= e) {  // the common case: the whole float4 in range
 #pragma unroll
-          for (int j = 0; j < 4; ++j) pr[j] = xs[j] >= tauf;
+          for (int j = 0; j < 4; ++j) mask |= (xs[j] >= tauf ? 1u : 0u) << (4 * v + j);
         } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) pr[j] = tile_in && s0 + j >= b && s0 + j < e && xs[j] >= tauf;
+          for (int j = 0; j < 4; ++j)
+            mask |= (tile_in && s0 + j >= b && s0 + j < e && xs[j] >= tauf ? 1u : 0u) << (4 * v + j);
         }
+      }
+      const int cnt = __popc(mask);
+      const int tot = __reduce_add_sync(0xffffffffu, cnt);
+      if (tot == 0) continue;  // warp-uniform
+      if (tot <= MF_SCAN_MAX) {
+        // few kept (long rows keep ~2K of L): one warp scan of the counts,
+        // then each lane writes its own (a ballot per score costs four
+        // times the instructions, and nearly every warp step keeps some)
+        int incl = cnt;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t m = __ballot_sync(0xffffffffu, pr[j]);
-          if (m) {  // warp-uniform: nothing to do when no lane keeps a score
+        for (int d = 1; d < 32; d <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += y;
+        }
+        int pos = wcnt + incl - cnt;
+        while (mask) {
+          const int q = __ffs(mask) - 1;
+          mask &= mask - 1u;
+          const int v = q >> 2, j = q & 3;
+          const float4 xv = v == 0 ? x[0] : v == 1 ? x[1] : v == 2 ? x[2] : x[MF_UNROLL - 1];
+          const float val = j == 0 ? xv.x : j == 1 ? xv.y : j == 2 ? xv.z : xv.w;
+          if (pos < wcap) {
+            ck[pos] = ordered_key(val);
+            ci[pos] = (t + 4 * v) * TILE + 4 * lane + j;
+          }
+          ++pos;
+        }
+      } else {
+        // many kept (ties at the threshold): a ballot per key position
+        // keeps the warp's stores in runs
+#pragma unroll
+        for (int q = 0; q < 4 * MF_UNROLL; ++q) {
+          const bool pr = (mask >> q) & 1u;
+          const uint32_t m = __ballot_sync(0xffffffffu, pr);
+          if (m) {  // warp-uniform
             const int pos = wcnt + __popc(m & lt);
-            if (pr[j] && pos < wcap) {
-              ck[pos] = ordered_key(xs[j]);
-              ci[pos] = s0 + j;
+            if (pr && pos < wcap) {
+              const float4 xv = x[q >> 2];
+              const float val = (q & 3) == 0 ? xv.x : (q & 3) == 1 ? xv.y : (q & 3) == 2 ? xv.z : xv.w;
+              ck[pos] = ordered_key(val);
+              ci[pos] = (t + 4 * (q >> 2)) * TILE + 4 * lane + (q & 3);
             }
             wcnt += __popc(m);
           }
         }
+        continue;
       }
+      wcnt += tot;
     }
     if (lane == 0) p.unit_count[(int64_t)row * p.max_units * UNIT_REGIONS + c * UNIT_REGIONS + quarter] = min(wcnt, wcap + 1);
   }
