@@ -201,6 +201,7 @@ struct Opts {
 // that for paged rows) exceed what the candidate selector reads: such rows
 // would all fail their certificate and go to repair.
 constexpr int REPAIR_CHUNK = 8;  // tiles per unit of the repair scorer
+constexpr int SHARED_GRID_MIN_ROWS = 256;  // dense rows above this share one gathered sample grid
 int min_chunk_for(const RowSpace& rs) {
   const int tiles = ceil_div(rs.N, TILE);
   const int per_unit = UNIT_REGIONS * (rs.paged ? 2 : 1);
@@ -284,7 +285,11 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
   uint32_t* tau = at<uint32_t>(a, L.tau);
   const int S = sample_stride_for(rs.N);
   const int ns = rs.N > SAMPLE_OFFSET ? ceil_div(rs.N - SAMPLE_OFFSET, S) : 0;
-  if (!rs.paged && ns > TILE) {
+  // dense grids of several tiles over many rows: the shared-grid chain
+  // below; few rows take the per-pair kernel in split mode (two launches
+  // instead of four)
+  const bool shared_grid = !rs.paged && ns > TILE && rs.R > SHARED_GRID_MIN_ROWS;
+  if (shared_grid) {
     // sampled thresholds: the grid keys gathered once, scored by the scorer
     // for every row, then one threshold per row (a grid of one tile or less
     // is cheaper in the per-pair sampling kernel below)
@@ -365,9 +370,10 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
     sp.tau = tau;
     sp.out = out;
     sp.stats = st;
-    // paged grids span up to 8 sample tiles: one CTA per (pair, tile), then
-    // one warp per row selects its threshold
-    sp.split = rs.paged;
+    // grids of several tiles (paged rows, and few dense rows over long key
+    // ranges; up to 8 tiles): one CTA per (pair, tile), then one warp per
+    // row selects its threshold
+    sp.split = rs.paged || ns > TILE;
     sp.sscores = at<float>(a, L.sscores);
     sp.sld = SAMPLE_LD;
     sp.srb = at<int32_t>(a, L.srb);
