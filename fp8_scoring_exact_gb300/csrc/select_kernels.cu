@@ -52,12 +52,43 @@ __device__ __forceinline__ int group_units(int lo, int hi, int chunk) {
   return ceil_div(tiles, chunk);
 }
 
+// A row's range for the main plan (validated input range, or the paged
+// row's causal range; an invalid one becomes empty and sets *bad) or for the
+// sample plan (the grid keys SAMPLE_OFFSET + j * S inside the row's main
+// range: j in [j0, j1)).
+__device__ __forceinline__ void plan_row_range(const PlanParams& p, int row, int& b, int& e, bool& bad) {
+  const RowSpace& rs = p.rs;
+  b = e = 0;
+  if (p.plan == PLAN_SAMPLE) {
+    const int S = p.sample_stride;
+    const int rb = p.row_begin_in[row], re = p.row_end_in[row];
+    b = rb > SAMPLE_OFFSET ? ceil_div(rb - SAMPLE_OFFSET, S) : 0;
+    e = max(b, re > SAMPLE_OFFSET ? ceil_div(re - SAMPLE_OFFSET, S) : 0);
+  } else if (!rs.paged) {
+    b = p.row_begin_in[row];
+    e = p.row_end_in[row];
+    if (b < 0 || e > rs.N || b > e) {
+      bad = true;
+      b = e = 0;
+    }
+  } else {
+    const int sq = row / rs.next_n, i = row % rs.next_n;
+    const int sl = rs.seq_lens[sq];
+    if (sl < 0 || sl > rs.max_pages * PAGE)
+      bad = true;
+    else
+      e = max(0, sl - rs.next_n + i + 1);
+  }
+}
+
 // Groups of a plan and their work-unit prefix (unit_start), by every thread
 // of the calling CTA (any multiple of 32 threads); G groups.  warp_sums: 32
-// ints and s_carry: one int of shared memory.  Failed-row entries are read
-// through L2: the repair plan may run in the CTA that finishes the
-// candidate selection, whose other CTAs queued them.
-__device__ void plan_groups(const PlanParams& p, int G, int* warp_sums, int* s_carry) {
+// ints and s_carry: one int of shared memory.  The main and sample plans
+// form their rows' ranges here (written to rb / re; *bad: an invalid main
+// range).  Failed-row entries are read through L2: the repair plan may run in
+// the CTA that finishes the candidate selection, whose other CTAs queued
+// them.
+__device__ void plan_groups(const PlanParams& p, int G, int* warp_sums, int* s_carry, bool* bad = nullptr) {
   const RowSpace& rs = p.rs;
   const int tid = threadIdx.x;
   if (tid == 0) *s_carry = 0;
@@ -76,7 +107,12 @@ __device__ void plan_groups(const PlanParams& p, int G, int* warp_sums, int* s_c
         const int nr = rows_of_group<GROUP_ROWS>(rs, g, rows);
         grp.seq = rs.paged ? rows[0] / rs.next_n : -1;
         for (int i = 0; i < nr; ++i) {
-          const int b = p.rb[rows[i]], e = p.re[rows[i]];
+          int b, e;
+          bool rbad = false;
+          plan_row_range(p, rows[i], b, e, rbad);
+          if (rbad && bad) *bad = true;
+          p.rb[rows[i]] = b;
+          p.re[rows[i]] = e;
           // the sample plan leaves out the rows the main plan calls trivial
           const int len = p.plan == PLAN_SAMPLE ? p.row_end_in[rows[i]] - p.row_begin_in[rows[i]] : e - b;
           if (len > p.trivial_len && e > b) {
@@ -148,57 +184,23 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
   __shared__ int warp_sums[32];
   __shared__ int s_carry;
   const RowSpace& rs = p.rs;
-  const int tid = threadIdx.x;
-  int G;
-  if (p.plan == PLAN_SAMPLE) {
-    // grid key j sits at SAMPLE_OFFSET + j * S: row [b, e) holds j in [j0, j1)
-    const int S = p.sample_stride;
-    for (int row = tid; row < rs.R; row += PLAN_THREADS) {
-      const int b = p.row_begin_in[row], e = p.row_end_in[row];
-      const int j0 = b > SAMPLE_OFFSET ? ceil_div(b - SAMPLE_OFFSET, S) : 0;
-      const int j1 = e > SAMPLE_OFFSET ? ceil_div(e - SAMPLE_OFFSET, S) : 0;
-      p.rb[row] = j0;
-      p.re[row] = max(j0, j1);
-    }
-    __syncthreads();
-    G = n_groups(rs);
-  } else if (p.plan == PLAN_MAIN) {
-    if (tid == 0) {
+  // main and sample plans: one thread per group forms its rows' ranges and
+  // the group (no pass over the rows before); the main plan's status block
+  // is written whole at the end (the call's other kernels start after)
+  const int G = p.plan == PLAN_REPAIR ? repair_groups(p) : n_groups(rs);
+  bool bad = false;
+  plan_groups(p, G, warp_sums, &s_carry, &bad);
+  if (p.plan == PLAN_MAIN) {
+    const bool any_bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
       Stats z = {};
       z.wait_ns = p.wait_ns;
+      z.status = any_bad ? ST_RANGE : 0;
+      z.n_groups = G;
+      z.total_units = s_carry;
       *p.stats = z;
     }
-    __syncthreads();
-    int bad = 0;
-    for (int row = tid; row < rs.R; row += PLAN_THREADS) {
-      int b = 0, e = 0;
-      if (!rs.paged) {
-        b = p.row_begin_in[row];
-        e = p.row_end_in[row];
-        if (b < 0 || e > rs.N || b > e) {
-          bad = 1;
-          b = e = 0;
-        }
-      } else {
-        const int sq = row / rs.next_n, i = row % rs.next_n;
-        const int sl = rs.seq_lens[sq];
-        if (sl < 0 || sl > rs.max_pages * PAGE) {
-          bad = 1;
-        } else {
-          e = max(0, sl - rs.next_n + i + 1);
-        }
-      }
-      p.rb[row] = b;
-      p.re[row] = e;
-    }
-    if (bad) atomicOr(&p.stats->status, ST_RANGE);
-    __syncthreads();
-    G = n_groups(rs);
-  } else {
-    G = repair_groups(p);
   }
-
-  plan_groups(p, G, warp_sums, &s_carry);
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
