@@ -47,6 +47,7 @@ struct Layout {
   size_t stats, rb, re, tau, groups, unit_start, rgroups, runit_start, unit_count, failed;
   size_t cand_key, cand_idx, scores;
   size_t srb, sre, sgroups, sunit_start, skeys, sks, sscores;  // dense sampled thresholds
+  size_t pair_cnt;                                             // split sampling tickets
   size_t total;
 };
 
@@ -86,6 +87,7 @@ Layout make_layout(int64_t R, int64_t G, int64_t cand_stride, int64_t max_units,
     L.skeys = take((size_t)(MAX_SAMPLES + 2) * D);
     L.sks = take((size_t)(MAX_SAMPLES + 2) * 4);
     L.sscores = take((size_t)R * SAMPLE_LD * 4);
+    L.pair_cnt = take(R * 4);
   }
   L.total = off;
   return L;
@@ -280,6 +282,8 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
   pp.failed_rows = at<int32_t>(a, L.failed);
   pp.stats = st;
   pp.wait_ns = o.wait_ns;
+  pp.pair_cnt = at<int>(a, L.pair_cnt);
+  pp.n_pairs = n_pairs(rs);
   DSA_LAUNCH(launch_plan(pp, stream));
 
   uint32_t* tau = at<uint32_t>(a, L.tau);
@@ -374,27 +378,12 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
     // ranges; up to 8 tiles): one CTA per (pair, tile), then one warp per
     // row selects its threshold
     sp.split = rs.paged || ns > TILE;
+    sp.pair_cnt = pp.pair_cnt;
     sp.sscores = at<float>(a, L.sscores);
     sp.sld = SAMPLE_LD;
     sp.srb = at<int32_t>(a, L.srb);
     sp.sre = at<int32_t>(a, L.sre);
     DSA_LAUNCH(launch_sample(tm_q, sp, n_pairs(rs), stream));
-    if (sp.split) {
-      SampleTauParams tp{};
-      tp.rs = rs;
-      tp.K = K;
-      tp.target16 = o.target16;
-      tp.tau_bias = o.bias;
-      tp.rb = pp.rb;
-      tp.re = pp.re;
-      tp.srb = sp.srb;
-      tp.sre = sp.sre;
-      tp.sscores = sp.sscores;
-      tp.sld = SAMPLE_LD;
-      tp.tau = tau;
-      tp.stats = st;
-      DSA_LAUNCH(launch_sample_tau(tp, stream));
-    }
   }
 
   ScoreParams cp{};

@@ -46,6 +46,8 @@ struct PlanParams {
   const int32_t* failed_rows;  // repair mode input
   Stats* stats;
   uint64_t wait_ns;            // main plan: the call's pipeline wait limit (stored in the status block)
+  int* pair_cnt;               // main plan: sampling tickets per row pair, zeroed (null: none)
+  int n_pairs;
 };
 
 struct SampleParams {
@@ -63,8 +65,10 @@ struct SampleParams {
   int32_t* out;                // [R, K] (trivial rows written here)
   Stats* stats;
   // split mode: one CTA per (row pair, 128-key sample tile) writes the
-  // sample scores and each row's sample range; sample_tau then selects
+  // sample scores; the pair's last tile CTA to finish (pair_cnt ticket,
+  // zeroed by the main plan) selects the pair's thresholds
   int split;
+  int* pair_cnt;               // [pairs]
   float* sscores;              // [R, sld]: row r's score of pair-grid sample j at r * sld + j
   int64_t sld;
   int32_t* srb;                // [R] first / end pair-grid sample inside the row's range

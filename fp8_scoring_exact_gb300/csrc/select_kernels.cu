@@ -191,6 +191,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(const PlanParams p) 
   bool bad = false;
   plan_groups(p, G, warp_sums, &s_carry, &bad);
   if (p.plan == PLAN_MAIN) {
+    if (p.pair_cnt)
+      for (int i = threadIdx.x; i < p.n_pairs; i += blockDim.x) p.pair_cnt[i] = 0;
     const bool any_bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) {
       Stats z = {};
@@ -334,6 +336,10 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
   sample_grid(lo, hi, &first, &m_u, &S);
   const int target = (int)(((int64_t)p.target16 * K) / 16);
   if (split) {
+    if (m_u == 0) {  // no grid key in the pair's ranges: every key passes
+      if (tile0 == 0 && tid < nact) p.tau[act[tid]] = 0u;
+      return;
+    }
     // each active row's samples: pair-grid indices [j0, j1) inside its range
     if (tile0 == 0 && tid < nact) {
       const int row = act[tid];
@@ -469,11 +475,20 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
     tc_fence_after();
     tmem_dealloc(tmem, TILE);
   }
-  if (split) return;
+  if (split) {
+    // the pair's last tile CTA to finish selects its thresholds from the
+    // sample scores the pair's CTAs wrote (each thread fenced its own)
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) misc[7] = atomicAdd(&p.pair_cnt[blockIdx.x], 1) == ceil_div(m_u, TILE) - 1;
+    __syncthreads();
+    if (!misc[7]) return;
+    __threadfence();
+  }
   // threshold of active row a (by warp a) from the samples inside its own
-  // range (at most one tile of them: a grid of more takes the shared-grid
-  // path; a larger m would leave the threshold at 0, every key a candidate,
-  // and the certificate would send the row to repair)
+  // range (a larger m than the selection holds would leave the threshold at
+  // 0, every key a candidate, and the certificate would send the row to
+  // repair)
   if (warp < nact) {
     const int row = act[warp];
     uint32_t tau = 0u;
@@ -483,19 +498,31 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 4) sample_kernel(const __grid_
       const int j1 = min(m_u, ceil_div(e - first, S));
       const int m = max(0, j1 - j0);
       const int rank = sample_rank(m, e - b, target);
-      if (m > 0 && m <= 4 * 32 && rank >= 1 && rank <= m) {
+      int* whist = (int*)(smem + SM_OFF_HIST) + warp * 256;
+      int* wpick = (int*)(smem + SM_OFF_PICK) + warp * 4;
+      if (split && m > 0 && m <= MAX_SAMPLES && rank >= 1 && rank <= m) {
+        // the pair's tiles: sample scores in global memory, up to 8 tiles
+        uint32_t key[MAX_SAMPLES / 32];
+        const float* sr = p.sscores + (int64_t)row * p.sld + j0;
+#pragma unroll
+        for (int q = 0; q < MAX_SAMPLES / 32; ++q) {
+          const int i = q * 32 + lane;
+          key[q] = i < m ? ordered_key(__ldcg(&sr[i])) : 0u;
+        }
+        tau = warp_select_rank<MAX_SAMPLES / 32>(key, m, rank, whist, wpick);
+      } else if (!split && m > 0 && m <= 4 * 32 && rank >= 1 && rank <= m) {
+        // one tile: the sample keys in shared memory
         uint32_t key[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int i = q * 32 + lane;
           key[q] = i < m ? samp[warp * MAX_SAMPLES + j0 + i] : 0u;
         }
-        tau = warp_select_rank<4>(key, m, rank, (int*)(smem + SM_OFF_HIST) + warp * 256,
-                                  (int*)(smem + SM_OFF_PICK) + warp * 4);
-        if (p.tau_bias != 0) {
-          const int64_t t = (int64_t)tau + p.tau_bias;
-          tau = (uint32_t)(t < 0 ? 0 : (t > 0xffffffffll ? 0xffffffffll : t));
-        }
+        tau = warp_select_rank<4>(key, m, rank, whist, wpick);
+      }
+      if (tau != 0u && p.tau_bias != 0) {
+        const int64_t t = (int64_t)tau + p.tau_bias;
+        tau = (uint32_t)(t < 0 ? 0 : (t > 0xffffffffll ? 0xffffffffll : t));
       }
     }
     if (lane == 0) p.tau[row] = tau;
