@@ -455,6 +455,33 @@ def test_topk_from_scores_exact(B):
         assert np.array_equal(got, want), t
 
 
+def test_topk_from_scores_long_rows_exact(B):
+    """Rows of 128K keys, where the filter keeps a few percent of the scores
+    (per-lane masks and one warp scan per step) or, with ties at the
+    threshold, many (a ballot per score): the sorted selected values equal a
+    full sort bit for bit."""
+    rng = np.random.default_rng(31)
+    Q, N, K = 8, 131072, 2048
+    sc = rng.standard_normal((Q, N)).astype(np.float32)
+    sc[1] = np.round(sc[1] * 2) / 2                      # heavy ties
+    sc[2] = rng.choice(np.float32([0.5, 1.0, 1.5, 2.0]), N)  # a few values
+    sc[3] = 3.0                                          # all equal
+    sc[5] = (sc[5] - 3.0).astype(np.float32)             # mostly negative, the top crossing zero
+    sc[6, ::3] = 7.0                                     # a third tied at the top
+    rb = np.zeros(Q, np.int32)
+    re = np.full(Q, N, np.int32)
+    rb[4], re[4] = 3, N - 1                              # off a 4-key boundary
+    rb[7], re[7] = 1, 40001
+    out = B.topk_from_scores(*to_dev(sc, rb, re), K=K).cpu().numpy()
+    _status_ok(B)
+    for t in range(Q):
+        sel = out[t]
+        assert len(np.unique(sel)) == K and np.all((sel >= rb[t]) & (sel < re[t])), t
+        want = np.sort(sc[t, rb[t]:re[t]])[::-1][:K]
+        got = np.sort(sc[t, sel])[::-1]
+        assert np.array_equal(got, want), t
+
+
 @pytest.mark.parametrize("bias,kind", [(0, None), (1 << 31, "underflow"), (-(1 << 33), "overflow")])
 def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind):
     """A padded row stride (ld > N, N not a multiple of 4), ranges that end at
