@@ -40,7 +40,6 @@ __host__ __device__ constexpr int region_cap(int nunits) {
 
 // -------------------------------------------------------------- selection --
 constexpr int MAX_K = 2048;        // largest K (the public header's DSA_MAX_K)
-constexpr int CAND_CAP = 8192;     // candidates selected per row (certificate capacity)
 constexpr int CAND_MAX_REGIONS = 1024;  // regions (units x 4) one row may have
 constexpr int SAMPLE_STRIDE = 200; // one sample per 200 keys: ~0.5% of the row
 constexpr int SAMPLE_OFFSET = 100; // samples at keys 100 mod 200
@@ -69,7 +68,7 @@ constexpr int ST_RANGE = 2;
 struct Stats {
   int status;
   int underflow;     // rows whose candidate set had fewer than K entries
-  int overflow;      // rows whose candidate set exceeded CAND_CAP
+  int overflow;      // rows of which a candidate region lost candidates (more than it holds)
   int trivial;       // rows with L <= K (remapping path)
   int cand_total;    // candidates appended (all rows)
   int fail_count;    // rows queued for repair

@@ -103,8 +103,8 @@ struct ScoreParams {
 };
 
 // Candidate selector: exact top-K of each planned row from the candidate
-// regions the filter left, with the certificate (K <= n, nothing lost,
-// n <= CAND_CAP); rows that fail it are queued for repair.
+// regions the filter left, with the certificate (K <= n, no region lost
+// candidates); rows that fail it are queued for repair.
 struct CandParams {
   RowSpace rs;
   int K;

@@ -968,7 +968,9 @@ __global__ void __launch_bounds__(NT, CTAS) cand_select_kernel(const CandParams 
     const int wcap = region_cap(max(nu, 1));
     const int32_t* cnt = p.unit_count + (int64_t)row * p.max_units * UNIT_REGIONS;
     const uint32_t tau = __ldcg(&p.tau[row]);
-    // certificate over the region counts (wcap + 1 = candidates were lost)
+    // certificate over the region counts (wcap + 1 = candidates were lost):
+    // n >= K and no region lost any (the regions hold at most ROW_SLOTS, and
+    // the candidates are read in place, so that bounds n)
     int tsum = 0;
     bool lost = nreg > CAND_MAX_REGIONS;
 #pragma unroll
@@ -992,7 +994,7 @@ __global__ void __launch_bounds__(NT, CTAS) cand_select_kernel(const CandParams 
     int n = 0;
 #pragma unroll
     for (int w = 0; w < NWARPS; ++w) n += misc[32 + w];
-    if (n < K || any_lost || n > CAND_CAP) {
+    if (n < K || any_lost) {
       if (tid == 0) {
         const int f = atomicAdd(&p.stats->fail_count, 1);
         p.failed_rows[f] = row;

@@ -279,8 +279,8 @@ def test_forced_repair_paged_is_exact(B, bias, kind):
     """The same for paged decode rows: groups of one and two rows (whose
     epilogue runs as two teams on alternate tiles) and of four rows, all
     through exact repair over the physical slots.  Every row is longer than
-    the 8192 candidates a row may keep, so a zero threshold overflows it."""
-    inp = S.make_paged(6, 5, K=256, seed=33, len_lo=9000, len_hi=20000, n_short=0)
+    the 16384 candidate slots of a row, so a zero threshold overflows it."""
+    inp = S.make_paged(6, 5, K=256, seed=33, len_lo=17000, len_hi=30000, n_short=0)
     B.set_option("tau_bias", bias)
     try:
         out = B.indexer_topk_paged(*paged_args(inp), K=inp.K).cpu().numpy()
@@ -486,8 +486,9 @@ def test_topk_from_scores_long_rows_exact(B):
 def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind):
     """A padded row stride (ld > N, N not a multiple of 4), ranges that end at
     N or start off a 4-key boundary, rows with ties; with the threshold pushed
-    to either end every row longer than K fails the certificate and is
-    selected again from its own matrix row, exactly."""
+    to the top every row longer than K fails the certificate, and with it at
+    zero every row longer than a row's 16384 candidate slots does; those are
+    selected again from their own matrix rows, and every row is exact."""
     import torch
     rng = np.random.default_rng(77)
     Q, N, K, ld = 14, 20001, 1024, 20008
@@ -507,10 +508,14 @@ def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind):
         counters = _status_ok(B)
     finally:
         B.set_option("tau_bias", 0)
-    long_rows = int(((re - rb) > K).sum())
-    if kind:
-        assert counters[kind] == long_rows
-        assert sorted(B.last_repaired_rows()) == sorted(np.nonzero((re - rb) > K)[0].tolist())
+    long_rows = np.nonzero((re - rb) > K)[0].tolist()
+    if kind == "underflow":
+        assert counters[kind] == len(long_rows)
+        assert sorted(B.last_repaired_rows()) == sorted(long_rows)
+    elif kind == "overflow":
+        past_slots = np.nonzero((re - rb) > 16384)[0].tolist()
+        repaired = sorted(B.last_repaired_rows())
+        assert counters[kind] == len(repaired) and set(past_slots) <= set(repaired) <= set(long_rows)
     for t in range(Q):
         L = int(re[t] - rb[t])
         n = min(L, K)
