@@ -296,7 +296,7 @@ typedef enum {
   DSA_OPT_TAU_BIAS = 2,       /* added to every sampled threshold key: >0 forces underflow, <0 overflow (test knob; default 0) */
   DSA_OPT_PROFILE = 3,        /* 1: time the main kernel of each call with CUDA events (default 0) */
   DSA_OPT_GRID_CTAS = 4,      /* CTAs of the persistent kernels (default: SM count) */
-  DSA_OPT_SAMPLE_TARGET = 5,  /* candidates the threshold aims at, in units of K/16 (default 32 = 2K) */
+  DSA_OPT_SAMPLE_TARGET = 5,  /* candidates the threshold aims at, in units of K/16 (default 36 = 2.25K) */
   DSA_OPT_HOST_CHUNK_ROWS = 6, /* rows per chunk of dsa_indexer_topk_host (default 0: chosen per call) */
   DSA_OPT_UNIT_ORDER = 7,      /* order the scorer's work units are handed out in: 0 plan order (default),
                                   1 last first; the result does not depend on it (test option) */
