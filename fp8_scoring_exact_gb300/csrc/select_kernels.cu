@@ -210,11 +210,14 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
 }
 
 // The rank-th largest (1 <= rank <= m) of a warp's m keys, key[q] of lane l
-// being key q * 32 + l (positions >= m ignored): 8-bit radix passes in a
-// per-warp histogram (hist: 256 ints, pick: 4 ints of shared memory), with
-// no CTA barrier.  The leading bytes every key shares are the answer's too
-// (a row's samples have similar magnitudes, so the first byte or two
-// usually are): the passes start below them.
+// being key q * 32 + l (positions >= m ignored): radix passes in a per-warp
+// histogram (hist: 256 ints, pick: 4 ints of shared memory), with no CTA
+// barrier.  Every key agrees above the highest bit where the smallest and
+// largest differ, so the first digit is the 8 bits just below and at that
+// bit (a row's samples spread over its bins instead of crowding into one or
+// two of a byte-aligned digit, whose shared-memory atomics then serialize);
+// the later digits are the next 8 bits down, and a digit whose bucket holds
+// a single key ends the search.
 template <int KPL>
 __device__ __forceinline__ uint32_t warp_select_rank(const uint32_t (&key)[KPL], int m, int rank, int* hist,
                                                      int* pick) {
@@ -230,32 +233,33 @@ __device__ __forceinline__ uint32_t warp_select_rank(const uint32_t (&key)[KPL],
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   const uint32_t diff = kmin ^ kmax;
-  const int shared_bytes = diff ? (int)(__clz(diff) >> 3) : 4;
-  uint32_t mask = shared_bytes ? (0xffffffffu << (32 - 8 * shared_bytes)) : 0u;
+  if (diff == 0u) return kmin;  // every key the same
+  int top = 31 - __clz(diff);   // the digit's highest bit
+  uint32_t mask = top == 31 ? 0u : ~((2u << top) - 1u);
   uint32_t prefix = kmin & mask;
   int rem = rank;
 #pragma unroll 1
-  for (int pass = shared_bytes; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
+  while (true) {
+    const int lo = max(0, top - 7);
+    const uint32_t dmask = (2u << (top - lo)) - 1u;  // the digit's bits, at bit 0
 #pragma unroll
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < KPL; ++q) {
       const int i = q * 32 + lane;
-      if (i < m && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & 0xFFu], 1);
+      if (i < m && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> lo) & dmask], 1);
     }
     __syncwarp();
     radix_pick_digit(hist, rem, pick);
     __syncwarp();
-    prefix |= (uint32_t)pick[0] << shift;
-    mask |= 0xFFu << shift;
+    prefix |= (uint32_t)pick[0] << lo;
+    mask |= dmask << lo;
     rem = pick[1];
     const int cnt = pick[2];
     __syncwarp();
     if (cnt == 1) {
-      // the answer is the only key in its bucket: read it whole instead of
-      // running the remaining passes
+      // the answer is the only key in its bucket: read it whole
       uint32_t found = 0u;
       bool have = false;
 #pragma unroll
@@ -267,11 +271,11 @@ __device__ __forceinline__ uint32_t warp_select_rank(const uint32_t (&key)[KPL],
         }
       }
       const unsigned b = __ballot_sync(0xffffffffu, have);
-      prefix = __shfl_sync(0xffffffffu, found, __ffs(b) - 1);
-      break;
+      return __shfl_sync(0xffffffffu, found, __ffs(b) - 1);
     }
+    if (lo == 0) return prefix;
+    top = lo - 1;
   }
-  return prefix;
 }
 
 // ================================================================== sample ==
