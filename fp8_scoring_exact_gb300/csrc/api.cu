@@ -310,7 +310,6 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
     sx.re = pp.re;
     sx.out = out;
     sx.stats = st;
-    DSA_LAUNCH(launch_sample_prep(sx, stream));
     PlanParams spl = pp;
     spl.plan = PLAN_SAMPLE;
     spl.sample_stride = S;
@@ -321,7 +320,8 @@ int run_fused(const RowSpace& rs_in, int K, const CUtensorMap& tm_q, const CUten
     spl.re = at<int32_t>(a, L.sre);
     spl.groups = at<Group>(a, L.sgroups);
     spl.unit_start = at<int32_t>(a, L.sunit_start);
-    DSA_LAUNCH(launch_plan(spl, stream));
+    sx.plan = spl;
+    DSA_LAUNCH(launch_sample_prep(sx, stream));
     {
       CUtensorMap tks;
       if (!tmap_rows_u8(&tks, sx.sk, (uint64_t)ns, TILE)) return DSA_ERR_CUDA;

@@ -174,6 +174,7 @@ struct SamplePrepParams {
   const int32_t* re;
   int32_t* out;                // [R, K]: trivial rows written
   Stats* stats;
+  PlanParams plan;             // the sample plan (PLAN_SAMPLE), built by the first CTA
 };
 struct SampleTauParams {
   RowSpace rs;

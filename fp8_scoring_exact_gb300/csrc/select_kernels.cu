@@ -546,12 +546,20 @@ cudaError_t launch_sample(const CUtensorMap& tm_q, const SampleParams& p, int n_
 // Dense rows sample one global grid of keys (SAMPLE_OFFSET + j * stride, the
 // same keys for every row; a row uses the grid keys inside its range), so
 // the grid is gathered once into a contiguous key set and scored by the
-// persistent scorer like any key set.  This kernel gathers it and writes the
-// rows with L <= K (their output is every valid index).
+// persistent scorer like any key set.  This kernel gathers it, builds the
+// sample plan and writes the rows with L <= K (their output is every valid
+// index).
 constexpr int PREP_THREADS = 256;
 
 __global__ void __launch_bounds__(PREP_THREADS) sample_prep_kernel(const SamplePrepParams p) {
   pdl_enter();
+  // the first CTA builds the sample plan (the groups over the rows' grid
+  // ranges) while the others gather: one launch fewer
+  if (blockIdx.x == 0) {
+    __shared__ int warp_sums[32];
+    __shared__ int s_carry;
+    plan_groups(p.plan, n_groups(p.rs), warp_sums, &s_carry);
+  }
   const int gt = blockIdx.x * PREP_THREADS + threadIdx.x;
   const int nthreads = gridDim.x * PREP_THREADS;
   // 8 threads per grid key: 16 bytes each
