@@ -587,9 +587,12 @@ __global__ void __launch_bounds__(PREP_THREADS) sample_prep_kernel(const SampleP
 // per-warp histogram), plus the test bias; 0 (every key passes) when the
 // rank falls outside the sample.
 constexpr int TAU_THREADS = 256;
-constexpr int TAU_KEYS_PER_LANE = MAX_SAMPLES / 32;
-
-__global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTauParams p) {
+// two builds: up to 672 samples per row (rows of up to ~134K keys: 64
+// registers, 4 blocks per SM, so 4096 rows take one wave) and up to
+// MAX_SAMPLES (127 registers, 2 blocks per SM)
+constexpr int TAU_KPL_SHORT = 21;
+template <int KPL>
+__global__ void __launch_bounds__(TAU_THREADS, KPL <= TAU_KPL_SHORT ? 4 : 2) sample_tau_kernel(const SampleTauParams p) {
   pdl_enter();
   __shared__ int hist_all[TAU_THREADS / 32][256];
   __shared__ int pick_all[TAU_THREADS / 32][4];
@@ -624,14 +627,17 @@ __global__ void __launch_bounds__(TAU_THREADS) sample_tau_kernel(const SampleTau
     m = min(m, MAX_SAMPLES);
     const int rank = sample_rank(m, L, target);
     uint32_t tau = 0u;
-    if (m > 0 && rank >= 1 && rank <= m) {
-      uint32_t key[TAU_KEYS_PER_LANE];
+    // (more samples than this build holds cannot occur: the launch picks
+    // the build from the longest row; a threshold of 0 would only send the
+    // row to repair)
+    if (m > 0 && m <= 32 * KPL && rank >= 1 && rank <= m) {
+      uint32_t key[KPL];
 #pragma unroll
-      for (int q = 0; q < TAU_KEYS_PER_LANE; ++q) {
+      for (int q = 0; q < KPL; ++q) {
         const int i = q * 32 + lane;
         key[q] = i < m ? ordered_key(__ldcg(&sr[(int64_t)i * stride])) : 0u;
       }
-      const uint32_t prefix = warp_select_rank<TAU_KEYS_PER_LANE>(key, m, rank, hist, pick);
+      const uint32_t prefix = warp_select_rank<KPL>(key, m, rank, hist, pick);
       tau = prefix;
       if (p.tau_bias != 0) {
         const int64_t t = (int64_t)tau + p.tau_bias;
@@ -648,7 +654,12 @@ cudaError_t launch_sample_prep(const SamplePrepParams& p, cudaStream_t s) {
 }
 cudaError_t launch_sample_tau(const SampleTauParams& p, cudaStream_t s) {
   const int blocks = max(1, min(1024, ceil_div(p.rs.R, TAU_THREADS / 32)));
-  return launch_pdl(sample_tau_kernel, dim3(blocks), dim3(TAU_THREADS), 0, s, p);
+  // a row of L keys has at most L / SAMPLE_STRIDE + 1 grid samples (the
+  // stride widens for longer rows, up to MAX_SAMPLES)
+  const int64_t max_m = std::min<int64_t>(MAX_SAMPLES, (int64_t)p.rs.N / SAMPLE_STRIDE + 2);
+  if (max_m <= 32 * TAU_KPL_SHORT)
+    return launch_pdl(sample_tau_kernel<TAU_KPL_SHORT>, dim3(blocks), dim3(TAU_THREADS), 0, s, p);
+  return launch_pdl(sample_tau_kernel<MAX_SAMPLES / 32>, dim3(blocks), dim3(TAU_THREADS), 0, s, p);
 }
 
 // ================================================================== select ==
