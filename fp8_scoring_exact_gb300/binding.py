@@ -23,7 +23,8 @@ DSA_OK, DSA_ERR_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_UNSUPPORTED", -3: "DSA_ERR_CUDA",
                 -4: "DSA_ERR_TIMEOUT", -5: "DSA_ERR_RANGE"}
 OPTIONS = {"chunk_tiles": 1, "tau_bias": 2, "profile": 3, "grid_ctas": 4, "sample_target": 5,
-           "host_chunk_rows": 6, "unit_order": 7, "wait_limit_us": 8, "test_withhold": 9}
+           "host_chunk_rows": 6, "unit_order": 7, "wait_limit_us": 8, "test_withhold": 9,
+           "matrix_row_min": 10}
 HEADS, HEAD_DIM, MAX_K = 64, 128, 2048
 
 _P = ctypes.c_void_p

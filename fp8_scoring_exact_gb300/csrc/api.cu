@@ -40,6 +40,7 @@ int64_t g_host_chunk_rows = 0;  // 0: chosen per call (host_chunk_rows)
 int64_t g_unit_order = 0;       // 1: scorer units handed out last first (test option)
 int64_t g_wait_us = WAIT_LIMIT_NS / 1000;  // limit of every pipeline wait
 int64_t g_withhold = 0;         // 1: the main scorer never signals its first accumulator (test option)
+int64_t g_matrix_row_min = -1;  // standalone top-K: rows from which CTAs take whole rows (-1: one wave)
 std::atomic<int64_t> g_launches{0};
 
 // ----------------------------------------------------------------- arena ----
@@ -192,6 +193,7 @@ struct Opts {
   int reverse_units;
   int withhold;
   uint64_t wait_ns;
+  int64_t matrix_row_min;
 };
 
 // Tiles per work unit: the option when set, else 64 for dense rows and 32
@@ -240,6 +242,7 @@ Opts read_opts() {
   o.reverse_units = g_unit_order != 0;
   o.withhold = g_withhold != 0;
   o.wait_ns = (uint64_t)g_wait_us * 1000ull;
+  o.matrix_row_min = g_matrix_row_min;
   const int sms = sm_count();
   o.grid = g_grid > 0 ? (int)g_grid : (sms > 0 ? sms : 1);
   return o;
@@ -799,6 +802,41 @@ int enqueue_matrix_select(Arena* a, const RowSpace& rs, int K, const Opts& o, co
   const Layout& L = a->L;
   Stats* st = pp.stats;
   uint32_t* tau = at<uint32_t>(a, L.tau);
+  const int sms = o.grid;
+  const int64_t row_min = o.matrix_row_min >= 0 ? o.matrix_row_min : (int64_t)MATRIX_TOPK_CTAS_PER_SM * sms;
+  if (rs.R >= row_min) {
+    // rows enough to fill the GPU: one CTA per row at a time (threshold,
+    // one pass, selection), then the repair of the rows that failed
+    MatrixTopkParams mt{};
+    mt.rs = rs;
+    mt.K = K;
+    mt.target16 = o.target16;
+    mt.tau_bias = o.bias;
+    mt.scores = scores;
+    mt.ld = ld;
+    mt.rb = pp.rb;
+    mt.re = pp.re;
+    mt.tau = tau;
+    mt.cand_key = at<uint32_t>(a, L.cand_key);
+    mt.cand_idx = at<int32_t>(a, L.cand_idx);
+    mt.failed_rows = at<int32_t>(a, L.failed);
+    mt.out = out;
+    mt.stats = st;
+    DSA_LAUNCH(launch_matrix_topk(mt, sms, stream));
+    WideParams wp{};
+    wp.rs = rs;
+    wp.K = K;
+    wp.list = mt.failed_rows;
+    wp.scores = scores;
+    wp.ld = ld;
+    wp.by_row = 1;
+    wp.rb = pp.rb;
+    wp.re = pp.re;
+    wp.out = out;
+    wp.stats = st;
+    DSA_LAUNCH(launch_wide_select(wp, o.grid / 2 > 0 ? o.grid / 2 : 1, stream));
+    return DSA_OK;
+  }
   SampleTauParams tp{};
   tp.rs = rs;
   tp.K = K;
@@ -1223,6 +1261,10 @@ int dsa_indexer_set_option(int option, int64_t value) {
       if (value != 0 && value != 1) return DSA_ERR_ARG;
       g_withhold = value;
       return DSA_OK;
+    case DSA_OPT_MATRIX_ROW_MIN:
+      if (value < -1) return DSA_ERR_ARG;
+      g_matrix_row_min = value;
+      return DSA_OK;
 
     default:
       return DSA_ERR_ARG;
@@ -1250,6 +1292,8 @@ int64_t dsa_indexer_get_option(int option) {
       return g_wait_us;
     case DSA_OPT_TEST_WITHHOLD:
       return g_withhold;
+    case DSA_OPT_MATRIX_ROW_MIN:
+      return g_matrix_row_min;
 
     default:
       return DSA_ERR_ARG;

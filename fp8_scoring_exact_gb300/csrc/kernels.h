@@ -218,6 +218,33 @@ struct MatrixFilterParams {
   Stats* stats;
 };
 
+// Exact top-K over a given fp32 score matrix with one CTA per row at a time
+// (the standalone top-K when the rows fill the GPU): the row's threshold
+// from its own sample grid, one pass over the row appending the scores at
+// or above it to the row's ROW_SLOTS candidate slots (one list), and the
+// candidate selector's passes over that list; rows that fail the
+// certificate are queued for repair.
+#ifndef DSA_RT_CTAS
+#define DSA_RT_CTAS 4
+#endif
+constexpr int MATRIX_TOPK_CTAS_PER_SM = DSA_RT_CTAS;
+struct MatrixTopkParams {
+  RowSpace rs;
+  int K;
+  int target16;
+  int64_t tau_bias;
+  const float* scores;         // [R, ld]
+  int64_t ld;
+  const int32_t* rb;           // validated ranges
+  const int32_t* re;
+  uint32_t* tau;               // [R] threshold keys (written)
+  uint32_t* cand_key;          // [R, ROW_SLOTS]
+  int32_t* cand_idx;
+  int32_t* failed_rows;        // [R] (appended, count in stats->fail_count)
+  int32_t* out;                // [R, K]
+  Stats* stats;
+};
+
 // A kernel launch with programmatic stream serialisation (the kernels open
 // with pdl_enter()); returns the launch's error.
 template <typename... KArgs, typename... Args>
@@ -288,6 +315,7 @@ cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t s);
 cudaError_t launch_cand_select(const CandParams& p, int sms, cudaStream_t s);  // grid: a few CTAs per SM
 cudaError_t launch_wide_select(const WideParams& p, int clusters, cudaStream_t s);
 cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStream_t s);
+cudaError_t launch_matrix_topk(const MatrixTopkParams& p, int sms, cudaStream_t s);  // grid: CTAs of one wave, at most R
 cudaError_t launch_sparse_attn(const SparseAttnParams& p, cudaStream_t s);
 int sparse_attn_ctas_per_sm();  // CTAs of the sparse-attention kernel resident per SM
 

@@ -303,9 +303,14 @@ typedef enum {
   DSA_OPT_WAIT_LIMIT_US = 8,   /* microseconds after which a pipeline wait inside a kernel gives up (default
                                   2000000, range 1..60000000): the kernel then lets the copies and MMAs it
                                   already issued land, returns early, and the call reports DSA_ERR_TIMEOUT */
-  DSA_OPT_TEST_WITHHOLD = 9    /* test option: 1 makes the fused operator's main scorer never signal its first
+  DSA_OPT_TEST_WITHHOLD = 9,   /* test option: 1 makes the fused operator's main scorer never signal its first
                                   accumulator, so that its epilogue's wait runs out after DSA_OPT_WAIT_LIMIT_US
                                   and the call reports DSA_ERR_TIMEOUT (its output is then undefined); default 0 */
+  DSA_OPT_MATRIX_ROW_MIN = 10  /* dsa_indexer_topk_from_scores and the unfused operator's selection: rows from
+                                  which each CTA takes whole rows (threshold, one pass over the row, selection)
+                                  instead of splitting rows over the SMs (default -1: chosen per call, one
+                                  wave of the per-row kernel's CTAs; 0: always; the result does not depend
+                                  on it) */
 } dsa_option;
 DSA_API int dsa_indexer_set_option(int option, int64_t value);
 DSA_API int64_t dsa_indexer_get_option(int option);

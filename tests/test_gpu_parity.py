@@ -427,7 +427,16 @@ def test_argument_errors_are_synchronous(B):
 
 
 # ----------------------------------------------------- standalone select ----
-def test_topk_from_scores_exact(B):
+@pytest.fixture(params=["split", "rows"])
+def matrix_path(B, request):
+    """The standalone top-K both ways: rows split over the SMs (threshold
+    kernel, filter, candidate selector) and one CTA per row at a time."""
+    B.set_option("matrix_row_min", 1 << 40 if request.param == "split" else 0)
+    yield request.param
+    B.set_option("matrix_row_min", -1)
+
+
+def test_topk_from_scores_exact(B, matrix_path):
     """Selection only: given fp32 scores the result is exactly determined up
     to ties, so the sorted selected values must equal a full sort bit for bit."""
     import torch
@@ -455,7 +464,7 @@ def test_topk_from_scores_exact(B):
         assert np.array_equal(got, want), t
 
 
-def test_topk_from_scores_long_rows_exact(B):
+def test_topk_from_scores_long_rows_exact(B, matrix_path):
     """Rows of 128K keys, where the filter keeps a few percent of the scores
     (per-lane masks and one warp scan per step) or, with ties at the
     threshold, many (a ballot per score): the sorted selected values equal a
@@ -483,7 +492,7 @@ def test_topk_from_scores_long_rows_exact(B):
 
 
 @pytest.mark.parametrize("bias,kind", [(0, None), (1 << 31, "underflow"), (-(1 << 33), "overflow")])
-def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind):
+def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind, matrix_path):
     """A padded row stride (ld > N, N not a multiple of 4), ranges that end at
     N or start off a 4-key boundary, rows with ties; with the threshold pushed
     to the top every row longer than K fails the certificate, and with it at
