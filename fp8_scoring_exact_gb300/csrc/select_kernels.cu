@@ -1608,27 +1608,27 @@ cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStre
 // ============================================================== row top-K ==
 // Exact top-K over a given fp32 score matrix, one CTA per row at a time
 // ("Fusing Indexer Scoring and Exact Top-k for DeepSeek-V3.2", sections 3.2
-// and 3.3, over a stored matrix): warp 0 takes the row's threshold from its
-// own sample grid (the threshold kernel's grid, rank and per-warp radix
-// select, so the thresholds are the same) while the other warps already
-// have the row's first scores in flight; then every warp streams the row,
-// appending the scores at or above the threshold to the row's candidate
-// slots as one list (a shared counter), and the CTA selects the row's top
-// K from that list with the candidate selector's passes (histogram over
-// key - tau, narrowing, counting-sort emission, rank counting of the
-// interval).  Several CTAs share an SM, so while one samples or selects
-// (latency-bound phases) the others stream: the matrix is read once, at the
-// pace of the stream alone.
-#ifndef DSA_RT_NT
-#define DSA_RT_NT 256
-#endif
+// and 3.3, over a stored matrix).  Eight warps: seven stream a row while the
+// eighth takes the next row and its threshold from that row's own sample
+// grid (the threshold kernel's grid, rank and per-warp radix select, so the
+// thresholds are the same); then all eight select the row's top K.  The
+// stream compares each score with the threshold's float image and appends
+// the scores at or above it to the row's candidate slots (one list, a
+// shared counter), with the next step's loads in flight while a step is
+// compared; the selection takes the candidate selector's passes over that
+// list (histogram over key - tau, narrowing, counting-sort emission, rank
+// counting of the interval).  Several CTAs share an SM: while one selects,
+// the others stream.
 #ifndef DSA_RT_U
 #define DSA_RT_U 4
 #endif
-constexpr int RT_NT = DSA_RT_NT, RT_CTAS = MATRIX_TOPK_CTAS_PER_SM;
-constexpr int RT_U = DSA_RT_U;  // float4s per thread and step of the stream (two steps in registers)
-constexpr int RT_SU = 2;  // 16-byte candidate loads per thread and selection pass round
-constexpr int RT_SCAN_MAX = 48;
+constexpr int RT_SW = 7;                // stream warps
+constexpr int RT_NS = RT_SW * 32;       // stream threads
+constexpr int RT_NT = RT_NS + 32;       // and the threshold warp: the selection's threads
+constexpr int RT_THREADS = RT_NT;
+constexpr int RT_CTAS = MATRIX_TOPK_CTAS_PER_SM;
+constexpr int RT_U = DSA_RT_U;          // float4s per thread and stream step (two steps in registers)
+constexpr int RT_SU = 2;                // 16-byte candidate loads per thread and selection round
 constexpr uint32_t RT_OFF_HIST = 0;
 constexpr uint32_t RT_OFF_HIST2 = RT_OFF_HIST + CS_BINS * 4;
 constexpr uint32_t RT_OFF_SKEY = RT_OFF_HIST2 + CS_BINS * 4;
@@ -1637,333 +1637,385 @@ constexpr uint32_t RT_OFF_OUT = RT_OFF_SIDX + CS_STAGE * 4;
 constexpr uint32_t RT_OFF_WHIST = RT_OFF_OUT + MAX_K * 4;
 constexpr uint32_t RT_OFF_WPICK = RT_OFF_WHIST + 256 * 4;
 constexpr uint32_t RT_OFF_MISC = RT_OFF_WPICK + 4 * 4;
-constexpr uint32_t RT_SMEM = RT_OFF_MISC + 64 * 4;
-static_assert(RT_CTAS * (RT_SMEM + 1024) <= 228 * 1024 && RT_CTAS * RT_NT <= 2048, "row top-K CTAs per SM");
-static_assert(CS_STAGE <= RT_NT && CS_BINS % RT_NT == 0, "one staged key per thread, bins per thread");
+constexpr uint32_t RT_OFF_STAGE = RT_OFF_MISC + 64 * 4;                   // per stream warp: a step's scores
+constexpr uint32_t RT_OFF_LIST = RT_OFF_STAGE + RT_SW * RT_U * 32 * 16;  // and the offsets of its kept ones
+constexpr uint32_t RT_SMEM = RT_OFF_LIST + RT_SW * RT_U * 32 * 4 * 2;
+static_assert(RT_CTAS * (RT_SMEM + 1024) <= 228 * 1024 && RT_CTAS * RT_THREADS <= 2048, "row top-K CTAs per SM");
+static_assert(CS_STAGE <= RT_NT && 1024 % RT_NT == 0 && 4 * RT_U <= 32, "staging, bins per thread, step mask");
 
+// The threshold key of row `row` over [b, e) (L > K) from its grid scores in
+// the matrix: the sample of descending rank ceil(m * target / L), plus the
+// test bias; 0 (every key passes) when the rank falls outside the sample.
 template <int KPL>
-__global__ void __launch_bounds__(RT_NT, RT_CTAS) matrix_topk_kernel(const MatrixTopkParams p) {
-  constexpr int NT = RT_NT, U = RT_U, SU = RT_SU;
-  pdl_enter();
-  extern __shared__ __align__(16) uint8_t smem[];
+__device__ __forceinline__ uint32_t rt_threshold(const MatrixTopkParams& p, int row, int b, int e, int target,
+                                                 int* whist, int* wpick) {
+  const int lane = threadIdx.x & 31;
+  int first, m, stride;
+  sample_grid(b, e, &first, &m, &stride);
+  m = min(m, MAX_SAMPLES);
+  const int rank = sample_rank(m, e - b, target);
+  uint32_t tau = 0u;
+  if (m > 0 && m <= 32 * KPL && rank >= 1 && rank <= m) {
+    const float* sr = p.scores + (int64_t)row * p.ld + first;
+    uint32_t key[KPL];
+#pragma unroll
+    for (int q = 0; q < KPL; ++q) {
+      const int i = q * 32 + lane;
+      key[q] = i < m ? ordered_key(__ldcg(&sr[(int64_t)i * stride])) : 0u;
+    }
+    tau = warp_select_rank<KPL>(key, m, rank, whist, wpick);
+    if (p.tau_bias != 0) {
+      const int64_t t = (int64_t)tau + p.tau_bias;
+      tau = (uint32_t)(t < 0 ? 0 : (t > 0xffffffffll ? 0xffffffffll : t));
+    }
+  }
+  return tau;
+}
+
+// 0xffffffff when x >= t, else 0 (false for NaN)
+__device__ __forceinline__ uint32_t ge_mask(float x, float t) {
+  uint32_t r;
+  asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(x), "f"(t));
+  return r;
+}
+
+// A stream thread's share of a row's whole float4s [fi0, fi1): float4
+// fi0 + t, then every RT_NS-th, RT_U per step, the next step's loads in
+// flight while a step is compared.  The warp's kept scores of a step go to
+// ck / ci at consecutive positions from the shared counter *count: each
+// lane stages its step in shared memory (stage: RT_U x 32 float4s, position
+// v, lane l at v * 32 + l) and lists the offsets of its kept scores there
+// (list, in lane order: a warp scan of the counts), then lane j writes
+// the list's j-th score.  Steps whose every float4 lies inside the range
+// (all but a row's last) take no per-lane range tests.
+__device__ __forceinline__ void rt_stream(const float4* s4, int fi0, int fi1, float tauf, uint32_t* ck, int32_t* ci,
+                                          int* count, float4* stage, uint16_t* list) {
+  constexpr int U = RT_U, NS = RT_NS;
+  const int lane = threadIdx.x & 31;
+  const int wt = (int)threadIdx.x - lane;  // the warp's first stream thread
+  const float* stagef = reinterpret_cast<const float*>(stage);
+  int fw = fi0 + wt;                       // lane 0's first float4 of the step
+  float4 x[U];
+#pragma unroll
+  for (int v = 0; v < U; ++v) {
+    const int f = fw + lane + v * NS;
+    x[v] = f < fi1 ? __ldcs(&s4[f]) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll 1
+  for (; fw < fi1; fw += U * NS) {  // (warp-uniform)
+    const int fn = fw + U * NS;     // the next step
+    float4 y[U];
+    if (fn + 31 + (U - 1) * NS < fi1) {
+#pragma unroll
+      for (int v = 0; v < U; ++v) y[v] = __ldcs(&s4[fn + lane + v * NS]);
+    } else {
+#pragma unroll
+      for (int v = 0; v < U; ++v) {
+        const int f = fn + lane + v * NS;
+        y[v] = f < fi1 ? __ldcs(&s4[f]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    uint32_t mask = 0u;
+    if (fw + 31 + (U - 1) * NS < fi1) {
+#pragma unroll
+      for (int v = 0; v < U; ++v) {
+        mask |= ge_mask(x[v].x, tauf) & (1u << (4 * v));
+        mask |= ge_mask(x[v].y, tauf) & (1u << (4 * v + 1));
+        mask |= ge_mask(x[v].z, tauf) & (1u << (4 * v + 2));
+        mask |= ge_mask(x[v].w, tauf) & (1u << (4 * v + 3));
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < U; ++v) {
+        if (fw + lane + v * NS < fi1) {
+          mask |= ge_mask(x[v].x, tauf) & (1u << (4 * v));
+          mask |= ge_mask(x[v].y, tauf) & (1u << (4 * v + 1));
+          mask |= ge_mask(x[v].z, tauf) & (1u << (4 * v + 2));
+          mask |= ge_mask(x[v].w, tauf) & (1u << (4 * v + 3));
+        }
+      }
+    }
+    const int cnt = __popc(mask);
+    int incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += t;
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (tot != 0) {  // warp-uniform
+      int base = 0;
+      if (lane == 31) base = atomicAdd(count, tot);
+#pragma unroll
+      for (int v = 0; v < U; ++v) stage[v * 32 + lane] = x[v];
+      int p = incl - cnt;
+      while (mask) {
+        const int q = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        list[p++] = (uint16_t)(((q >> 2) * 32 + lane) * 4 + (q & 3));
+      }
+      base = __shfl_sync(0xffffffffu, base, 31);
+      __syncwarp();
+      for (int j = lane; j < tot; j += 32) {
+        const int code = list[j];
+        const int pos = base + j;
+        if (pos < ROW_SLOTS) {
+          ck[pos] = ordered_key(stagef[code]);
+          ci[pos] = 4 * (fw + ((code >> 2) & 31) + (code >> 7) * NS) + (code & 3);
+        }
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int v = 0; v < U; ++v) x[v] = y[v];
+  }
+}
+
+// The exact top K of a row's n candidates (K <= n <= ROW_SLOTS, every key at
+// or above tau) into o, by every thread of the CTA; false when a candidate
+// lies below tau.
+__device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci, int n, uint32_t tau, int K,
+                                          int32_t* o, uint8_t* smem, int* misc) {
+  constexpr int NT = RT_NT, SU = RT_SU;
   int* hist = (int*)(smem + RT_OFF_HIST);
   int* hist2 = (int*)(smem + RT_OFF_HIST2);
   uint32_t* skey = (uint32_t*)(smem + RT_OFF_SKEY);
   int32_t* sidx = (int32_t*)(smem + RT_OFF_SIDX);
   int32_t* so = (int32_t*)(smem + RT_OFF_OUT);
-  // [2..4] bin pick, [8] tau, [9] candidates appended, [17] staged count,
-  // [21] theta, [22] rr, [23..25] emission counters, [27] next row,
-  // [32..63] warp sums
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < CS_BINS / NT; ++j) hist[tid + NT * j] = 0;
+  if (tid == 0) misc[17] = misc[23] = misc[24] = misc[25] = 0;
+  __syncthreads();
+  const uint4* ck4 = reinterpret_cast<const uint4*>(ck);
+  const int4* ci4 = reinterpret_cast<const int4*>(ci);
+  const int n4 = (n + 3) >> 2;  // (the slots past n up to a multiple of 4 are read, not used)
+  // pass 1: histogram of (key - tau) >> CS_SHIFT0, and a check that no
+  // candidate is below tau
+  bool below = false;
+#pragma unroll 1
+  for (int e4 = tid; e4 < n4; e4 += SU * NT) {
+    uint4 v[SU];
+#pragma unroll
+    for (int u = 0; u < SU; ++u) v[u] = e4 + u * NT < n4 ? __ldcg(&ck4[e4 + u * NT]) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < SU; ++u) {
+      const uint32_t kk[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (4 * (e4 + u * NT) + c < n) {
+          below |= kk[c] < tau;
+          atomicAdd(&hist[min((kk[c] - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1))], 1);
+        }
+      }
+    }
+  }
+  if (__syncthreads_or(below)) return false;  // (never: the stream keeps keys at or above tau)
+  desc_scan_pick<NT>(hist, CS_BINS, K, misc, true);  // hist now holds each bin's first slot
+  const uint32_t b0 = (uint32_t)misc[2];
+  int rem = misc[3], bc = misc[4];
+  unsigned long long lo = (unsigned long long)tau + ((unsigned long long)b0 << CS_SHIFT0);
+  unsigned long long hi = 1ull << 32;
+  if (b0 < CS_BINS - 1) hi = min(hi, lo + (1ull << CS_SHIFT0));
+  // narrowing passes while the K-th key's interval holds more keys than the
+  // stage
+#pragma unroll 1
+  while (bc > CS_STAGE && hi - lo > 1) {
+    const int sh = max(0, 64 - __clzll((long long)(hi - lo - 1)) - 10);
+    const uint32_t lo32 = (uint32_t)lo, hin = (uint32_t)(hi - 1);
+#pragma unroll
+    for (int j = 0; j < CS_BINS / NT; ++j) hist2[tid + NT * j] = 0;
+    __syncthreads();
+#pragma unroll 1
+    for (int e4 = tid; e4 < n4; e4 += NT) {
+      const uint4 v = __ldcg(&ck4[e4]);
+      const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (4 * e4 + c < n && kk[c] >= lo32 && kk[c] <= hin) atomicAdd(&hist2[(kk[c] - lo32) >> sh], 1);
+    }
+    __syncthreads();
+    desc_scan_pick<NT>(hist2, CS_BINS, rem, misc, false);
+    rem = misc[3];
+    bc = misc[4];
+    lo += (unsigned long long)misc[2] << sh;
+    hi = min(hi, lo + (1ull << sh));
+  }
+  const bool single = hi - lo == 1;  // the interval is one key value: theta
+  const uint32_t lo32 = (uint32_t)lo, hin = (uint32_t)(hi - 1);
+  // last pass (slots in the shared copy of the row's output): the bins above
+  // b0 to their slots, the keys of b0 above the interval next, the
+  // interval's keys staged (or, for a single value, its first rem keys to
+  // [K - rem, K))
+#pragma unroll 1
+  for (int e4 = tid; e4 < n4; e4 += SU * NT) {
+    uint4 v[SU];
+    int4 d[SU];
+#pragma unroll
+    for (int u = 0; u < SU; ++u) {
+      const bool ok = e4 + u * NT < n4;
+      v[u] = ok ? __ldcg(&ck4[e4 + u * NT]) : make_uint4(0, 0, 0, 0);
+      d[u] = ok ? __ldcg(&ci4[e4 + u * NT]) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int c = 0; c < 4 * SU; ++c) {
+      const uint4 vu = v[c >> 2];
+      const int4 du = d[c >> 2];
+      const uint32_t k = (c & 3) == 0 ? vu.x : (c & 3) == 1 ? vu.y : (c & 3) == 2 ? vu.z : vu.w;
+      const int32_t idc = (c & 3) == 0 ? du.x : (c & 3) == 1 ? du.y : (c & 3) == 2 ? du.z : du.w;
+      if (4 * (e4 + (c >> 2) * NT) + (c & 3) < n) {
+        const uint32_t bin = min((k - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1));
+        if (bin > b0) {
+          so[atomicAdd(&hist[bin], 1)] = idc;
+        } else if (bin == b0) {
+          if (k > hin) {
+            so[atomicAdd(&hist[b0], 1)] = idc;
+          } else if (k >= lo32) {
+            if (single) {
+              const int q = atomicAdd(&misc[25], 1);
+              if (q < rem) so[K - rem + q] = idc;
+            } else {
+              const int q = atomicAdd(&misc[17], 1);
+              skey[q] = k;
+              sidx[q] = idc;
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (!single) {
+    // the rem-th largest of the bc staged keys and its ties
+    const bool mine = tid < bc;
+    const uint32_t me = mine ? skey[tid] : 0u;
+    if (mine) {
+      int gt = 0, eq = 0, eqb = 0;
+      for (int j = 0; j < bc; ++j) {
+        const uint32_t y = skey[j];
+        gt += y > me;
+        eq += y == me;
+        eqb += (y == me) & (j < tid);
+      }
+      if (eqb == 0 && gt < rem && rem <= gt + eq) {
+        misc[21] = (int)me;
+        misc[22] = rem - gt;
+      }
+    }
+    __syncthreads();
+    const uint32_t theta = (uint32_t)misc[21];
+    const int rr = misc[22];
+    if (mine) {
+      if (me > theta) {
+        so[K - rem + atomicAdd(&misc[23], 1)] = sidx[tid];
+      } else if (me == theta) {
+        const int q = atomicAdd(&misc[24], 1);
+        if (q < rr) so[K - rr + q] = sidx[tid];
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < K; i += NT) o[i] = so[i];
+  return true;
+}
+
+template <int KPL>
+__global__ void __launch_bounds__(RT_THREADS, RT_CTAS) matrix_topk_kernel(const MatrixTopkParams p) {
+  pdl_enter();
+  extern __shared__ __align__(16) uint8_t smem[];
+  int* whist = (int*)(smem + RT_OFF_WHIST);
+  int* wpick = (int*)(smem + RT_OFF_WPICK);
+  // [2..4] bin pick, [8] the next row's threshold, [10] the next row's
+  // item, [12] candidates appended, [17] staged count, [21] theta, [22] rr,
+  // [23..25] emission counters, [32..39] warp sums
   int* misc = (int*)(smem + RT_OFF_MISC);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t lt = lanemask_lt();
   const int K = p.K, R = p.rs.R;
   const int target = (int)(((int64_t)p.target16 * K) / 16);
+  // items (row R - 1 - item: prefill chunks, the longest rows first): the
+  // CTA's own first, then from a counter; the threshold warp takes each one
+  // row ahead of the stream
+  if (warp == RT_SW) {
+    const int it = blockIdx.x;
+    uint32_t tau = 0u;
+    if (it < R) {
+      const int row = R - 1 - it, b = p.rb[row], e = p.re[row];
+      if (e - b > K) tau = rt_threshold<KPL>(p, row, b, e, target, whist, wpick);
+    }
+    if (lane == 0) {
+      misc[10] = it;
+      misc[8] = (int)tau;
+    }
+  }
+  __syncthreads();
   int ntriv = 0;
-  for (int it = blockIdx.x; it < R;) {
-    const int row = R - 1 - it;  // (prefill chunks: the longest rows first)
+  while (true) {
+    const int it = misc[10];
+    if (it >= R) break;  // uniform
+    const uint32_t tau = (uint32_t)misc[8];
+    const int row = R - 1 - it;
     const int b = p.rb[row], e = p.re[row], L = e - b;
     int32_t* o = p.out + (int64_t)row * K;
-    const float* srow = p.scores + (int64_t)row * p.ld;
-    if (L <= K) {  // every valid index, then -1
-      for (int i = tid; i < K; i += NT) o[i] = i < L ? b + i : -1;
-      ntriv += tid == 0;
-    } else {
-      do {
-        // the row's float4s wholly inside [b, e): [fi0, fi1); the keys
-        // before and after them (fewer than 4 at each end) go one by one
-        const int fi0 = (b + 3) >> 2, fi1 = e >> 2;
+    uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
+    int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
+    if (tid == 0) misc[12] = 0;
+    __syncthreads();  // the row is taken from the slot
+    if (warp == RT_SW) {
+      int itn = 0;
+      if (lane == 0) itn = (int)gridDim.x + atomicAdd(&p.stats->cs_next, 1);
+      itn = __shfl_sync(0xffffffffu, itn, 0);
+      uint32_t taun = 0u;
+      if (itn < R) {
+        const int rn = R - 1 - itn, bn = p.rb[rn], en = p.re[rn];
+        if (en - bn > K) taun = rt_threshold<KPL>(p, rn, bn, en, target, whist, wpick);
+      }
+      if (lane == 0) {
+        misc[10] = itn;
+        misc[8] = (int)taun;
+      }
+    } else if (L > K) {
+      // the row's float4s wholly inside [b, e) by the stream warps; the
+      // keys before and after them (fewer than 4 at each end) one by one
+      const int fi0 = (b + 3) >> 2, fi1 = e >> 2;
+      const float tauf = key_threshold_float(tau);
+      const float* srow = p.scores + (int64_t)row * p.ld;
+      rt_stream(reinterpret_cast<const float4*>(srow), fi0, fi1, tauf, ck, ci, &misc[12],
+                reinterpret_cast<float4*>(smem + RT_OFF_STAGE) + warp * RT_U * 32,
+                reinterpret_cast<uint16_t*>(smem + RT_OFF_LIST) + warp * RT_U * 32 * 4);
+      if (warp == 0 && lane < 2) {
         const int head_hi = min(e, 4 * fi0), tail_lo = max(4 * fi1, head_hi);
-        const float4* s4 = reinterpret_cast<const float4*>(srow);
-        // the first step's loads go out before the threshold's select
-        // (in the build for up to 672 samples: with more, they would spill)
-        constexpr bool early = KPL <= TAU_KPL_SHORT;
-        float4 x[U];
-        int f = fi0 + tid;
-        if (early) {
-#pragma unroll
-          for (int v = 0; v < U; ++v)
-            x[v] = f + v * NT < fi1 ? __ldcs(&s4[f + v * NT]) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (warp == 0) {
-          int first, m, stride;
-          sample_grid(b, e, &first, &m, &stride);
-          m = min(m, MAX_SAMPLES);
-          const int rank = sample_rank(m, L, target);
-          uint32_t tau = 0u;  // every key passes (the row goes to repair)
-          if (m > 0 && m <= 32 * KPL && rank >= 1 && rank <= m) {
-            const float* sr = srow + first;
-            uint32_t key[KPL];
-#pragma unroll
-            for (int q = 0; q < KPL; ++q) {
-              const int i = q * 32 + lane;
-              key[q] = i < m ? ordered_key(__ldcg(&sr[(int64_t)i * stride])) : 0u;
-            }
-            tau = warp_select_rank<KPL>(key, m, rank, (int*)(smem + RT_OFF_WHIST), (int*)(smem + RT_OFF_WPICK));
-            if (p.tau_bias != 0) {
-              const int64_t t = (int64_t)tau + p.tau_bias;
-              tau = (uint32_t)(t < 0 ? 0 : (t > 0xffffffffll ? 0xffffffffll : t));
-            }
-          }
-          if (lane == 0) {
-            misc[8] = (int)tau;
-            p.tau[row] = tau;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < CS_BINS / NT; ++j) hist[tid + NT * j] = 0;
-        if (tid == 0) misc[9] = misc[17] = misc[23] = misc[24] = misc[25] = 0;
-        __syncthreads();
-        if (!early) {
-#pragma unroll
-          for (int v = 0; v < U; ++v)
-            x[v] = f + v * NT < fi1 ? __ldcs(&s4[f + v * NT]) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        const uint32_t tau = (uint32_t)misc[8];
-        const float tauf = key_threshold_float(tau);
-        uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
-        int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
-        if (tid < 2) {  // the partial float4s at the row's ends
-          const int lo = tid == 0 ? b : tail_lo, hi = tid == 0 ? head_hi : e;
-          for (int s = lo; s < hi; ++s) {
-            const float val = srow[s];
-            if (val >= tauf) {
-              const int pos = atomicAdd(&misc[9], 1);
-              if (pos < ROW_SLOTS) {
-                ck[pos] = ordered_key(val);
-                ci[pos] = s;
-              }
+        const int lo = lane == 0 ? b : tail_lo, hi = lane == 0 ? head_hi : e;
+        for (int s = lo; s < hi; ++s) {
+          const float val = srow[s];
+          if (val >= tauf) {
+            const int pos = atomicAdd(&misc[12], 1);
+            if (pos < ROW_SLOTS) {
+              ck[pos] = ordered_key(val);
+              ci[pos] = s;
             }
           }
         }
-        // the stream: step U float4s per thread, the next step's loads in
-        // flight while this one is compared
-#pragma unroll 1
-        for (; f - lane < fi1; f += U * NT) {  // (warp-uniform: lane 0's float4)
-          float4 y[U];
-#pragma unroll
-          for (int v = 0; v < U; ++v) {
-            const int fn = f + (U + v) * NT;
-            y[v] = fn < fi1 ? __ldcs(&s4[fn]) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          uint32_t mask = 0u;
-#pragma unroll
-          for (int v = 0; v < U; ++v) {
-            const bool in = f + v * NT < fi1;
-            mask |= (in && x[v].x >= tauf ? 1u : 0u) << (4 * v);
-            mask |= (in && x[v].y >= tauf ? 1u : 0u) << (4 * v + 1);
-            mask |= (in && x[v].z >= tauf ? 1u : 0u) << (4 * v + 2);
-            mask |= (in && x[v].w >= tauf ? 1u : 0u) << (4 * v + 3);
-          }
-          const int cnt = __popc(mask);
-          const int tot = __reduce_add_sync(0xffffffffu, cnt);
-          if (tot != 0) {  // warp-uniform
-            int base = 0;
-            if (lane == 0) base = atomicAdd(&misc[9], tot);
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (tot <= RT_SCAN_MAX) {
-              // few kept: a warp scan of the counts, each lane writes its own
-              int incl = cnt;
-#pragma unroll
-              for (int d = 1; d < 32; d <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d) incl += t;
-              }
-              int pos = base + incl - cnt;
-              while (mask) {
-                const int q = __ffs(mask) - 1;
-                mask &= mask - 1u;
-                const int v = q >> 2, j = q & 3;
-                float4 xv = x[0];
-#pragma unroll
-                for (int w = 1; w < U; ++w)
-                  if (v == w) xv = x[w];
-                const float val = j == 0 ? xv.x : j == 1 ? xv.y : j == 2 ? xv.z : xv.w;
-                if (pos < ROW_SLOTS) {
-                  ck[pos] = ordered_key(val);
-                  ci[pos] = 4 * (f + v * NT) + j;
-                }
-                ++pos;
-              }
-            } else {
-              // many kept (ties at the threshold): a ballot per key position
-              // keeps the warp's stores in runs
-              int pos = base;
-#pragma unroll
-              for (int q = 0; q < 4 * U; ++q) {
-                const bool pr = (mask >> q) & 1u;
-                const uint32_t bm = __ballot_sync(0xffffffffu, pr);
-                if (bm) {
-                  const int at = pos + __popc(bm & lt);
-                  if (pr && at < ROW_SLOTS) {
-                    const float4 xv = x[q >> 2];
-                    const float val = (q & 3) == 0 ? xv.x : (q & 3) == 1 ? xv.y : (q & 3) == 2 ? xv.z : xv.w;
-                    ck[at] = ordered_key(val);
-                    ci[at] = 4 * (f + (q >> 2) * NT) + (q & 3);
-                  }
-                  pos += __popc(bm);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int v = 0; v < U; ++v) x[v] = y[v];
-        }
-        __syncthreads();
-        const int n = misc[9];
-        // certificate: at least K candidates, none lost (the row's slots
-        // hold ROW_SLOTS)
-        if (n < K || n > ROW_SLOTS) {
-          if (tid == 0) {
-            const int fr = atomicAdd(&p.stats->fail_count, 1);
-            p.failed_rows[fr] = row;
-            atomicAdd(n < K ? &p.stats->underflow : &p.stats->overflow, 1);
-          }
-          break;
-        }
-        if (tid == 0) atomicAdd(&p.stats->cand_total, n);
-        const uint4* ck4 = reinterpret_cast<const uint4*>(ck);
-        const int4* ci4 = reinterpret_cast<const int4*>(ci);
-        const int n4 = (n + 3) >> 2;  // (the slots past n up to a multiple of 4 are read, not used)
-        // pass 1: histogram of (key - tau) >> CS_SHIFT0, and a check that no
-        // candidate is below tau
-        bool below = false;
-#pragma unroll 1
-        for (int e4 = tid; e4 < n4; e4 += SU * NT) {
-          uint4 v[SU];
-#pragma unroll
-          for (int u = 0; u < SU; ++u) v[u] = e4 + u * NT < n4 ? __ldcg(&ck4[e4 + u * NT]) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int u = 0; u < SU; ++u) {
-            const uint32_t kk[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              if (4 * (e4 + u * NT) + c < n) {
-                below |= kk[c] < tau;
-                atomicAdd(&hist[min((kk[c] - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1))], 1);
-              }
-            }
-          }
-        }
-        if (__syncthreads_or(below)) {  // (never taken: the stream keeps keys at or above tau)
-          if (tid == 0) {
-            const int fr = atomicAdd(&p.stats->fail_count, 1);
-            p.failed_rows[fr] = row;
-            atomicAdd(&p.stats->overflow, 1);
-          }
-          break;
-        }
-        desc_scan_pick<NT>(hist, CS_BINS, K, misc, true);  // hist now holds each bin's first slot
-        const uint32_t b0 = (uint32_t)misc[2];
-        int rem = misc[3], bc = misc[4];
-        unsigned long long lo = (unsigned long long)tau + ((unsigned long long)b0 << CS_SHIFT0);
-        unsigned long long hi = 1ull << 32;
-        if (b0 < CS_BINS - 1) hi = min(hi, lo + (1ull << CS_SHIFT0));
-        // narrowing passes while the K-th key's interval holds more keys
-        // than the stage
-#pragma unroll 1
-        while (bc > CS_STAGE && hi - lo > 1) {
-          const int sh = max(0, 64 - __clzll((long long)(hi - lo - 1)) - 10);
-          const uint32_t lo32 = (uint32_t)lo, hin = (uint32_t)(hi - 1);
-#pragma unroll
-          for (int j = 0; j < CS_BINS / NT; ++j) hist2[tid + NT * j] = 0;
-          __syncthreads();
-#pragma unroll 1
-          for (int e4 = tid; e4 < n4; e4 += NT) {
-            const uint4 v = __ldcg(&ck4[e4]);
-            const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              if (4 * e4 + c < n && kk[c] >= lo32 && kk[c] <= hin) atomicAdd(&hist2[(kk[c] - lo32) >> sh], 1);
-          }
-          __syncthreads();
-          desc_scan_pick<NT>(hist2, CS_BINS, rem, misc, false);
-          rem = misc[3];
-          bc = misc[4];
-          lo += (unsigned long long)misc[2] << sh;
-          hi = min(hi, lo + (1ull << sh));
-        }
-        const bool single = hi - lo == 1;  // the interval is one key value: theta
-        const uint32_t lo32 = (uint32_t)lo, hin = (uint32_t)(hi - 1);
-        // last pass (slots in the shared copy of the row's output): the bins
-        // above b0 to their slots, the keys of b0 above the interval next,
-        // the interval's keys staged (or, for a single value, its first rem
-        // keys to [K - rem, K))
-#pragma unroll 1
-        for (int e4 = tid; e4 < n4; e4 += SU * NT) {
-          uint4 v[SU];
-          int4 d[SU];
-#pragma unroll
-          for (int u = 0; u < SU; ++u) {
-            const bool ok = e4 + u * NT < n4;
-            v[u] = ok ? __ldcg(&ck4[e4 + u * NT]) : make_uint4(0, 0, 0, 0);
-            d[u] = ok ? __ldcg(&ci4[e4 + u * NT]) : make_int4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int c = 0; c < 4 * SU; ++c) {
-            const uint4 vu = v[c >> 2];
-            const int4 du = d[c >> 2];
-            const uint32_t k = (c & 3) == 0 ? vu.x : (c & 3) == 1 ? vu.y : (c & 3) == 2 ? vu.z : vu.w;
-            const int32_t idc = (c & 3) == 0 ? du.x : (c & 3) == 1 ? du.y : (c & 3) == 2 ? du.z : du.w;
-            if (4 * (e4 + (c >> 2) * NT) + (c & 3) < n) {
-              const uint32_t bin = min((k - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1));
-              if (bin > b0) {
-                so[atomicAdd(&hist[bin], 1)] = idc;
-              } else if (bin == b0) {
-                if (k > hin) {
-                  so[atomicAdd(&hist[b0], 1)] = idc;
-                } else if (k >= lo32) {
-                  if (single) {
-                    const int q = atomicAdd(&misc[25], 1);
-                    if (q < rem) so[K - rem + q] = idc;
-                  } else {
-                    const int q = atomicAdd(&misc[17], 1);
-                    skey[q] = k;
-                    sidx[q] = idc;
-                  }
-                }
-              }
-            }
-          }
-        }
-        __syncthreads();
-        if (!single) {
-          // the rem-th largest of the bc staged keys and its ties
-          const bool mine = tid < bc;
-          const uint32_t me = mine ? skey[tid] : 0u;
-          if (mine) {
-            int gt = 0, eq = 0, eqb = 0;
-            for (int j = 0; j < bc; ++j) {
-              const uint32_t y = skey[j];
-              gt += y > me;
-              eq += y == me;
-              eqb += (y == me) & (j < tid);
-            }
-            if (eqb == 0 && gt < rem && rem <= gt + eq) {
-              misc[21] = (int)me;
-              misc[22] = rem - gt;
-            }
-          }
-          __syncthreads();
-          const uint32_t theta = (uint32_t)misc[21];
-          const int rr = misc[22];
-          if (mine) {
-            if (me > theta) {
-              so[K - rem + atomicAdd(&misc[23], 1)] = sidx[tid];
-            } else if (me == theta) {
-              const int q = atomicAdd(&misc[24], 1);
-              if (q < rr) so[K - rr + q] = sidx[tid];
-            }
-          }
-        }
-        __syncthreads();
-        for (int i = tid; i < K; i += NT) o[i] = so[i];
-      } while (false);
+      }
+    } else {  // every valid index, then -1
+      for (int i = tid; i < K; i += RT_NS) o[i] = i < L ? b + i : -1;
+      ntriv += tid == 0;
     }
-    // the next row (a counter: rows differ in length)
-    if (tid == 0) misc[27] = (int)gridDim.x + atomicAdd(&p.stats->cs_next, 1);
-    __syncthreads();
-    it = misc[27];
+    __syncthreads();  // the row is streamed, the next row's threshold is in the slot
+    if (L > K) {
+      // certificate: at least K candidates, none lost (the row's slots hold
+      // ROW_SLOTS)
+      const int n = misc[12];
+      bool ok = n >= K && n <= ROW_SLOTS;
+      if (ok) {
+        if (tid == 0) atomicAdd(&p.stats->cand_total, n);
+        ok = rt_select(ck, ci, n, tau, K, o, smem, misc);
+      }
+      if (!ok && tid == 0) {
+        const int fr = atomicAdd(&p.stats->fail_count, 1);
+        p.failed_rows[fr] = row;
+        atomicAdd(n < K ? &p.stats->underflow : &p.stats->overflow, 1);
+      }
+    }
     __syncthreads();
   }
   if (tid == 0 && ntriv) atomicAdd(&p.stats->trivial, ntriv);
@@ -1972,19 +2024,19 @@ __global__ void __launch_bounds__(RT_NT, RT_CTAS) matrix_topk_kernel(const Matri
 cudaError_t launch_matrix_topk(const MatrixTopkParams& p, int sms, cudaStream_t s) {
   static DeviceFlags attr_short, attr_long;
   const int grid = max(1, min(p.rs.R, RT_CTAS * sms));
-  // the threshold's grid keys sit in warp 0's registers: the build holding
-  // up to 672 (rows of up to ~134K keys) or MAX_SAMPLES
+  // the threshold's grid keys sit in the threshold warp's registers: the
+  // build holding up to 672 (rows of up to ~134K keys) or MAX_SAMPLES
   const int64_t max_m = std::min<int64_t>(MAX_SAMPLES, (int64_t)p.rs.N / SAMPLE_STRIDE + 2);
   if (max_m <= 32 * TAU_KPL_SHORT) {
     auto k = matrix_topk_kernel<TAU_KPL_SHORT>;
     cudaError_t e = set_smem_attr_once(k, RT_SMEM, attr_short);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, dim3(grid), dim3(RT_NT), RT_SMEM, s, p);
+    return launch_pdl(k, dim3(grid), dim3(RT_THREADS), RT_SMEM, s, p);
   }
   auto k = matrix_topk_kernel<MAX_SAMPLES / 32>;
   cudaError_t e = set_smem_attr_once(k, RT_SMEM, attr_long);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(grid), dim3(RT_NT), RT_SMEM, s, p);
+  return launch_pdl(k, dim3(grid), dim3(RT_THREADS), RT_SMEM, s, p);
 }
 
 
