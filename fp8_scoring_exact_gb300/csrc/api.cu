@@ -790,6 +790,21 @@ int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uin
   return run_fused(rs, K, tq, tk, k_cache, k_cache_scale, q_scale, w, nullptr, nullptr, out_idx, stream);
 }
 
+// The standalone top-K takes whole rows (or half rows per item, the ticket
+// of each row in the plan's zeroed pair_cnt) once the rows fill a wave of
+// the per-row kernel's CTAs; fewer rows are split over the SMs.
+bool matrix_by_rows(const Opts& o, const RowSpace& rs) {
+  const int64_t row_min = o.matrix_row_min >= 0 ? o.matrix_row_min : (int64_t)MATRIX_TOPK_CTAS_PER_SM * o.grid;
+  return rs.R >= row_min;
+}
+// Items per row of the per-row kernel: half rows for three waves of rows or
+// more of at least 64K keys (measured on GB300: 4096 x 131072 0.453 ->
+// 0.437 ms; fewer or shorter rows were slower in halves: 1216 x 131072
+// 0.155 -> 0.167 ms, 2048 x 16384 0.105 -> 0.124 ms).
+int matrix_parts(const Opts& o, const RowSpace& rs) {
+  return rs.R >= 3LL * MATRIX_TOPK_CTAS_PER_SM * o.grid && rs.N >= 65536 ? 2 : 1;
+}
+
 // Exact top-K over a given fp32 score matrix [R, ld] (the standalone
 // selector and the unfused pipeline's second stage), after a main plan `pp`
 // (trivial_len = K) on the same arena: one threshold per row from its own
@@ -803,8 +818,7 @@ int enqueue_matrix_select(Arena* a, const RowSpace& rs, int K, const Opts& o, co
   Stats* st = pp.stats;
   uint32_t* tau = at<uint32_t>(a, L.tau);
   const int sms = o.grid;
-  const int64_t row_min = o.matrix_row_min >= 0 ? o.matrix_row_min : (int64_t)MATRIX_TOPK_CTAS_PER_SM * sms;
-  if (rs.R >= row_min) {
+  if (matrix_by_rows(o, rs)) {
     // rows enough to fill the GPU: one CTA per row at a time (threshold,
     // one pass, selection), then the repair of the rows that failed
     MatrixTopkParams mt{};
@@ -822,6 +836,9 @@ int enqueue_matrix_select(Arena* a, const RowSpace& rs, int K, const Opts& o, co
     mt.failed_rows = at<int32_t>(a, L.failed);
     mt.out = out;
     mt.stats = st;
+    mt.parts = matrix_parts(o, rs);
+    mt.half_count = at<int32_t>(a, L.unit_count);
+    mt.row_ticket = pp.pair_cnt;
     DSA_LAUNCH(launch_matrix_topk(mt, sms, stream));
     WideParams wp{};
     wp.rs = rs;
@@ -934,6 +951,10 @@ static int scores_impl(const uint8_t* q_fp8, const float* q_scale, const uint8_t
   pp.groups = at<Group>(a, L.groups);
   pp.unit_start = at<int32_t>(a, L.unit_start);
   pp.failed_rows = at<int32_t>(a, L.failed);
+  if (out_idx && matrix_by_rows(o, rs)) {  // the rows' tickets, zeroed by the plan
+    pp.pair_cnt = at<int>(a, L.pair_cnt);
+    pp.n_pairs = Q;
+  }
   pp.stats = st;
   pp.wait_ns = o.wait_ns;
   DSA_LAUNCH(launch_plan(pp, stream));
@@ -1009,6 +1030,10 @@ int dsa_indexer_topk_from_scores(const float* scores, int64_t ld, const int32_t*
   pp.groups = at<Group>(a, L.groups);
   pp.unit_start = at<int32_t>(a, L.unit_start);
   pp.failed_rows = at<int32_t>(a, L.failed);
+  if (matrix_by_rows(o, rs)) {  // the rows' tickets, zeroed by the plan
+    pp.pair_cnt = at<int>(a, L.pair_cnt);
+    pp.n_pairs = Q;
+  }
   pp.stats = at<Stats>(a, L.stats);
   pp.wait_ns = o.wait_ns;
   DSA_LAUNCH(launch_plan(pp, stream));

@@ -340,12 +340,10 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
-// from global to shared memory, completing on `bar` (whose expected
-// transaction count the issuing thread raised by `bytes`).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(bar)
+// Prefetch of `bytes` (a multiple of 16, from a 16-byte aligned address)
+// from global memory into L2, with no destination and nothing to wait for.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(src)), "r"(bytes)
                : "memory");
 }
 

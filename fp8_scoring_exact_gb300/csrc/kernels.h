@@ -218,12 +218,12 @@ struct MatrixFilterParams {
   Stats* stats;
 };
 
-// Exact top-K over a given fp32 score matrix with one CTA per row at a time
-// (the standalone top-K when the rows fill the GPU): the row's threshold
-// from its own sample grid, one pass over the row appending the scores at
-// or above it to the row's ROW_SLOTS candidate slots (one list), and the
-// candidate selector's passes over that list; rows that fail the
-// certificate are queued for repair.
+// Exact top-K over a given fp32 score matrix by whole or half rows (the
+// standalone top-K when the rows fill the GPU): an item's scores at or
+// above the row's threshold (from its own sample grid) go to its share of
+// the row's ROW_SLOTS candidate slots, and the CTA that finishes a row
+// selects it from its lists; rows that fail the certificate are queued for
+// repair.
 #ifndef DSA_RT_CTAS
 #define DSA_RT_CTAS 4
 #endif
@@ -243,6 +243,9 @@ struct MatrixTopkParams {
   int32_t* failed_rows;        // [R] (appended, count in stats->fail_count)
   int32_t* out;                // [R, K]
   Stats* stats;
+  int parts;                   // items per row: 1 (whole rows) or 2 (half rows)
+  int* half_count;             // half rows: [R, 2] candidates of each half of a row
+  int* row_ticket;             // half rows: [R] halves streamed (zeroed by the plan)
 };
 
 // A kernel launch with programmatic stream serialisation (the kernels open

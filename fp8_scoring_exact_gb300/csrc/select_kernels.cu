@@ -1606,19 +1606,23 @@ cudaError_t launch_matrix_filter(const MatrixFilterParams& p, int grid, cudaStre
 }
 
 // ============================================================== row top-K ==
-// Exact top-K over a given fp32 score matrix, one CTA per row at a time
-// ("Fusing Indexer Scoring and Exact Top-k for DeepSeek-V3.2", sections 3.2
-// and 3.3, over a stored matrix).  Eight warps: seven stream a row while the
-// eighth takes the next row and its threshold from that row's own sample
-// grid (the threshold kernel's grid, rank and per-warp radix select, so the
-// thresholds are the same); then all eight select the row's top K.  The
-// stream compares each score with the threshold's float image and appends
-// the scores at or above it to the row's candidate slots (one list, a
-// shared counter), with the next step's loads in flight while a step is
-// compared; the selection takes the candidate selector's passes over that
-// list (histogram over key - tau, narrowing, counting-sort emission, rank
-// counting of the interval).  Several CTAs share an SM: while one selects,
-// the others stream.
+// Exact top-K over a given fp32 score matrix ("Fusing Indexer Scoring and
+// Exact Top-k for DeepSeek-V3.2", sections 3.2 and 3.3, over a stored
+// matrix) in items of a whole row or, for many long rows, half a row.
+// Eight warps per CTA: seven stream an item while the eighth takes the next
+// item and its row's threshold from that row's own sample grid (the
+// threshold kernel's grid, rank and per-warp radix select, so both halves
+// of a row get the same threshold).  The stream compares each score with
+// the threshold's float image and appends the scores at or above it to the
+// item's candidate slots (one list per item, a shared counter), the next
+// step's loads in flight while a step is compared.  The CTA that finishes a
+// row (the second of its halves: a ticket per row) selects the row's top K
+// from its lists with the candidate selector's passes (histogram over
+// key - tau, narrowing, counting-sort emission, rank counting of the
+// interval).  With half rows the selections fall at scattered times, so
+// while some CTAs select the others keep the stream going (whole rows of
+// equal length keep the CTAs in step: they all select at once), and the
+// last items are short.
 #ifndef DSA_RT_U
 #define DSA_RT_U 4
 #endif
@@ -1628,6 +1632,7 @@ constexpr int RT_NT = RT_NS + 32;       // and the threshold warp: the selection
 constexpr int RT_THREADS = RT_NT;
 constexpr int RT_CTAS = MATRIX_TOPK_CTAS_PER_SM;
 constexpr int RT_U = DSA_RT_U;          // float4s per thread and stream step (two steps in registers)
+constexpr int RT_HALF = ROW_SLOTS / 2;  // candidate slots of each half of a row (items of half rows)
 constexpr int RT_SU = 2;                // 16-byte candidate loads per thread and selection round
 constexpr uint32_t RT_OFF_HIST = 0;
 constexpr uint32_t RT_OFF_HIST2 = RT_OFF_HIST + CS_BINS * 4;
@@ -1682,14 +1687,15 @@ __device__ __forceinline__ uint32_t ge_mask(float x, float t) {
 // A stream thread's share of a row's whole float4s [fi0, fi1): float4
 // fi0 + t, then every RT_NS-th, RT_U per step, the next step's loads in
 // flight while a step is compared.  The warp's kept scores of a step go to
-// ck / ci at consecutive positions from the shared counter *count: each
+// ck / ci (cap slots) at consecutive positions from the shared counter
+// *count: each
 // lane stages its step in shared memory (stage: RT_U x 32 float4s, position
 // v, lane l at v * 32 + l) and lists the offsets of its kept scores there
 // (list, in lane order: a warp scan of the counts), then lane j writes
 // the list's j-th score.  Steps whose every float4 lies inside the range
 // (all but a row's last) take no per-lane range tests.
 __device__ __forceinline__ void rt_stream(const float4* s4, int fi0, int fi1, float tauf, uint32_t* ck, int32_t* ci,
-                                          int* count, float4* stage, uint16_t* list) {
+                                          int cap, int* count, float4* stage, uint16_t* list) {
   constexpr int U = RT_U, NS = RT_NS;
   const int lane = threadIdx.x & 31;
   const int wt = (int)threadIdx.x - lane;  // the warp's first stream thread
@@ -1759,7 +1765,7 @@ __device__ __forceinline__ void rt_stream(const float4* s4, int fi0, int fi1, fl
       for (int j = lane; j < tot; j += 32) {
         const int code = list[j];
         const int pos = base + j;
-        if (pos < ROW_SLOTS) {
+        if (pos < cap) {
           ck[pos] = ordered_key(stagef[code]);
           ci[pos] = 4 * (fw + ((code >> 2) & 31) + (code >> 7) * NS) + (code & 3);
         }
@@ -1771,11 +1777,14 @@ __device__ __forceinline__ void rt_stream(const float4* s4, int fi0, int fi1, fl
   }
 }
 
-// The exact top K of a row's n candidates (K <= n <= ROW_SLOTS, every key at
-// or above tau) into o, by every thread of the CTA; false when a candidate
-// lies below tau.
-__device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci, int n, uint32_t tau, int K,
-                                          int32_t* o, uint8_t* smem, int* misc) {
+// The exact top K of a row's candidates into o, by every thread of the CTA:
+// the two halves' lists, slots [0, na) and [RT_HALF, RT_HALF + nb) of the
+// row's (a whole row's list: nb = 0; K <= na + nb, every key at or above
+// tau); false when a candidate lies below tau.  The lists are read as one sequence of 16-byte groups
+// (a half's last group holds fewer than 4 of its keys).
+template <bool TWO>
+__device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci, int na, int nb, uint32_t tau,
+                                          int K, int32_t* o, uint8_t* smem, int* misc) {
   constexpr int NT = RT_NT, SU = RT_SU;
   int* hist = (int*)(smem + RT_OFF_HIST);
   int* hist2 = (int*)(smem + RT_OFF_HIST2);
@@ -1789,21 +1798,36 @@ __device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci,
   __syncthreads();
   const uint4* ck4 = reinterpret_cast<const uint4*>(ck);
   const int4* ci4 = reinterpret_cast<const int4*>(ci);
-  const int n4 = (n + 3) >> 2;  // (the slots past n up to a multiple of 4 are read, not used)
+  const int na4 = (na + 3) >> 2, n4 = na4 + ((nb + 3) >> 2);
+  // group e4 of the sequence: its place in the slots (in groups) and how
+  // many of its 4 keys are candidates (the slots past a list's end up to a
+  // multiple of 4 are read, not used)
+  auto group = [&](int e4, int& lim) {
+    if (!TWO || e4 < na4) {
+      lim = na - 4 * e4;
+      return e4;
+    }
+    lim = nb - 4 * (e4 - na4);
+    return RT_HALF / 4 + (e4 - na4);
+  };
   // pass 1: histogram of (key - tau) >> CS_SHIFT0, and a check that no
   // candidate is below tau
   bool below = false;
 #pragma unroll 1
   for (int e4 = tid; e4 < n4; e4 += SU * NT) {
     uint4 v[SU];
+    int lim[SU];
 #pragma unroll
-    for (int u = 0; u < SU; ++u) v[u] = e4 + u * NT < n4 ? __ldcg(&ck4[e4 + u * NT]) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < SU; ++u) {
+      lim[u] = 0;
+      v[u] = e4 + u * NT < n4 ? __ldcg(&ck4[group(e4 + u * NT, lim[u])]) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
     for (int u = 0; u < SU; ++u) {
       const uint32_t kk[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        if (4 * (e4 + u * NT) + c < n) {
+        if (c < lim[u]) {
           below |= kk[c] < tau;
           atomicAdd(&hist[min((kk[c] - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1))], 1);
         }
@@ -1828,11 +1852,12 @@ __device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci,
     __syncthreads();
 #pragma unroll 1
     for (int e4 = tid; e4 < n4; e4 += NT) {
-      const uint4 v = __ldcg(&ck4[e4]);
+      int lim;
+      const uint4 v = __ldcg(&ck4[group(e4, lim)]);
       const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        if (4 * e4 + c < n && kk[c] >= lo32 && kk[c] <= hin) atomicAdd(&hist2[(kk[c] - lo32) >> sh], 1);
+        if (c < lim && kk[c] >= lo32 && kk[c] <= hin) atomicAdd(&hist2[(kk[c] - lo32) >> sh], 1);
     }
     __syncthreads();
     desc_scan_pick<NT>(hist2, CS_BINS, rem, misc, false);
@@ -1851,11 +1876,14 @@ __device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci,
   for (int e4 = tid; e4 < n4; e4 += SU * NT) {
     uint4 v[SU];
     int4 d[SU];
+    int lim[SU];
 #pragma unroll
     for (int u = 0; u < SU; ++u) {
+      lim[u] = 0;
       const bool ok = e4 + u * NT < n4;
-      v[u] = ok ? __ldcg(&ck4[e4 + u * NT]) : make_uint4(0, 0, 0, 0);
-      d[u] = ok ? __ldcg(&ci4[e4 + u * NT]) : make_int4(0, 0, 0, 0);
+      const int g = ok ? group(e4 + u * NT, lim[u]) : 0;
+      v[u] = ok ? __ldcg(&ck4[g]) : make_uint4(0, 0, 0, 0);
+      d[u] = ok ? __ldcg(&ci4[g]) : make_int4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int c = 0; c < 4 * SU; ++c) {
@@ -1863,7 +1891,7 @@ __device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci,
       const int4 du = d[c >> 2];
       const uint32_t k = (c & 3) == 0 ? vu.x : (c & 3) == 1 ? vu.y : (c & 3) == 2 ? vu.z : vu.w;
       const int32_t idc = (c & 3) == 0 ? du.x : (c & 3) == 1 ? du.y : (c & 3) == 2 ? du.z : du.w;
-      if (4 * (e4 + (c >> 2) * NT) + (c & 3) < n) {
+      if ((c & 3) < lim[c >> 2]) {
         const uint32_t bin = min((k - tau) >> CS_SHIFT0, (uint32_t)(CS_BINS - 1));
         if (bin > b0) {
           so[atomicAdd(&hist[bin], 1)] = idc;
@@ -1919,101 +1947,120 @@ __device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci,
   return true;
 }
 
-template <int KPL>
+template <int KPL, int PARTS>
 __global__ void __launch_bounds__(RT_THREADS, RT_CTAS) matrix_topk_kernel(const MatrixTopkParams p) {
   pdl_enter();
   extern __shared__ __align__(16) uint8_t smem[];
   int* whist = (int*)(smem + RT_OFF_WHIST);
   int* wpick = (int*)(smem + RT_OFF_WPICK);
-  // [2..4] bin pick, [8] the next row's threshold, [10] the next row's
-  // item, [12] candidates appended, [17] staged count, [21] theta, [22] rr,
-  // [23..25] emission counters, [32..39] warp sums
+  // [2..4] bin pick, [8] the next item's threshold, [10] the next item, [12]
+  // candidates appended, [13] the row's ticket, [14] the other half's
+  // count, [17] staged count, [21] theta, [22] rr, [23..25] emission
+  // counters, [32..39] warp sums
   int* misc = (int*)(smem + RT_OFF_MISC);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K, R = p.rs.R;
+  constexpr int parts = PARTS, cap = ROW_SLOTS / PARTS;  // items per row (1 or 2), candidate slots per item
+  const int items = parts * R;
   const int target = (int)(((int64_t)p.target16 * K) / 16);
-  // items (row R - 1 - item: prefill chunks, the longest rows first): the
-  // CTA's own first, then from a counter; the threshold warp takes each one
-  // row ahead of the stream
-  if (warp == RT_SW) {
-    const int it = blockIdx.x;
+  // items: part (item % parts) of row R - 1 - item / parts (prefill
+  // chunks: the longest rows first); the CTA's own first, then from a
+  // counter, each taken with its row's threshold by the threshold warp one
+  // item ahead of the stream
+  auto take = [&](int it) {
     uint32_t tau = 0u;
-    if (it < R) {
-      const int row = R - 1 - it, b = p.rb[row], e = p.re[row];
+    if (it < items) {
+      const int row = R - 1 - it / parts, b = p.rb[row], e = p.re[row];
       if (e - b > K) tau = rt_threshold<KPL>(p, row, b, e, target, whist, wpick);
+      if (lane == 0 && it % parts == 0) p.tau[row] = tau;
     }
     if (lane == 0) {
       misc[10] = it;
       misc[8] = (int)tau;
     }
-  }
+  };
+  if (warp == RT_SW) take(blockIdx.x);
   __syncthreads();
   int ntriv = 0;
   while (true) {
     const int it = misc[10];
-    if (it >= R) break;  // uniform
+    if (it >= items) break;  // uniform
     const uint32_t tau = (uint32_t)misc[8];
-    const int row = R - 1 - it;
+    const int row = R - 1 - it / parts, half = it % parts;
     const int b = p.rb[row], e = p.re[row], L = e - b;
-    int32_t* o = p.out + (int64_t)row * K;
     uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
     int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
     if (tid == 0) misc[12] = 0;
-    __syncthreads();  // the row is taken from the slot
+    __syncthreads();  // the item is taken from the slot
     if (warp == RT_SW) {
       int itn = 0;
       if (lane == 0) itn = (int)gridDim.x + atomicAdd(&p.stats->cs_next, 1);
-      itn = __shfl_sync(0xffffffffu, itn, 0);
-      uint32_t taun = 0u;
-      if (itn < R) {
-        const int rn = R - 1 - itn, bn = p.rb[rn], en = p.re[rn];
-        if (en - bn > K) taun = rt_threshold<KPL>(p, rn, bn, en, target, whist, wpick);
-      }
-      if (lane == 0) {
-        misc[10] = itn;
-        misc[8] = (int)taun;
-      }
+      take(__shfl_sync(0xffffffffu, itn, 0));
     } else if (L > K) {
-      // the row's float4s wholly inside [b, e) by the stream warps; the
-      // keys before and after them (fewer than 4 at each end) one by one
+      // the item's share of the row's float4s wholly inside [b, e) by the
+      // stream warps, into the item's slots; the keys before and after
+      // them (fewer than 4 at each end) one by one, with the row's first
+      // and last item
       const int fi0 = (b + 3) >> 2, fi1 = e >> 2;
+      const int fm = fi0 + max(fi1 - fi0, 0) / 2;
       const float tauf = key_threshold_float(tau);
       const float* srow = p.scores + (int64_t)row * p.ld;
-      rt_stream(reinterpret_cast<const float4*>(srow), fi0, fi1, tauf, ck, ci, &misc[12],
-                reinterpret_cast<float4*>(smem + RT_OFF_STAGE) + warp * RT_U * 32,
+      uint32_t* hk = ck + half * cap;
+      int32_t* hi_ = ci + half * cap;
+      rt_stream(reinterpret_cast<const float4*>(srow), half ? fm : fi0, half == parts - 1 ? fi1 : fm, tauf, hk,
+                hi_, cap, &misc[12], reinterpret_cast<float4*>(smem + RT_OFF_STAGE) + warp * RT_U * 32,
                 reinterpret_cast<uint16_t*>(smem + RT_OFF_LIST) + warp * RT_U * 32 * 4);
-      if (warp == 0 && lane < 2) {
+      if (warp == 0 && ((lane == 0 && half == 0) || (lane == 1 && half == parts - 1))) {
         const int head_hi = min(e, 4 * fi0), tail_lo = max(4 * fi1, head_hi);
-        const int lo = lane == 0 ? b : tail_lo, hi = lane == 0 ? head_hi : e;
+        const int lo = lane ? tail_lo : b, hi = lane ? e : head_hi;
         for (int s = lo; s < hi; ++s) {
           const float val = srow[s];
           if (val >= tauf) {
             const int pos = atomicAdd(&misc[12], 1);
-            if (pos < ROW_SLOTS) {
-              ck[pos] = ordered_key(val);
-              ci[pos] = s;
+            if (pos < cap) {
+              hk[pos] = ordered_key(val);
+              hi_[pos] = s;
             }
           }
         }
       }
-    } else {  // every valid index, then -1
+    } else if (half == 0) {  // every valid index, then -1
+      int32_t* o = p.out + (int64_t)row * K;
       for (int i = tid; i < K; i += RT_NS) o[i] = i < L ? b + i : -1;
       ntriv += tid == 0;
     }
-    __syncthreads();  // the row is streamed, the next row's threshold is in the slot
+    __syncthreads();  // the half is streamed, the next item's threshold is in the slot
     if (L > K) {
-      // certificate: at least K candidates, none lost (the row's slots hold
-      // ROW_SLOTS)
-      const int n = misc[12];
-      bool ok = n >= K && n <= ROW_SLOTS;
-      if (ok) {
-        if (tid == 0) atomicAdd(&p.stats->cand_total, n);
-        ok = rt_select(ck, ci, n, tau, K, o, smem, misc);
+      // half rows: the half's count, then the row's ticket (the CTA that
+      // streamed the second of the two halves selects the row)
+      if (parts == 2) {
+        if (tid == 0) {
+          p.half_count[2 * row + half] = misc[12];
+          __threadfence();
+          const int t = atomicAdd(&p.row_ticket[row], 1);
+          misc[13] = t;
+          if (t == 1) {
+            __threadfence();
+            misc[14] = __ldcg(&p.half_count[2 * row + (half ^ 1)]);
+          }
+        }
+        __syncthreads();
       }
-      if (!ok && tid == 0) {
-        const int fr = atomicAdd(&p.stats->fail_count, 1);
-        p.failed_rows[fr] = row;
-        atomicAdd(n < K ? &p.stats->underflow : &p.stats->overflow, 1);
+      if (parts == 1 || misc[13] == 1) {
+        // certificate: at least K candidates, none lost (an item's slots
+        // hold cap)
+        const int na = parts == 1 ? misc[12] : half ? misc[14] : misc[12];
+        const int nb = parts == 1 ? 0 : half ? misc[12] : misc[14];
+        bool ok = na + nb >= K && na <= cap && nb <= cap;
+        if (ok) {
+          if (tid == 0) atomicAdd(&p.stats->cand_total, na + nb);
+          ok = rt_select<PARTS == 2>(ck, ci, na, nb, tau, K, p.out + (int64_t)row * K, smem, misc);
+        }
+        if (!ok && tid == 0) {
+          const int fr = atomicAdd(&p.stats->fail_count, 1);
+          p.failed_rows[fr] = row;
+          atomicAdd(na + nb < K ? &p.stats->underflow : &p.stats->overflow, 1);
+        }
       }
     }
     __syncthreads();
@@ -2021,22 +2068,27 @@ __global__ void __launch_bounds__(RT_THREADS, RT_CTAS) matrix_topk_kernel(const 
   if (tid == 0 && ntriv) atomicAdd(&p.stats->trivial, ntriv);
 }
 
-cudaError_t launch_matrix_topk(const MatrixTopkParams& p, int sms, cudaStream_t s) {
+template <int PARTS>
+static cudaError_t launch_matrix_topk_parts(const MatrixTopkParams& p, int sms, cudaStream_t s) {
   static DeviceFlags attr_short, attr_long;
-  const int grid = max(1, min(p.rs.R, RT_CTAS * sms));
+  const int grid = max(1, min(PARTS * p.rs.R, RT_CTAS * sms));
   // the threshold's grid keys sit in the threshold warp's registers: the
   // build holding up to 672 (rows of up to ~134K keys) or MAX_SAMPLES
   const int64_t max_m = std::min<int64_t>(MAX_SAMPLES, (int64_t)p.rs.N / SAMPLE_STRIDE + 2);
   if (max_m <= 32 * TAU_KPL_SHORT) {
-    auto k = matrix_topk_kernel<TAU_KPL_SHORT>;
+    auto k = matrix_topk_kernel<TAU_KPL_SHORT, PARTS>;
     cudaError_t e = set_smem_attr_once(k, RT_SMEM, attr_short);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, dim3(grid), dim3(RT_THREADS), RT_SMEM, s, p);
   }
-  auto k = matrix_topk_kernel<MAX_SAMPLES / 32>;
+  auto k = matrix_topk_kernel<MAX_SAMPLES / 32, PARTS>;
   cudaError_t e = set_smem_attr_once(k, RT_SMEM, attr_long);
   if (e != cudaSuccess) return e;
   return launch_pdl(k, dim3(grid), dim3(RT_THREADS), RT_SMEM, s, p);
+}
+
+cudaError_t launch_matrix_topk(const MatrixTopkParams& p, int sms, cudaStream_t s) {
+  return p.parts == 2 ? launch_matrix_topk_parts<2>(p, sms, s) : launch_matrix_topk_parts<1>(p, sms, s);
 }
 
 

@@ -536,6 +536,60 @@ def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind, matrix_
         assert np.array_equal(got, want), t
 
 
+@pytest.mark.parametrize("bias,kind", [(0, None), (1 << 31, "underflow"), (-(1 << 33), "overflow")])
+def test_topk_from_scores_half_rows_exact(B, bias, kind):
+    """Many long rows go by half rows (two items per row, the second to
+    finish selects the row from both halves' lists): with the grid narrowed
+    to 8 SMs, 200 rows of up to 70001 keys take that path.  Ranges off a
+    4-key boundary, short and trivial rows, ties (an all-equal row overflows
+    its halves and is repaired); with the threshold pushed to the top every
+    row longer than K fails the certificate, with it at zero every row whose
+    halves overflow does; every row is exact."""
+    rng = np.random.default_rng(53)
+    Q, N, K, ld = 200, 70001, 2048, 70004
+    sc = np.full((Q, ld), np.nan, np.float32)   # the padding is never read
+    sc[:, :N] = rng.standard_normal((Q, N)).astype(np.float32)
+    sc[7, :N] = np.round(sc[7, :N] * 2) / 2     # heavy ties
+    sc[8, :N] = 1.0                             # all equal
+    rb = rng.integers(0, 2000, Q).astype(np.int32)
+    re = np.full(Q, N, np.int32)
+    re[1::3] = (rb[1::3] + rng.integers(K + 1, N - 2000, len(re[1::3]))).astype(np.int32)
+    rb[3], re[3] = 4097, N - 3                  # off a 4-key boundary at both ends
+    re[5] = rb[5] + K                           # exactly K: trivial path
+    re[6] = rb[6] + 3                           # fewer than K
+    re[9] = rb[9] + K + 1                       # one key more than K
+    d = to_dev(sc, rb, re)
+    B.set_option("grid_ctas", 8)
+    B.set_option("tau_bias", bias)
+    try:
+        out = B.topk_from_scores(d[0], d[1], d[2], K=K, N=N).cpu().numpy()
+        counters = _status_ok(B)
+    finally:
+        B.set_option("tau_bias", 0)
+        B.set_option("grid_ctas", 0)
+    long_rows = np.nonzero((re - rb) > K)[0].tolist()
+    if kind == "underflow":
+        # (a row shorter than the aim, 36 K / 16 keys, has its threshold's
+        # rank outside its sample: every key passes, the bias does not
+        # apply, and the row is selected without repair)
+        repaired = sorted(B.last_repaired_rows())
+        sampled = np.nonzero((re - rb) >= 2 * (36 * K // 16))[0].tolist()
+        assert counters[kind] == len(repaired) and set(sampled) <= set(repaired) <= set(long_rows)
+    elif kind == "overflow":
+        repaired = sorted(B.last_repaired_rows())
+        past_halves = np.nonzero((re - rb) > 2 * 8192 + 8)[0].tolist()
+        assert counters[kind] == len(repaired) and set(past_halves) <= set(repaired) <= set(long_rows)
+    for t in range(Q):
+        L = int(re[t] - rb[t])
+        n = min(L, K)
+        sel = out[t, :n]
+        assert (out[t, n:] == -1).all()
+        assert len(np.unique(sel)) == n and np.all((sel >= rb[t]) & (sel < re[t])), t
+        want = np.sort(sc[t, rb[t]:re[t]])[::-1][:n]
+        got = np.sort(sc[t, sel])[::-1]
+        assert np.array_equal(got, want), t
+
+
 # ------------------------------------------------------------- CUDA graph ----
 def test_fused_call_replays_from_a_cuda_graph(B):
     """The fused call enqueues kernels only (no host synchronisation, no
