@@ -307,10 +307,10 @@ typedef enum {
                                   accumulator, so that its epilogue's wait runs out after DSA_OPT_WAIT_LIMIT_US
                                   and the call reports DSA_ERR_TIMEOUT (its output is then undefined); default 0 */
   DSA_OPT_MATRIX_ROW_MIN = 10  /* dsa_indexer_topk_from_scores and the unfused operator's selection: rows from
-                                  which each CTA takes whole rows (threshold, one pass over the row, selection)
-                                  instead of splitting rows over the SMs (default -1: chosen per call, one
-                                  wave of the per-row kernel's CTAs; 0: always; the result does not depend
-                                  on it) */
+                                  which CTAs take whole rows, or half rows when there are many long ones
+                                  (threshold, one pass over the row, selection by the CTA that finishes the
+                                  row), instead of splitting rows over the SMs (default -1: chosen per call,
+                                  one row per SM; 0: always; the result does not depend on it) */
 } dsa_option;
 DSA_API int dsa_indexer_set_option(int option, int64_t value);
 DSA_API int64_t dsa_indexer_get_option(int option);
