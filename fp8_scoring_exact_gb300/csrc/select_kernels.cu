@@ -1688,14 +1688,22 @@ __device__ __forceinline__ uint32_t ge_mask(float x, float t) {
 // fi0 + t, then every RT_NS-th, RT_U per step, the next step's loads in
 // flight while a step is compared.  The warp's kept scores of a step go to
 // ck / ci (cap slots) at consecutive positions from the shared counter
-// *count: each
-// lane stages its step in shared memory (stage: RT_U x 32 float4s, position
-// v, lane l at v * 32 + l) and lists the offsets of its kept scores there
-// (list, in lane order: a warp scan of the counts), then lane j writes
-// the list's j-th score.  Steps whose every float4 lies inside the range
-// (all but a row's last) take no per-lane range tests.
-__device__ __forceinline__ void rt_stream(const float4* s4, int fi0, int fi1, float tauf, uint32_t* ck, int32_t* ci,
-                                          int cap, int* count, float4* stage, uint16_t* list) {
+// *count: each lane stages its step in shared memory (stage: RT_U x 32
+// float4s, position v, lane l at v * 32 + l) and lists the offsets of its
+// kept scores there (list, in lane order: a warp scan of the counts), then
+// lane j writes the list's j-th score.  With TIES, a score whose key equals
+// the threshold key tau is kept only while the item holds fewer than K
+// such (the shared counter *ties): a top K takes at most K keys equal to
+// its K-th, and the keys at tau are below it unless tau is the K-th, so a
+// row whose threshold falls on a heavily tied value (zeros) does not fill
+// its slots with them (the second pass over an item whose list overflowed;
+// the first places the warp's run before it forms the keys).  Steps whose
+// every float4 lies inside the range (all but a row's last) take no
+// per-lane range tests.
+template <bool TIES>
+__device__ __forceinline__ void rt_stream(const float4* s4, int fi0, int fi1, float tauf, uint32_t tau, int K,
+                                          uint32_t* ck, int32_t* ci, int cap, int* count, int* ties, float4* stage,
+                                          uint16_t* list) {
   constexpr int U = RT_U, NS = RT_NS;
   const int lane = threadIdx.x & 31;
   const int wt = (int)threadIdx.x - lane;  // the warp's first stream thread
@@ -1751,7 +1759,7 @@ __device__ __forceinline__ void rt_stream(const float4* s4, int fi0, int fi1, fl
     const int tot = __shfl_sync(0xffffffffu, incl, 31);
     if (tot != 0) {  // warp-uniform
       int base = 0;
-      if (lane == 31) base = atomicAdd(count, tot);
+      if (!TIES && lane == 31) base = atomicAdd(count, tot);
 #pragma unroll
       for (int v = 0; v < U; ++v) stage[v * 32 + lane] = x[v];
       int p = incl - cnt;
@@ -1760,13 +1768,38 @@ __device__ __forceinline__ void rt_stream(const float4* s4, int fi0, int fi1, fl
         mask &= mask - 1u;
         list[p++] = (uint16_t)(((q >> 2) * 32 + lane) * 4 + (q & 3));
       }
-      base = __shfl_sync(0xffffffffu, base, 31);
       __syncwarp();
-      for (int j = lane; j < tot; j += 32) {
-        const int code = list[j];
-        const int pos = base + j;
-        if (pos < cap) {
-          ck[pos] = ordered_key(stagef[code]);
+      if (!TIES) {
+        base = __shfl_sync(0xffffffffu, base, 31);
+        for (int j = lane; j < tot; j += 32) {
+          const int code = list[j];
+          const int pos = base + j;
+          if (pos < cap) {
+            ck[pos] = ordered_key(stagef[code]);
+            ci[pos] = 4 * (fw + ((code >> 2) & 31) + (code >> 7) * NS) + (code & 3);
+          }
+        }
+      }
+      for (int jb = 0; TIES && jb < tot; jb += 32) {  // (warp-uniform)
+        const int j = jb + lane;
+        const bool active = j < tot;
+        const int code = active ? list[j] : 0;
+        const uint32_t key = ordered_key(stagef[code]);
+        const bool tie = active && key == tau;
+        bool keep = active && !tie;
+        const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+        if (tb) {
+          int t0 = 0;
+          if (lane == 0) t0 = atomicAdd(ties, __popc(tb));
+          t0 = __shfl_sync(0xffffffffu, t0, 0);
+          keep |= tie && t0 + __popc(tb & lanemask_lt()) < K;
+        }
+        const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+        if (lane == 0 && kb) base = atomicAdd(count, __popc(kb));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int pos = base + __popc(kb & lanemask_lt());
+        if (keep && pos < cap) {
+          ck[pos] = key;
           ci[pos] = 4 * (fw + ((code >> 2) & 31) + (code >> 7) * NS) + (code & 3);
         }
       }
@@ -1947,6 +1980,43 @@ __device__ __forceinline__ bool rt_select(const uint32_t* ck, const int32_t* ci,
   return true;
 }
 
+// A stream warp's part of item `half` (of `parts`) of row `row` over [b, e):
+// the item's share of the row's float4s wholly inside [b, e) into the
+// item's slots (misc[12]: the count, misc[15]: keys at the threshold); the
+// keys before and after them (fewer than 4 at each end) one by one, with
+// the row's first and last item.
+template <bool TIES>
+__device__ __forceinline__ void rt_item(const MatrixTopkParams& p, int row, int b, int e, int half, int parts,
+                                        uint32_t tau, int K, int* misc) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cap = ROW_SLOTS / parts;
+  const int fi0 = (b + 3) >> 2, fi1 = e >> 2;
+  const int fm = fi0 + max(fi1 - fi0, 0) / 2;
+  const float tauf = key_threshold_float(tau);
+  const float* srow = p.scores + (int64_t)row * p.ld;
+  uint32_t* hk = p.cand_key + (int64_t)row * ROW_SLOTS + half * cap;
+  int32_t* hi_ = p.cand_idx + (int64_t)row * ROW_SLOTS + half * cap;
+  rt_stream<TIES>(reinterpret_cast<const float4*>(srow), half ? fm : fi0, half == parts - 1 ? fi1 : fm, tauf, tau, K,
+                  hk, hi_, cap, &misc[12], &misc[15], reinterpret_cast<float4*>(smem + RT_OFF_STAGE) + warp * RT_U * 32,
+                  reinterpret_cast<uint16_t*>(smem + RT_OFF_LIST) + warp * RT_U * 32 * 4);
+  if (warp == 0 && ((lane == 0 && half == 0) || (lane == 1 && half == parts - 1))) {
+    const int head_hi = min(e, 4 * fi0), tail_lo = max(4 * fi1, head_hi);
+    const int lo = lane ? tail_lo : b, hi = lane ? e : head_hi;
+    for (int s = lo; s < hi; ++s) {
+      const float val = srow[s];
+      const uint32_t key = ordered_key(val);
+      if (val >= tauf && (!TIES || key != tau || atomicAdd(&misc[15], 1) < K)) {
+        const int pos = atomicAdd(&misc[12], 1);
+        if (pos < cap) {
+          hk[pos] = key;
+          hi_[pos] = s;
+        }
+      }
+    }
+  }
+}
+
 template <int KPL, int PARTS>
 __global__ void __launch_bounds__(RT_THREADS, RT_CTAS) matrix_topk_kernel(const MatrixTopkParams p) {
   pdl_enter();
@@ -1955,8 +2025,8 @@ __global__ void __launch_bounds__(RT_THREADS, RT_CTAS) matrix_topk_kernel(const 
   int* wpick = (int*)(smem + RT_OFF_WPICK);
   // [2..4] bin pick, [8] the next item's threshold, [10] the next item, [12]
   // candidates appended, [13] the row's ticket, [14] the other half's
-  // count, [17] staged count, [21] theta, [22] rr, [23..25] emission
-  // counters, [32..39] warp sums
+  // count, [15] keys at the threshold met, [17] staged count, [21] theta,
+  // [22] rr, [23..25] emission counters, [32..39] warp sums
   int* misc = (int*)(smem + RT_OFF_MISC);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K, R = p.rs.R;
@@ -1990,46 +2060,30 @@ __global__ void __launch_bounds__(RT_THREADS, RT_CTAS) matrix_topk_kernel(const 
     const int b = p.rb[row], e = p.re[row], L = e - b;
     uint32_t* ck = p.cand_key + (int64_t)row * ROW_SLOTS;
     int32_t* ci = p.cand_idx + (int64_t)row * ROW_SLOTS;
-    if (tid == 0) misc[12] = 0;
+    if (tid == 0) misc[12] = misc[15] = 0;
     __syncthreads();  // the item is taken from the slot
     if (warp == RT_SW) {
       int itn = 0;
       if (lane == 0) itn = (int)gridDim.x + atomicAdd(&p.stats->cs_next, 1);
       take(__shfl_sync(0xffffffffu, itn, 0));
     } else if (L > K) {
-      // the item's share of the row's float4s wholly inside [b, e) by the
-      // stream warps, into the item's slots; the keys before and after
-      // them (fewer than 4 at each end) one by one, with the row's first
-      // and last item
-      const int fi0 = (b + 3) >> 2, fi1 = e >> 2;
-      const int fm = fi0 + max(fi1 - fi0, 0) / 2;
-      const float tauf = key_threshold_float(tau);
-      const float* srow = p.scores + (int64_t)row * p.ld;
-      uint32_t* hk = ck + half * cap;
-      int32_t* hi_ = ci + half * cap;
-      rt_stream(reinterpret_cast<const float4*>(srow), half ? fm : fi0, half == parts - 1 ? fi1 : fm, tauf, hk,
-                hi_, cap, &misc[12], reinterpret_cast<float4*>(smem + RT_OFF_STAGE) + warp * RT_U * 32,
-                reinterpret_cast<uint16_t*>(smem + RT_OFF_LIST) + warp * RT_U * 32 * 4);
-      if (warp == 0 && ((lane == 0 && half == 0) || (lane == 1 && half == parts - 1))) {
-        const int head_hi = min(e, 4 * fi0), tail_lo = max(4 * fi1, head_hi);
-        const int lo = lane ? tail_lo : b, hi = lane ? e : head_hi;
-        for (int s = lo; s < hi; ++s) {
-          const float val = srow[s];
-          if (val >= tauf) {
-            const int pos = atomicAdd(&misc[12], 1);
-            if (pos < cap) {
-              hk[pos] = ordered_key(val);
-              hi_[pos] = s;
-            }
-          }
-        }
-      }
+      rt_item<false>(p, row, b, e, half, parts, tau, K, misc);
     } else if (half == 0) {  // every valid index, then -1
       int32_t* o = p.out + (int64_t)row * K;
       for (int i = tid; i < K; i += RT_NS) o[i] = i < L ? b + i : -1;
       ntriv += tid == 0;
     }
-    __syncthreads();  // the half is streamed, the next item's threshold is in the slot
+    __syncthreads();  // the item is streamed, the next item's threshold is in the slot
+    if (L > K && misc[12] > cap) {
+      // the list overflowed: once more with the keys at the threshold kept
+      // up to K (a threshold on a heavily tied value), before the row goes
+      // to the repair
+      __syncthreads();
+      if (tid == 0) misc[12] = misc[15] = 0;
+      __syncthreads();
+      if (warp < RT_SW) rt_item<true>(p, row, b, e, half, parts, tau, K, misc);
+      __syncthreads();
+    }
     if (L > K) {
       // half rows: the half's count, then the row's ticket (the CTA that
       // streamed the second of the two halves selects the row)
