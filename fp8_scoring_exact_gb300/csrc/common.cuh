@@ -340,13 +340,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Prefetch of `bytes` (a multiple of 16, from a 16-byte aligned address)
-// from global memory into L2, with no destination and nothing to wait for.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(src)), "r"(bytes)
-               : "memory");
-}
-
 // --------------------------------------------------------------- tcgen05 ----
 // Shared-memory matrix descriptor for a K-major operand stored in the 128-byte
 // swizzled layout TMA writes (rows of 128 bytes, 8-row / 1024-byte swizzle

@@ -92,6 +92,15 @@ def test_options_roundtrip_and_validate():
         binding.set_option(name, 1)
         assert binding.get_option(name) == 1
         binding.set_option(name, 0)
+    # the standalone top-K's path: -1 chosen per call (the default), 0 and up a row count
+    assert binding.get_option("matrix_row_min") == -1
+    binding.set_option("matrix_row_min", 0)
+    assert binding.get_option("matrix_row_min") == 0
+    binding.set_option("matrix_row_min", 1 << 40)
+    assert binding.get_option("matrix_row_min") == 1 << 40
+    with pytest.raises(binding.IndexerError):
+        binding.set_option("matrix_row_min", -2)
+    binding.set_option("matrix_row_min", -1)
 
 
 def test_product_path_has_no_cpu_fallback():
