@@ -175,9 +175,13 @@ DSA_API int dsa_indexer_scores(const uint8_t* q_fp8, const float* q_scale,
                        int Q, int N, float* scores, int64_t ld, dsa_stream_t stream);
 
 /*
- * Standalone exact top-K over a given fp32 score matrix (section 3: sampled
- * threshold, compare-and-append, four-pass radix select, certificate, and a
- * full-row radix select when the certificate fails).  Row t considers
+ * Standalone exact top-K over a given fp32 score matrix (section 3: each
+ * row's threshold from a sample of its own scores, compare-and-append of the
+ * scores at or above it, exact selection of those candidates with a
+ * certificate, and a full-row radix select for the rows that fail it).  From
+ * one row per SM on, CTAs take whole rows (half rows when there are many
+ * long ones) and select each row as its last part is streamed, so the
+ * matrix is read once; fewer rows are split over the SMs.  Row t considers
  * scores[t, s] for s in [row_begin[t], row_end[t]) and returns the indices s.
  * NaN scores are not supported.  scores is [Q, ld] fp32.
  */
