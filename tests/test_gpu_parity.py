@@ -491,6 +491,40 @@ def test_topk_from_scores_long_rows_exact(B, matrix_path):
         assert np.array_equal(got, want), t
 
 
+@pytest.mark.parametrize("K", [1, 5, 64])
+def test_topk_from_scores_small_k_and_tiny_rows(B, matrix_path, K):
+    """Small K and rows a few keys long: rows inside one 4-key group (only the
+    keys before and after a row's whole float4s are read one by one), rows
+    of K, K + 1 and up to 12 keys, rows off a 4-key boundary, ties and -0;
+    every row exact against a full sort."""
+    rng = np.random.default_rng(91 + K)
+    Q, N, ld = 48, 9001, 9004
+    sc = np.full((Q, ld), np.nan, np.float32)           # the padding is never read
+    sc[:, :N] = rng.standard_normal((Q, N)).astype(np.float32)
+    sc[::7, :N] = np.round(sc[::7, :N] * 2) / 2          # ties
+    sc[5, 0:N:3] = -0.0
+    sc[5, 1:N:3] = 0.0
+    rb = rng.integers(0, N - 20, Q).astype(np.int32)
+    re = np.minimum(rb + rng.integers(0, 13, Q), N).astype(np.int32)
+    re[0::4] = np.minimum(rb[0::4] + rng.integers(K + 1, 4000, len(re[0::4])), N)
+    rb[1], re[1] = 5, 7                                  # inside one 4-key group
+    rb[2], re[2] = 9, 9 + K                              # exactly K
+    rb[3], re[3] = 10, 11 + K                            # K + 1
+    rb[6], re[6] = 0, N                                  # the whole row, N odd
+    d = to_dev(sc, rb, re)
+    out = B.topk_from_scores(d[0], d[1], d[2], K=K, N=N).cpu().numpy()
+    _status_ok(B)
+    for t in range(Q):
+        L = int(re[t] - rb[t])
+        n = min(L, K)
+        sel = out[t, :n]
+        assert (out[t, n:] == -1).all(), t
+        assert len(np.unique(sel)) == n and np.all((sel >= rb[t]) & (sel < re[t])), t
+        want = np.sort(sc[t, rb[t]:re[t]])[::-1][:n]
+        got = np.sort(sc[t, sel])[::-1]
+        assert np.array_equal(got, want), t
+
+
 @pytest.mark.parametrize("bias,kind", [(0, None), (1 << 31, "underflow"), (-(1 << 33), "overflow")])
 def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind, matrix_path):
     """A padded row stride (ld > N, N not a multiple of 4), ranges that end at
