@@ -790,21 +790,24 @@ int dsa_indexer_topk_paged(const uint8_t* q_fp8, const float* q_scale, const uin
   return run_fused(rs, K, tq, tk, k_cache, k_cache_scale, q_scale, w, nullptr, nullptr, out_idx, stream);
 }
 
-// The standalone top-K takes whole rows (or half rows per item, the ticket
-// of each row in the plan's zeroed pair_cnt) from one row per SM on; fewer
-// rows are split over the SMs (measured on GB300, rows of 131072 keys, split
-// against whole rows: 152 rows 0.063 / 0.061 ms, 384 rows 0.107 / 0.075 ms,
-// 4096 rows 0.655 / 0.438 ms).
+// The standalone top-K takes whole or half rows per CTA item (the ticket of
+// each row in the plan's zeroed pair_cnt) from a third of a row per SM on;
+// fewer rows are split over the SMs (measured on GB300, rows of 131072 keys,
+// split path against the per-row kernel: 48 rows 0.048 / 0.046 ms, 128 rows
+// 0.061 / 0.048 ms, 384 rows 0.107 / 0.075 ms, 4096 rows 0.655 / 0.438 ms;
+// 8 rows 0.041 / 0.056 ms).
 bool matrix_by_rows(const Opts& o, const RowSpace& rs) {
-  const int64_t row_min = o.matrix_row_min >= 0 ? o.matrix_row_min : (int64_t)o.grid;
+  const int64_t row_min = o.matrix_row_min >= 0 ? o.matrix_row_min : ((int64_t)o.grid + 2) / 3;
   return rs.R >= row_min;
 }
-// Items per row of the per-row kernel: half rows for three waves of rows or
-// more of at least 64K keys (measured on GB300: 4096 x 131072 0.453 ->
-// 0.437 ms; fewer or shorter rows were slower in halves: 1216 x 131072
-// 0.155 -> 0.167 ms, 2048 x 16384 0.105 -> 0.124 ms).
+// Items per row of the per-row kernel: half rows for fewer rows than SMs
+// (twice the items: 128 x 131072 0.057 -> 0.048 ms) and for three waves of
+// rows or more of at least 64K keys (4096 x 131072 0.453 -> 0.437 ms);
+// whole rows in between, where halves were slower (1216 x 131072 0.155 ->
+// 0.167 ms, 2048 x 16384 0.105 -> 0.124 ms).  Measured on GB300.
 int matrix_parts(const Opts& o, const RowSpace& rs) {
-  return rs.R >= 3LL * MATRIX_TOPK_CTAS_PER_SM * o.grid && rs.N >= 65536 ? 2 : 1;
+  const bool many_long = rs.R >= 3LL * MATRIX_TOPK_CTAS_PER_SM * o.grid && rs.N >= 65536;
+  return many_long || rs.R < o.grid ? 2 : 1;
 }
 
 // Exact top-K over a given fp32 score matrix [R, ld] (the standalone

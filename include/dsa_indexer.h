@@ -179,9 +179,9 @@ DSA_API int dsa_indexer_scores(const uint8_t* q_fp8, const float* q_scale,
  * row's threshold from a sample of its own scores, compare-and-append of the
  * scores at or above it, exact selection of those candidates with a
  * certificate, and a full-row radix select for the rows that fail it).  From
- * one row per SM on, CTAs take whole rows (half rows when there are many
- * long ones) and select each row as its last part is streamed, so the
- * matrix is read once; fewer rows are split over the SMs.  Row t considers
+ * a third of a row per SM on, CTAs take whole or half rows and select each
+ * row as its last part is streamed, so the matrix is read once; fewer rows
+ * are split over the SMs.  Row t considers
  * scores[t, s] for s in [row_begin[t], row_end[t]) and returns the indices s.
  * NaN scores are not supported.  scores is [Q, ld] fp32.
  */
@@ -314,7 +314,7 @@ typedef enum {
                                   which CTAs take whole rows, or half rows when there are many long ones
                                   (threshold, one pass over the row, selection by the CTA that finishes the
                                   row), instead of splitting rows over the SMs (default -1: chosen per call,
-                                  one row per SM; 0: always; the result does not depend on it) */
+                                  a third of a row per SM; 0: always; the result does not depend on it) */
 } dsa_option;
 DSA_API int dsa_indexer_set_option(int option, int64_t value);
 DSA_API int64_t dsa_indexer_get_option(int option);

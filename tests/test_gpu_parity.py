@@ -570,17 +570,19 @@ def test_topk_from_scores_padded_stride_and_forced_repair(B, bias, kind, matrix_
         assert np.array_equal(got, want), t
 
 
+@pytest.mark.parametrize("Q", [200, 60, 10])
 @pytest.mark.parametrize("bias,kind", [(0, None), (1 << 31, "underflow"), (-(1 << 33), "overflow")])
-def test_topk_from_scores_half_rows_exact(B, bias, kind):
-    """Many long rows go by half rows (two items per row, the second to
-    finish selects the row from both halves' lists): with the grid narrowed
-    to 8 SMs, 200 rows of up to 70001 keys take that path.  Ranges off a
-    4-key boundary, short and trivial rows, ties (an all-equal row overflows
-    its halves and is repaired); with the threshold pushed to the top every
-    row longer than K fails the certificate, with it at zero every row whose
-    halves overflow does; every row is exact."""
-    rng = np.random.default_rng(53)
-    Q, N, K, ld = 200, 70001, 2048, 70004
+def test_topk_from_scores_whole_and_half_rows_exact(B, bias, kind, Q):
+    """The per-row path's items, with the grid narrowed to 8 SMs: 200 rows of
+    up to 70001 keys (many long rows) and 10 rows (fewer than SMs) go by half
+    rows (two items per row, the second to finish selects the row from both
+    halves' lists), 60 rows by whole rows.  Ranges off a 4-key boundary,
+    short and trivial rows, ties (an all-equal row keeps at most K keys at
+    its threshold); with the threshold pushed to the top every row longer
+    than K fails the certificate, with it at zero every row whose lists
+    overflow does; every row is exact."""
+    rng = np.random.default_rng(53 + Q)
+    N, K, ld = 70001, 2048, 70004
     sc = np.full((Q, ld), np.nan, np.float32)   # the padding is never read
     sc[:, :N] = rng.standard_normal((Q, N)).astype(np.float32)
     sc[7, :N] = np.round(sc[7, :N] * 2) / 2     # heavy ties
